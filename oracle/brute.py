@@ -1,0 +1,96 @@
+"""Pure-Python brute force of the DSA step for tiny inputs.  TEST INFRASTRUCTURE ONLY.
+
+Independent of ``dsa_oracle``: no numpy arithmetic, plain loops over Python
+floats (IEEE double), written straight from the definitions, so that the
+float64 oracle can be pinned against something other than itself.
+"""
+from __future__ import annotations
+
+import math
+import struct
+
+
+def bf16(bits: int) -> float:
+    """Value of a bf16 bit pattern: it is the upper half of a float32."""
+    return struct.unpack("<f", struct.pack("<I", (int(bits) & 0xFFFF) << 16))[0]
+
+
+def e4m3_value(code: int) -> float:
+    """Value of an OCP E4M3 code (sign, 4-bit exponent with bias 7, 3-bit mantissa)."""
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return math.nan
+    if e == 0:
+        return sign * m * 2.0 ** -9
+    return sign * (8 + m) * 2.0 ** (e - 10)
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest finite E4M3 code by exhaustive search; ties go to the even mantissa; clamp at 448."""
+    best, best_d = None, None
+    for code in range(0x80):
+        if code == 0x7F:
+            continue
+        d = abs(abs(x) - e4m3_value(code))
+        if best is None or d < best_d or (d == best_d and (code & 1) == 0 and (best & 1) == 1):
+            best, best_d = code, d
+    if x < 0 or (x == 0 and math.copysign(1.0, x) < 0):
+        best |= 0x80
+    return best
+
+
+def f32(x: float) -> float:
+    """Round a double to float32."""
+    return struct.unpack("<f", struct.pack("<f", x))[0]
+
+
+def quantize_key(values_f32: list) -> tuple[list, float]:
+    amax = max(abs(v) for v in values_f32)
+    scale = f32(amax / 448.0) if amax > 0 else 1.0
+    return [e4m3_encode(f32(v / scale)) for v in values_f32], scale
+
+
+def score(q_heads: list, w: list, key: list) -> float:
+    """sum over heads of w[h] * ReLU(sum_d q[h][d] * key[d])."""
+    total = 0.0
+    for h in range(len(q_heads)):
+        dot = 0.0
+        for d in range(len(key)):
+            dot += q_heads[h][d] * key[d]
+        total += w[h] * (dot if dot > 0 else 0.0)
+    return total
+
+
+def topk(scores: list, k: int) -> list:
+    """Sorted positions of the k best (score desc, position asc), or all positions if <= k."""
+    n = len(scores)
+    if n <= k:
+        return list(range(n))
+    ranked = sorted(range(n), key=lambda s: (-scores[s], s))
+    return sorted(ranked[:k])
+
+
+def attention(q_heads: list, rows: list, scale: float, d_latent: int) -> tuple[list, list]:
+    """Per head: softmax over rows of scale * (q . row), output sum p * row[:d_latent], and lse."""
+    outs, lses = [], []
+    for qh in q_heads:
+        z = []
+        for row in rows:
+            acc = 0.0
+            for d in range(len(row)):
+                acc += qh[d] * row[d]
+            z.append(scale * acc)
+        m = max(z)
+        e = [math.exp(v - m) for v in z]
+        l = sum(e)
+        out = [0.0] * d_latent
+        for j, row in enumerate(rows):
+            p = e[j] / l
+            for d in range(d_latent):
+                out[d] += p * row[d]
+        outs.append(out)
+        lses.append(m + math.log(l))
+    return outs, lses

@@ -1,0 +1,334 @@
+"""Float64 CPU oracle of the GLM-5.2 DSA step.  TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its ``cpu_baseline``
+leg and ``--impl reference``) may import this module.  The product path in
+``deepseek_sparse_mla_gb300`` never imports, links or runs it, and this module
+shares no code with it.
+
+Every value is widened exactly to float64 from its stored format (bf16, OCP
+e4m3, float32) and every step below is the plain definition, in the order the
+pages give it, with numpy's matmul / sort as library primitives and no
+blocking, fusion or reordering.
+
+Definitions (R query rows, B requests, P page size):
+
+* addressing -- token s of request b lives at slot
+  ``block_table[b, s // P] * P + s % P`` ("GLM-5.2 on vLLM Ascend:
+  Request-to-Backend Inference Path", section 8 "The SFA backend, step by
+  step": the slot mapping scatters new latent KV and indexer keys into their
+  physical pages, the kernels receive block tables);
+* position of a row -- row i of request b sits at ``L_b - q_len_b + i`` and
+  sees positions ``0 .. pos`` inclusive ("Making GLM-5.2 Sparse on TPUs",
+  "Pack requests and reuse prefixes": causality uses P + i; the row's own token
+  is written before selection, per the SFA backend steps);
+* indexer -- ``I(r, s) = sum_h w[r,h] * max(0, q_idx[r,h] . K[s])`` over 32
+  heads of width 128 ("vLLM Inference Path: GLM-5.2 as an Example", "DSA
+  Indexer" and the Model Shape table; "Making GLM-5.2 Sparse on TPUs",
+  "Separate the indexer from the attention it controls": a weighted sum of
+  ReLU-transformed query-key dot products);  K[s] is the bf16 key, or the e4m3
+  code times the token's float32 scale;
+* top-k -- the k highest-scoring visible positions, larger score first and the
+  smaller position on ties; every visible position when there are at most k
+  ("vLLM Inference Path", "DSA Indexer": Top-2048, contexts shorter than 2,048
+  keep nearly every position);  emitted sorted ascending, padded with -1;
+* sparse absorbed MLA -- for each head h and selected s:
+  ``z = scale * (q_lat[h] . c_KV[s] + q_rope[h] . k_R[s])``, softmax over the
+  selection, ``out[h] = sum_s p_s c_KV[s]`` (512-wide latent, before the
+  value-up projection) and ``lse[h] = m + ln(sum exp(z - m))``, scale
+  1/sqrt(192 + 64) ("Making GLM-5.2 Sparse on TPUs", "Separate the indexer
+  ..." : absorbed MLA, scale tied to the original 192 + 64 q/k width; "vLLM
+  Inference Path", "MLA Projections and KV State" and "Sparse MLA Attention");
+  entries outside ``0 .. pos`` (including -1 padding) are skipped, and a row
+  with no valid entry gets out = 0, lse = -inf;
+* IndexShare -- layers marked shared reuse the index buffer of the nearest
+  preceding full (owner) layer ("vLLM Inference Path", "DSA Indexer";
+  "Serving GLM-5.2-504B on 8x RTX PRO 6000 GPUs", "Root cause: a missing
+  index_topk_pattern": full -> F, shared -> S);
+* fp8 index-key append -- per token, ``scale = amax / 448`` in float32 (1 if
+  amax = 0) and ``code = e4m3_rne_satfinite(x / scale)`` with IEEE float32
+  division.  The pages name "FP8 e4m3 keys with FP32 scales" ("GLM-5.2 on
+  vLLM Ascend", section 7) without fixing the scale rule: amax/448 is the
+  reading taken here.  The e4m3 format is the OCP 8-bit floating point
+  specification's E4M3 (bias 7, no infinities, S.1111.111 = NaN, max 448).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+E4M3_MAX = 448.0
+
+
+# ---------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------
+def bf16_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns -> float64 (exact: bf16 is the top half of a float32)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """OCP E4M3 codes -> float64.
+
+    Field layout s.eeee.mmm, exponent bias 7.  Exponent field 0 is subnormal:
+    (m/8) * 2^-6.  Otherwise (1 + m/8) * 2^(e-7).  S.1111.111 is NaN; there
+    are no infinities, so S.1111.110 = 448 is the largest finite value.
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where((c & 0x80) != 0, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    out = sign * mag
+    return np.where((c & 0x7F) == 0x7F, np.nan, out)
+
+
+def f32_to_e4m3(x) -> np.ndarray:
+    """float32 -> OCP E4M3 code, round to nearest (ties to even), saturating to +-448.
+
+    For |x| in [2^e, 2^(e+1)) with e >= -6 the representable spacing is 2^(e-3);
+    below 2^-6 (the subnormal range) it is 2^-9.  Dividing by the spacing is
+    exact in float64, np.rint rounds half to even, and a magnitude that rounds
+    up into the next binade is still representable.
+    """
+    v = np.asarray(x, dtype=np.float32).astype(np.float64)
+    neg = np.signbit(v)
+    a = np.abs(v)
+    _, ex = np.frexp(a)                       # a = f * 2^ex, f in [0.5, 1)
+    e = np.maximum(ex - 1, -6)                # floor(log2 a), clamped to the subnormal binade
+    step = np.ldexp(1.0, e - 3)
+    q = np.minimum(np.rint(a / step) * step, E4M3_MAX)
+    # encode the (exactly representable) magnitude q
+    _, qex = np.frexp(np.where(q > 0, q, 1.0))
+    qe = qex - 1
+    normal = q >= 2.0 ** -6
+    exp_field = np.where(normal, qe + 7, 0)
+    mant = np.where(normal, q / np.ldexp(1.0, qe) - 1.0, q / 2.0 ** -9) * np.where(normal, 8.0, 1.0)
+    code = (exp_field.astype(np.int64) << 3) | np.rint(mant).astype(np.int64)
+    code = np.where(q == 0, 0, code)
+    code = code | np.where(neg, 0x80, 0)
+    return code.astype(np.uint8)
+
+
+def quantize_index_keys(bits) -> tuple[np.ndarray, np.ndarray]:
+    """bf16 index keys [T, 128] -> (e4m3 codes [T, 128], float32 scales [T]).
+
+    scale = amax / 448 in float32 (1 when amax = 0); code = e4m3(x / scale) with
+    the division done in IEEE float32, as the append step does.
+    """
+    x = bf16_to_f64(bits).astype(np.float32)          # exact: bf16 values are float32 values
+    amax = np.max(np.abs(x), axis=-1)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    codes = f32_to_e4m3((x / scale[..., None]).astype(np.float32))
+    return codes, scale
+
+
+# ---------------------------------------------------------------------------
+# the paged caches
+# ---------------------------------------------------------------------------
+class PagedCache:
+    """One layer's caches: latent pages [N_pg, P, 576] bf16 and, for an
+    indexer-owning layer, index-key pages [N_pg, P, 128] (bf16, or e4m3 codes
+    with float32 scales [N_pg, P]).  Unwritten slots hold 0."""
+
+    def __init__(self, num_pages: int, page_size: int, key_format: str | None, d_latent=512, d_rope=64, d_index=128):
+        self.num_pages, self.page_size, self.key_format = num_pages, page_size, key_format
+        self.d_latent, self.d_rope, self.d_index = d_latent, d_rope, d_index
+        self.latent = np.zeros((num_pages, page_size, d_latent + d_rope), dtype=np.uint16)
+        self.index_keys = None
+        self.index_scales = None
+        if key_format == "bf16":
+            self.index_keys = np.zeros((num_pages, page_size, d_index), dtype=np.uint16)
+        elif key_format == "fp8":
+            self.index_keys = np.zeros((num_pages, page_size, d_index), dtype=np.uint8)
+            self.index_scales = np.zeros((num_pages, page_size), dtype=np.float32)
+        elif key_format is not None:
+            raise ValueError(key_format)
+
+    def append(self, c_kv_bits, k_rope_bits, slot_mapping, k_idx_bits=None, k_idx_codes=None, k_idx_scales=None):
+        """Write new tokens at their slots (page = slot // P, offset = slot % P).
+
+        The latent row is the bit-exact concatenation [c_KV | k_R].  Index keys
+        are stored as given (bf16), quantised here (bf16 given, fp8 cache), or
+        stored as given codes + scales (pre-quantised input)."""
+        slot = np.asarray(slot_mapping, dtype=np.int64)
+        pg, off = slot // self.page_size, slot % self.page_size
+        self.latent[pg, off, :self.d_latent] = c_kv_bits
+        self.latent[pg, off, self.d_latent:] = k_rope_bits
+        if self.key_format is None:
+            return
+        if self.key_format == "bf16":
+            self.index_keys[pg, off] = k_idx_bits
+        elif k_idx_codes is not None:
+            self.index_keys[pg, off] = k_idx_codes
+            self.index_scales[pg, off] = k_idx_scales
+        else:
+            codes, scales = quantize_index_keys(k_idx_bits)
+            self.index_keys[pg, off] = codes
+            self.index_scales[pg, off] = scales
+
+    def slots(self, block_row, positions) -> tuple[np.ndarray, np.ndarray]:
+        positions = np.asarray(positions, dtype=np.int64)
+        pages = np.asarray(block_row, dtype=np.int64)[positions // self.page_size]
+        return pages, positions % self.page_size
+
+    def latent_rows(self, block_row, positions) -> np.ndarray:
+        """[n, 576] float64 cached rows [c_KV | k_R] at logical positions of one request."""
+        pg, off = self.slots(block_row, positions)
+        return bf16_to_f64(self.latent[pg, off])
+
+    def index_key_rows(self, block_row, positions) -> np.ndarray:
+        """[n, 128] float64 index keys: the bf16 value, or e4m3 value times the token's scale."""
+        pg, off = self.slots(block_row, positions)
+        if self.key_format == "bf16":
+            return bf16_to_f64(self.index_keys[pg, off])
+        return e4m3_to_f64(self.index_keys[pg, off]) * self.index_scales[pg, off].astype(np.float64)[:, None]
+
+
+# ---------------------------------------------------------------------------
+# batch metadata
+# ---------------------------------------------------------------------------
+def row_positions(seq_lens, query_start_loc) -> tuple[np.ndarray, np.ndarray]:
+    """(request of each row, absolute position of each row = L_b - q_len_b + i)."""
+    req, pos = [], []
+    for b in range(len(seq_lens)):
+        q_len = int(query_start_loc[b + 1]) - int(query_start_loc[b])
+        for i in range(q_len):
+            req.append(b)
+            pos.append(int(seq_lens[b]) - q_len + i)
+    return np.asarray(req, dtype=np.int64), np.asarray(pos, dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# the lightning indexer and top-k selection
+# ---------------------------------------------------------------------------
+def index_scores(q_idx_row, w_row, keys) -> np.ndarray:
+    """I[s] = sum_h w[h] * max(0, q_idx[h] . K[s]) for the given keys [n, d].
+
+    q_idx_row [H_I, d] and w_row [H_I] float64."""
+    dots = keys @ np.asarray(q_idx_row, dtype=np.float64).T          # [n, H_I]
+    return np.maximum(dots, 0.0) @ np.asarray(w_row, dtype=np.float64)
+
+
+def topk_select(scores, k: int) -> np.ndarray:
+    """k positions with the largest score (ties: smaller position first), or all
+    positions when len(scores) <= k; sorted ascending, padded with -1 to k."""
+    scores = np.asarray(scores, dtype=np.float64)
+    n = scores.shape[0]
+    if n <= k:
+        chosen = np.arange(n)
+    else:
+        order = np.lexsort((np.arange(n), -scores))   # primary: score descending, then position ascending
+        chosen = np.sort(order[:k])
+    out = np.full(k, -1, dtype=np.int32)
+    out[:chosen.shape[0]] = chosen
+    return out
+
+
+def indexer_topk(cache: PagedCache, block_table, seq_lens, query_start_loc, q_idx_bits, w, topk: int,
+                 rows=None):
+    """Scores and top-k for every query row (or the listed rows).
+
+    Returns (idx [n_rows, topk] int32, scores: list of float64 arrays over 0..pos)."""
+    if cache.index_keys is None:
+        raise ValueError("layer holds no index keys: a shared layer must reuse an owner's index buffer")
+    req, pos = row_positions(seq_lens, query_start_loc)
+    rows = range(len(req)) if rows is None else rows
+    q = bf16_to_f64(q_idx_bits)
+    w = np.asarray(w, dtype=np.float64)
+    idx, all_scores = [], []
+    key_cache = {}
+    for r in rows:
+        b, p = int(req[r]), int(pos[r])
+        if b not in key_cache:
+            key_cache = {b: cache.index_key_rows(block_table[b], np.arange(int(seq_lens[b])))}
+        keys = key_cache[b][:p + 1]                        # visible positions 0..pos only
+        s = index_scores(q[r], w[r], keys)
+        all_scores.append(s)
+        idx.append(topk_select(s, topk))
+    return np.stack(idx), all_scores
+
+
+# ---------------------------------------------------------------------------
+# sparse absorbed MLA
+# ---------------------------------------------------------------------------
+def attend(q_row, rows, scale: float, d_latent: int = 512) -> tuple[np.ndarray, np.ndarray]:
+    """Softmax attention of every head of one query row over the given cached rows.
+
+    q_row [H, d_latent + d_rope] = [q_latent | q_rope] per head, rows [m, d_latent + d_rope]
+    = [c_KV | k_R].  Returns (out [H, d_latent] = sum_s p_s c_KV[s], lse [H])."""
+    q_row = np.asarray(q_row, dtype=np.float64)
+    n_heads = q_row.shape[0]
+    if rows.shape[0] == 0:
+        return np.zeros((n_heads, d_latent)), np.full(n_heads, -np.inf)
+    c_kv, k_r = rows[:, :d_latent], rows[:, d_latent:]
+    q_lat, q_rope = q_row[:, :d_latent], q_row[:, d_latent:]
+    z = scale * (q_lat @ c_kv.T + q_rope @ k_r.T)           # [H, m]
+    m = z.max(axis=1, keepdims=True)
+    p = np.exp(z - m)
+    l = p.sum(axis=1, keepdims=True)
+    out = (p / l) @ c_kv
+    return out, (m + np.log(l))[:, 0]
+
+
+def valid_selection(idx_row, pos: int) -> np.ndarray:
+    """Entries of an index-buffer row that name a visible position (0 <= s <= pos)."""
+    idx_row = np.asarray(idx_row, dtype=np.int64)
+    return idx_row[(idx_row >= 0) & (idx_row <= pos)]
+
+
+def sparse_mla(cache: PagedCache, block_table, seq_lens, query_start_loc, q_bits, topk_idx, scale: float,
+               rows=None):
+    """Absorbed sparse MLA of every (or the listed) query row over its selected positions.
+
+    Returns (out [n_rows, H, 512] float64, lse [n_rows, H] float64)."""
+    req, pos = row_positions(seq_lens, query_start_loc)
+    rows = range(len(req)) if rows is None else rows
+    outs, lses = [], []
+    for r in rows:
+        b, p = int(req[r]), int(pos[r])
+        sel = valid_selection(topk_idx[r], p)
+        cached = cache.latent_rows(block_table[b], sel)
+        o, l = attend(bf16_to_f64(q_bits[r]), cached, scale, cache.d_latent)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)
+
+
+def lse_merge(parts) -> tuple[np.ndarray, np.ndarray]:
+    """Combine attention results over disjoint pieces of one selection.
+
+    parts: list of (out [H, d], lse [H]) where out is the softmax-weighted mean
+    of its piece.  The whole is sum_j exp(lse_j - lse) out_j with
+    lse = ln sum_j exp(lse_j)."""
+    lse = np.stack([p[1] for p in parts])                    # [J, H]
+    mx = np.max(lse, axis=0)
+    safe = np.where(np.isfinite(mx), mx, 0.0)
+    wts = np.exp(lse - safe)                                 # [J, H]
+    tot = wts.sum(axis=0)
+    out = sum(wts[j][:, None] * parts[j][0] for j in range(len(parts)))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        out = np.where(tot[:, None] > 0, out / tot[:, None], 0.0)
+        merged = np.where(tot > 0, safe + np.log(tot), -np.inf)
+    return out, merged
+
+
+# ---------------------------------------------------------------------------
+# IndexShare layer schedule
+# ---------------------------------------------------------------------------
+def indexshare_pattern(indexer_types) -> str:
+    """Per-layer F/S string from a checkpoint's indexer_types: full -> F, shared -> S."""
+    table = {"full": "F", "shared": "S"}
+    return "".join(table[t] for t in indexer_types)
+
+
+def owner_of_layer(pattern: str) -> list[int]:
+    """For each layer, the index of the nearest full layer at or before it."""
+    owners, last = [], None
+    for i, c in enumerate(pattern):
+        if c == "F":
+            last = i
+        if last is None:
+            raise ValueError("layer %d is shared but no full layer precedes it" % i)
+        owners.append(last)
+    return owners
