@@ -1,0 +1,498 @@
+#!/usr/bin/env python3
+"""Throughput of the GLM-5.2 DSA decode step on GB300.
+
+One step = one IndexShare group of the decode workload "decode batch 64,
+contexts U[16K, 128K], page size 64, fp8 index keys, 1 owner + 3 shared layers":
+append the step's 64 new tokens to 4 layers, score + top-k on the owner layer,
+and absorbed sparse MLA on all 4 layers with the owner's index buffer.  The
+metric is layer-steps/s (4 per group step).
+
+Default run: N=1.  Under torchrun every rank runs its own replica (requests are
+independent; no collective on the data path) and the JSON line reports the
+aggregate over ranks ("scaling": "weak").
+
+  python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference] [--workload NAME]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wlm  # noqa: E402
+
+METRIC = "sparse-DSA decode layer-steps/s (indexer+top-k+MLA) @128K ctx; % of HBM roofline"
+UNIT = "layer-steps/s"
+DEFAULT_WORKLOAD = "decode_b64_fp8_indexshare"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# the workload resident on the device
+# ---------------------------------------------------------------------------
+class DeviceProblem:
+    """A full-size workload resident in HBM: every layer's paged cache holds each request's
+    prefix (drawn on the device with torch's seeded generator and appended through the
+    library), and the step's inputs (new tokens, queries, metadata) are on the device."""
+
+    def __init__(self, wl: wlm.Workload, device="cuda"):
+        import torch
+        import deepseek_sparse_mla_gb300 as dsa
+        self.wl, self.dev = wl, device
+        B, R, layers = wl.num_requests, wl.num_rows, wl.layers
+        self.caches = [dsa.LayerCache(wl.num_pages, wl.page_size, wl.key_format if l == 0 else None, device)
+                       for l in range(layers)]
+        self.block_table = torch.from_numpy(wl.block_table).to(device)
+        self.seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=device)
+        self.qsl = None if wl.is_decode else torch.from_numpy(wl.query_start_loc).to(device)
+        self.batch = dsa.Batch(self.block_table, self.seq_lens, self.qsl, num_rows=R, max_seq_len=wl.max_seq_len)
+        new_c, new_r, new_k = [[] for _ in range(layers)], [[] for _ in range(layers)], []
+        for b in range(B):
+            L, q = wl.seq_lens[b], wl.q_lens[b]
+            pre = torch.from_numpy(wl.slots(b, np.arange(L - q))).to(device)
+            for l in range(layers):
+                x = wlm.request_latent_device(wl, b, l, device)
+                k = wlm.request_index_keys_device(wl, b, device) if l == 0 else None
+                if L - q > 0:
+                    dsa.kv_append(self.caches[l], x[:L - q, :512].contiguous(), x[:L - q, 512:].contiguous(), pre,
+                                  k_idx=None if k is None else k[:L - q].contiguous())
+                new_c[l].append(x[L - q:, :512])
+                new_r[l].append(x[L - q:, 512:])
+                if l == 0:
+                    new_k.append(k[L - q:])
+            torch.cuda.synchronize()
+        self.new_c = [torch.cat(v).contiguous() for v in new_c]
+        self.new_r = [torch.cat(v).contiguous() for v in new_r]
+        self.new_k = torch.cat(new_k).contiguous()
+        self.slots = torch.from_numpy(wl.new_token_slots()).to(device)
+        q_idx, w = wlm.indexer_queries(wl)
+        self.q_idx = wlm.bits_to_torch(q_idx, device)
+        self.w = torch.from_numpy(w).to(device)
+        self.q = [wlm.bits_to_torch(wlm.mla_queries(wl, l), device) for l in range(layers)]
+        self.topk_idx = torch.empty((R, wl.topk), dtype=torch.int32, device=device)
+        self.out = [torch.empty((R, 64, 512), dtype=torch.bfloat16, device=device) for _ in range(layers)]
+        self.lse = [torch.empty((R, 64), dtype=torch.float32, device=device) for _ in range(layers)]
+        self.ws_idx = torch.empty(dsa.indexer_workspace_bytes(R, wl.max_seq_len, wl.topk), dtype=torch.uint8,
+                                  device=device)
+        self.ws_mla = torch.empty(dsa.mla_workspace_bytes(R, wl.topk), dtype=torch.uint8, device=device)
+        torch.cuda.synchronize()
+
+    def step(self, marks=None):
+        """One DSA step of the layer group on the current stream."""
+        import deepseek_sparse_mla_gb300 as dsa
+        wl = self.wl
+        mla = dsa.sparse_mla_decode if wl.is_decode else dsa.sparse_mla_prefill
+        if marks is not None:
+            marks.mark("append")
+        for l in range(wl.layers):
+            dsa.kv_append(self.caches[l], self.new_c[l], self.new_r[l], self.slots,
+                          k_idx=self.new_k if l == 0 else None)
+        if marks is not None:
+            marks.mark("indexer")
+        dsa.indexer_scores_topk(self.caches[0], self.batch, self.q_idx, self.w, wl.topk, topk_idx=self.topk_idx,
+                                workspace=self.ws_idx)
+        for l in range(wl.layers):
+            if marks is not None:
+                marks.mark("attention")
+            mla(self.caches[l], self.batch, self.q[l], self.topk_idx, wl.scale, out=self.out[l], lse=self.lse[l],
+                workspace=self.ws_mla)
+        if marks is not None:
+            marks.mark(None)
+
+    # per-step host<->device traffic of the end-to-end measurement
+    def step_inputs(self):
+        return (self.new_c + self.new_r + [self.new_k, self.slots, self.q_idx, self.w] + self.q +
+                [self.block_table, self.seq_lens] + ([self.qsl] if self.qsl is not None else []))
+
+    def step_outputs(self):
+        return self.out + self.lse
+
+
+class Marks:
+    """CUDA events between the library calls of a step (same stream as the launches)."""
+
+    def __init__(self):
+        self.spans = {}
+        self._open = []
+
+    def mark(self, name):
+        import torch
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        if self._open:
+            self._open[-1][2] = e
+        if name is not None:
+            self._open.append([name, e, None])
+
+    def collect(self):
+        for name, a, b in self._open:
+            self.spans.setdefault(name, []).append(a.elapsed_time(b))
+        self._open = []
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what the step must move; scores/partials are overhead)
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(wl: wlm.Workload) -> dict:
+    pos = wl.row_position()
+    R, k = wl.num_rows, wl.topk
+    selected = np.minimum(k, pos + 1).sum()
+    keys = sum(wl.seq_lens) * wl.key_bytes_per_token()
+    indexer = keys + R * 32 * 128 * 2 + R * 32 * 4 + R * k * 4
+    attention = selected * 1152 + R * 64 * 576 * 2 + R * 64 * 512 * 2 + R * 64 * 4 + R * k * 4
+    key_in = 256
+    key_out = wl.key_bytes_per_token()
+    append_owner = R * (1152 * 2 + key_in + key_out)
+    append_shared = R * 1152 * 2
+    return {"indexer": float(indexer), "attention": float(attention), "append_owner": float(append_owner),
+            "append_shared": float(append_shared), "index_key_bytes": float(keys),
+            "gather_bytes_per_layer": float(selected * 1152),
+            "step": float(indexer + wl.layers * attention + append_owner + (wl.layers - 1) * append_shared)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic(kernel_file: str, kernel_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        ent = d[kernel_name]
+        src = os.path.join(ROOT, "deepseek_sparse_mla_gb300", "csrc", kernel_file)
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if ent.get("source_sha256_16") != digest:
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+
+    def start(self):
+        import torch
+        ident = None
+        try:
+            ident = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+            if not ident.startswith("GPU-"):
+                ident = "GPU-" + ident
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")
+            ident = vis[torch.cuda.current_device()] if vis and vis[0] else "0"
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: no collective on the data path)
+# ---------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    import torch
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# the oracle as a CPU baseline (bounded sample)
+# ---------------------------------------------------------------------------
+def oracle_request_problem(wl, b, device):
+    """One request of the workload as a stand-alone oracle problem (its own pages, identity page table).
+
+    Data come from the same seeded device generator the GPU problem was built from."""
+    from oracle import dsa_oracle as o
+    L, q = wl.seq_lens[b], wl.q_lens[b]
+    P = wl.page_size
+    pages = -(-L // P)
+    bt = np.arange(pages, dtype=np.int32)[None, :]
+    slots = np.arange(L, dtype=np.int64)
+    caches = []
+    for l in range(wl.layers):
+        lat = wlm.torch_to_bits(wlm.request_latent_device(wl, b, l, device))
+        keys = wlm.torch_to_bits(wlm.request_index_keys_device(wl, b, device)) if l == 0 else None
+        c = o.PagedCache(pages, P, wl.key_format if l == 0 else None)
+        c.append(lat[:L - q, :512], lat[:L - q, 512:], slots[:L - q],
+                 k_idx_bits=None if keys is None else keys[:L - q])
+        caches.append((c, lat[L - q:], None if keys is None else keys[L - q:]))
+    return caches, bt
+
+
+def time_oracle_request(wl, b, caches, bt, q_idx, w, qs):
+    """Seconds the oracle takes for request b's share of one step (append, indexer, top-k, all layers)."""
+    from oracle import dsa_oracle as o
+    L, q = wl.seq_lens[b], wl.q_lens[b]
+    r0 = int(wl.query_start_loc[b])
+    qsl = np.array([0, q], dtype=np.int32)
+    t0 = time.perf_counter()
+    for l, (c, new_lat, new_keys) in enumerate(caches):
+        c.append(new_lat[:, :512], new_lat[:, 512:], np.arange(L - q, L), k_idx_bits=new_keys)
+    idx, _ = o.indexer_topk(caches[0][0], bt, [L], qsl, q_idx[r0:r0 + q], w[r0:r0 + q], wl.topk)
+    for l, (c, _, _) in enumerate(caches):
+        o.sparse_mla(c, bt, [L], qsl, qs[l][r0:r0 + q], idx, wl.scale)
+    return time.perf_counter() - t0
+
+
+def stratified_requests(wl, n):
+    order = np.argsort(wl.seq_lens, kind="stable")
+    pick = order[np.unique(np.linspace(0, len(order) - 1, n).round().astype(int))]
+    return [int(b) for b in pick]
+
+
+def cpu_baseline(wl, device, n_req=3):
+    q_idx, w = wlm.indexer_queries(wl)
+    qs = [wlm.mla_queries(wl, l) for l in range(wl.layers)]
+    total = 0.0
+    picked = stratified_requests(wl, n_req)
+    for b in picked:
+        caches, bt = oracle_request_problem(wl, b, device)
+        total += time_oracle_request(wl, b, caches, bt, q_idx, w, qs)
+    step_s = total * wl.num_requests / len(picked)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": wl.layers / step_s, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"float64 numpy oracle on {len(picked)} of {wl.num_requests} requests (stratified by "
+                       f"context length: {[wl.seq_lens[b] for b in picked]}), append + indexer + top-k + "
+                       f"{wl.layers} attention layers, {total:.2f} s, scaled by request count"),
+            "seconds": total}
+
+
+# ---------------------------------------------------------------------------
+# main arms
+# ---------------------------------------------------------------------------
+def reference_main(args):
+    rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import torch
+    wl = wlm.FULL[args.workload]()
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    q_idx, w = wlm.indexer_queries(wl)
+    qs = [wlm.mla_queries(wl, l) for l in range(wl.layers)]
+    picked = stratified_requests(wl, max(1, args.steps + args.warmup))
+    times = []
+    for i in range(args.warmup + args.steps):
+        b = picked[i % len(picked)]
+        caches, bt = oracle_request_problem(wl, b, device)
+        t = time_oracle_request(wl, b, caches, bt, q_idx, w, qs)
+        if i >= args.warmup:
+            times.append(t * wl.num_requests)        # one request's share, scaled to the whole step
+    step_s = float(np.mean(times))
+    value = wl.layers / step_s
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = (f"each step: float64 numpy oracle on one request of {wl.num_requests} (stratified by context "
+              f"length), append + indexer + top-k + {wl.layers} attention layers, scaled by request count")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, **{k: v for k, v in wl.summary().items() if k != "workload"}},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wlm.FULL))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-requests", type=int, default=3)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return reference_main(args)
+
+    import torch
+    import deepseek_sparse_mla_gb300 as dsa
+    from deepseek_sparse_mla_gb300 import _lib
+    rank, world = dist_setup(args.gpus)
+    wl = wlm.FULL[args.workload]()
+    prob = DeviceProblem(wl)
+    lib = _lib.load()
+
+    # ---- device-resident timing --------------------------------------------------------
+    for _ in range(args.warmup):
+        prob.step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = lib.dsa_kernel_launches()
+    clocks = ClockSampler()
+    clocks.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        prob.step()
+    t1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    launches = int(lib.dsa_kernel_launches() - launches0)
+    barrier(world)
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    ms_per_step = elapsed_ms / args.steps
+    value = world * wl.layers * args.steps / (elapsed_ms / 1e3)
+
+    # ---- per-call breakdown (events between the library calls) --------------------------
+    marks = Marks()
+    for _ in range(max(3, min(args.steps, 20))):
+        prob.step(marks)
+        torch.cuda.synchronize()
+        marks.collect()
+    per_call = {k: float(np.mean(v)) for k, v in marks.spans.items()}     # ms per call
+    per_call["append"] /= wl.layers                                         # one span covers every layer's append
+    calls = {"append": wl.layers, "indexer": 1, "attention": wl.layers}
+    share = {k: per_call[k] * calls[k] for k in per_call}
+    tot = sum(share.values())
+    alg = algorithmic_bytes(wl)
+    peak, peak_kind = load_peaks()
+    bytes_of = {"indexer": alg["indexer"], "attention": alg["attention"],
+                "append": (alg["append_owner"] + (wl.layers - 1) * alg["append_shared"]) / wl.layers}
+    files = {"indexer": ("indexer.cu", "indexer_scores_kernel"), "attention": ("sparse_mla.cu", "sparse_mla_kernel"),
+             "append": ("kv_append.cu", "kv_append_kernel")}
+    dom = max(share, key=share.get)
+    achieved = bytes_of[dom] / (per_call[dom] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": files[dom][1], "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_kind": peak_kind,
+                "traffic": kernel_traffic(*files[dom]),
+                "algorithmic_bytes_per_launch": bytes_of[dom]}
+    kernels = {k: {"ms_per_call": per_call[k], "calls_per_step": calls[k], "share": share[k] / tot,
+                   "algorithmic_GBps": bytes_of[k] / (per_call[k] * 1e-3) / 1e9,
+                   "frac_of_peak": bytes_of[k] / (per_call[k] * 1e-3) / 1e9 / peak} for k in per_call}
+    step_gbps = alg["step"] / (ms_per_step * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers ---------------------------
+    ins = prob.step_inputs()
+    outs = prob.step_outputs()
+    h_in = [t.cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = int(sum(t.numel() * t.element_size() for t in h_in))
+    d2h = int(sum(t.numel() * t.element_size() for t in h_out))
+
+    def e2e_step():
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        prob.step()
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e = {"value": world * wl.layers * args.steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, "cuda", args.cpu_sample_requests)
+
+    if rank == 0:
+        summary = wl.summary()
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": wl.name, **{k: v for k, v in summary.items() if k != "workload"},
+                           "l2": "no flush: each step reads %.0f MB (> 129 MB L2)" % (alg["step"] / 1e6),
+                           "parallelism": "replicas" if world > 1 else "single GPU"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clk, "kernels": kernels,
+                "step_algorithmic_GBps": step_gbps, "step_frac_of_peak": step_gbps / peak,
+                "step_frac_of_8TBps": step_gbps / 8000.0}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

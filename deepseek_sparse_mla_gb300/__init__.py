@@ -1,0 +1,184 @@
+"""GLM-5.2 DeepSeek Sparse Attention (DSA) step on GB300 (sm_103a) behind a C ABI.
+
+The step of one decoder layer over a paged KV cache: append the step's tokens,
+score every visible cached position with the lightning indexer, select the
+top-k positions into a shared index buffer, and run absorbed sparse MLA over
+the selected positions (IndexShare layers reuse the owner's buffer).
+
+This module is a thin binding over ``libdsa.so`` (``include/dsa.h``): it checks
+tensor dtypes and shapes, passes raw device pointers and the current CUDA
+stream, and raises on a non-OK status.  Every step of the computation runs in
+the library's CUDA kernels; there is no other implementation to fall back to.
+PyTorch only provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import DsaError, KEY_BF16, KEY_FP8_E4M3  # noqa: F401
+
+INDEX_HEADS, INDEX_DIM, HEADS, LATENT_DIM, ROPE_DIM, ROW_DIM = 32, 128, 64, 512, 64, 576
+DEFAULT_SCALE = 1.0 / 16.0     # 1/sqrt(192 + 64)
+_FORMATS = {"bf16": KEY_BF16, "fp8": KEY_FP8_E4M3, None: KEY_BF16}
+
+__all__ = ["LayerCache", "Batch", "kv_append", "indexer_scores_topk", "sparse_mla_decode", "sparse_mla_prefill",
+           "cache_bytes", "indexer_workspace_bytes", "mla_workspace_bytes", "DsaError", "DEFAULT_SCALE"]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, shape, name):
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+class LayerCache:
+    """One layer's paged caches (device tensors owned by this object).
+
+    latent [num_pages, page_size, 576] bf16; for an indexer-owning layer also
+    index_keys [num_pages, page_size, 128] (bf16, or uint8 e4m3 codes) and, for
+    e4m3, index_scales [num_pages, page_size] fp32.  key_format None makes an
+    IndexShare layer that holds only latent pages."""
+
+    def __init__(self, num_pages: int, page_size: int, key_format: str | None = None, device="cuda"):
+        self.num_pages, self.page_size, self.key_format = int(num_pages), int(page_size), key_format
+        self.latent = torch.zeros((num_pages, page_size, ROW_DIM), dtype=torch.bfloat16, device=device)
+        self.index_keys = self.index_scales = None
+        if key_format == "bf16":
+            self.index_keys = torch.zeros((num_pages, page_size, INDEX_DIM), dtype=torch.bfloat16, device=device)
+        elif key_format == "fp8":
+            self.index_keys = torch.zeros((num_pages, page_size, INDEX_DIM), dtype=torch.uint8, device=device)
+            self.index_scales = torch.zeros((num_pages, page_size), dtype=torch.float32, device=device)
+        elif key_format is not None:
+            raise ValueError(f"key_format {key_format!r}")
+
+    def struct(self) -> _lib.DsaCache:
+        return _lib.DsaCache(self.latent.data_ptr(), 0 if self.index_keys is None else self.index_keys.data_ptr(),
+                             0 if self.index_scales is None else self.index_scales.data_ptr(), self.num_pages,
+                             self.page_size, _FORMATS[self.key_format])
+
+
+class Batch:
+    """Batch metadata on the device: block_table [B, stride] int32, seq_lens [B] int32 (KV length
+    after this step's append), query_start_loc [B+1] int32 or None (decode: one row per request)."""
+
+    def __init__(self, block_table, seq_lens, query_start_loc=None, num_rows: int | None = None,
+                 max_seq_len: int | None = None):
+        self.block_table = block_table.to(torch.int32).contiguous()
+        self.seq_lens = seq_lens.to(torch.int32).contiguous()
+        self.query_start_loc = None if query_start_loc is None else query_start_loc.to(torch.int32).contiguous()
+        self.num_requests = int(self.seq_lens.shape[0])
+        if num_rows is None:
+            num_rows = self.num_requests if query_start_loc is None else int(self.query_start_loc[-1].item())
+        if max_seq_len is None:
+            max_seq_len = int(self.seq_lens.max().item())
+        self.num_rows, self.max_seq_len = int(num_rows), int(max_seq_len)
+
+    def struct(self) -> _lib.DsaBatch:
+        return _lib.DsaBatch(self.block_table.data_ptr(), self.seq_lens.data_ptr(),
+                             0 if self.query_start_loc is None else self.query_start_loc.data_ptr(),
+                             self.num_requests, self.num_rows, self.max_seq_len, int(self.block_table.shape[1]))
+
+
+def cache_bytes(num_pages: int, page_size: int, key_format: str | None, owner: bool) -> int:
+    return int(_lib.load().dsa_cache_bytes(num_pages, page_size, _FORMATS[key_format], int(owner)))
+
+
+def indexer_workspace_bytes(num_rows: int, max_seq_len: int, topk: int) -> int:
+    return int(_lib.load().dsa_indexer_workspace_bytes(num_rows, max_seq_len, topk))
+
+
+def mla_workspace_bytes(num_rows: int, topk: int) -> int:
+    return int(_lib.load().dsa_mla_workspace_bytes(num_rows, topk))
+
+
+def _workspace(nbytes, device):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def kv_append(cache: LayerCache, c_kv, k_rope, slot_mapping, k_idx=None, k_idx_scales=None, stream=None):
+    """Scatter T new tokens into the layer's pages (bf16 keys are quantised for an fp8 cache)."""
+    T = int(slot_mapping.shape[0])
+    _need(c_kv, torch.bfloat16, (T, LATENT_DIM), "c_kv")
+    _need(k_rope, torch.bfloat16, (T, ROPE_DIM), "k_rope")
+    _need(slot_mapping, torch.int64, (T,), "slot_mapping")
+    fmt = KEY_BF16
+    if k_idx is not None:
+        if k_idx.dtype == torch.uint8:
+            fmt = KEY_FP8_E4M3
+            _need(k_idx, torch.uint8, (T, INDEX_DIM), "k_idx")
+            _need(k_idx_scales, torch.float32, (T,), "k_idx_scales")
+        else:
+            _need(k_idx, torch.bfloat16, (T, INDEX_DIM), "k_idx")
+    c = cache.struct()
+    _lib.check(_lib.load().dsa_kv_append(ctypes.byref(c), _ptr(c_kv), _ptr(k_rope), _ptr(k_idx), fmt,
+                                         _ptr(k_idx_scales), _ptr(slot_mapping), T, _stream(stream)))
+
+
+def indexer_scores_topk(owner: LayerCache, batch: Batch, q_idx, w, topk: int, topk_idx=None, scores_out=None,
+                        workspace=None, stream=None):
+    """Lightning-indexer scores and top-k selection; returns the index buffer [R, topk] int32."""
+    R = batch.num_rows
+    _need(q_idx, torch.bfloat16, (R, INDEX_HEADS, INDEX_DIM), "q_idx")
+    _need(w, torch.float32, (R, INDEX_HEADS), "w")
+    if topk_idx is None:
+        topk_idx = torch.empty((R, topk), dtype=torch.int32, device=q_idx.device)
+    _need(topk_idx, torch.int32, (R, topk), "topk_idx")
+    if scores_out is not None:
+        _need(scores_out, torch.float32, (R, batch.max_seq_len), "scores_out")
+    need = indexer_workspace_bytes(R, batch.max_seq_len, topk)
+    if workspace is None:
+        workspace = _workspace(need, q_idx.device)
+    c, b = owner.struct(), batch.struct()
+    _lib.check(_lib.load().dsa_indexer_scores_topk(ctypes.byref(c), ctypes.byref(b), _ptr(q_idx), _ptr(w), topk,
+                                                   _ptr(topk_idx), _ptr(scores_out), _ptr(workspace),
+                                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+    return topk_idx
+
+
+def _sparse_mla(fn, layer, batch, q, topk_idx, scale, out, lse, workspace, stream):
+    R = batch.num_rows
+    _need(q, torch.bfloat16, (R, HEADS, ROW_DIM), "q")
+    if topk_idx is None:
+        raise ValueError("topk_idx is required: a shared layer reuses the owner layer's index buffer")
+    topk = int(topk_idx.shape[1])
+    _need(topk_idx, torch.int32, (R, topk), "topk_idx")
+    if out is None:
+        out = torch.empty((R, HEADS, LATENT_DIM), dtype=torch.bfloat16, device=q.device)
+    _need(out, torch.bfloat16, (R, HEADS, LATENT_DIM), "out")
+    if lse is not None:
+        _need(lse, torch.float32, (R, HEADS), "lse")
+    if workspace is None:
+        workspace = _workspace(mla_workspace_bytes(R, topk), q.device)
+    c, b = layer.struct(), batch.struct()
+    _lib.check(fn(ctypes.byref(c), ctypes.byref(b), _ptr(q), _ptr(topk_idx), topk, float(scale), _ptr(out), _ptr(lse),
+                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse
+
+
+def sparse_mla_decode(layer: LayerCache, batch: Batch, q, topk_idx, scale: float = DEFAULT_SCALE, out=None, lse=None,
+                      workspace=None, stream=None):
+    """Sparse absorbed MLA for decode rows (one per request); returns (out [R,64,512] bf16, lse)."""
+    return _sparse_mla(_lib.load().dsa_sparse_mla_decode, layer, batch, q, topk_idx, scale, out, lse, workspace, stream)
+
+
+def sparse_mla_prefill(layer: LayerCache, batch: Batch, q, topk_idx, scale: float = DEFAULT_SCALE, out=None, lse=None,
+                       workspace=None, stream=None):
+    """Sparse absorbed MLA for extend/prefill/verify rows (causal per row); returns (out, lse)."""
+    return _sparse_mla(_lib.load().dsa_sparse_mla_prefill, layer, batch, q, topk_idx, scale, out, lse, workspace, stream)

@@ -1,0 +1,260 @@
+// Host side of libdsa: the C ABI entry points of include/dsa.h.
+//
+// Every entry point validates its arguments on the host, sizes nothing
+// dynamically, allocates nothing and never synchronises: it records launches
+// on the caller's stream.  Launch plans are pure functions of the shape, so the
+// workspace sizes reported to the caller are exactly what the launches use.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "dsa_internal.cuh"
+
+namespace dsa {
+
+static thread_local std::string g_last_error;
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+static dsa_status fail(dsa_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+static dsa_status ok() { return DSA_OK; }
+
+static dsa_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+IndexerPlan plan_indexer(int num_rows, int max_seq_len, int topk) {
+  (void)topk;
+  IndexerPlan p;
+  p.score_stride = ((int64_t)max_seq_len + 255) / 256 * 256;
+  int64_t per_row = p.score_stride * (int64_t)sizeof(float);
+  int64_t fit = (int64_t)kScoreBlockBytes / per_row;
+  if (fit < 1) fit = 1;
+  p.rows_per_block = (int)(num_rows < fit ? num_rows : fit);
+  if (p.rows_per_block < 1) p.rows_per_block = 1;
+  p.workspace_bytes = kWorkspaceHeader + (size_t)p.rows_per_block * (size_t)per_row;
+  return p;
+}
+
+MlaPlan plan_mla(int num_rows, int topk) {
+  MlaPlan p;
+  int splits = num_rows >= kSplitTargetCtas ? 1 : (kSplitTargetCtas + num_rows - 1) / num_rows;
+  int max_splits = topk / 64 > 0 ? topk / 64 : 1;   // keep at least 64 selected entries per split
+  if (splits > max_splits) splits = max_splits;
+  if (splits > 32) splits = 32;
+  if (splits < 1) splits = 1;
+  p.tokens_per_split = (topk + splits - 1) / splits;
+  p.splits = (topk + p.tokens_per_split - 1) / p.tokens_per_split;
+  size_t partial = 0;
+  if (p.splits > 1)
+    partial = (size_t)num_rows * p.splits * kHeads * (kLatent + 2) * sizeof(float);
+  p.workspace_bytes = kWorkspaceHeader + partial;
+  return p;
+}
+
+static dsa_status check_cache(const dsa_cache* c, bool need_keys) {
+  if (!c) return fail(DSA_ERR_INVALID_ARG, "cache is NULL");
+  if (!c->latent) return fail(DSA_ERR_INVALID_ARG, "cache.latent is NULL");
+  if (!aligned16(c->latent)) return fail(DSA_ERR_INVALID_ARG, "cache.latent is not 16-byte aligned");
+  if (c->num_pages <= 0) return fail(DSA_ERR_INVALID_ARG, "cache.num_pages must be positive (got %d)", c->num_pages);
+  if (!pow2(c->page_size) || c->page_size > 1024)
+    return fail(DSA_ERR_INVALID_ARG, "cache.page_size must be a power of two in 1..1024 (got %d)", c->page_size);
+  if ((int64_t)c->num_pages * c->page_size > (int64_t)INT32_MAX)
+    return fail(DSA_ERR_UNSUPPORTED, "cache holds more than 2^31 slots");
+  if (c->index_keys) {
+    if (c->key_format != DSA_KEY_BF16 && c->key_format != DSA_KEY_FP8_E4M3)
+      return fail(DSA_ERR_INVALID_ARG, "cache.key_format %d is not a dsa_key_format", c->key_format);
+    if (!aligned16(c->index_keys)) return fail(DSA_ERR_INVALID_ARG, "cache.index_keys is not 16-byte aligned");
+    if (c->key_format == DSA_KEY_FP8_E4M3 && !c->index_scales)
+      return fail(DSA_ERR_INVALID_ARG, "e4m3 index keys need cache.index_scales");
+    if (c->key_format == DSA_KEY_BF16 && c->index_scales)
+      return fail(DSA_ERR_INVALID_ARG, "bf16 index keys take no cache.index_scales (layouts are not interchangeable)");
+    if (c->index_scales && (reinterpret_cast<uintptr_t>(c->index_scales) & 3u))
+      return fail(DSA_ERR_INVALID_ARG, "cache.index_scales is not 4-byte aligned");
+  } else if (need_keys) {
+    return fail(DSA_ERR_INVALID_ARG,
+                "layer has no indexer keys (cache.index_keys is NULL): a shared layer must reuse the owner's "
+                "index buffer instead of scoring");
+  }
+  return ok();
+}
+
+static dsa_status check_batch(const dsa_batch* b, bool need_qsl) {
+  if (!b) return fail(DSA_ERR_INVALID_ARG, "batch is NULL");
+  if (b->num_requests <= 0) return fail(DSA_ERR_INVALID_ARG, "batch.num_requests must be positive");
+  if (b->num_rows < 0) return fail(DSA_ERR_INVALID_ARG, "batch.num_rows is negative");
+  if (b->max_seq_len <= 0) return fail(DSA_ERR_INVALID_ARG, "batch.max_seq_len must be positive");
+  if (!b->block_table || !b->seq_lens) return fail(DSA_ERR_INVALID_ARG, "batch.block_table / seq_lens is NULL");
+  if (b->block_table_stride <= 0) return fail(DSA_ERR_INVALID_ARG, "batch.block_table_stride must be positive");
+  if (need_qsl && !b->query_start_loc)
+    return fail(DSA_ERR_INVALID_ARG, "batch.query_start_loc is required when requests have several rows");
+  if (!b->query_start_loc && b->num_rows != b->num_requests)
+    return fail(DSA_ERR_INVALID_ARG, "without query_start_loc every request has exactly one row (num_rows %d != "
+                "num_requests %d)", b->num_rows, b->num_requests);
+  return ok();
+}
+
+static RowMeta row_meta(const dsa_batch* b, bool decode) {
+  RowMeta m;
+  m.block_table = b->block_table;
+  m.seq_lens = b->seq_lens;
+  m.query_start_loc = decode ? nullptr : b->query_start_loc;
+  m.num_requests = b->num_requests;
+  m.block_table_stride = b->block_table_stride;
+  return m;
+}
+
+static dsa_status sparse_mla_common(const dsa_cache* layer, const dsa_batch* batch, const void* q,
+                                    const int32_t* topk_idx, int32_t topk, float scale, void* out, float* lse,
+                                    void* workspace, size_t workspace_bytes, void* stream, bool decode) {
+  dsa_status st = check_cache(layer, false);
+  if (st != DSA_OK) return st;
+  st = check_batch(batch, !decode);
+  if (st != DSA_OK) return st;
+  if (!topk_idx)
+    return fail(DSA_ERR_INVALID_ARG, "topk_idx is NULL: a shared layer must be given the owner layer's index buffer");
+  if (topk < 1 || topk > DSA_MAX_TOPK) return fail(DSA_ERR_INVALID_ARG, "topk must be in 1..%d (got %d)", DSA_MAX_TOPK, topk);
+  if (!q || !out) return fail(DSA_ERR_INVALID_ARG, "q / out is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(DSA_ERR_INVALID_ARG, "q / out is not 16-byte aligned");
+  if (!(scale > 0.f) || scale != scale || scale > 1e30f) return fail(DSA_ERR_INVALID_ARG, "scale must be finite and positive");
+  if (decode && batch->num_rows != batch->num_requests)
+    return fail(DSA_ERR_INVALID_ARG, "decode takes one row per request (num_rows %d, num_requests %d)",
+                batch->num_rows, batch->num_requests);
+  if (batch->num_rows == 0) return ok();
+  MlaPlan plan = plan_mla(batch->num_rows, topk);
+  if (plan.workspace_bytes > 0 && (!workspace || workspace_bytes < plan.workspace_bytes))
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes dsa_mla_workspace_bytes requires",
+                workspace_bytes, plan.workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(DSA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  RowMeta m = row_meta(batch, decode);
+  cudaError_t e = launch_sparse_mla(*layer, m, batch->num_rows, q, topk_idx, topk, scale, out, lse, workspace, plan,
+                                    (cudaStream_t)stream);
+  return cuda_status(e, "sparse MLA launch");
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+const char* dsa_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t dsa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t dsa_cache_bytes(int32_t num_pages, int32_t page_size, int32_t key_format, int32_t owner) {
+  if (num_pages <= 0 || page_size <= 0) return 0;
+  size_t slots = (size_t)num_pages * (size_t)page_size;
+  size_t bytes = slots * kRow * 2;
+  if (owner) {
+    if (key_format == DSA_KEY_BF16) bytes += slots * kIndexDim * 2;
+    else if (key_format == DSA_KEY_FP8_E4M3) bytes += slots * (kIndexDim + sizeof(float));
+    else return 0;
+  }
+  return bytes;
+}
+
+size_t dsa_indexer_workspace_bytes(int32_t num_rows, int32_t max_seq_len, int32_t topk) {
+  if (num_rows < 0 || max_seq_len <= 0 || topk < 1) return 0;
+  return plan_indexer(num_rows > 0 ? num_rows : 1, max_seq_len, topk).workspace_bytes;
+}
+
+size_t dsa_mla_workspace_bytes(int32_t num_rows, int32_t topk) {
+  if (num_rows < 0 || topk < 1) return 0;
+  return plan_mla(num_rows > 0 ? num_rows : 1, topk).workspace_bytes;
+}
+
+dsa_status dsa_kv_append(const dsa_cache* cache, const void* c_kv, const void* k_rope, const void* k_idx,
+                         int32_t k_idx_format, const float* k_idx_scales, const int64_t* slot_mapping,
+                         int32_t num_tokens, void* stream) {
+  dsa_status st = check_cache(cache, false);
+  if (st != DSA_OK) return st;
+  if (num_tokens < 0) return fail(DSA_ERR_INVALID_ARG, "num_tokens is negative");
+  if (num_tokens == 0) return ok();
+  if (!c_kv || !k_rope || !slot_mapping) return fail(DSA_ERR_INVALID_ARG, "c_kv / k_rope / slot_mapping is NULL");
+  if (!aligned16(c_kv) || !aligned16(k_rope)) return fail(DSA_ERR_INVALID_ARG, "c_kv / k_rope is not 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) return fail(DSA_ERR_INVALID_ARG, "slot_mapping is not 8-byte aligned");
+  if (cache->index_keys) {
+    if (!k_idx) return fail(DSA_ERR_INVALID_ARG, "this layer owns an indexer cache: k_idx is required");
+    if (!aligned16(k_idx)) return fail(DSA_ERR_INVALID_ARG, "k_idx is not 16-byte aligned");
+    if (k_idx_format == DSA_KEY_FP8_E4M3) {
+      if (cache->key_format != DSA_KEY_FP8_E4M3)
+        return fail(DSA_ERR_INVALID_ARG, "e4m3 index keys cannot be stored into a bf16 indexer cache");
+      if (!k_idx_scales) return fail(DSA_ERR_INVALID_ARG, "pre-quantised e4m3 keys need k_idx_scales");
+      if (reinterpret_cast<uintptr_t>(k_idx_scales) & 3u) return fail(DSA_ERR_INVALID_ARG, "k_idx_scales is not 4-byte aligned");
+    } else if (k_idx_format != DSA_KEY_BF16) {
+      return fail(DSA_ERR_INVALID_ARG, "k_idx_format %d is not a dsa_key_format", k_idx_format);
+    }
+  } else if (k_idx) {
+    return fail(DSA_ERR_INVALID_ARG, "k_idx given for a layer without an indexer cache (cache.index_keys is NULL)");
+  }
+  cudaError_t e = launch_kv_append(*cache, c_kv, k_rope, cache->index_keys ? k_idx : nullptr, k_idx_format, k_idx_scales,
+                                   slot_mapping, num_tokens, (cudaStream_t)stream);
+  return cuda_status(e, "kv append launch");
+}
+
+dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_batch* batch, const void* q_idx, const float* w,
+                                   int32_t topk, int32_t* topk_idx, float* scores_out, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  dsa_status st = check_cache(owner, true);
+  if (st != DSA_OK) return st;
+  st = check_batch(batch, false);
+  if (st != DSA_OK) return st;
+  if (topk < 1 || topk > DSA_MAX_TOPK) return fail(DSA_ERR_INVALID_ARG, "topk must be in 1..%d (got %d)", DSA_MAX_TOPK, topk);
+  if (!q_idx || !w || !topk_idx) return fail(DSA_ERR_INVALID_ARG, "q_idx / w / topk_idx is NULL");
+  if (!aligned16(q_idx)) return fail(DSA_ERR_INVALID_ARG, "q_idx is not 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(w) & 3u) || (reinterpret_cast<uintptr_t>(topk_idx) & 3u) ||
+      (reinterpret_cast<uintptr_t>(scores_out) & 3u))
+    return fail(DSA_ERR_INVALID_ARG, "w / topk_idx / scores_out is not 4-byte aligned");
+  if (batch->num_rows == 0) return ok();
+  IndexerPlan plan = plan_indexer(batch->num_rows, batch->max_seq_len, topk);
+  if (!workspace || workspace_bytes < plan.workspace_bytes)
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes dsa_indexer_workspace_bytes requires",
+                workspace_bytes, plan.workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(DSA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  RowMeta m = row_meta(batch, batch->query_start_loc == nullptr);
+  cudaStream_t s = (cudaStream_t)stream;
+  float* block = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeader);
+  for (int row0 = 0; row0 < batch->num_rows; row0 += plan.rows_per_block) {
+    int n = batch->num_rows - row0 < plan.rows_per_block ? batch->num_rows - row0 : plan.rows_per_block;
+    float* scores = scores_out ? scores_out + (int64_t)row0 * batch->max_seq_len : block;
+    int64_t stride = scores_out ? (int64_t)batch->max_seq_len : plan.score_stride;
+    cudaError_t e = launch_indexer_scores(*owner, m, row0, n, batch->max_seq_len, q_idx, w, scores, stride, s);
+    if (e != cudaSuccess) return cuda_status(e, "indexer launch");
+    e = launch_topk(m, row0, n, scores, stride, topk, topk_idx, s);
+    if (e != cudaSuccess) return cuda_status(e, "top-k launch");
+  }
+  return ok();
+}
+
+dsa_status dsa_sparse_mla_decode(const dsa_cache* layer, const dsa_batch* batch, const void* q, const int32_t* topk_idx,
+                                 int32_t topk, float scale, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  return sparse_mla_common(layer, batch, q, topk_idx, topk, scale, out, lse, workspace, workspace_bytes, stream, true);
+}
+
+dsa_status dsa_sparse_mla_prefill(const dsa_cache* layer, const dsa_batch* batch, const void* q, const int32_t* topk_idx,
+                                  int32_t topk, float scale, void* out, float* lse, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return sparse_mla_common(layer, batch, q, topk_idx, topk, scale, out, lse, workspace, workspace_bytes, stream, false);
+}
+
+}  // extern "C"

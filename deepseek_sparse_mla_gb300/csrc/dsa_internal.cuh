@@ -1,0 +1,107 @@
+// Internal declarations shared by the CUDA translation units of libdsa.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+constexpr int kIndexHeads = DSA_INDEX_HEADS;   // 32
+constexpr int kIndexDim = DSA_INDEX_DIM;       // 128
+constexpr int kHeads = DSA_HEADS;              // 64
+constexpr int kLatent = DSA_LATENT_DIM;        // 512
+constexpr int kRope = DSA_ROPE_DIM;            // 64
+constexpr int kRow = DSA_ROW_DIM;              // 576
+
+// Split-k target: enough (row, split) CTAs to cover the GPU about twice.
+constexpr int kSplitTargetCtas = 2 * 152;
+// Upper bound on the fp32 score block the indexer materialises per launch group.
+constexpr size_t kScoreBlockBytes = size_t(256) << 20;
+constexpr size_t kWorkspaceHeader = 256;
+
+// ---------------------------------------------------------------------------
+// launch plans: shared by the *_workspace_bytes functions and the launches
+// ---------------------------------------------------------------------------
+struct IndexerPlan {
+  int64_t score_stride;   // floats per row in the score block
+  int rows_per_block;     // rows scored and selected per pass
+  size_t workspace_bytes;
+};
+IndexerPlan plan_indexer(int num_rows, int max_seq_len, int topk);
+
+struct MlaPlan {
+  int splits;             // split-k pieces of each row's selection
+  int tokens_per_split;
+  size_t workspace_bytes;
+};
+MlaPlan plan_mla(int num_rows, int topk);
+
+// Counts every kernel launch the library issues (reported by dsa_kernel_launches).
+void count_launches(int n);
+
+// ---------------------------------------------------------------------------
+// launchers (defined next to their kernels)
+// ---------------------------------------------------------------------------
+cudaError_t launch_kv_append(const dsa_cache& c, const void* c_kv, const void* k_rope, const void* k_idx,
+                             int k_idx_format, const float* k_idx_scales, const int64_t* slot_mapping,
+                             int num_tokens, cudaStream_t s);
+
+struct RowMeta {
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;   // nullptr: decode (row r = request r)
+  int32_t num_requests;
+  int32_t block_table_stride;
+};
+
+cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0, int nrows, int max_seq_len,
+                                  const void* q_idx, const float* w, float* scores, int64_t score_stride,
+                                  cudaStream_t s);
+
+cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scores, int64_t score_stride,
+                        int topk, int32_t* topk_idx, cudaStream_t s);
+
+cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows, const void* q,
+                              const int32_t* topk_idx, int topk, float scale, void* out, float* lse,
+                              void* workspace, const MlaPlan& plan, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+// Request and absolute position of query row r: row i of request b sits at L_b - q_len_b + i.
+__device__ __forceinline__ void row_info(const RowMeta& m, int r, int& b, int& pos) {
+  if (m.query_start_loc == nullptr) {
+    b = r;
+    pos = m.seq_lens[r] - 1;
+    return;
+  }
+  int lo = 0, hi = m.num_requests - 1;   // largest b with query_start_loc[b] <= r
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (m.query_start_loc[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  b = lo;
+  int q_len = m.query_start_loc[b + 1] - m.query_start_loc[b];
+  pos = m.seq_lens[b] - q_len + (r - m.query_start_loc[b]);
+}
+
+// Physical slot of logical position s of request b, or -1 when the page table or page id is out of range.
+__device__ __forceinline__ int64_t token_slot(const RowMeta& m, int b, int s, int log2_page, int num_pages) {
+  int lp = s >> log2_page;
+  if (s < 0 || lp >= m.block_table_stride) return -1;
+  int page = m.block_table[(int64_t)b * m.block_table_stride + lp];
+  if (page < 0 || page >= num_pages) return -1;
+  return ((int64_t)page << log2_page) + (s & ((1 << log2_page) - 1));
+}
+
+__host__ __device__ inline int ilog2(int x) {
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+
+}  // namespace dsa

@@ -1,0 +1,78 @@
+// Paged KV append: scatter this step's tokens into one layer's latent pages and,
+// for an indexer-owning layer, its index-key pages.
+//
+// "Making GLM-5.2 Sparse on TPUs", "Append new KV without moving the resident
+// cache": the cost must scale with the new rows, never with the resident pool,
+// and every other slot keeps its contents.  Here one warp owns one new token
+// and moves its 1152-byte latent row with 16-byte stores straight into its
+// slot; nothing else in the pool is read or written.
+#include "dsa_internal.cuh"
+
+namespace dsa {
+
+__global__ void __launch_bounds__(256) kv_append_kernel(
+    uint4* __restrict__ latent, int64_t total_slots, uint8_t* __restrict__ index_keys, float* __restrict__ index_scales,
+    int cache_key_format, const uint4* __restrict__ c_kv, const uint4* __restrict__ k_rope,
+    const uint8_t* __restrict__ k_idx, int k_idx_format, const float* __restrict__ k_idx_scales,
+    const int64_t* __restrict__ slot_mapping, int num_tokens) {
+  const int t = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= num_tokens) return;
+  const int64_t slot = slot_mapping[t];
+  if (slot < 0 || slot >= total_slots) return;
+
+  // latent row [c_KV(512) | k_R(64)] bf16 = 64 + 8 chunks of 16 bytes, copied bit-exactly
+  constexpr int kChunksC = kLatent * 2 / 16, kChunksR = kRope * 2 / 16;
+  uint4* dst = latent + slot * (kChunksC + kChunksR);
+  const uint4* src_c = c_kv + (int64_t)t * kChunksC;
+  const uint4* src_r = k_rope + (int64_t)t * kChunksR;
+  for (int i = lane; i < kChunksC + kChunksR; i += 32) dst[i] = i < kChunksC ? src_c[i] : src_r[i - kChunksC];
+
+  if (index_keys == nullptr) return;
+  if (cache_key_format == DSA_KEY_BF16) {             // 256 bytes per key, copied
+    if (lane < 16)
+      reinterpret_cast<uint4*>(index_keys)[slot * 16 + lane] = reinterpret_cast<const uint4*>(k_idx)[(int64_t)t * 16 + lane];
+    return;
+  }
+  if (k_idx_format == DSA_KEY_FP8_E4M3) {             // pre-quantised: 128 code bytes + scale, copied
+    if (lane < 8)
+      reinterpret_cast<uint4*>(index_keys)[slot * 8 + lane] = reinterpret_cast<const uint4*>(k_idx)[(int64_t)t * 8 + lane];
+    if (lane == 0) index_scales[slot] = k_idx_scales[t];
+    return;
+  }
+  // quantise a bf16 key into e4m3: scale = amax / 448 (1 if amax = 0), code = rne_satfinite(x / scale)
+  const uint2 raw = reinterpret_cast<const uint2*>(k_idx)[(int64_t)t * 32 + lane];   // 4 bf16 per lane
+  float x[4];
+  {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+    x[0] = __low2float(a); x[1] = __high2float(a); x[2] = __low2float(b); x[3] = __high2float(b);
+  }
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(__fdiv_rn(x[i], scale), __NV_SATFINITE, __NV_E4M3);
+    packed |= (uint32_t)c << (8 * i);
+  }
+  reinterpret_cast<uint32_t*>(index_keys)[slot * 32 + lane] = packed;
+  if (lane == 0) index_scales[slot] = scale;
+}
+
+cudaError_t launch_kv_append(const dsa_cache& c, const void* c_kv, const void* k_rope, const void* k_idx,
+                             int k_idx_format, const float* k_idx_scales, const int64_t* slot_mapping,
+                             int num_tokens, cudaStream_t s) {
+  const int threads = 256, per_block = threads / 32;
+  const int blocks = (num_tokens + per_block - 1) / per_block;
+  kv_append_kernel<<<blocks, threads, 0, s>>>(
+      static_cast<uint4*>(c.latent), (int64_t)c.num_pages * c.page_size, static_cast<uint8_t*>(c.index_keys),
+      c.index_scales, c.key_format, static_cast<const uint4*>(c_kv), static_cast<const uint4*>(k_rope),
+      static_cast<const uint8_t*>(k_idx), k_idx_format, k_idx_scales, slot_mapping, num_tokens);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

@@ -1,0 +1,236 @@
+/*
+ * dsa.h -- C ABI of the GLM-5.2 DeepSeek Sparse Attention (DSA) step on sm_103a.
+ *
+ * One decoder layer's DSA step over a paged KV cache, in two stages:
+ *   1. the lightning indexer scores every visible cached position of every
+ *      query row and keeps the top-k positions in an index buffer that
+ *      IndexShare layers reuse without rescoring;
+ *   2. absorbed sparse MLA attention runs over the selected positions only.
+ * The step's own new tokens are first scattered into the caches (append).
+ *
+ * Sources: "GLM-5.2 on vLLM Ascend: Request-to-Backend Inference Path",
+ * section 8 "The SFA backend, step by step" (write paged cache, select tokens,
+ * run sparse attention; the indexer consumes paged indexer keys, sequence
+ * lengths and block tables and returns top-k token indices; sparse attention
+ * takes the latent query, the separate RoPE query/key, the block table, exact
+ * lengths and the indices) and "Failure and Correctness Boundaries";
+ * "vLLM Inference Path: GLM-5.2 as an Example", sections "Model Shape",
+ * "MLA Projections and KV State", "DSA Indexer" and "Sparse MLA Attention";
+ * "Making GLM-5.2 Sparse on TPUs", sections "Separate the indexer from the
+ * attention it controls", "Pack requests and reuse prefixes" and "Append new
+ * KV without moving the resident cache".
+ *
+ * Conventions that hold for every entry point:
+ *   - Pointers named "device" point to GPU memory owned by the caller; the
+ *     library never allocates, frees or retains them.  Structs are read on the
+ *     host during the call only.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  No call synchronises the host or allocates memory, so
+ *     the calls can be placed in a captured CUDA graph.
+ *   - Argument errors are detected on the host before any launch and return a
+ *     negative dsa_status; dsa_last_error() then describes the problem.  A
+ *     failed launch returns DSA_ERR_CUDA.  Nothing is written on error.
+ *   - Device-side metadata (block tables, lengths, slot mappings, indices)
+ *     cannot be checked on the host: kernels skip a slot, page id or index
+ *     that falls outside its buffer rather than touching memory out of range.
+ *   - bf16 is IEEE bfloat16; e4m3 is the OCP FP8 E4M3 format.
+ *   - All pointers to 16-bit or 8-bit data must be 16-byte aligned.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Entry points are exported from libdsa.so; everything else in it is hidden. */
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+/* Fixed widths of GLM-5.2's DSA layer ("vLLM Inference Path", Model Shape table). */
+#define DSA_INDEX_HEADS 32   /* lightning-indexer heads                          */
+#define DSA_INDEX_DIM 128    /* indexer head width (query and shared key)        */
+#define DSA_HEADS 64         /* MLA attention heads                              */
+#define DSA_LATENT_DIM 512   /* c_KV latent width (also the output width)        */
+#define DSA_ROPE_DIM 64      /* k_R / q_rope width                               */
+#define DSA_ROW_DIM 576      /* one cached latent row: [c_KV(512) | k_R(64)]     */
+#define DSA_MAX_TOPK 8192    /* largest supported top-k budget                   */
+
+#define DSA_ABI_VERSION 1
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = -1, /* NULL/unaligned pointer, bad size, incompatible layout */
+  DSA_ERR_UNSUPPORTED = -2, /* valid request outside what this build implements     */
+  DSA_ERR_WORKSPACE = -3,   /* workspace missing or smaller than the *_workspace_bytes figure */
+  DSA_ERR_CUDA = -4         /* a kernel launch failed                                */
+} dsa_status;
+
+typedef enum {
+  DSA_KEY_BF16 = 0,     /* index keys stored as bf16 [.., 128]                        */
+  DSA_KEY_FP8_E4M3 = 1  /* index keys stored as e4m3 codes [.., 128] + fp32 scale per token */
+} dsa_key_format;
+
+/*
+ * One layer's paged caches (caller-owned device memory).
+ *   latent       [num_pages, page_size, 576] bf16: row = [c_KV(0..511) | k_R(512..575)].
+ *   index_keys   [num_pages, page_size, 128] bf16 or e4m3 codes; only on a layer that owns
+ *                an indexer.  NULL on an IndexShare (shared) layer, which keeps only its
+ *                latent pages and reuses the owner's index buffer.
+ *   index_scales [num_pages, page_size] fp32, e4m3 keys only (dequantised key = code * scale);
+ *                NULL otherwise.
+ * Token s of request b is stored at slot block_table[b][s / page_size] * page_size
+ * + s % page_size ("GLM-5.2 on vLLM Ascend", section 8: the slot mapping scatters new
+ * latent KV and indexer keys into their physical cache pages).
+ */
+typedef struct {
+  void* latent;
+  void* index_keys;
+  float* index_scales;
+  int32_t num_pages;
+  int32_t page_size;  /* power of two, 1..1024 */
+  int32_t key_format; /* dsa_key_format of index_keys */
+} dsa_cache;
+
+/*
+ * Per-call batch metadata ("GLM-5.2 on vLLM Ascend", section 4 "NPU batch preparation and
+ * attention metadata": cumulative query lengths, sequence lengths, block tables; "Making GLM-5.2 Sparse on TPUs", "Pack requests
+ * and reuse prefixes": each query row carries its request, absolute position, valid KV length
+ * and page-table base).
+ *   block_table      device int32 [num_requests, block_table_stride]: physical page ids.
+ *   seq_lens         device int32 [num_requests]: L_b, the KV length of request b after this
+ *                    step's append.
+ *   query_start_loc  device int32 [num_requests + 1]: rows of request b are
+ *                    [query_start_loc[b], query_start_loc[b+1]); row i of request b sits at
+ *                    position L_b - q_len_b + i and sees positions 0..L_b - q_len_b + i.
+ *                    May be NULL in decode calls: then row r is request r's single row.
+ *   num_rows         total query rows R (= num_requests in decode).
+ *   max_seq_len      host-side upper bound on every seq_lens[b] (sizes the score workspace).
+ */
+typedef struct {
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int32_t num_requests;
+  int32_t num_rows;
+  int32_t max_seq_len;
+  int32_t block_table_stride;
+} dsa_batch;
+
+/* ABI version (DSA_ABI_VERSION) of the loaded library. */
+DSA_API int32_t dsa_abi_version(void);
+
+/* Thread-local description of the last non-OK status returned on this thread ("" if none). */
+DSA_API const char* dsa_last_error(void);
+
+/* Number of CUDA kernels this library has launched since it was loaded (all threads). */
+DSA_API uint64_t dsa_kernel_launches(void);
+
+/*
+ * Bytes of one layer's caches: latent pages, plus for an owner layer (owner != 0) the index
+ * keys and, for e4m3 keys, their fp32 scales.  Counting the indexer keys matters: leaving
+ * them out of admission left memory unbudgeted ("Making GLM-5.2 Sparse on TPUs", "Use
+ * independent oracles and test the tests").  Returns 0 for invalid arguments.
+ */
+DSA_API size_t dsa_cache_bytes(int32_t num_pages, int32_t page_size, int32_t key_format, int32_t owner);
+
+/*
+ * Scratch bytes dsa_indexer_scores_topk needs for num_rows rows of up to max_seq_len keys
+ * with budget topk.  The figure never depends on the data, so a workspace sized once per
+ * shape can be locked and reused ("Serving GLM-5.2-504B on 8x RTX PRO 6000 GPUs",
+ * "Reaching 240K context with DCP": a growable workspace locked too small killed the engine).
+ */
+DSA_API size_t dsa_indexer_workspace_bytes(int32_t num_rows, int32_t max_seq_len, int32_t topk);
+
+/* Scratch bytes dsa_sparse_mla_decode / _prefill need for num_rows rows and budget topk. */
+DSA_API size_t dsa_mla_workspace_bytes(int32_t num_rows, int32_t topk);
+
+/*
+ * Append this step's tokens to one layer's caches.
+ * ("GLM-5.2 on vLLM Ascend", section 8, "Write paged cache"; "Making GLM-5.2 Sparse on TPUs",
+ * "Append new KV without moving the resident cache": cost scales with the new rows only and
+ * every other slot keeps its contents.)
+ *   c_kv          device bf16 [num_tokens, 512]   new latents
+ *   k_rope        device bf16 [num_tokens, 64]    new RoPE keys (already rotated)
+ *   k_idx         device [num_tokens, 128] new index keys, or NULL.  Required when the cache
+ *                 has index_keys, rejected when it has none.  k_idx_format says how it is
+ *                 stored: DSA_KEY_BF16 (copied to a bf16 cache, or quantised into an e4m3
+ *                 cache: scale = amax / 448 in fp32, or 1 if amax = 0; code =
+ *                 round-to-nearest-even, saturating e4m3 of x / scale in IEEE fp32) or
+ *                 DSA_KEY_FP8_E4M3 (pre-quantised codes, copied with k_idx_scales [num_tokens]
+ *                 fp32 into an e4m3 cache).
+ *   slot_mapping  device int64 [num_tokens]: physical slot (page * page_size + offset) of each
+ *                 token; a negative slot skips that token, as does one >= num_pages*page_size.
+ * Rows are copied bit-exactly.  num_tokens = 0 is a no-op.
+ */
+DSA_API dsa_status dsa_kv_append(const dsa_cache* cache, const void* c_kv, const void* k_rope, const void* k_idx,
+                         int32_t k_idx_format, const float* k_idx_scales, const int64_t* slot_mapping,
+                         int32_t num_tokens, void* stream);
+
+/*
+ * Lightning indexer scores and top-k selection for every query row.
+ * ("vLLM Inference Path", "DSA Indexer"; "Making GLM-5.2 Sparse on TPUs", "Separate the indexer
+ * from the attention it controls".)
+ *   I(r, s) = sum_{h<32} w[r,h] * max(0, sum_{d<128} q_idx[r,h,d] * K[s,d])  for 0 <= s <= pos(r),
+ *   K[s] = bf16 key, or e4m3 code * scale[s].
+ *   topk_idx[r] = the topk positions with the largest I (ties: smaller position first), sorted
+ *   ascending; every visible position when pos(r) + 1 <= topk; padded with -1.
+ *   owner       cache of the indexer-owning layer (index_keys must be non-NULL).
+ *   q_idx       device bf16 [num_rows, 32, 128]
+ *   w           device fp32 [num_rows, 32]
+ *   topk        1..DSA_MAX_TOPK
+ *   topk_idx    device int32 [num_rows, topk] (output: the shared index buffer)
+ *   scores_out  optional device fp32 [num_rows, max_seq_len]: I(r, s) for s <= pos(r), -inf
+ *               beyond; NULL to skip.
+ *   workspace   device scratch of at least dsa_indexer_workspace_bytes(num_rows, max_seq_len,
+ *               topk) bytes, 256-byte aligned.
+ */
+DSA_API dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_batch* batch, const void* q_idx,
+                                   const float* w, int32_t topk, int32_t* topk_idx, float* scores_out,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Sparse absorbed MLA over the selected positions, decode form: one query row
+ * per request at position seq_lens[b] - 1 (query_start_loc is ignored and may be NULL).
+ * ("vLLM Inference Path", "MLA Projections and KV State" and "Sparse MLA Attention";
+ * "Making GLM-5.2 Sparse on TPUs", "Separate the indexer ...": absorbed MLA, scale tied to
+ * the unabsorbed 192 + 64 width.)
+ *   For every row r and head h, over the valid entries s of topk_idx[r] (0 <= s <= pos(r);
+ *   -1 padding and out-of-range entries are skipped):
+ *     z_s = scale * (q[r,h,0:512] . c_KV[s] + q[r,h,512:576] . k_R[s]),
+ *     out[r,h,:] = sum_s softmax(z)_s c_KV[s]   (bf16),   lse[r,h] = ln sum_s exp(z_s)  (fp32).
+ *   A row with no valid entry gets out = 0 and lse = -inf.
+ *   layer     this layer's cache (only latent is read; index_keys may be NULL).
+ *   q         device bf16 [num_rows, 64, 576]: [q_latent (W^UK absorbed) | q_rope] per head.
+ *   topk_idx  device int32 [num_rows, topk]: the owner layer's index buffer.  IndexShare layers
+ *             pass the owner's buffer; NULL is rejected ("GLM-5.2 on vLLM Ascend", "Failure and
+ *             Correctness Boundaries": a shared layer without the shared buffer is rejected).
+ *   scale     softmax scale, normally 1/sqrt(192 + 64) = 1/16.
+ *   out       device bf16 [num_rows, 64, 512];  lse: optional device fp32 [num_rows, 64].
+ *   workspace device scratch of at least dsa_mla_workspace_bytes(num_rows, topk) bytes.
+ */
+DSA_API dsa_status dsa_sparse_mla_decode(const dsa_cache* layer, const dsa_batch* batch, const void* q,
+                                 const int32_t* topk_idx, int32_t topk, float scale, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Same operation for extend/prefill/verify batches: several query rows per request, causal per
+ * row (row i of request b sees positions 0..L_b - q_len_b + i; query_start_loc is required).
+ * ("Making GLM-5.2 Sparse on TPUs", "Carry sparse reads through prefill" and "Pack requests and
+ * reuse prefixes": causality uses P + i, not an offset reset at each chunk.)
+ */
+DSA_API dsa_status dsa_sparse_mla_prefill(const dsa_cache* layer, const dsa_batch* batch, const void* q,
+                                  const int32_t* topk_idx, int32_t topk, float scale, void* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -1,0 +1,134 @@
+"""The C ABI on the host: the library loads, exports every declared entry point, and rejects
+bad arguments before any launch (no GPU needed; no call here reaches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+INVALID, UNSUPPORTED, WORKSPACE = -1, -2, -3
+A = 1 << 20          # a fake, 256-byte aligned "device" address: never dereferenced on these paths
+
+
+def declared():
+    text = open(HEADER).read()
+    return re.findall(r"^DSA_API\s+[\w\s\*]+?\b(dsa_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for n in ("dsa_kv_append", "dsa_indexer_scores_topk", "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from deepseek_sparse_mla_gb300 import _lib
+    for n in declared():
+        assert hasattr(lib, n), n
+    assert set(declared()) == set(_lib.EXPORTS)
+    assert lib.dsa_abi_version() == 1
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    from deepseek_sparse_mla_gb300 import _lib
+    saved = _lib._lib
+    _lib._lib = None
+    try:
+        with pytest.raises(ImportError):
+            _lib.load(str(tmp_path / "libdsa.so"))
+    finally:
+        _lib._lib = saved
+
+
+def _cache(latent=A, keys=A, scales=A, pages=16, P=64, fmt=1):
+    from deepseek_sparse_mla_gb300._lib import DsaCache
+    return DsaCache(latent, keys, scales, pages, P, fmt)
+
+
+def _batch(B=2, rows=2, L=300, qsl=0, bt=A, sl=A):
+    from deepseek_sparse_mla_gb300._lib import DsaBatch
+    return DsaBatch(bt, sl, qsl, B, rows, L, 8)
+
+
+def _err(lib):
+    return lib.dsa_last_error().decode()
+
+
+def test_cache_bytes_counts_index_keys_and_scales(lib):
+    pages, P = 1000, 64
+    latent = pages * P * 576 * 2
+    assert lib.dsa_cache_bytes(pages, P, 1, 1) == latent + pages * P * (128 + 4)
+    assert lib.dsa_cache_bytes(pages, P, 0, 1) == latent + pages * P * 256
+    assert lib.dsa_cache_bytes(pages, P, 1, 0) == latent
+    assert lib.dsa_cache_bytes(0, P, 1, 1) == 0 and lib.dsa_cache_bytes(pages, P, 7, 1) == 0
+
+
+def test_workspace_sizes_depend_only_on_shape(lib):
+    a = lib.dsa_indexer_workspace_bytes(64, 131072, 2048)
+    assert a == lib.dsa_indexer_workspace_bytes(64, 131072, 2048) and a >= 64 * 131072 * 4
+    big = lib.dsa_indexer_workspace_bytes(4096, 65536, 2048)
+    assert big <= (256 << 20) + 65536 * 4 + 4096          # score block is bounded, not R x L
+    assert lib.dsa_mla_workspace_bytes(64, 2048) >= 256
+    assert lib.dsa_mla_workspace_bytes(4096, 2048) == 256      # enough rows: no split partials
+    assert lib.dsa_indexer_workspace_bytes(1, 0, 2048) == 0
+
+
+def test_append_rejects_bad_arguments(lib):
+    T, P = 4, ctypes.c_void_p
+    assert lib.dsa_kv_append(None, P(A), P(A), P(A), 0, None, P(A), T, None) == INVALID
+    c = _cache(P=48)
+    assert lib.dsa_kv_append(ctypes.byref(c), P(A), P(A), P(A), 0, None, P(A), T, None) == INVALID
+    assert "power of two" in _err(lib)
+    c = _cache(latent=A + 8)
+    assert lib.dsa_kv_append(ctypes.byref(c), P(A), P(A), P(A), 0, None, P(A), T, None) == INVALID
+    c = _cache()
+    assert lib.dsa_kv_append(ctypes.byref(c), P(A), P(A), None, 0, None, P(A), T, None) == INVALID
+    assert "k_idx is required" in _err(lib)
+    shared = _cache(keys=0, scales=0)
+    assert lib.dsa_kv_append(ctypes.byref(shared), P(A), P(A), P(A), 0, None, P(A), T, None) == INVALID
+    bf16_cache = _cache(scales=0, fmt=0)
+    assert lib.dsa_kv_append(ctypes.byref(bf16_cache), P(A), P(A), P(A), 1, P(A), P(A), T, None) == INVALID
+    c = _cache()
+    assert lib.dsa_kv_append(ctypes.byref(c), P(A), P(A), P(A), 1, None, P(A), T, None) == INVALID   # no scales
+    bad_layout = _cache(fmt=0)                                          # bf16 keys with a scale array
+    assert lib.dsa_kv_append(ctypes.byref(bad_layout), P(A), P(A), P(A), 0, None, P(A), T, None) == INVALID
+    assert "not interchangeable" in _err(lib)
+    assert lib.dsa_kv_append(ctypes.byref(c), P(A), P(A), P(A), 0, None, P(A), 0, None) == 0   # empty: no-op
+
+
+def test_indexer_rejects_bad_arguments(lib):
+    P = ctypes.c_void_p
+    ws = lib.dsa_indexer_workspace_bytes(2, 300, 128)
+    shared = _cache(keys=0, scales=0)
+    b = _batch()
+    args = lambda k, wsb: (P(A), P(A), k, P(A), None, P(A), wsb, None)   # noqa: E731
+    assert lib.dsa_indexer_scores_topk(ctypes.byref(shared), ctypes.byref(b), *args(128, ws)) == INVALID
+    assert "shared layer" in _err(lib)
+    c = _cache()
+    assert lib.dsa_indexer_scores_topk(ctypes.byref(c), ctypes.byref(b), *args(0, ws)) == INVALID
+    assert lib.dsa_indexer_scores_topk(ctypes.byref(c), ctypes.byref(b), *args(9000, ws)) == INVALID
+    assert lib.dsa_indexer_scores_topk(ctypes.byref(c), ctypes.byref(b), *args(128, ws - 1)) == WORKSPACE
+    multi = _batch(B=2, rows=5)                                         # several rows per request need query_start_loc
+    assert lib.dsa_indexer_scores_topk(ctypes.byref(c), ctypes.byref(multi), *args(128, ws)) == INVALID
+    nometa = _batch(bt=0)
+    assert lib.dsa_indexer_scores_topk(ctypes.byref(c), ctypes.byref(nometa), *args(128, ws)) == INVALID
+
+
+def test_sparse_mla_rejects_bad_arguments(lib):
+    P = ctypes.c_void_p
+    c = _cache(keys=0, scales=0)                     # attention reads only latent pages
+    b = _batch()
+    ws = lib.dsa_mla_workspace_bytes(2, 128)
+    call = lib.dsa_sparse_mla_decode
+    assert call(ctypes.byref(c), ctypes.byref(b), P(A), None, 128, 0.0625, P(A), None, P(A), ws, None) == INVALID
+    assert "owner layer's index buffer" in _err(lib)
+    assert call(ctypes.byref(c), ctypes.byref(b), P(A), P(A), 128, -1.0, P(A), None, P(A), ws, None) == INVALID
+    assert call(ctypes.byref(c), ctypes.byref(b), P(A), P(A), 128, 0.0625, P(A), None, P(A), ws - 1, None) == WORKSPACE
+    multi = _batch(B=2, rows=6, qsl=A)
+    assert call(ctypes.byref(c), ctypes.byref(multi), P(A), P(A), 128, 0.0625, P(A), None, P(A), ws, None) == INVALID
+    # prefill needs query_start_loc
+    assert lib.dsa_sparse_mla_prefill(ctypes.byref(c), ctypes.byref(_batch(rows=2)), P(A), P(A), 128, 0.0625, P(A),
+                                      None, P(A), ws, None) == INVALID
