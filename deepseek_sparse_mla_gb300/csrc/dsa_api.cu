@@ -239,7 +239,7 @@ dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_batch* batc
     int64_t stride = scores_out ? (int64_t)batch->max_seq_len : plan.score_stride;
     cudaError_t e = launch_indexer_scores(*owner, m, row0, n, batch->max_seq_len, q_idx, w, scores, stride, s);
     if (e != cudaSuccess) return cuda_status(e, "indexer launch");
-    e = launch_topk(m, row0, n, scores, stride, topk, topk_idx, s);
+    e = launch_topk(m, row0, n, scores, stride, batch->max_seq_len, topk, topk_idx, s);
     if (e != cudaSuccess) return cuda_status(e, "top-k launch");
   }
   return ok();

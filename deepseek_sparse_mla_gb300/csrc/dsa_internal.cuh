@@ -63,7 +63,7 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
                                   cudaStream_t s);
 
 cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scores, int64_t score_stride,
-                        int topk, int32_t* topk_idx, cudaStream_t s);
+                        int max_seq_len, int topk, int32_t* topk_idx, cudaStream_t s);
 
 cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows, const void* q,
                               const int32_t* topk_idx, int topk, float scale, void* out, float* lse,

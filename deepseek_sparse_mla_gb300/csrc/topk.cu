@@ -52,14 +52,16 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
 }
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0, const float* __restrict__ scores,
-                                                            int64_t stride, int k, int32_t* __restrict__ topk_idx) {
+                                                            int64_t stride, int max_seq_len, int k,
+                                                            int32_t* __restrict__ topk_idx) {
   __shared__ uint32_t hist[2048];
   __shared__ uint32_t warp_tot[33];
   __shared__ uint32_t sh_bin, sh_krem;
   const int r = row0 + blockIdx.x;
   int b, pos;
   row_info(m, r, b, pos);
-  const int n = pos + 1 > 0 ? pos + 1 : 0;
+  int n = pos + 1 > 0 ? pos + 1 : 0;
+  if (n > max_seq_len) n = max_seq_len;   // never read past the row's scores, whatever seq_lens says
   int32_t* out = topk_idx + (int64_t)r * k;
   const float* sc = scores + (int64_t)blockIdx.x * stride;
   const int tid = threadIdx.x;
@@ -131,11 +133,13 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       if (s0 + j >= n) break;
+      // slots are < k by construction; the guard only keeps inconsistent input inside the row
       if (key[j] > T) {
-        out[gt_before + (eq_before < need_eq ? eq_before : need_eq)] = s0 + j;
+        const uint32_t slot = gt_before + (eq_before < need_eq ? eq_before : need_eq);
+        if (slot < (uint32_t)k) out[slot] = s0 + j;
         ++gt_before;
       } else if (key[j] == T) {
-        if (eq_before < need_eq) out[gt_before + eq_before] = s0 + j;
+        if (eq_before < need_eq && gt_before + eq_before < (uint32_t)k) out[gt_before + eq_before] = s0 + j;
         ++eq_before;
       }
     }
@@ -144,9 +148,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
   }
 }
 
-cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scores, int64_t score_stride, int topk,
-                        int32_t* topk_idx, cudaStream_t s) {
-  topk_kernel<<<nrows, kTopkThreads, 0, s>>>(m, row0, scores, score_stride, topk, topk_idx);
+cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scores, int64_t score_stride,
+                        int max_seq_len, int topk, int32_t* topk_idx, cudaStream_t s) {
+  topk_kernel<<<nrows, kTopkThreads, 0, s>>>(m, row0, scores, score_stride, max_seq_len, topk, topk_idx);
   count_launches(1);
   return cudaGetLastError();
 }
