@@ -320,7 +320,7 @@ def stratified_requests(wl, n):
     return [int(b) for b in pick]
 
 
-def cpu_baseline(wl, device, n_req=3):
+def cpu_baseline(wl, device, n_req=64):
     q_idx, w = wlm.indexer_queries(wl)
     qs = [wlm.mla_queries(wl, l) for l in range(wl.layers)]
     total = 0.0
@@ -379,7 +379,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wlm.FULL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-requests", type=int, default=3)
+    ap.add_argument("--cpu-sample-requests", type=int, default=64)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

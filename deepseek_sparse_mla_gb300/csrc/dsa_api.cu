@@ -52,22 +52,6 @@ IndexerPlan plan_indexer(int num_rows, int max_seq_len, int topk) {
   return p;
 }
 
-MlaPlan plan_mla(int num_rows, int topk) {
-  MlaPlan p;
-  int splits = num_rows >= kSplitTargetCtas ? 1 : (kSplitTargetCtas + num_rows - 1) / num_rows;
-  int max_splits = topk / 64 > 0 ? topk / 64 : 1;   // keep at least 64 selected entries per split
-  if (splits > max_splits) splits = max_splits;
-  if (splits > 32) splits = 32;
-  if (splits < 1) splits = 1;
-  p.tokens_per_split = (topk + splits - 1) / splits;
-  p.splits = (topk + p.tokens_per_split - 1) / p.tokens_per_split;
-  size_t partial = 0;
-  if (p.splits > 1)
-    partial = (size_t)num_rows * p.splits * kHeads * (kLatent + 2) * sizeof(float);
-  p.workspace_bytes = kWorkspaceHeader + partial;
-  return p;
-}
-
 static dsa_status check_cache(const dsa_cache* c, bool need_keys) {
   if (!c) return fail(DSA_ERR_INVALID_ARG, "cache is NULL");
   if (!c->latent) return fail(DSA_ERR_INVALID_ARG, "cache.latent is NULL");

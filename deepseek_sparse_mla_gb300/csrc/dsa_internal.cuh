@@ -17,8 +17,8 @@ constexpr int kLatent = DSA_LATENT_DIM;        // 512
 constexpr int kRope = DSA_ROPE_DIM;            // 64
 constexpr int kRow = DSA_ROW_DIM;              // 576
 
-// Split-k target: enough (row, split) CTAs to cover the GPU about twice.
-constexpr int kSplitTargetCtas = 2 * 152;
+// Persistent attention grid: one CTA per SM of a GB300 (152 SMs).
+constexpr int kMlaCtas = 152;
 // Upper bound on the fp32 score block the indexer materialises per launch group.
 constexpr size_t kScoreBlockBytes = size_t(256) << 20;
 constexpr size_t kWorkspaceHeader = 256;
@@ -34,9 +34,10 @@ struct IndexerPlan {
 IndexerPlan plan_indexer(int num_rows, int max_seq_len, int topk);
 
 struct MlaPlan {
-  int splits;             // split-k pieces of each row's selection
-  int tokens_per_split;
-  size_t workspace_bytes;
+  int tiles;              // 64-entry tiles per row of the index buffer
+  int units;              // rows x tiles, split into one contiguous range per CTA
+  int ctas;               // persistent CTAs (at most one per SM)
+  size_t workspace_bytes; // header + two (64 x 512 + 64 x 2) fp32 partial slots per CTA
 };
 MlaPlan plan_mla(int num_rows, int topk);
 

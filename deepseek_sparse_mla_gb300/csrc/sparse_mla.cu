@@ -1,230 +1,550 @@
-// Sparse absorbed MLA over the selected positions, with split-k over the
-// selection and a log-sum-exp merge.
+// Sparse absorbed MLA over the selected positions, on tcgen05 tensor cores.
 //
 // For row r, head h and valid selected s (0 <= s <= pos(r)):
 //   z_s = scale * (q[r,h,:512] . c_KV[s] + q[r,h,512:] . k_R[s])
 //   out[r,h,:] = sum_s softmax(z)_s c_KV[s],  lse[r,h] = ln sum_s exp(z_s)
 // ("vLLM Inference Path: GLM-5.2 as an Example", "MLA Projections and KV State"
 // and "Sparse MLA Attention"; "Making GLM-5.2 Sparse on TPUs", "Separate the
-// indexer from the attention it controls": absorbed MLA with the scale tied to
-// the unabsorbed 192 + 64 width, and "Carry sparse reads through prefill":
-// online softmax over the selected entries).
+// indexer from the attention it controls": absorbed MLA, scale tied to the
+// unabsorbed 192 + 64 width; "Carry sparse reads through prefill": online
+// softmax over the selected entries).
 //
-// Grid = (split, row).  A CTA streams its slice of the row's index buffer in
-// tiles of 32 cached rows gathered through the page table, keeps a running
-// max / sum per head (online softmax) and the 64 x 512 output accumulator in
-// registers.  With one split it writes the bf16 output directly; otherwise it
-// writes (acc, m, l) partials that the merge kernel combines by LSE.
+// Work: the rows' index buffers are cut into tiles of 64 entries; the
+// (row, tile) units are split into one contiguous range per CTA (persistent,
+// one CTA per SM).  A row cut between CTAs is finished by an LSE merge of the
+// pieces; a row inside one CTA is written directly.
+//
+// Per CTA (192 threads):
+//   warp 0     producer: TMA-loads the row's 64 x 576 query (9 boxes of 64
+//              heads x 64 columns) and gathers each tile's 64 cached rows
+//              straight out of the paged pool with TMA gather4 (four 128-byte
+//              row pieces per instruction, 128-byte swizzle), two stages deep;
+//   warp 1     MMA issuer: S^T = K Q^T (M = 64 tokens, N = 64 heads, K = 576)
+//              into TMEM, then O^T += V^T P^T (M = 128 latent dims x 4,
+//              N = 64 heads, K = 64 tokens) with V read from the same gathered
+//              tile (MN-major) and P^T from shared memory;
+//   warps 2-5  softmax: per-head tile maxima with redux.sync, exp2 into bf16
+//              P^T rows (one 128-byte row per token, no transpose needed), a
+//              lazy rescale of the TMEM accumulator only when a head's running
+//              maximum grows by more than 2^8, and the epilogue.
+// Shared memory: Q 72 KB + 2 x 72 KB tiles + 8 KB P^T.  TMEM: 2 x 64 columns
+// for S^T and 4 x 64 columns for O^T.
+#include <mutex>
+
 #include "dsa_internal.cuh"
+#include "sm100.cuh"
+#include "tmap.cuh"
 
 namespace dsa {
+using namespace sm100;
 
-constexpr int kTileTokens = 32;
-constexpr int kThreadsMla = 512;           // thread = (head h = tid / 8, lane-in-head j = tid % 8)
-constexpr int kRowPad = kRow + 8;          // padded smem row: 1168 bytes, keeps 8 rows on distinct banks
-constexpr int kChunksRow = kRow / 8;       // 72 chunks of 8 bf16 per cached row
+namespace mla {
+constexpr int kTok = 64;                           // selected entries per tile (MMA M of S^T)
+constexpr int kChunks = kRow / 64;                 // 9 column chunks of 64 bf16 (128 bytes)
+constexpr int kChunkBytes = kTok * 128;            // one chunk of a tile
+constexpr int kStageBytes = kChunks * kChunkBytes; // 72 KB
+constexpr int kQChunkBytes = kHeads * 128;
+constexpr int kQBytes = kChunks * kQChunkBytes;    // 72 KB
+constexpr int kPBytes = kTok * 128;                // P^T: 64 tokens x 64 heads bf16
+constexpr int kSmemBytes = kQBytes + 2 * kStageBytes + kPBytes + 1024;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;                      // S^T of stage b at columns 64 b
+constexpr uint32_t kColO = 128;                    // O^T chunk k (dims 128k..) at columns 128 + 64 k
+constexpr float kRescaleLog2 = 8.f;
+constexpr uint32_t kPolls = 1u << 22;
+}  // namespace mla
 
-__device__ __forceinline__ float dot8(const uint4 a, const uint4 b, float acc) {
-  const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a);
-  const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 fx = __bfloat1622float2(x[i]), fy = __bfloat1622float2(y[i]);
-    acc = fmaf(fx.x, fy.x, fmaf(fx.y, fy.y, acc));
-  }
-  return acc;
+struct MlaArgs {
+  RowMeta m;
+  const int32_t* topk_idx;
+  int topk, tiles, units, ctas;
+  int log2_page, num_pages;
+  float scale_log2;               // softmax scale * log2(e)
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;                  // [2 * ctas][64][512]
+  float* part_ml;                 // [2 * ctas][64][2]
+  uint32_t* err;
+};
+
+__device__ __forceinline__ int unit_start(int c, int units, int ctas) {
+  return (int)(((int64_t)c * units) / ctas);
 }
 
-__global__ void __launch_bounds__(kThreadsMla) sparse_mla_kernel(
-    const uint4* __restrict__ latent, int log2_page, int num_pages, RowMeta m, const uint4* __restrict__ q,
-    const int32_t* __restrict__ topk_idx, int topk, float scale, int tokens_per_split, int splits,
-    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o, float* __restrict__ part_ml) {
-  extern __shared__ uint4 smem[];
-  uint4* qs = smem;                                   // [64][kRowPad/8] chunks
-  uint4* kv = qs + kHeads * (kRowPad / 8);            // [32][kRowPad/8]
-  float* ps = reinterpret_cast<float*>(kv + kTileTokens * (kRowPad / 8));   // [64][32]
-  __shared__ int64_t tok_slot[kTileTokens];
+__device__ __forceinline__ int cta_of_unit(int u, int units, int ctas) {
+  int c = (int)(((int64_t)u * ctas) / units);
+  while (c + 1 < ctas && unit_start(c + 1, units, ctas) <= u) ++c;
+  while (c > 0 && unit_start(c, units, ctas) > u) --c;
+  return c;
+}
 
-  const int r = blockIdx.y, split = blockIdx.x;
-  const int tid = threadIdx.x, h = tid >> 3, j = tid & 7;
-  int b, pos;
-  row_info(m, r, b, pos);
+__global__ void __launch_bounds__(mla::kThreads, 1)
+    sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+                         const MlaArgs a) {
+  using namespace mla;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + kQBytes;
+  uint8_t* sP = sKV + 2 * kStageBytes;
 
-  const uint4* qg = q + (int64_t)r * kHeads * kChunksRow;
-  for (int i = tid; i < kHeads * kChunksRow; i += kThreadsMla) qs[(i / kChunksRow) * (kRowPad / 8) + i % kChunksRow] = qg[i];
+  __shared__ uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2];
+  __shared__ uint64_t p_full, p_empty, q_full, q_empty, o_full, o_empty, mma_done;
+  __shared__ uint64_t tile_mask[2];
+  __shared__ float red[4][kHeads];
+  __shared__ float mref[kHeads], alpha[kHeads], lfin[kHeads];
+  __shared__ int rescale_tag;
+  __shared__ uint32_t tmem_base;
 
-  float m_run = -INFINITY, l_run = 0.f;
-  float acc[64];   // dims (c * 8 + j) * 8 + e for c, e in 0..7
-#pragma unroll
-  for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x;
+  const int T = a.tiles;
+  const int u0 = unit_start(cta, a.units, a.ctas), u1 = unit_start(cta + 1, a.units, a.ctas);
 
-  const int t_begin = split * tokens_per_split;
-  const int t_end = min(topk, t_begin + tokens_per_split);
-  const int32_t* idx_row = topk_idx + (int64_t)r * topk;
-  for (int t0 = t_begin; t0 < t_end; t0 += kTileTokens) {
-    __syncthreads();
-    if (tid < kTileTokens) {
-      const int t = t0 + tid;
-      int64_t sl = -1;
-      if (t < t_end) {
-        const int s = idx_row[t];
-        if (s >= 0 && s <= pos) sl = token_slot(m, b, s, log2_page, num_pages);
-      }
-      tok_slot[tid] = sl;
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&kv_full[b], 1);
+      mbar_init(&kv_empty[b], 1);
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_empty[b], 4);
     }
-    __syncthreads();
-    for (int i = tid; i < kTileTokens * kChunksRow; i += kThreadsMla) {
-      const int tt = i / kChunksRow, c = i % kChunksRow;
-      const int64_t sl = tok_slot[tt];
-      kv[tt * (kRowPad / 8) + c] = sl >= 0 ? latent[sl * kChunksRow + c] : make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();
+    mbar_init(&p_full, 1);
+    mbar_init(&p_empty, 1);
+    mbar_init(&q_full, 1);
+    mbar_init(&q_empty, 1);
+    mbar_init(&o_full, 1);
+    mbar_init(&o_empty, 4);
+    mbar_init(&mma_done, 1);
+    rescale_tag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&kv_map);
+    prefetch_tmap(&q_map);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
 
-    float sc[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int tt = j + 8 * u;
-      const uint4* qrow = qs + h * (kRowPad / 8);
-      const uint4* krow = kv + tt * (kRowPad / 8);
-      float d = 0.f;
-#pragma unroll 8
-      for (int c = 0; c < kChunksRow; ++c) d = dot8(qrow[c], krow[c], d);
-      sc[u] = tok_slot[tt] >= 0 ? d * scale : -INFINITY;
-    }
-    float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-    const float m_new = fmaxf(m_run, tmax);
-    const float alpha = m_new == -INFINITY ? 1.f : expf(m_run - m_new);
-    float psum = 0.f;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float p = sc[u] == -INFINITY ? 0.f : expf(sc[u] - m_new);
-      ps[h * kTileTokens + j + 8 * u] = p;
-      psum += p;
-    }
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
-    l_run = l_run * alpha + psum;
-    m_run = m_new;
-    __syncthreads();
-
-#pragma unroll
-    for (int i = 0; i < 64; ++i) acc[i] *= alpha;
-    for (int tt = 0; tt < kTileTokens; ++tt) {
-      const float p = ps[h * kTileTokens + tt];
-      if (p == 0.f) continue;
-      const uint4* krow = kv + tt * (kRowPad / 8);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = krow[c * 8 + j];
-        const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(x[e]);
-          acc[c * 8 + 2 * e] = fmaf(p, f.x, acc[c * 8 + 2 * e]);
-          acc[c * 8 + 2 * e + 1] = fmaf(p, f.y, acc[c * 8 + 2 * e + 1]);
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    int q_loads = 0, cur_row = -1, req = 0, pos = -1;
+    int filled[2] = {0, 0};
+    for (int u = u0; u < u1; ++u) {
+      const int i = u - u0, b = i & 1, n = i >> 1;
+      const int r = u / T, j = u - r * T;
+      if (n > 0 && !mbar_wait(&kv_empty[b], (n - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
+      if (r != cur_row) {
+        if (q_loads > 0 && !mbar_wait(&q_empty, (q_loads - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&q_full, kQBytes);
+          for (int c = 0; c < kChunks; ++c) tma_load_2d(sQ + c * kQChunkBytes, &q_map, c * 64, r * kHeads, &q_full);
         }
+        ++q_loads;
+        cur_row = r;
+        row_info(a.m, r, req, pos);
+      }
+      // entry `lane` and `lane + 32` of the tile
+      const int32_t* idx = a.topk_idx + (int64_t)r * a.topk + (int64_t)j * kTok;
+      int64_t sl[2];
+      uint32_t vb[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int t = lane + 32 * h;
+        const int e = (j * kTok + t < a.topk) ? idx[t] : -1;
+        sl[h] = (e >= 0 && e <= pos) ? token_slot(a.m, req, e, a.log2_page, a.num_pages) : -1;
+        vb[h] = __ballot_sync(0xffffffffu, sl[h] >= 0);
+      }
+      const uint64_t mask = (uint64_t)vb[0] | ((uint64_t)vb[1] << 32);
+      if (mask != 0) {
+        // invalid entries re-read a valid row of the tile (finite data); their probability is 0
+        const int t0 = __ffsll((long long)mask) - 1;
+        const int64_t s0 = __shfl_sync(0xffffffffu, sl[0], t0 & 31), s1 = __shfl_sync(0xffffffffu, sl[1], t0 & 31);
+        const int64_t sub = t0 < 32 ? s0 : s1;
+        if (sl[0] < 0) sl[0] = sub;
+        if (sl[1] < 0) sl[1] = sub;
+      }
+      if (lane == 0) {
+        tile_mask[b] = mask;
+        mbar_arrive_expect_tx(&kv_full[b], mask ? (uint32_t)kStageBytes : 0u);
+      }
+      __syncwarp();
+      ++filled[b];
+      if (mask != 0) {
+        uint8_t* stage = sKV + b * kStageBytes;
+        const int g = lane & 15;        // entries 4g .. 4g+3
+        const int hsel = g >> 3;        // held in sl[hsel] by lanes (4g .. 4g+3) % 32
+        int32_t y[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int src = (4 * g + k) & 31;
+          const int64_t v0 = __shfl_sync(0xffffffffu, sl[0], src), v1 = __shfl_sync(0xffffffffu, sl[1], src);
+          y[k] = (int32_t)(hsel ? v1 : v0);
+        }
+        for (int c = lane >> 4; c < kChunks; c += 2)
+          tma_gather4(stage + c * kChunkBytes + g * 4 * 128, &kv_map, c * 64, y[0], y[1], y[2], y[3], &kv_full[b]);
+      }
+    }
+    // nothing may still be landing in shared memory when the CTA exits
+    for (int b = 0; b < 2; ++b)
+      if (filled[b] > 0) mbar_wait(&kv_full[b], (filled[b] - 1) & 1, a.err, kErrTmaTimeout, kPolls);
+    if (q_loads > 0) mbar_wait(&q_full, (q_loads - 1) & 1, a.err, kErrTmaTimeout, kPolls);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_f16(64, kHeads, true, true, false, false);
+      const uint32_t id_pv = idesc_f16(128, kHeads, true, true, true, true);
+      const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
+      int q_loads = 0, seg = 0, prev_row = -1;
+      bool o_init = false, ok = true;
+      auto pv = [&](int i) -> bool {
+        const int u = u0 + i, b = i & 1, r = u / T, j = u - r * T;
+        const bool seg_first = (u == u0) || j == 0;
+        const bool seg_last = (u == u1 - 1) || j == T - 1;
+        if (!mbar_wait(&p_full, i & 1, a.err, kErrMmaTimeout, kPolls)) return false;
+        if (seg_first) {
+          o_init = false;
+          if (seg > 0 && !mbar_wait(&o_empty, (seg - 1) & 1, a.err, kErrMmaTimeout, kPolls)) return false;
+        }
+        tc_fence_after();
+        if (tile_mask[b] != 0) {
+          const uint32_t stage = smem_u32(sKV + b * kStageBytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t da = smem_desc(stage + 2 * k * kChunkBytes + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
+              const uint64_t db = smem_desc(p_addr + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
+              mma_ss(tmem + kColO + 64 * k, da, db, id_pv, o_init || kk > 0);
+            }
+          o_init = true;
+        }
+        mma_commit(&kv_empty[b]);
+        mma_commit(&p_empty);
+        if (seg_last) {
+          mma_commit(&o_full);
+          ++seg;
+        }
+        return true;
+      };
+      for (int u = u0; u < u1; ++u) {
+        const int i = u - u0, b = i & 1, n = i >> 1, r = u / T;
+        if (!mbar_wait(&kv_full[b], n & 1, a.err, kErrTmaTimeout, kPolls)) { ok = false; break; }
+        if (r != prev_row) {
+          if (!mbar_wait(&q_full, q_loads & 1, a.err, kErrTmaTimeout, kPolls)) { ok = false; break; }
+          ++q_loads;
+          prev_row = r;
+        }
+        if (n > 0 && !mbar_wait(&s_empty[b], (n - 1) & 1, a.err, kErrMmaTimeout, kPolls)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t stage = smem_u32(sKV + b * kStageBytes);
+#pragma unroll 4
+        for (int kk = 0; kk < kChunks * 4; ++kk) {
+          const int c = kk >> 2, off = (kk & 3) * 32;
+          mma_ss(tmem + kColS + 64 * b, smem_desc(stage + c * kChunkBytes + off, 16, 1024, kSwizzle128B),
+                 smem_desc(q_addr + c * kQChunkBytes + off, 16, 1024, kSwizzle128B), id_qk, kk > 0);
+        }
+        mma_commit(&s_full[b]);
+        if (u == u1 - 1 || (u + 1) / T != r) mma_commit(&q_empty);
+        if (i > 0 && !pv(i - 1)) { ok = false; break; }
+      }
+      if (ok && u1 > u0) pv(u1 - u0 - 1);
+      // every MMA issued here has finished before TMEM is released
+      mma_commit(&mma_done);
+      mbar_wait(&mma_done, 0, a.err, kErrMmaTimeout, kPolls);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax + epilogue
+    const int quarter = warp & 3;                       // TMEM lanes this warp may touch
+    const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+    const int tok = 16 * quarter + lane;                // S^T row held by this lane (lanes 0..15)
+    const int st = threadIdx.x - 64;                    // 0..127
+    const int first_row = u0 / T;
+    float l_acc[kHeads];
+    int seg = 0;
+    for (int u = u0; u < u1; ++u) {
+      const int i = u - u0, b = i & 1, n = i >> 1, r = u / T, j = u - r * T;
+      const bool seg_first = (u == u0) || j == 0;
+      const bool seg_last = (u == u1 - 1) || j == T - 1;
+      if (seg_first) {
+#pragma unroll
+        for (int h = 0; h < kHeads; ++h) l_acc[h] = 0.f;
+        if (st < kHeads) mref[st] = -INFINITY;
+      }
+      if (!mbar_wait(&kv_full[b], n & 1, a.err, kErrTmaTimeout, kPolls)) break;
+      if (!mbar_wait(&s_full[b], n & 1, a.err, kErrMmaTimeout, kPolls)) break;
+      tc_fence_after();
+      uint32_t s_lo[32], s_hi[32];
+      tmem_ld32(tmem + lane_base + kColS + 64 * b, s_lo);
+      tmem_ld32(tmem + lane_base + kColS + 64 * b + 32, s_hi);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[b]);
+      const uint64_t mask = tile_mask[b];
+      const bool valid = lane < 16 && ((mask >> tok) & 1ull);
+      float z[kHeads];
+#pragma unroll
+      for (int h = 0; h < 32; ++h) {
+        z[h] = valid ? __uint_as_float(s_lo[h]) * a.scale_log2 : -INFINITY;
+        z[h + 32] = valid ? __uint_as_float(s_hi[h]) * a.scale_log2 : -INFINITY;
+      }
+#pragma unroll
+      for (int h = 0; h < kHeads; ++h) {
+        const float mx = warp_max_f32(z[h]);
+        if (lane == 0) red[quarter][h] = mx;
+      }
+      named_bar_sync(1, 128);
+      if (st < kHeads) {
+        const int h = st;
+        const float M = fmaxf(fmaxf(red[0][h], red[1][h]), fmaxf(red[2][h], red[3][h]));
+        const float old = mref[h];
+        float al = 1.f;
+        if (M > -INFINITY && (old == -INFINITY || M > old + kRescaleLog2)) {
+          al = old == -INFINITY ? 0.f : exp2f(old - M);
+          if (old != -INFINITY) rescale_tag = i + 1;
+          mref[h] = M;
+        }
+        alpha[h] = al;
+      }
+      named_bar_sync(1, 128);
+      const bool do_rescale = rescale_tag == i + 1;
+      uint32_t pk[32];
+#pragma unroll
+      for (int h = 0; h < kHeads; h += 2) {
+        const float m0 = mref[h], m1 = mref[h + 1];
+        const float p0 = z[h] == -INFINITY ? 0.f : exp2f(z[h] - m0);
+        const float p1 = z[h + 1] == -INFINITY ? 0.f : exp2f(z[h + 1] - m1);
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+        l_acc[h] = fmaf(l_acc[h], alpha[h], p0);          // the denominator keeps the fp32 probabilities
+        l_acc[h + 1] = fmaf(l_acc[h + 1], alpha[h + 1], p1);
+        pk[h >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+      }
+      // P^T is free once the previous tile's PV has completed (which also settles O^T)
+      if (i > 0 && !mbar_wait(&p_empty, (i - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
+      if (lane < 16) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(sP + sw128_offset(tok, c)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
+      if (do_rescale) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k)
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            uint32_t o[32];
+            const uint32_t addr = tmem + lane_base + kColO + 64 * k + 32 * half;
+            tmem_ld32(addr, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) o[jj] = __float_as_uint(__uint_as_float(o[jj]) * alpha[32 * half + jj]);
+            tmem_st32(addr, o);
+          }
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(1, 128);
+      if (st == 0) mbar_arrive(&p_full);
+
+      if (seg_last) {
+#pragma unroll
+        for (int h = 0; h < kHeads; ++h) {
+          float v = l_acc[h];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) red[quarter][h] = v;
+        }
+        named_bar_sync(1, 128);
+        if (st < kHeads) lfin[st] = (red[0][st] + red[1][st]) + (red[2][st] + red[3][st]);
+        named_bar_sync(1, 128);
+        if (!mbar_wait(&o_full, seg & 1, a.err, kErrMmaTimeout, kPolls)) break;
+        tc_fence_after();
+        const int seg_start = u0 > r * T ? u0 : r * T;
+        const bool whole = seg_start == r * T && j == T - 1;
+        const int slot = r == first_row ? 2 * cta : 2 * cta + 1;
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {
+          const int d = 128 * k + 32 * quarter + lane;
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_base + kColO + 64 * k + 32 * half, o);
+            tmem_wait_ld();
+            if (whole) {
+              __nv_bfloat16* dst = a.out + (int64_t)r * kHeads * kLatent + d;
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const int h = 32 * half + jj;
+                const float L = lfin[h];
+                dst[(int64_t)h * kLatent] = __float2bfloat16_rn(L > 0.f ? __uint_as_float(o[jj]) / L : 0.f);
+              }
+            } else {
+              float* dst = a.part_o + (int64_t)slot * kHeads * kLatent + d;
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) dst[(int64_t)(32 * half + jj) * kLatent] = __uint_as_float(o[jj]);
+            }
+          }
+        }
+        if (st < kHeads) {
+          const int h = st;
+          const float L = lfin[h];
+          if (whole) {
+            if (a.lse) a.lse[(int64_t)r * kHeads + h] = L > 0.f ? (mref[h] + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+          } else {
+            a.part_ml[((int64_t)slot * kHeads + h) * 2] = L > 0.f ? mref[h] * 0.69314718055994530942f : -INFINITY;
+            a.part_ml[((int64_t)slot * kHeads + h) * 2 + 1] = L;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&o_empty);
+        ++seg;
       }
     }
   }
 
-  if (splits == 1) {
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    __nv_bfloat16* o = out + ((int64_t)r * kHeads + h) * kLatent;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint4 v;
-      __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&v);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) x[e] = __floats2bfloat162_rn(acc[c * 8 + 2 * e] * inv, acc[c * 8 + 2 * e + 1] * inv);
-      reinterpret_cast<uint4*>(o)[c * 8 + j] = v;
-    }
-    if (lse && j == 0) lse[(int64_t)r * kHeads + h] = l_run > 0.f ? m_run + logf(l_run) : -INFINITY;
-  } else {
-    const int64_t base = ((int64_t)r * splits + split) * kHeads + h;
-    float4* o = reinterpret_cast<float4*>(part_o + base * kLatent);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      o[(c * 8 + j) * 2] = make_float4(acc[c * 8], acc[c * 8 + 1], acc[c * 8 + 2], acc[c * 8 + 3]);
-      o[(c * 8 + j) * 2 + 1] = make_float4(acc[c * 8 + 4], acc[c * 8 + 5], acc[c * 8 + 6], acc[c * 8 + 7]);
-    }
-    if (j == 0) {
-      part_ml[base * 2] = m_run;
-      part_ml[base * 2 + 1] = l_run;
-    }
-  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// LSE merge of split partials: O = sum_j e^{m_j - M} acc_j / sum_j e^{m_j - M} l_j, lse = M + ln L.
-__global__ void __launch_bounds__(kThreadsMla) mla_merge_kernel(const float* __restrict__ part_o,
-                                                                const float* __restrict__ part_ml, int splits,
-                                                                __nv_bfloat16* __restrict__ out,
-                                                                float* __restrict__ lse) {
-  const int r = blockIdx.x, tid = threadIdx.x, h = tid >> 3, j = tid & 7;
+// LSE merge of the pieces of rows that were cut between CTAs:
+//   out = sum_j e^{m_j - M} O_j / sum_j e^{m_j - M} l_j,  lse = M + ln sum_j e^{m_j - M} l_j.
+__global__ void __launch_bounds__(512) mla_merge_kernel(MlaArgs a) {
+  const int r = blockIdx.x, tid = threadIdx.x, h = tid >> 3, jl = tid & 7;
+  const int T = a.tiles;
+  const int c_first = cta_of_unit(r * T, a.units, a.ctas), c_last = cta_of_unit(r * T + T - 1, a.units, a.ctas);
+  if (c_first == c_last) return;    // written directly by the attention kernel
   float M = -INFINITY;
-  for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, part_ml[(((int64_t)r * splits + sp) * kHeads + h) * 2]);
+  for (int c = c_first; c <= c_last; ++c) {
+    const int slot = r == unit_start(c, a.units, a.ctas) / T ? 2 * c : 2 * c + 1;
+    M = fmaxf(M, a.part_ml[((int64_t)slot * kHeads + h) * 2]);
+  }
   float L = 0.f;
   float acc[64];
 #pragma unroll
-  for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-  for (int sp = 0; sp < splits; ++sp) {
-    const int64_t base = ((int64_t)r * splits + sp) * kHeads + h;
-    const float mj = part_ml[base * 2], lj = part_ml[base * 2 + 1];
+  for (int x = 0; x < 64; ++x) acc[x] = 0.f;
+  for (int c = c_first; c <= c_last; ++c) {
+    const int slot = r == unit_start(c, a.units, a.ctas) / T ? 2 * c : 2 * c + 1;
+    const float mj = a.part_ml[((int64_t)slot * kHeads + h) * 2], lj = a.part_ml[((int64_t)slot * kHeads + h) * 2 + 1];
     if (!(lj > 0.f)) continue;
     const float wgt = expf(mj - M);
     L = fmaf(wgt, lj, L);
-    const float4* o = reinterpret_cast<const float4*>(part_o + base * kLatent);
+    const float4* o = reinterpret_cast<const float4*>(a.part_o + ((int64_t)slot * kHeads + h) * kLatent);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const float4 a = o[(c * 8 + j) * 2], bq = o[(c * 8 + j) * 2 + 1];
-      acc[c * 8 + 0] = fmaf(wgt, a.x, acc[c * 8 + 0]);
-      acc[c * 8 + 1] = fmaf(wgt, a.y, acc[c * 8 + 1]);
-      acc[c * 8 + 2] = fmaf(wgt, a.z, acc[c * 8 + 2]);
-      acc[c * 8 + 3] = fmaf(wgt, a.w, acc[c * 8 + 3]);
-      acc[c * 8 + 4] = fmaf(wgt, bq.x, acc[c * 8 + 4]);
-      acc[c * 8 + 5] = fmaf(wgt, bq.y, acc[c * 8 + 5]);
-      acc[c * 8 + 6] = fmaf(wgt, bq.z, acc[c * 8 + 6]);
-      acc[c * 8 + 7] = fmaf(wgt, bq.w, acc[c * 8 + 7]);
+    for (int cc = 0; cc < 8; ++cc) {
+      const float4 x = o[(cc * 8 + jl) * 2], y = o[(cc * 8 + jl) * 2 + 1];
+      acc[cc * 8 + 0] = fmaf(wgt, x.x, acc[cc * 8 + 0]);
+      acc[cc * 8 + 1] = fmaf(wgt, x.y, acc[cc * 8 + 1]);
+      acc[cc * 8 + 2] = fmaf(wgt, x.z, acc[cc * 8 + 2]);
+      acc[cc * 8 + 3] = fmaf(wgt, x.w, acc[cc * 8 + 3]);
+      acc[cc * 8 + 4] = fmaf(wgt, y.x, acc[cc * 8 + 4]);
+      acc[cc * 8 + 5] = fmaf(wgt, y.y, acc[cc * 8 + 5]);
+      acc[cc * 8 + 6] = fmaf(wgt, y.z, acc[cc * 8 + 6]);
+      acc[cc * 8 + 7] = fmaf(wgt, y.w, acc[cc * 8 + 7]);
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  __nv_bfloat16* o = out + ((int64_t)r * kHeads + h) * kLatent;
+  __nv_bfloat16* o = a.out + ((int64_t)r * kHeads + h) * kLatent;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int cc = 0; cc < 8; ++cc) {
     uint4 v;
     __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&v);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) x[e] = __floats2bfloat162_rn(acc[c * 8 + 2 * e] * inv, acc[c * 8 + 2 * e + 1] * inv);
-    reinterpret_cast<uint4*>(o)[c * 8 + j] = v;
+    for (int e = 0; e < 4; ++e) x[e] = __floats2bfloat162_rn(acc[cc * 8 + 2 * e] * inv, acc[cc * 8 + 2 * e + 1] * inv);
+    reinterpret_cast<uint4*>(o)[cc * 8 + jl] = v;
   }
-  if (lse && j == 0) lse[(int64_t)r * kHeads + h] = L > 0.f ? M + logf(L) : -INFINITY;
+  if (a.lse && jl == 0) a.lse[(int64_t)r * kHeads + h] = L > 0.f ? M + logf(L) : -INFINITY;
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+namespace {
+struct MapKey {
+  const void* ptr;
+  uint64_t rows;
+  bool operator==(const MapKey& o) const { return ptr == o.ptr && rows == o.rows; }
+};
+struct MapCache {
+  std::mutex mu;
+  MapKey key[16] = {};
+  CUtensorMap map[16];
+  int next = 0;
+  // 2-D bf16 tensor [rows, 576] with 1152-byte rows, box {64 columns, box_rows}
+  bool get(const void* ptr, uint64_t rows, uint32_t box_rows, CUtensorMap* out) {
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < 16; ++i)
+      if (key[i] == MapKey{ptr, rows} && key[i].ptr) {
+        *out = map[i];
+        return true;
+      }
+    CUtensorMap m;
+    if (!encode_2d(&m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kRow, rows, kRow * 2, 64, box_rows)) return false;
+    key[next] = MapKey{ptr, rows};
+    map[next] = m;
+    next = (next + 1) % 16;
+    *out = m;
+    return true;
+  }
+};
+MapCache g_kv_maps, g_q_maps;
+}  // namespace
+
+MlaPlan plan_mla(int num_rows, int topk) {
+  MlaPlan p;
+  p.tiles = (topk + mla::kTok - 1) / mla::kTok;
+  p.units = (int64_t)num_rows * p.tiles > INT32_MAX ? INT32_MAX : num_rows * p.tiles;
+  p.ctas = p.units < kMlaCtas ? p.units : kMlaCtas;
+  if (p.ctas < 1) p.ctas = 1;
+  p.workspace_bytes = kWorkspaceHeader + (size_t)2 * p.ctas * kHeads * (kLatent + 2) * sizeof(float);
+  return p;
 }
 
 cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows, const void* q,
                               const int32_t* topk_idx, int topk, float scale, void* out, float* lse,
                               void* workspace, const MlaPlan& plan, cudaStream_t s) {
-  const size_t smem = (size_t)(kHeads + kTileTokens) * kRowPad * 2 + (size_t)kHeads * kTileTokens * 4;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         mla::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  float* part_o = nullptr;
-  float* part_ml = nullptr;
-  if (plan.splits > 1) {
-    part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeader);
-    part_ml = part_o + (size_t)num_rows * plan.splits * kHeads * kLatent;
-  }
-  dim3 grid(plan.splits, num_rows);
-  sparse_mla_kernel<<<grid, kThreadsMla, smem, s>>>(
-      static_cast<const uint4*>(c.latent), ilog2(c.page_size), c.num_pages, m, static_cast<const uint4*>(q), topk_idx,
-      topk, scale, plan.tokens_per_split, plan.splits, static_cast<__nv_bfloat16*>(out), lse, part_o, part_ml);
+  CUtensorMap kv_map, q_map;
+  if (!g_kv_maps.get(c.latent, (uint64_t)c.num_pages * c.page_size, 1, &kv_map)) return cudaErrorInvalidValue;
+  if (!g_q_maps.get(q, (uint64_t)num_rows * kHeads, 64, &q_map)) return cudaErrorInvalidValue;
+  uint32_t* err = static_cast<uint32_t*>(workspace);
+  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  MlaArgs a;
+  a.m = m;
+  a.topk_idx = topk_idx;
+  a.topk = topk;
+  a.tiles = plan.tiles;
+  a.units = plan.units;
+  a.ctas = plan.ctas;
+  a.log2_page = ilog2(c.page_size);
+  a.num_pages = c.num_pages;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeader);
+  a.part_ml = a.part_o + (size_t)2 * plan.ctas * kHeads * kLatent;
+  a.err = err;
+  sparse_mla_tc_kernel<<<plan.ctas, mla::kThreads, mla::kSmemBytes, s>>>(kv_map, q_map, a);
   count_launches(1);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || plan.splits == 1) return e;
-  mla_merge_kernel<<<num_rows, kThreadsMla, 0, s>>>(part_o, part_ml, plan.splits, static_cast<__nv_bfloat16*>(out), lse);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mla_merge_kernel<<<num_rows, 512, 0, s>>>(a);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -172,6 +172,41 @@ def test_prequantised_keys_are_copied():
     assert torch.equal(c.index_scales.view(-1)[[0, 9, 31]], scales)
 
 
+def test_selection_order_does_not_matter_and_forces_rescales():
+    """The index buffer is a set: entries sorted by ascending score make every later tile raise the
+    running maximum (so the accumulator is rescaled several times) and must give the oracle's result."""
+    import torch
+    wl = wlm.Workload("rescale", [5000, 4100], [1, 1], 64, "bf16", 2048, 1, 3008)
+    hp = HostProblem(wl)
+    gp = GpuProblem(hp)
+    gp.append_step()
+    o_idx, _ = hp.oracle_topk()
+    q = o.bf16_to_f64(hp.q[0])
+    ordered = o_idx.copy()
+    for r in range(wl.num_rows):
+        sel = o_idx[r]
+        rows = hp.caches[0].latent_rows(wl.block_table[r], sel)
+        z0 = rows @ q[r, 0]                                   # head 0's logits
+        ordered[r] = sel[np.argsort(z0)]
+    out, lse = gp.attention(0, torch.from_numpy(ordered).cuda())
+    o_out, o_lse = hp.oracle_attention(0, o_idx)
+    check_attention(bf16_tensor_to_f64(out), lse.cpu().numpy(), o_out, o_lse)
+
+
+def test_device_status_word_is_clear_after_calls():
+    """Kernels record bounded-wait timeouts in the first word of the workspace; a normal call leaves 0."""
+    import torch
+    import deepseek_sparse_mla_gb300 as dsa
+    wl = wlm.reduced("decode_b64_fp8_indexshare")
+    gp = GpuProblem(HostProblem(wl))
+    gp.append_step()
+    idx, _ = gp.indexer()
+    ws = torch.full((dsa.mla_workspace_bytes(wl.num_rows, wl.topk),), 0xFF, dtype=torch.uint8, device="cuda")
+    dsa.sparse_mla_decode(gp.caches[1], gp.batch, gp.q[1], idx, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0
+
+
 def test_results_are_deterministic_across_calls():
     import torch
     wl = wlm.reduced("decode_b64_fp8_indexshare")
