@@ -48,7 +48,9 @@ IndexerPlan plan_indexer(int num_rows, int max_seq_len, int topk) {
   if (fit < 1) fit = 1;
   p.rows_per_block = (int)(num_rows < fit ? num_rows : fit);
   if (p.rows_per_block < 1) p.rows_per_block = 1;
-  p.workspace_bytes = kWorkspaceHeader + (size_t)p.rows_per_block * (size_t)per_row;
+  p.groups_offset = kWorkspaceHeader;
+  p.scores_offset = p.groups_offset + ((size_t)(4 + 3 * p.rows_per_block) * sizeof(int32_t) + 255) / 256 * 256;
+  p.workspace_bytes = p.scores_offset + (size_t)p.rows_per_block * (size_t)per_row;
   return p;
 }
 
@@ -216,12 +218,18 @@ dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_batch* batc
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(DSA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
   RowMeta m = row_meta(batch, batch->query_start_loc == nullptr);
   cudaStream_t s = (cudaStream_t)stream;
-  float* block = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeader);
+  char* ws = static_cast<char*>(workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+  int32_t* groups = reinterpret_cast<int32_t*>(ws + plan.groups_offset);
+  float* block = reinterpret_cast<float*>(ws + plan.scores_offset);
+  cudaError_t e0 = cudaMemsetAsync(err, 0, sizeof(uint32_t), s);
+  if (e0 != cudaSuccess) return cuda_status(e0, "workspace status reset");
   for (int row0 = 0; row0 < batch->num_rows; row0 += plan.rows_per_block) {
     int n = batch->num_rows - row0 < plan.rows_per_block ? batch->num_rows - row0 : plan.rows_per_block;
     float* scores = scores_out ? scores_out + (int64_t)row0 * batch->max_seq_len : block;
     int64_t stride = scores_out ? (int64_t)batch->max_seq_len : plan.score_stride;
-    cudaError_t e = launch_indexer_scores(*owner, m, row0, n, batch->max_seq_len, q_idx, w, scores, stride, s);
+    cudaError_t e = launch_indexer_scores(*owner, m, row0, n, batch->max_seq_len, q_idx, w, scores, stride,
+                                          scores_out != nullptr, groups, err, s);
     if (e != cudaSuccess) return cuda_status(e, "indexer launch");
     e = launch_topk(m, row0, n, scores, stride, batch->max_seq_len, topk, topk_idx, s);
     if (e != cudaSuccess) return cuda_status(e, "top-k launch");

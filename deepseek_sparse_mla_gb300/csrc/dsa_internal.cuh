@@ -29,6 +29,8 @@ constexpr size_t kWorkspaceHeader = 256;
 struct IndexerPlan {
   int64_t score_stride;   // floats per row in the score block
   int rows_per_block;     // rows scored and selected per pass
+  size_t groups_offset;   // int32 scratch of 4 + 3 * rows_per_block entries (row groups)
+  size_t scores_offset;   // fp32 score block [rows_per_block][score_stride]
   size_t workspace_bytes;
 };
 IndexerPlan plan_indexer(int num_rows, int max_seq_len, int topk);
@@ -59,9 +61,11 @@ struct RowMeta {
   int32_t block_table_stride;
 };
 
+// Scores of rows [row0, row0 + nrows) into scores[(r - row0) * score_stride + s].  group_scratch holds
+// 4 + 3 * nrows ints; err is the device status word; fill_tail writes -inf past each row's last key tile.
 cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0, int nrows, int max_seq_len,
                                   const void* q_idx, const float* w, float* scores, int64_t score_stride,
-                                  cudaStream_t s);
+                                  bool fill_tail, int32_t* group_scratch, uint32_t* err, cudaStream_t s);
 
 cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scores, int64_t score_stride,
                         int max_seq_len, int topk, int32_t* topk_idx, cudaStream_t s);
