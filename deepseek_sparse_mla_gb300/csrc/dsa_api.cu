@@ -49,7 +49,7 @@ IndexerPlan plan_indexer(int num_rows, int max_seq_len, int topk) {
   p.rows_per_block = (int)(num_rows < fit ? num_rows : fit);
   if (p.rows_per_block < 1) p.rows_per_block = 1;
   p.groups_offset = kWorkspaceHeader;
-  p.scores_offset = p.groups_offset + ((size_t)(4 + 3 * p.rows_per_block) * sizeof(int32_t) + 255) / 256 * 256;
+  p.scores_offset = p.groups_offset + ((size_t)(4 + 5 * p.rows_per_block + 1) * sizeof(int32_t) + 255) / 256 * 256;
   p.workspace_bytes = p.scores_offset + (size_t)p.rows_per_block * (size_t)per_row;
   return p;
 }
@@ -71,8 +71,8 @@ static dsa_status check_cache(const dsa_cache* c, bool need_keys) {
       return fail(DSA_ERR_INVALID_ARG, "e4m3 index keys need cache.index_scales");
     if (c->key_format == DSA_KEY_BF16 && c->index_scales)
       return fail(DSA_ERR_INVALID_ARG, "bf16 index keys take no cache.index_scales (layouts are not interchangeable)");
-    if (c->index_scales && (reinterpret_cast<uintptr_t>(c->index_scales) & 3u))
-      return fail(DSA_ERR_INVALID_ARG, "cache.index_scales is not 4-byte aligned");
+    if (c->index_scales && (reinterpret_cast<uintptr_t>(c->index_scales) & 15u))
+      return fail(DSA_ERR_INVALID_ARG, "cache.index_scales is not 16-byte aligned");
   } else if (need_keys) {
     return fail(DSA_ERR_INVALID_ARG,
                 "layer has no indexer keys (cache.index_keys is NULL): a shared layer must reuse the owner's "

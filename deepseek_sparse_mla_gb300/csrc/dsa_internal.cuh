@@ -29,7 +29,7 @@ constexpr size_t kWorkspaceHeader = 256;
 struct IndexerPlan {
   int64_t score_stride;   // floats per row in the score block
   int rows_per_block;     // rows scored and selected per pass
-  size_t groups_offset;   // int32 scratch of 4 + 3 * rows_per_block entries (row groups)
+  size_t groups_offset;   // int32 scratch: 4 counts, rows_per_block int4 groups, rows_per_block + 1 tile offsets
   size_t scores_offset;   // fp32 score block [rows_per_block][score_stride]
   size_t workspace_bytes;
 };
@@ -62,7 +62,7 @@ struct RowMeta {
 };
 
 // Scores of rows [row0, row0 + nrows) into scores[(r - row0) * score_stride + s].  group_scratch holds
-// 4 + 3 * nrows ints; err is the device status word; fill_tail writes -inf past each row's last key tile.
+// 4 + 5 * nrows + 1 ints; err is the device status word; fill_tail writes -inf past each row's last key tile.
 cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0, int nrows, int max_seq_len,
                                   const void* q_idx, const float* w, float* scores, int64_t score_stride,
                                   bool fill_tail, int32_t* group_scratch, uint32_t* err, cudaStream_t s);

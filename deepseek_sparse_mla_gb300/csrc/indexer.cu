@@ -35,10 +35,11 @@ using namespace sm100;
 
 namespace idx {
 constexpr int kTileKeys = 128;
-constexpr int kThreads = 192;
+constexpr int kProducers = 3;                      // warps issuing the key copies (TMA issue is per-warp limited)
+constexpr int kThreads = 32 * (kProducers + 2 + 8);  // producers, MMA, B loader, two epilogue warpgroups
 constexpr int kBBytes = 65536;                      // up to 256 (row, head) query vectors of 128 bf16/f16
-constexpr int kRingBytes = 131072;                  // key stages
-constexpr int kSmemBytes = kBBytes + kRingBytes + 8 * 512 + 1024;
+constexpr int kRingBytes = 98304;                   // key stages: 6 x 16 KB e4m3 or 3 x 32 KB bf16
+constexpr int kSmemBytes = kBBytes + kRingBytes + 6 * 512 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPolls = 1u << 22;
 constexpr int kMaxRows = 8;
@@ -47,12 +48,12 @@ constexpr int kGroupCache = 1024;                    // group descriptors staged
 
 struct IdxArgs {
   RowMeta m;
-  const int32_t* groups;         // [max_groups][3] = (request, first row, rows); nullptr in decode
-  const int32_t* n_groups;       // device count of groups (nullptr in decode)
+  const int4* groups;            // [n][ (request, first row, rows, position of the first row) ]
+  const int32_t* tile_start;     // [n + 1] exclusive prefix of each group's key tiles
+  const int32_t* counts;         // [0] = groups, [1] = total key tiles
   int max_groups;
-  int row0, nrows_block;         // rows this launch scores; scores row (r - row0)
-  int block_tiles;               // key tiles per work unit
-  int key_blocks;                // ceil(max_seq_len / (128 * block_tiles))
+  int row0;                      // scores row = r - row0
+  int rows_per_group;            // rows of one group at most (1 in decode)
   int log2_page, num_pages, box_rows;
   const float* key_scales;       // e4m3 keys only
   const __nv_bfloat16* q_idx;
@@ -63,397 +64,502 @@ struct IdxArgs {
   uint32_t* err;
 };
 
-struct GroupInfo {
-  int req, row, nrows, pos_first;
+// Walks one CTA's contiguous range of the flattened (group, key tile) list.
+struct TileCursor {
+  int tau, tau_end;      // flattened tile index and end of this CTA's range
+  int g, g_end_tile;     // current group and the flattened index where it ends
+  int4 G;                // (request, first row, rows, first position) of group g
+  int t;                 // key tile within the group
+  __device__ bool valid() const { return tau < tau_end; }
 };
 
-__device__ __forceinline__ bool load_group_global(const IdxArgs& a, int g, GroupInfo& G) {
-  if (a.groups == nullptr) {
-    if (g >= a.nrows_block) return false;
-    G.row = a.row0 + g;
-    G.req = G.row;
-    G.nrows = 1;
-    G.pos_first = a.m.seq_lens[G.req] - 1;
-    return true;
+__device__ __forceinline__ int4 group_at(const IdxArgs& a, const int4* gcache, int g) {
+  return g < idx::kGroupCache ? gcache[g] : a.groups[g];
+}
+
+__device__ __forceinline__ int tile_start_at(const IdxArgs& a, const int* tcache, int g) {
+  return g <= idx::kGroupCache ? tcache[g] : a.tile_start[g];
+}
+
+__device__ __forceinline__ void cursor_init(TileCursor& c, const IdxArgs& a, const int4* gcache, const int* tcache,
+                                            int ngroups, int tau0, int tau1) {
+  c.tau = tau0;
+  c.tau_end = tau1;
+  if (tau0 >= tau1) return;
+  int lo = 0, hi = ngroups - 1;          // last group whose first tile is <= tau0
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_start_at(a, tcache, mid) <= tau0) lo = mid; else hi = mid - 1;
   }
-  if (g >= *a.n_groups) return false;
-  G.req = a.groups[3 * g];
-  G.row = a.groups[3 * g + 1];
-  G.nrows = a.groups[3 * g + 2];
-  const int q0 = a.m.query_start_loc[G.req], q1 = a.m.query_start_loc[G.req + 1];
-  G.pos_first = a.m.seq_lens[G.req] - (q1 - q0) + (G.row - q0);
+  c.g = lo;
+  while (tile_start_at(a, tcache, c.g + 1) <= tau0) ++c.g;   // skip groups without tiles
+  c.g_end_tile = tile_start_at(a, tcache, c.g + 1);
+  c.G = group_at(a, gcache, c.g);
+  c.t = tau0 - tile_start_at(a, tcache, c.g);
+}
+
+// Advance one tile; returns true when the next tile starts a new group.
+__device__ __forceinline__ bool cursor_next(TileCursor& c, const IdxArgs& a, const int4* gcache, const int* tcache) {
+  ++c.tau;
+  ++c.t;
+  if (c.tau < c.g_end_tile || c.tau >= c.tau_end) return false;
+  do {
+    ++c.g;
+    c.g_end_tile = tile_start_at(a, tcache, c.g + 1);
+  } while (c.g_end_tile <= c.tau);
+  c.G = group_at(a, gcache, c.g);
+  c.t = 0;
   return true;
 }
 
-// Group g from the shared-memory copy (nrows == 0 marks a missing group) or from global memory.
-__device__ __forceinline__ bool load_group(const IdxArgs& a, const int4* gcache, int g, GroupInfo& G) {
-  if (g < idx::kGroupCache) {
-    const int4 v = gcache[g];
-    G.req = v.x;
-    G.row = v.y;
-    G.nrows = v.z;
-    G.pos_first = v.w;
-    return v.z > 0;
+
+// Exponent that moves a (row, head) query vector into the e4m3 split range: with q' = q * 2^(7-e),
+// max |q'| lies in [128, 256).  q' = t1 + t2/16 with t1 = e4m3(q') and t2 = e4m3(16 (q' - t1)) is exact
+// for every element above the e4m3 subnormal range (the rounding residual of a 4-bit mantissa has at
+// most 4 significant bits), so the score needs no f16/bf16 operand.  Returns e; raw gets the query.
+__device__ __forceinline__ int query_exponent(const IdxArgs& a, int row, int h, uint4 (&raw)[16]) {
+  const __nv_bfloat16* qv = a.q_idx + ((int64_t)row * kIndexHeads + h) * kIndexDim;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) raw[c] = reinterpret_cast<const uint4*>(qv)[c];
+  float amax = 0.f;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&raw[c]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(x[e]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
   }
-  return load_group_global(a, g, G);
+  return amax > 0.f ? ilogbf(amax) : 0;
 }
 
-// Tiles [t_begin, t_end) of work unit u, or false when the unit has no visible key.
-__device__ __forceinline__ bool unit_tiles(const IdxArgs& a, const int4* gcache, int u, GroupInfo& G, int& t_begin,
-                                           int& t_end) {
-  const int g = u / a.key_blocks, kb = u - g * a.key_blocks;
-  if (!load_group(a, gcache, g, G)) return false;
-  const int pos_last = G.pos_first + G.nrows - 1;
-  if (pos_last < 0) return false;
-  t_begin = kb * a.block_tiles;
-  const int tiles_needed = pos_last / idx::kTileKeys + 1;
-  t_end = min(t_begin + a.block_tiles, tiles_needed);
-  return t_begin < t_end;
-}
-
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  return (uint32_t)__nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3) |
+         ((uint32_t)__nv_cvt_float_to_fp8(b, __NV_SATFINITE, __NV_E4M3) << 8) |
+         ((uint32_t)__nv_cvt_float_to_fp8(c, __NV_SATFINITE, __NV_E4M3) << 16) |
+         ((uint32_t)__nv_cvt_float_to_fp8(d, __NV_SATFINITE, __NV_E4M3) << 24);
 }
 
 template <bool kFp8>
 __global__ void __launch_bounds__(idx::kThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap key_map, const IdxArgs a) {
   using namespace idx;
-  constexpr int kStages = kFp8 ? 8 : 4;
+  constexpr int kStages = kFp8 ? 6 : 3;
   constexpr int kStageBytes = kFp8 ? 16384 : 32768;
   constexpr int kRowsMax = kFp8 ? 4 : 8;
+  constexpr int kTerms = kFp8 ? 2 : 1;               // B rows per (row, head): e4m3 split terms
+  constexpr int kLoaderWarp = kProducers + 1;
+  constexpr int kEpiWarp0 = kProducers + 2;           // two epilogue warpgroups take alternate tiles
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sB = smem;
   uint8_t* sRing = smem + kBBytes;
-  float* sScale = reinterpret_cast<float*>(sRing + kRingBytes);        // [kStages][128] (e4m3 keys)
+  float* sScale = reinterpret_cast<float*>(sRing + kStages * kStageBytes);   // [kStages][128] staged by copies
 
   __shared__ uint64_t st_full[kStages], st_empty[kStages];
-  __shared__ uint64_t a_full[2], a_empty[2], d_full[2], d_empty[2], b_full, b_empty, mma_done;
-  __shared__ float wq[2][kMaxRows][32];     // head weights (times the query prescale) per unit parity
+  __shared__ uint64_t d_full[4], d_empty[4], b_full[2], b_empty[2];
+  __shared__ uint64_t mma_done;
+  __shared__ float wq_e[2][kMaxRows][32];   // each epilogue warpgroup's head weights for its current group
   __shared__ int4 gcache[kGroupCache];
+  __shared__ int tcache[kGroupCache + 1];
   __shared__ uint32_t tmem_base;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int units = a.max_groups * a.key_blocks;
   const uint32_t box_bytes = (uint32_t)a.box_rows * 128u;
   const int loads_per_tile = kTileKeys / a.box_rows;
+  const int ngroups = a.counts[0], total_tiles = a.counts[1];
+  const int tau0 = (int)(((int64_t)blockIdx.x * total_tiles) / gridDim.x);
+  const int tau1 = (int)(((int64_t)(blockIdx.x + 1) * total_tiles) / gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&st_full[s], 1);
-      mbar_init(&st_empty[s], kFp8 ? 4 : 1);
+      mbar_init(&st_empty[s], kFp8 ? 2 : 1);       // the MMA (+ the epilogue that reads the scales)
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&a_full[b], 4);
-      mbar_init(&a_empty[b], 1);
+    for (int b = 0; b < 4; ++b) {
       mbar_init(&d_full[b], 1);
       mbar_init(&d_empty[b], 4);
     }
-    mbar_init(&b_full, 1);
-    mbar_init(&b_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&b_full[b], 1);
+      mbar_init(&b_empty[b], 1);
+    }
     mbar_init(&mma_done, 1);
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kProducers) {
     tmem_alloc(&tmem_base, kTmemCols);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) prefetch_tmap(&key_map);
-  for (int g = threadIdx.x; g < kGroupCache; g += blockDim.x) {
-    GroupInfo G;
-    int4 v = make_int4(0, 0, 0, 0);
-    if (g < a.max_groups && load_group_global(a, g, G)) v = make_int4(G.req, G.row, G.nrows, G.pos_first);
-    gcache[g] = v;
+  for (int g = threadIdx.x; g <= kGroupCache; g += blockDim.x) {
+    if (g < kGroupCache) gcache[g] = g < ngroups ? a.groups[g] : make_int4(0, 0, 0, 0);
+    tcache[g] = g <= ngroups ? a.tile_start[g] : total_tiles;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  // TMEM: e4m3 -> A buffers at columns 0 / 64 and D buffers at 128 / 256; bf16 -> D at 0 / 256
-  const uint32_t colA = 0;
-  const uint32_t colD = kFp8 ? 128u : 0u, strideD = kFp8 ? 128u : 256u;
+  const int n_cap = 32 * kTerms * a.rows_per_group;                // D buffer width (columns)
+  const int DD = min(4, 512 / n_cap);                               // D ring depth
+  const int row_bytes = kFp8 ? 128 : 256;                           // one query vector in B
+  const int nB = n_cap * row_bytes <= kBBytes / 2 ? 2 : 1;         // B buffers (queries of one group each)
+  const int b_bytes = kBBytes / nB;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ producer
-    int tiles = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      GroupInfo G;
-      int tb, te;
-      if (!unit_tiles(a, gcache, u, G, tb, te)) continue;
-      const int pos_last = G.pos_first + G.nrows - 1;
-      const int32_t* bt = a.m.block_table + (int64_t)G.req * a.m.block_table_stride;
-      for (int t = tb; t < te; ++t, ++tiles) {
-        const int s = tiles % kStages, n = tiles / kStages;
-        if (n > 0 && !mbar_wait(&st_empty[s], (n - 1) & 1, a.err, kErrMmaTimeout, kPolls)) { ok = false; break; }
-        const int k0 = t * kTileKeys;
-        uint8_t* stage = sRing + s * kStageBytes;
-        // page of each sub-box; a box past the row's last key, or on a bad page, is not loaded
-        uint32_t nvalid = 0;
-        for (int i0 = 0; i0 < loads_per_tile; i0 += 32) {
-          const int i = i0 + lane;
-          bool v = false;
-          if (i < loads_per_tile) {
-            const int key = k0 + i * a.box_rows;
-            const int lp = key >> a.log2_page;
-            if (key <= pos_last && lp < a.m.block_table_stride) {
-              const int page = bt[lp];
-              v = page >= 0 && page < a.num_pages;
-              if (!v) atomicOr(a.err, kErrBadPage);
-            }
-          }
-          nvalid += __popc(__ballot_sync(0xffffffffu, v));
-        }
-        if (kFp8) {
-          float* sc = sScale + s * kTileKeys;
-          for (int k = lane; k < kTileKeys; k += 32) {
-            const int key = k0 + k;
-            const int lp = key >> a.log2_page;
-            float v = 0.f;
-            if (key <= pos_last && lp < a.m.block_table_stride) {
-              const int page = bt[lp];
-              if (page >= 0 && page < a.num_pages)
-                v = a.key_scales[((int64_t)page << a.log2_page) + (key & ((1 << a.log2_page) - 1))];
-            }
-            sc[k] = v;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&st_full[s], nvalid * box_bytes * (kFp8 ? 1u : 2u));
-        __syncwarp();
-        for (int i = lane; i < loads_per_tile; i += 32) {
-          const int key = k0 + i * a.box_rows;
-          const int lp = key >> a.log2_page;
-          if (key > pos_last || lp >= a.m.block_table_stride) continue;
-          const int page = bt[lp];
-          if (page < 0 || page >= a.num_pages) continue;
-          const int y = (page << a.log2_page) + (key & ((1 << a.log2_page) - 1));
-          tma_load_2d(stage + i * box_bytes, &key_map, 0, y, &st_full[s]);
-          if (!kFp8) tma_load_2d(stage + 16384 + i * box_bytes, &key_map, 64, y, &st_full[s]);
+  if (warp < kProducers) {
+    // ------------------------------------------------------------------ producers (tiles round-robin)
+    // Each warp keeps a register window of 32 page ids (one per lane) and loads the next window
+    // ahead of use, so page-table reads never sit between a free stage and its copy.
+    const bool bulk_scales = kFp8 && a.box_rows >= 4;
+    const uint32_t tile_tx = (kFp8 ? 1u : 2u) * box_bytes + (bulk_scales ? (uint32_t)a.box_rows * 4u : 0u);
+    const bool windowed = loads_per_tile <= 32;
+    TileCursor cur;
+    cursor_init(cur, a, gcache, tcache, ngroups, tau0, tau1);
+    int win_base = -1, win_req = -1, win_page = -1, nxt_page = -1;
+    int last_tile = -1;
+    for (int i = 0; cur.valid(); ++i, cursor_next(cur, a, gcache, tcache)) {
+      if (i % kProducers != warp) continue;
+      const int s = i % kStages, n = i / kStages;
+      const int req = cur.G.x, pos_last = cur.G.w + cur.G.z - 1;
+      const int32_t* bt = a.m.block_table + (int64_t)req * a.m.block_table_stride;
+      const int k0 = cur.t * kTileKeys;
+      const int lp_first = k0 >> a.log2_page;
+      if (windowed) {
+        const int lp_last = (k0 + kTileKeys - 1) >> a.log2_page;
+        if (req != win_req || lp_first < win_base || lp_last >= win_base + 64) {
+          win_req = req;
+          win_base = lp_first;
+          const int l0 = win_base + lane, l1 = win_base + 32 + lane;
+          win_page = l0 < a.m.block_table_stride ? bt[l0] : -1;
+          nxt_page = l1 < a.m.block_table_stride ? bt[l1] : -1;
+        } else if (lp_last >= win_base + 32) {
+          // slide by one window: the next one was loaded a window ago
+          win_base += 32;
+          win_page = nxt_page;
+          const int l1 = win_base + 32 + lane;
+          nxt_page = l1 < a.m.block_table_stride ? bt[l1] : -1;
         }
       }
+      auto page_of = [&](int lp) -> int {      // called by all 32 lanes together
+        if (windowed) {
+          const int off = lp - win_base;
+          const int v0 = __shfl_sync(0xffffffffu, win_page, off & 31), v1 = __shfl_sync(0xffffffffu, nxt_page, off & 31);
+          if (lp >= a.m.block_table_stride) return -1;
+          return off < 32 ? v0 : v1;
+        }
+        return lp < a.m.block_table_stride ? bt[lp] : -1;
+      };
+      if (n > 0 && !mbar_wait(&st_empty[s], (n - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
+      uint8_t* stage = sRing + s * kStageBytes;
+      float* sc = sScale + s * kTileKeys;
+      // sub-box j holds keys k0 + j*box_rows ..; it is loaded when it starts at a visible key of a valid page
+      uint32_t nvalid = 0;
+      int my_page[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        my_page[q] = -1;
+        const int j0 = 32 * q;
+        if (j0 < loads_per_tile) {
+          const int j = j0 + lane;
+          const int key = k0 + j * a.box_rows;
+          const int page = page_of(key >> a.log2_page);     // every lane takes part in the shuffles
+          bool v = false;
+          if (j < loads_per_tile && key <= pos_last) {
+            v = page >= 0 && page < a.num_pages;
+            if (!v) atomicOr(a.err, kErrBadPage);
+          }
+          my_page[q] = v ? page : -1;
+          nvalid += __popc(__ballot_sync(0xffffffffu, v));
+        }
+      }
+      if (kFp8 && !bulk_scales) {        // pages of fewer than 4 keys: scales through registers
+        for (int k = lane; k < kTileKeys; k += 32) {
+          const int key = k0 + k;
+          const int lp = key >> a.log2_page;
+          float v = 0.f;
+          if (key <= pos_last && lp < a.m.block_table_stride) {
+            const int page = bt[lp];
+            if (page >= 0 && page < a.num_pages)
+              v = a.key_scales[((int64_t)page << a.log2_page) + (key & ((1 << a.log2_page) - 1))];
+          }
+          sc[k] = v;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&st_full[s], nvalid * tile_tx);
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = 32 * q + lane;
+        const int page = my_page[q];
+        if (page < 0) continue;
+        const int key = k0 + j * a.box_rows;
+        const int y = (page << a.log2_page) + (key & ((1 << a.log2_page) - 1));
+        tma_load_2d(stage + j * box_bytes, &key_map, 0, y, &st_full[s]);
+        if (!kFp8) tma_load_2d(stage + 16384 + j * box_bytes, &key_map, 64, y, &st_full[s]);
+        if (bulk_scales) bulk_load(sc + j * a.box_rows, a.key_scales + y, (uint32_t)a.box_rows * 4u, &st_full[s]);
+      }
+      last_tile = i;
     }
-    // drain: no copy may still be in flight at exit
-    for (int s = 0; s < kStages; ++s) {
-      const int uses = tiles / kStages + (s < tiles % kStages ? 1 : 0);
-      if (uses > 0) mbar_wait(&st_full[s], (uses - 1) & 1, a.err, kErrTmaTimeout, kPolls);
-    }
-  } else if (warp == 1) {
+    // drain: no copy of this warp may still be in flight at exit
+    if (last_tile >= 0) mbar_wait(&st_full[last_tile % kStages], (last_tile / kStages) & 1, a.err, kErrTmaTimeout, kPolls);
+  } else if (warp == kProducers) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int tiles = 0, unit_count = 0;
-      bool ok = true;
-      const uint32_t b_addr = smem_u32(sB);
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        GroupInfo G;
-        int tb, te;
-        if (!unit_tiles(a, gcache, u, G, tb, te)) continue;
-        const int N = 32 * G.nrows;
-        const uint32_t idesc = idesc_f16(128, N, !kFp8, !kFp8, false, false);
-        if (!mbar_wait(&b_full, unit_count & 1, a.err, kErrMmaTimeout, kPolls)) { ok = false; break; }
-        for (int t = tb; t < te; ++t, ++tiles) {
-          const int s = tiles % kStages, n = tiles / kStages, ab = tiles & 1, nb = tiles >> 1;
-          if (kFp8) {
-            if (!mbar_wait(&a_full[ab], nb & 1, a.err, kErrMmaTimeout, kPolls)) { ok = false; break; }
-          } else {
-            if (!mbar_wait(&st_full[s], n & 1, a.err, kErrTmaTimeout, kPolls)) { ok = false; break; }
+      TileCursor cur;
+      cursor_init(cur, a, gcache, tcache, ngroups, tau0, tau1);
+      int gcount = 0;
+      bool ok = true, new_group = true;
+      uint32_t b_addr = 0, idesc = 0;
+      int N = 0, ub = 0;
+      for (int i = 0; cur.valid() && ok; ++i) {
+        if (new_group) {
+          if (i > 0) {
+            mma_commit(&b_empty[ub]);
+            ++gcount;
           }
-          if (nb > 0 && !mbar_wait(&d_empty[ab], (nb - 1) & 1, a.err, kErrMmaTimeout, kPolls)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t d = tmem + colD + ab * strideD;
-          const uint32_t stage = smem_u32(sRing + s * kStageBytes);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t bd = smem_desc(b_addr + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-            if (kFp8) {
-              mma_ts(d, tmem + colA + 64 * ab + 8 * kk, bd, idesc, kk > 0);
-            } else {
-              const uint64_t ad = smem_desc(stage + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-              mma_ss(d, ad, bd, idesc, kk > 0);
-            }
-          }
-          mma_commit(&d_full[ab]);
-          if (kFp8) mma_commit(&a_empty[ab]);
-          else mma_commit(&st_empty[s]);
+          N = 32 * kTerms * cur.G.z;
+          idesc = kFp8 ? idesc_e4m3(128, N) : idesc_f16(128, N, true, true, false, false);
+          ub = gcount % nB;
+          if (!mbar_wait(&b_full[ub], (gcount / nB) & 1, a.err, kErrMmaTimeout, kPolls)) { ok = false; break; }
+          b_addr = smem_u32(sB + ub * b_bytes);
         }
-        if (!ok) break;
-        mma_commit(&b_empty);
-        ++unit_count;
+        const int s = i % kStages, n = i / kStages, db = i % DD, nd = i / DD;
+        if (!mbar_wait(&st_full[s], n & 1, a.err, kErrTmaTimeout, kPolls)) { ok = false; break; }
+        if (nd > 0 && !mbar_wait(&d_empty[db], (nd - 1) & 1, a.err, kErrMmaTimeout, kPolls)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + db * (uint32_t)n_cap;
+        const uint32_t stage = smem_u32(sRing + s * kStageBytes);
+        if (kFp8) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss_f8(d, smem_desc(stage + kk * 32, 16, 1024, kSwizzle128B),
+                      smem_desc(b_addr + kk * 32, 16, 1024, kSwizzle128B), idesc, kk > 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(d, smem_desc(stage + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B),
+                   smem_desc(b_addr + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B), idesc, kk > 0);
+        }
+        mma_commit(&d_full[db]);
+        mma_commit(&st_empty[s]);
+        new_group = cursor_next(cur, a, gcache, tcache);
       }
       mma_commit(&mma_done);
       mbar_wait(&mma_done, 0, a.err, kErrMmaTimeout, kPolls);
     }
+  } else if (warp == kLoaderWarp) {
+    // ------------------------------------------------------------------ B loader: each group's queries
+    TileCursor cur;
+    cursor_init(cur, a, gcache, tcache, ngroups, tau0, tau1);
+    int gcount = 0;
+    bool new_group = true;
+    for (int i = 0; cur.valid(); ++i) {
+      if (new_group) {
+        const int N = 32 * kTerms * cur.G.z, ub = gcount % nB;
+        uint8_t* bbuf = sB + ub * b_bytes;
+        if (gcount >= nB && !mbar_wait(&b_empty[ub], (gcount / nB - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
+        for (int p = lane; p < 32 * cur.G.z; p += 32) {
+          const int rr = p >> 5, h = p & 31;
+          uint4 raw[16];
+          if (kFp8) {
+            const int e = query_exponent(a, cur.G.y + rr, h, raw);
+            const float up = ldexpf(1.f, 7 - e);
+            const int n_hi = rr * 64 + h, n_lo = rr * 64 + 32 + h;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {        // 16-byte units of the 128-byte e4m3 rows
+              uint32_t t1[4], t2[4];
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw[2 * c + half]);
+#pragma unroll
+                for (int e2 = 0; e2 < 2; ++e2) {
+                  const float2 f0 = __bfloat1622float2(v[2 * e2]), f1 = __bfloat1622float2(v[2 * e2 + 1]);
+                  const float x[4] = {f0.x * up, f0.y * up, f1.x * up, f1.y * up};
+                  float r[4];
+#pragma unroll
+                  for (int z = 0; z < 4; ++z) {
+                    const float v1 = __half2float(__nv_cvt_fp8_to_halfraw(
+                        __nv_cvt_float_to_fp8(x[z], __NV_SATFINITE, __NV_E4M3), __NV_E4M3));
+                    r[z] = (x[z] - v1) * 16.f;
+                  }
+                  t1[2 * half + e2] = e4m3x4(x[0], x[1], x[2], x[3]);
+                  t2[2 * half + e2] = e4m3x4(r[0], r[1], r[2], r[3]);
+                }
+              }
+              *reinterpret_cast<uint4*>(bbuf + sw128_offset(n_hi, c)) = make_uint4(t1[0], t1[1], t1[2], t1[3]);
+              *reinterpret_cast<uint4*>(bbuf + sw128_offset(n_lo, c)) = make_uint4(t2[0], t2[1], t2[2], t2[3]);
+            }
+          } else {
+            const __nv_bfloat16* qv = a.q_idx + ((int64_t)(cur.G.y + rr) * kIndexHeads + h) * kIndexDim;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) raw[c] = reinterpret_cast<const uint4*>(qv)[c];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              *reinterpret_cast<uint4*>(bbuf + (c >> 3) * (N * 128) + sw128_offset(p, c & 7)) = raw[c];
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&b_full[ub]);
+        ++gcount;
+      }
+      new_group = cursor_next(cur, a, gcache, tcache);
+    }
   } else {
-    // ------------------------------------------------------------------ workers: B operand, conversion, epilogue
+    // ------------------------------------------------------------------ epilogues: ReLU . w, scale, mask, store
+    const int eg = (warp - kEpiWarp0) >> 2;          // warpgroup 0 takes even tiles, 1 odd tiles
     const int quarter = warp & 3;
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
-    const int key_local = 32 * quarter + lane;       // TMEM lane = key within the tile
-    const int wt = threadIdx.x - 64;                 // 0..127
-    int tiles = 0, unit_count = 0;
-    bool ok = true;
-    // epilogue state of the tile converted last
-    bool have_prev = false;
-    int prev_tile = 0, prev_k0 = 0, prev_row = 0, prev_rows = 0, prev_pos = 0, prev_par = 0;
-    float prev_scale = 1.f, cur_scale = 1.f;
-
-    auto epilogue = [&](int tile, int k0, int row, int rows, int pos_first, int par, float kscale) -> bool {
-      const int ab = tile & 1, nb = tile >> 1;
-      if (!mbar_wait(&d_full[ab], nb & 1, a.err, kErrMmaTimeout, kPolls)) return false;
-      tc_fence_after();
-      float score[kRowsMax];
-#pragma unroll
-      for (int rr = 0; rr < kRowsMax; ++rr) {
-        score[rr] = 0.f;
-        if (rr < rows) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + colD + ab * strideD + 32 * rr, v);
-          tmem_wait_ld();
-          float acc = 0.f;
-#pragma unroll
-          for (int h = 0; h < 32; ++h) acc = fmaf(wq[par][rr][h], fmaxf(__uint_as_float(v[h]), 0.f), acc);
-          score[rr] = acc * kscale;
+    const int key_local = 32 * quarter + lane;
+    const int et = threadIdx.x - 32 * (kEpiWarp0 + 4 * eg);   // 0..127 within the warpgroup
+    TileCursor cur;
+    cursor_init(cur, a, gcache, tcache, ngroups, tau0, tau1);
+    bool new_group = true;
+    for (int i = 0; cur.valid(); ++i) {
+      if (new_group) {
+        named_bar_sync(2 + eg, 128);                 // the previous group's weights are no longer read
+        for (int p = et; p < 32 * cur.G.z; p += 128) {
+          const int rr = p >> 5, h = p & 31;
+          float wgt = a.w[(int64_t)(cur.G.y + rr) * kIndexHeads + h];
+          if (kFp8) {
+            uint4 raw[16];
+            wgt = ldexpf(wgt, query_exponent(a, cur.G.y + rr, h, raw) - 7);
+          }
+          wq_e[eg][rr][h] = wgt;
         }
+        named_bar_sync(2 + eg, 128);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&d_empty[ab]);
-      const int s = k0 + key_local;
-      if (s < a.max_seq_len) {
+      if ((i & 1) == eg) {
+        const int s = i % kStages, n = i / kStages, db = i % DD, nd = i / DD;
+        if (!mbar_wait(&d_full[db], nd & 1, a.err, kErrMmaTimeout, kPolls)) break;
+        tc_fence_after();
+        float score[kRowsMax];
 #pragma unroll
-        for (int rr = 0; rr < kRowsMax; ++rr)
-          if (rr < rows)
-            a.scores[(int64_t)(row + rr - a.row0) * a.stride + s] = s <= pos_first + rr ? score[rr] : -INFINITY;
-      }
-      return true;
-    };
-
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      GroupInfo G;
-      int tb, te;
-      if (!unit_tiles(a, gcache, u, G, tb, te)) continue;
-      const int par = unit_count & 1;
-      const int N = 32 * G.nrows;
-      // ---- B operand and head weights for this group (after the previous unit's MMAs are done)
-      if (unit_count > 0 && !mbar_wait(&b_empty, (unit_count - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
-      for (int p = wt; p < N; p += 128) {
-        const int rr = p >> 5, h = p & 31;
-        const __nv_bfloat16* qv = a.q_idx + ((int64_t)(G.row + rr) * kIndexHeads + h) * kIndexDim;
-        float wgt = a.w[(int64_t)(G.row + rr) * kIndexHeads + h];
-        uint4 raw[16];
+        for (int rr = 0; rr < kRowsMax; ++rr) {
+          score[rr] = 0.f;
+          if (rr < cur.G.z) {
+            uint32_t v[32];
+            float acc = 0.f;
+            const uint32_t col = tmem + lane_base + db * (uint32_t)n_cap + 32 * kTerms * rr;
+            tmem_ld32(col, v);
+            if (kFp8) {
+              uint32_t lo[32];
+              tmem_ld32(col + 32, lo);
+              tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 16; ++c) raw[c] = reinterpret_cast<const uint4*>(qv)[c];
+              for (int h = 0; h < 32; ++h)
+                acc = fmaf(wq_e[eg][rr][h], fmaxf(fmaf(__uint_as_float(lo[h]), 0.0625f, __uint_as_float(v[h])), 0.f), acc);
+            } else {
+              tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < 32; ++h) acc = fmaf(wq_e[eg][rr][h], fmaxf(__uint_as_float(v[h]), 0.f), acc);
+            }
+            score[rr] = acc;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&d_empty[db]);
         if (kFp8) {
-          float amax = 0.f;
+          // the tile's key scales sit beside its keys; the stage is refilled only after this read
+          if (!mbar_wait(&st_full[s], n & 1, a.err, kErrTmaTimeout, kPolls)) break;
+          const float ks = sScale[s * kTileKeys + key_local];
+          named_bar_sync(4 + eg, 128);
+          if (et == 0) mbar_arrive(&st_empty[s]);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&raw[c]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(x[e]);
-              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-            }
-          }
-          // exact power-of-two move into f16 range: max |q'| in [2^13, 2^14)
-          const int ex = amax > 0.f ? ilogbf(amax) : 0;
-          const float up = ldexpf(1.f, 13 - ex);
-          wgt = ldexpf(wgt, ex - 13);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&raw[c]);
-            uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(x[e]);
-              const __half2 hv = __floats2half2_rn(f.x * up, f.y * up);
-              o[e] = *reinterpret_cast<const uint32_t*>(&hv);
-            }
-            raw[c] = make_uint4(o[0], o[1], o[2], o[3]);
-          }
+          for (int rr = 0; rr < kRowsMax; ++rr) score[rr] *= ks;
         }
+        const int skey = cur.t * kTileKeys + key_local;
+        if (skey < a.max_seq_len) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          *reinterpret_cast<uint4*>(sB + (c >> 3) * (N * 128) + sw128_offset(p, c & 7)) = raw[c];
-        wq[par][rr][h] = wgt;
+          for (int rr = 0; rr < kRowsMax; ++rr)
+            if (rr < cur.G.z)
+              a.scores[(int64_t)(cur.G.y + rr - a.row0) * a.stride + skey] = skey <= cur.G.w + rr ? score[rr] : -INFINITY;
+        }
       }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (wt == 0) mbar_arrive(&b_full);
-
-      for (int t = tb; t < te; ++t, ++tiles) {
-        const int s = tiles % kStages, n = tiles / kStages, ab = tiles & 1, nb = tiles >> 1;
-        if (kFp8) {
-          // ---- convert this tile's e4m3 keys into the TMEM A operand
-          if (!mbar_wait(&st_full[s], n & 1, a.err, kErrTmaTimeout, kPolls)) { ok = false; break; }
-          const uint8_t* stage = sRing + s * kStageBytes;
-          uint4 raw[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4*>(stage + sw128_offset(key_local, c));
-          cur_scale = sScale[s * kTileKeys + key_local];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&st_empty[s]);
-          if (nb > 0 && !mbar_wait(&a_empty[ab], (nb - 1) & 1, a.err, kErrMmaTimeout, kPolls)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t o[32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const uint4 v = raw[half * 4 + c];
-              o[8 * c + 0] = e4m3x2_to_f16x2(v.x);
-              o[8 * c + 1] = e4m3x2_to_f16x2(v.x >> 16);
-              o[8 * c + 2] = e4m3x2_to_f16x2(v.y);
-              o[8 * c + 3] = e4m3x2_to_f16x2(v.y >> 16);
-              o[8 * c + 4] = e4m3x2_to_f16x2(v.z);
-              o[8 * c + 5] = e4m3x2_to_f16x2(v.z >> 16);
-              o[8 * c + 6] = e4m3x2_to_f16x2(v.w);
-              o[8 * c + 7] = e4m3x2_to_f16x2(v.w >> 16);
-            }
-            tmem_st32(tmem + lane_base + colA + 64 * ab + 32 * half, o);
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[ab]);
-        }
-        if (have_prev && !epilogue(prev_tile, prev_k0, prev_row, prev_rows, prev_pos, prev_par, prev_scale)) {
-          ok = false;
-          break;
-        }
-        have_prev = true;
-        prev_tile = tiles;
-        prev_k0 = t * kTileKeys;
-        prev_row = G.row;
-        prev_rows = G.nrows;
-        prev_pos = G.pos_first;
-        prev_par = par;
-        prev_scale = kFp8 ? cur_scale : 1.f;
-      }
-      ++unit_count;
+      new_group = cursor_next(cur, a, gcache, tcache);
     }
-    if (ok && have_prev) epilogue(prev_tile, prev_k0, prev_row, prev_rows, prev_pos, prev_par, prev_scale);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kProducers) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Row groups of one launch: consecutive rows of one request, at most `rg` per group.
-__global__ void indexer_groups_kernel(RowMeta m, int row0, int nrows, int rg, int32_t* groups, int32_t* n_groups) {
-  if (threadIdx.x != 0) return;
-  int g = 0;
-  for (int b = 0; b < m.num_requests; ++b) {
-    const int lo = max(m.query_start_loc[b], row0), hi = min(m.query_start_loc[b + 1], row0 + nrows);
-    for (int r = lo; r < hi; r += rg) {
-      groups[3 * g] = b;
-      groups[3 * g + 1] = r;
-      groups[3 * g + 2] = min(rg, hi - r);
-      ++g;
+// Row groups of rows [row0, row0 + nrows): consecutive rows of one request, at most `rg` per group,
+// each with its count of 128-key tiles, and the exclusive prefix of those counts (one CTA).
+__global__ void __launch_bounds__(1024) indexer_groups_kernel(RowMeta m, int row0, int nrows, int rg, int4* groups,
+                                                              int32_t* tile_start, int32_t* counts) {
+  __shared__ int carry, warp_tot[33];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  // number of groups: in decode one per row; otherwise walk the requests
+  int ngroups = 0;
+  if (m.query_start_loc == nullptr) {
+    ngroups = nrows;
+    for (int g = tid; g < nrows; g += blockDim.x) {
+      const int r = row0 + g;
+      groups[g] = make_int4(r, r, 1, m.seq_lens[r] - 1);
     }
+  } else {
+    if (tid == 0) {
+      int g = 0;
+      for (int b = 0; b < m.num_requests; ++b) {
+        const int q0 = m.query_start_loc[b], q1 = m.query_start_loc[b + 1];
+        const int lo = max(q0, row0), hi = min(q1, row0 + nrows);
+        for (int r = lo; r < hi; r += rg) {
+          groups[g] = make_int4(b, r, min(rg, hi - r), m.seq_lens[b] - (q1 - q0) + (r - q0));
+          ++g;
+        }
+      }
+      carry = g;
+    }
+    __syncthreads();
+    ngroups = carry;
   }
-  *n_groups = g;
+  __syncthreads();
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  // tiles per group and their exclusive prefix, 1024 groups per pass
+  for (int base = 0; base < ngroups; base += blockDim.x) {
+    const int g = base + tid;
+    int tiles = 0;
+    if (g < ngroups) {
+      const int4 G = groups[g];
+      const int pos_last = G.w + G.z - 1;
+      tiles = pos_last < 0 ? 0 : pos_last / idx::kTileKeys + 1;
+    }
+    int inc = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (lane == 31) warp_tot[wid] = inc;
+    __syncthreads();
+    if (wid == 0) {
+      const int x = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+      int xi = x;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, xi, o);
+        if (lane >= o) xi += t;
+      }
+      warp_tot[lane] = xi - x;
+      if (lane == 31) warp_tot[32] = xi;
+    }
+    __syncthreads();
+    if (g < ngroups) tile_start[g] = carry + warp_tot[wid] + inc - tiles;
+    __syncthreads();
+    if (tid == 0) carry += warp_tot[32];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    tile_start[ngroups] = carry;
+    counts[0] = ngroups;
+    counts[1] = carry;
+  }
 }
 
 // -inf for the positions of a caller-visible score row that no tile covered (s beyond the row's last tile).
@@ -535,25 +641,22 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
   if (!g_key_maps.get(c.index_keys, (uint64_t)c.num_pages * c.page_size, c.key_format, box_rows, &map))
     return cudaErrorInvalidValue;
 
+  // group table: counts[4] | groups int4[nrows] | tile_start[nrows + 1]
+  int32_t* counts = group_scratch;
+  int4* groups = reinterpret_cast<int4*>(group_scratch + 4);
+  int32_t* tile_start = group_scratch + 4 + 4 * nrows;
+  const int rg = indexer_rows_per_group(c, decode);
+  indexer_groups_kernel<<<1, 1024, 0, s>>>(m, row0, nrows, rg, groups, tile_start, counts);
+  count_launches(1);
+
   IdxArgs a;
   a.m = m;
-  const int rg = indexer_rows_per_group(c, decode);
-  if (decode) {
-    a.groups = nullptr;
-    a.n_groups = nullptr;
-    a.max_groups = nrows;
-  } else {
-    a.groups = group_scratch + 4;
-    a.n_groups = group_scratch;
-    a.max_groups = nrows;                        // every group holds at least one row
-    indexer_groups_kernel<<<1, 32, 0, s>>>(m, row0, nrows, rg, group_scratch + 4, group_scratch);
-    count_launches(1);
-  }
+  a.groups = groups;
+  a.tile_start = tile_start;
+  a.counts = counts;
+  a.max_groups = nrows;
   a.row0 = row0;
-  a.nrows_block = nrows;
-  // long key blocks amortise the group's query load when requests carry many rows (prefill)
-  a.block_tiles = (!decode && nrows >= 8 * m.num_requests) ? 32 : 8;
-  a.key_blocks = (max_seq_len + idx::kTileKeys * a.block_tiles - 1) / (idx::kTileKeys * a.block_tiles);
+  a.rows_per_group = rg;
   a.log2_page = ilog2(c.page_size);
   a.num_pages = c.num_pages;
   a.box_rows = (int)box_rows;
@@ -564,8 +667,7 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
   a.stride = score_stride;
   a.max_seq_len = max_seq_len;
   a.err = err;
-  const int64_t units = (int64_t)a.max_groups * a.key_blocks;
-  const int grid = (int)(units < g_sm_count ? units : g_sm_count);
+  const int grid = g_sm_count;
   if (fp8)
     indexer_tc_kernel<true><<<grid, idx::kThreads, idx::kSmemBytes, s>>>(map, a);
   else

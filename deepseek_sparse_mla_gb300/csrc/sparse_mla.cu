@@ -14,16 +14,18 @@
 // one CTA per SM).  A row cut between CTAs is finished by an LSE merge of the
 // pieces; a row inside one CTA is written directly.
 //
-// Per CTA (192 threads):
-//   warp 0     producer: TMA-loads the row's 64 x 576 query (9 boxes of 64
-//              heads x 64 columns) and gathers each tile's 64 cached rows
+// Per CTA (224 threads):
+//   warps 0-1  producers: TMA-load the row's 64 x 576 query (9 boxes of 64
+//              heads x 64 columns) and gather each tile's 64 cached rows
 //              straight out of the paged pool with TMA gather4 (four 128-byte
 //              row pieces per instruction, 128-byte swizzle), two stages deep;
-//   warp 1     MMA issuer: S^T = K Q^T (M = 64 tokens, N = 64 heads, K = 576)
+//              each warp issues half of a tile's gathers, because one warp
+//              alone cannot issue TMA copies fast enough to fill HBM;
+//   warp 2     MMA issuer: S^T = K Q^T (M = 64 tokens, N = 64 heads, K = 576)
 //              into TMEM, then O^T += V^T P^T (M = 128 latent dims x 4,
 //              N = 64 heads, K = 64 tokens) with V read from the same gathered
 //              tile (MN-major) and P^T from shared memory;
-//   warps 2-5  softmax: per-head tile maxima with redux.sync, exp2 into bf16
+//   warps 3-6  softmax: per-head tile maxima with redux.sync, exp2 into bf16
 //              P^T rows (one 128-byte row per token, no transpose needed), a
 //              lazy rescale of the TMEM accumulator only when a head's running
 //              maximum grows by more than 2^8, and the epilogue.
@@ -47,7 +49,8 @@ constexpr int kQChunkBytes = kHeads * 128;
 constexpr int kQBytes = kChunks * kQChunkBytes;    // 72 KB
 constexpr int kPBytes = kTok * 128;                // P^T: 64 tokens x 64 heads bf16
 constexpr int kSmemBytes = kQBytes + 2 * kStageBytes + kPBytes + 1024;
-constexpr int kThreads = 192;
+constexpr int kProducers = 2;                      // warps issuing the gathers (TMA issue is per-warp limited)
+constexpr int kThreads = 32 * (kProducers + 1 + 4);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;                      // S^T of stage b at columns 64 b
 constexpr uint32_t kColO = 128;                    // O^T chunk k (dims 128k..) at columns 128 + 64 k
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&kv_full[b], 1);
+      mbar_init(&kv_full[b], kProducers);
       mbar_init(&kv_empty[b], 1);
       mbar_init(&s_full[b], 1);
       mbar_init(&s_empty[b], 4);
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     rescale_tag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kProducers) {
     tmem_alloc(&tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -132,36 +135,42 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ producer
-    int q_loads = 0, cur_row = -1, req = 0, pos = -1;
+  if (warp < kProducers) {
+    // ------------------------------------------------------------------ producers
+    // The physical slots of tile i+1 are looked up (index buffer -> page table) while tile i's
+    // gathers are in flight, so the two dependent global loads stay off the critical path.
+    int q_loads = 0, cur_row = -1;
     int filled[2] = {0, 0};
-    for (int u = u0; u < u1; ++u) {
-      const int i = u - u0, b = i & 1, n = i >> 1;
+    auto lookup = [&](int u, int64_t (&sl)[2]) {
       const int r = u / T, j = u - r * T;
-      if (n > 0 && !mbar_wait(&kv_empty[b], (n - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
-      if (r != cur_row) {
-        if (q_loads > 0 && !mbar_wait(&q_empty, (q_loads - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&q_full, kQBytes);
-          for (int c = 0; c < kChunks; ++c) tma_load_2d(sQ + c * kQChunkBytes, &q_map, c * 64, r * kHeads, &q_full);
-        }
-        ++q_loads;
-        cur_row = r;
-        row_info(a.m, r, req, pos);
-      }
-      // entry `lane` and `lane + 32` of the tile
+      int req, pos;
+      row_info(a.m, r, req, pos);
       const int32_t* idx = a.topk_idx + (int64_t)r * a.topk + (int64_t)j * kTok;
-      int64_t sl[2];
-      uint32_t vb[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int t = lane + 32 * h;
         const int e = (j * kTok + t < a.topk) ? idx[t] : -1;
         sl[h] = (e >= 0 && e <= pos) ? token_slot(a.m, req, e, a.log2_page, a.num_pages) : -1;
-        vb[h] = __ballot_sync(0xffffffffu, sl[h] >= 0);
       }
-      const uint64_t mask = (uint64_t)vb[0] | ((uint64_t)vb[1] << 32);
+    };
+    int64_t nxt[2] = {-1, -1};
+    if (u0 < u1) lookup(u0, nxt);
+    for (int u = u0; u < u1; ++u) {
+      const int i = u - u0, b = i & 1, n = i >> 1;
+      const int r = u / T;
+      int64_t sl[2] = {nxt[0], nxt[1]};
+      if (n > 0 && !mbar_wait(&kv_empty[b], (n - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
+      if (r != cur_row) {
+        if (q_loads > 0 && !mbar_wait(&q_empty, (q_loads - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
+        if (warp == 0 && lane == 0) {
+          mbar_arrive_expect_tx(&q_full, kQBytes);
+          for (int c = 0; c < kChunks; ++c) tma_load_2d(sQ + c * kQChunkBytes, &q_map, c * 64, r * kHeads, &q_full);
+        }
+        ++q_loads;
+        cur_row = r;
+      }
+      const uint32_t vb0 = __ballot_sync(0xffffffffu, sl[0] >= 0), vb1 = __ballot_sync(0xffffffffu, sl[1] >= 0);
+      const uint64_t mask = (uint64_t)vb0 | ((uint64_t)vb1 << 32);
       if (mask != 0) {
         // invalid entries re-read a valid row of the tile (finite data); their probability is 0
         const int t0 = __ffsll((long long)mask) - 1;
@@ -171,15 +180,16 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         if (sl[1] < 0) sl[1] = sub;
       }
       if (lane == 0) {
-        tile_mask[b] = mask;
-        mbar_arrive_expect_tx(&kv_full[b], mask ? (uint32_t)kStageBytes : 0u);
+        if (warp == 0) tile_mask[b] = mask;
+        mbar_arrive_expect_tx(&kv_full[b], mask ? (uint32_t)(kStageBytes / kProducers) : 0u);
       }
       __syncwarp();
       ++filled[b];
       if (mask != 0) {
+        // this warp gathers entry groups 8w .. 8w+7 (4 entries each) for all 9 column chunks
         uint8_t* stage = sKV + b * kStageBytes;
-        const int g = lane & 15;        // entries 4g .. 4g+3
-        const int hsel = g >> 3;        // held in sl[hsel] by lanes (4g .. 4g+3) % 32
+        const int g = 8 * warp + (lane & 7);   // entries 4g .. 4g+3
+        const int hsel = g >> 3;               // held in sl[hsel] by lanes (4g .. 4g+3) % 32
         int32_t y[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -187,15 +197,16 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
           const int64_t v0 = __shfl_sync(0xffffffffu, sl[0], src), v1 = __shfl_sync(0xffffffffu, sl[1], src);
           y[k] = (int32_t)(hsel ? v1 : v0);
         }
-        for (int c = lane >> 4; c < kChunks; c += 2)
+        for (int c = lane >> 3; c < kChunks; c += 4)
           tma_gather4(stage + c * kChunkBytes + g * 4 * 128, &kv_map, c * 64, y[0], y[1], y[2], y[3], &kv_full[b]);
       }
+      if (u + 1 < u1) lookup(u + 1, nxt);
     }
     // nothing may still be landing in shared memory when the CTA exits
     for (int b = 0; b < 2; ++b)
       if (filled[b] > 0) mbar_wait(&kv_full[b], (filled[b] - 1) & 1, a.err, kErrTmaTimeout, kPolls);
     if (q_loads > 0) mbar_wait(&q_full, (q_loads - 1) & 1, a.err, kErrTmaTimeout, kPolls);
-  } else if (warp == 1) {
+  } else if (warp == kProducers) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id_qk = idesc_f16(64, kHeads, true, true, false, false);
@@ -264,7 +275,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     const int quarter = warp & 3;                       // TMEM lanes this warp may touch
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     const int tok = 16 * quarter + lane;                // S^T row held by this lane (lanes 0..15)
-    const int st = threadIdx.x - 64;                    // 0..127
+    const int st = threadIdx.x - 32 * (kProducers + 1);  // 0..127
     const int first_row = u0 / T;
     float l_acc[kHeads];
     int seg = 0;
@@ -413,7 +424,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kProducers) tmem_dealloc(tmem, kTmemCols);
 }
 
 // LSE merge of the pieces of rows that were cut between CTAs:
