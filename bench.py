@@ -191,12 +191,22 @@ def kernel_traffic(kernel_file: str, kernel_name: str):
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    """nvidia-smi samples every 200 ms; started before warm-up so its start-up never overlaps the
+    timed region, and only the samples taken inside [t_begin, t_end] are kept."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self):
         self.proc = None
+        self.t_begin = None
+        self.t_end = None
+
+    def mark_begin(self):
+        self.t_begin = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
 
     def start(self):
         import torch
@@ -225,22 +235,30 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out = ""
-        sm, mx, reasons = [], [], set()
+        import datetime
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 7:
+            if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:8]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[3:7]):
+        inside = [r for r in rows if self.t_begin is not None and self.t_begin - 0.25 <= r[0] <= (self.t_end or 1e30) + 0.25]
+        use = inside if inside else rows[-3:]
+        reasons = set()
+        for r in use:
+            for n, v in zip(names, r[3]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+        sm = [r[1] for r in use]
+        mx = [r[2] for r in use]
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(inside),
+                "window": "timed region" if inside else "last samples before stop (timed region shorter than 200 ms)"}
 
 
 # ---------------------------------------------------------------------------
@@ -394,20 +412,23 @@ def main():
     lib = _lib.load()
 
     # ---- device-resident timing --------------------------------------------------------
+    clocks = ClockSampler()
+    clocks.start()
     for _ in range(args.warmup):
         prob.step()
     torch.cuda.synchronize()
+    time.sleep(0.5)                      # nvidia-smi is up and sampling before the timed region
     barrier(world)
     torch.cuda.synchronize()
     launches0 = lib.dsa_kernel_launches()
-    clocks = ClockSampler()
-    clocks.start()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark_begin()
     t0.record()
     for _ in range(args.steps):
         prob.step()
     t1.record()
     torch.cuda.synchronize()
+    clocks.mark_end()
     clk = clocks.stop()
     launches = int(lib.dsa_kernel_launches() - launches0)
     barrier(world)

@@ -429,8 +429,10 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
 // LSE merge of the pieces of rows that were cut between CTAs:
 //   out = sum_j e^{m_j - M} O_j / sum_j e^{m_j - M} l_j,  lse = M + ln sum_j e^{m_j - M} l_j.
+// Grid (row, group of 8 heads); thread = (head, 8 consecutive latent dims).
 __global__ void __launch_bounds__(512) mla_merge_kernel(MlaArgs a) {
-  const int r = blockIdx.x, tid = threadIdx.x, h = tid >> 3, jl = tid & 7;
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const int h = blockIdx.y * 8 + (tid >> 6), d0 = (tid & 63) * 8;
   const int T = a.tiles;
   const int c_first = cta_of_unit(r * T, a.units, a.ctas), c_last = cta_of_unit(r * T + T - 1, a.units, a.ctas);
   if (c_first == c_last) return;    // written directly by the attention kernel
@@ -439,41 +441,31 @@ __global__ void __launch_bounds__(512) mla_merge_kernel(MlaArgs a) {
     const int slot = r == unit_start(c, a.units, a.ctas) / T ? 2 * c : 2 * c + 1;
     M = fmaxf(M, a.part_ml[((int64_t)slot * kHeads + h) * 2]);
   }
-  float L = 0.f;
-  float acc[64];
-#pragma unroll
-  for (int x = 0; x < 64; ++x) acc[x] = 0.f;
+  float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int c = c_first; c <= c_last; ++c) {
     const int slot = r == unit_start(c, a.units, a.ctas) / T ? 2 * c : 2 * c + 1;
     const float mj = a.part_ml[((int64_t)slot * kHeads + h) * 2], lj = a.part_ml[((int64_t)slot * kHeads + h) * 2 + 1];
     if (!(lj > 0.f)) continue;
     const float wgt = expf(mj - M);
     L = fmaf(wgt, lj, L);
-    const float4* o = reinterpret_cast<const float4*>(a.part_o + ((int64_t)slot * kHeads + h) * kLatent);
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-      const float4 x = o[(cc * 8 + jl) * 2], y = o[(cc * 8 + jl) * 2 + 1];
-      acc[cc * 8 + 0] = fmaf(wgt, x.x, acc[cc * 8 + 0]);
-      acc[cc * 8 + 1] = fmaf(wgt, x.y, acc[cc * 8 + 1]);
-      acc[cc * 8 + 2] = fmaf(wgt, x.z, acc[cc * 8 + 2]);
-      acc[cc * 8 + 3] = fmaf(wgt, x.w, acc[cc * 8 + 3]);
-      acc[cc * 8 + 4] = fmaf(wgt, y.x, acc[cc * 8 + 4]);
-      acc[cc * 8 + 5] = fmaf(wgt, y.y, acc[cc * 8 + 5]);
-      acc[cc * 8 + 6] = fmaf(wgt, y.z, acc[cc * 8 + 6]);
-      acc[cc * 8 + 7] = fmaf(wgt, y.w, acc[cc * 8 + 7]);
-    }
+    const float4* o = reinterpret_cast<const float4*>(a.part_o + ((int64_t)slot * kHeads + h) * kLatent + d0);
+    const float4 x = o[0], y = o[1];
+    acc[0] = fmaf(wgt, x.x, acc[0]);
+    acc[1] = fmaf(wgt, x.y, acc[1]);
+    acc[2] = fmaf(wgt, x.z, acc[2]);
+    acc[3] = fmaf(wgt, x.w, acc[3]);
+    acc[4] = fmaf(wgt, y.x, acc[4]);
+    acc[5] = fmaf(wgt, y.y, acc[5]);
+    acc[6] = fmaf(wgt, y.z, acc[6]);
+    acc[7] = fmaf(wgt, y.w, acc[7]);
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  __nv_bfloat16* o = a.out + ((int64_t)r * kHeads + h) * kLatent;
+  uint4 v;
+  __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&v);
 #pragma unroll
-  for (int cc = 0; cc < 8; ++cc) {
-    uint4 v;
-    __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&v);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) x[e] = __floats2bfloat162_rn(acc[cc * 8 + 2 * e] * inv, acc[cc * 8 + 2 * e + 1] * inv);
-    reinterpret_cast<uint4*>(o)[cc * 8 + jl] = v;
-  }
-  if (a.lse && jl == 0) a.lse[(int64_t)r * kHeads + h] = L > 0.f ? M + logf(L) : -INFINITY;
+  for (int e = 0; e < 4; ++e) x[e] = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+  *reinterpret_cast<uint4*>(a.out + ((int64_t)r * kHeads + h) * kLatent + d0) = v;
+  if (a.lse && (tid & 63) == 0) a.lse[(int64_t)r * kHeads + h] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
 // ---------------------------------------------------------------------------
@@ -555,7 +547,7 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
   count_launches(1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mla_merge_kernel<<<num_rows, 512, 0, s>>>(a);
+  mla_merge_kernel<<<dim3(num_rows, kHeads / 8), 512, 0, s>>>(a);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -6,11 +6,22 @@
 // short contexts keep nearly every position).  Output is sorted ascending and
 // padded with -1.
 //
-// Radix select on order-preserving 32-bit keys (MSB-first digits of 11, 11 and
-// 10 bits, shared-memory histograms) finds the k-th largest key T; a final
-// ordered pass writes every position with key > T and the first (in position
-// order) of those with key == T until k are taken.  The result is unique and
-// deterministic.
+// Scores are compared as order-preserving 32-bit keys.  Per row (one CTA of
+// 32 warps):
+//   1. radix select over a strided sample of 4096 keys gives the key a safety
+//      margin below the sample's k-th rank: a threshold that the true k-th
+//      key clears with high probability;
+//   2. each warp scans its contiguous share of the row and keeps the
+//      positions at or above the threshold, in order, in its own
+//      shared-memory segment;
+//   3. if the segments hold at least k entries and none overflowed they hold
+//      the answer: radix select over the candidates finds the k-th key T and
+//      how many keys equal to T are taken (the smallest positions first), and
+//      the warps emit their kept positions in order through two 32-entry
+//      prefix sums.  Otherwise (an unlucky sample) the same radix select runs
+//      over the whole row followed by an ordered pass.
+// Radix selects use MSB-first digits of 11, 11 and 10 bits and warp-aggregated
+// shared-memory histograms.  Both paths give the same unique result.
 #include "dsa_internal.cuh"
 
 namespace dsa {
@@ -21,6 +32,10 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 constexpr int kTopkThreads = 1024;
+constexpr int kWarps = kTopkThreads / 32;
+constexpr int kSample = 4096;
+constexpr int kSeg = 256;                                   // candidate capacity of one warp
+constexpr size_t kTopkSmem = (size_t)kWarps * kSeg * 8 + 2048 * 4;   // (key, position) segments + histogram
 
 // Block-wide exclusive scan of a 32-bit value; returns the exclusive prefix and the block total.
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_tot, uint32_t& total) {
@@ -51,35 +66,30 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
   return ex;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0, const float* __restrict__ scores,
-                                                            int64_t stride, int max_seq_len, int k,
-                                                            int32_t* __restrict__ topk_idx) {
-  __shared__ uint32_t hist[2048];
-  __shared__ uint32_t warp_tot[33];
-  __shared__ uint32_t sh_bin, sh_krem;
-  const int r = row0 + blockIdx.x;
-  int b, pos;
-  row_info(m, r, b, pos);
-  int n = pos + 1 > 0 ? pos + 1 : 0;
-  if (n > max_seq_len) n = max_seq_len;   // never read past the row's scores, whatever seq_lens says
-  int32_t* out = topk_idx + (int64_t)r * k;
-  const float* sc = scores + (int64_t)blockIdx.x * stride;
-  const int tid = threadIdx.x;
-  if (n <= k) {
-    for (int i = tid; i < k; i += kTopkThreads) out[i] = i < n ? i : -1;
-    return;
-  }
+// Histogram increment aggregated over the lanes of a warp that hit the same bin.
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool active) {
+  const uint32_t act = __ballot_sync(0xffffffffu, active);
+  if (!active) return;
+  const uint32_t peers = __match_any_sync(act, bin);
+  if ((threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+}
 
-  uint32_t prefix = 0, mask = 0;
-  uint32_t krem = (uint32_t)k;
+// Radix select: the k-th largest of the keys produced by get(i), i < n (k <= n).  Returns T and
+// the number of keys equal to T that belong to the top k.  The whole block calls it.
+template <typename Get>
+__device__ void radix_select(Get get, int n, uint32_t k, uint32_t* hist, uint32_t* sh, uint32_t& T,
+                             uint32_t& need_eq) {
+  const int tid = threadIdx.x;
+  uint32_t prefix = 0, mask = 0, krem = k;
   const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = shifts[pass], nb = 1 << widths[pass];
     for (int i = tid; i < nb; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
-    for (int s = tid; s < n; s += kTopkThreads) {
-      const uint32_t key = order_key(sc[s]);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+    for (int i0 = 0; i0 < n; i0 += kTopkThreads) {
+      const int i = i0 + tid;
+      const uint32_t key = i < n ? get(i) : 0u;
+      hist_add(hist, (key >> shift) & (nb - 1), i < n && (key & mask) == prefix);
     }
     __syncthreads();
     if (tid < 32) {
@@ -100,8 +110,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
         for (int j = 0; j < per; ++j) {
           const uint32_t h = hist[top - j];
           if (c + h >= krem) {
-            sh_bin = (uint32_t)(top - j);
-            sh_krem = krem - c;
+            sh[0] = (uint32_t)(top - j);
+            sh[1] = krem - c;
             break;
           }
           c += h;
@@ -109,48 +119,207 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
       }
     }
     __syncthreads();
-    prefix |= sh_bin << shift;
+    prefix |= sh[0] << shift;
     mask |= (uint32_t)(nb - 1) << shift;
-    krem = sh_krem;
+    krem = sh[1];
     __syncthreads();
   }
-  const uint32_t T = prefix;       // key of the k-th largest score
-  const uint32_t need_eq = krem;   // how many entries equal to T are taken (smallest positions first)
+  T = prefix;
+  need_eq = krem;
+}
 
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0, const float* __restrict__ scores,
+                                                            int64_t stride, int max_seq_len, int k,
+                                                            int32_t* __restrict__ topk_idx) {
+  extern __shared__ uint64_t topk_smem[];
+  uint64_t* seg = topk_smem;                                                  // [kWarps][kSeg] key << 32 | position
+  uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem + kWarps * kSeg);    // [2048]
+  __shared__ uint32_t warp_tot[33];
+  __shared__ uint32_t cnt[kWarps], eq_before[kWarps], sel_before[kWarps];
+  __shared__ uint32_t sh[4];
+  const int r = row0 + blockIdx.x;
+  int b, pos;
+  row_info(m, r, b, pos);
+  int n = pos + 1 > 0 ? pos + 1 : 0;
+  if (n > max_seq_len) n = max_seq_len;   // never read past the row's scores, whatever seq_lens says
+  int32_t* out = topk_idx + (int64_t)r * k;
+  const float* sc = scores + (int64_t)blockIdx.x * stride;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (n <= k) {
+    for (int i = tid; i < k; i += kTopkThreads) out[i] = i < n ? i : -1;
+    return;
+  }
+
+  // ---- 1. threshold: a key ranked a margin below k * S / n in a strided sample
+  const int S = n < kSample ? n : kSample;
+  const int rank = (int)(((int64_t)k * S) / n);
+  const int margin = 3 * (int)sqrtf((float)rank + 1.f) + 8;
+  uint32_t t_low = 0;
+  if (rank + margin < S) {
+    uint32_t T, eq;
+    radix_select([&](int i) { return order_key(sc[(int64_t)i * n / S]); }, S, (uint32_t)(rank + margin + 1), hist,
+                 sh, T, eq);
+    t_low = T;
+  }
+
+  // ---- 2. each warp keeps its share's positions at or above the threshold, in order
+  const int per_warp = (n + kWarps - 1) / kWarps;
+  const int w0 = warp * per_warp, w1 = min(n, w0 + per_warp);
+  uint32_t kept = 0;
+  bool overflow = false;
+  for (int s0 = w0; s0 < w1; s0 += 32) {
+    const int s = s0 + lane;
+    const uint32_t key = s < w1 ? order_key(sc[s]) : 0u;
+    const bool take = s < w1 && key >= t_low;
+    const uint32_t ballot = __ballot_sync(0xffffffffu, take);
+    const uint32_t slot = kept + __popc(ballot & ((1u << lane) - 1u));
+    if (take) {
+      if (slot < (uint32_t)kSeg) seg[warp * kSeg + slot] = ((uint64_t)key << 32) | (uint32_t)s;
+      else overflow = true;
+    }
+    kept += __popc(ballot);
+  }
+  overflow = __any_sync(0xffffffffu, overflow);
+  if (lane == 0) {
+    cnt[warp] = overflow ? 0xFFFFFFFFu : kept;
+    if (warp == 0) sh[2] = 0;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const uint32_t c = cnt[tid];
+    const bool bad = __any_sync(0xffffffffu, c == 0xFFFFFFFFu);
+    uint32_t tot = bad ? 0 : c;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (tid == 0) sh[2] = bad ? 0u : tot;
+  }
+  __syncthreads();
+  const uint32_t total = sh[2];
+
+  if (total >= (uint32_t)k) {
+    // ---- 3a. exact k-th key among the candidates, then an ordered emission
+    // candidate i of the concatenated segments: warp w holds indices [sum_{v<w} cnt_v, ...)
+    if (tid < 32) {
+      uint32_t c = cnt[tid], inc = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (tid >= o) inc += t;
+      }
+      warp_tot[tid] = inc - c;          // first candidate index of each warp
+    }
+    __syncthreads();
+    uint32_t T, need_eq;
+    radix_select(
+        [&](int i) {
+          int lo = 0, hi = kWarps - 1;   // warp whose segment holds candidate i
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (warp_tot[mid] <= (uint32_t)i) lo = mid; else hi = mid - 1;
+          }
+          return (uint32_t)(seg[lo * kSeg + (i - warp_tot[lo])] >> 32);
+        },
+        (int)total, (uint32_t)k, hist, sh, T, need_eq);
+    // per-warp counts of keys > T and == T, then exclusive prefixes in warp (= position) order
+    uint32_t gt = 0, eq = 0;
+    for (uint32_t j = lane; j < kept; j += 32) {
+      const uint32_t key = (uint32_t)(seg[warp * kSeg + j] >> 32);
+      gt += key > T;
+      eq += key == T;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      gt += __shfl_xor_sync(0xffffffffu, gt, o);
+      eq += __shfl_xor_sync(0xffffffffu, eq, o);
+    }
+    if (lane == 0) {
+      cnt[warp] = gt;
+      eq_before[warp] = eq;
+    }
+    __syncthreads();
+    if (tid < 32) {
+      // selected entries of warp w: all of its keys > T plus its share of the first need_eq keys == T
+      uint32_t e = eq_before[tid], einc = e;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, einc, o);
+        if (tid >= o) einc += t;
+      }
+      const uint32_t e_ex = einc - e;
+      const uint32_t take_eq = e_ex >= need_eq ? 0u : min(e, need_eq - e_ex);
+      uint32_t sel = cnt[tid] + take_eq, sinc = sel;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, sinc, o);
+        if (tid >= o) sinc += t;
+      }
+      sel_before[tid] = sinc - sel;
+      eq_before[tid] = e_ex;
+    }
+    __syncthreads();
+    uint32_t out_at = sel_before[warp], eq_seen = eq_before[warp];
+    for (uint32_t j0 = 0; j0 < kept; j0 += 32) {
+      const uint32_t j = j0 + lane;
+      const uint64_t v = j < kept ? seg[warp * kSeg + j] : 0ull;
+      const uint32_t key = (uint32_t)(v >> 32);
+      const bool is_eq = j < kept && key == T;
+      const uint32_t eq_ballot = __ballot_sync(0xffffffffu, is_eq);
+      const uint32_t my_eq = eq_seen + __popc(eq_ballot & ((1u << lane) - 1u));
+      const bool sel = j < kept && (key > T || (is_eq && my_eq < need_eq));
+      const uint32_t sel_ballot = __ballot_sync(0xffffffffu, sel);
+      if (sel) {
+        const uint32_t o = out_at + __popc(sel_ballot & ((1u << lane) - 1u));
+        if (o < (uint32_t)k) out[o] = (int32_t)(uint32_t)v;
+      }
+      out_at += __popc(sel_ballot);
+      eq_seen += __popc(eq_ballot);
+    }
+    return;
+  }
+
+  // ---- 3b. radix select over the whole row, then an ordered pass
+  uint32_t T, need_eq;
+  radix_select([&](int i) { return order_key(sc[i]); }, n, (uint32_t)k, hist, sh, T, need_eq);
   uint32_t base_gt = 0, base_eq = 0;
   for (int c0 = 0; c0 < n; c0 += 4 * kTopkThreads) {
     const int s0 = c0 + 4 * tid;
     uint32_t key[4];
-    uint32_t cnt = 0;
+    uint32_t c = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       key[j] = s0 + j < n ? order_key(sc[s0 + j]) : 0u;
-      if (s0 + j < n) cnt += (key[j] > T ? 1u : 0u) + (key[j] == T ? 0x10000u : 0u);
+      if (s0 + j < n) c += (key[j] > T ? 1u : 0u) + (key[j] == T ? 0x10000u : 0u);
     }
-    uint32_t total;
-    const uint32_t ex = block_exclusive_scan(cnt, warp_tot, total);
-    uint32_t gt_before = base_gt + (ex & 0xFFFFu), eq_before = base_eq + (ex >> 16);
+    uint32_t tot;
+    const uint32_t ex = block_exclusive_scan(c, warp_tot, tot);
+    uint32_t gt_before = base_gt + (ex & 0xFFFFu), eqb = base_eq + (ex >> 16);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       if (s0 + j >= n) break;
       // slots are < k by construction; the guard only keeps inconsistent input inside the row
       if (key[j] > T) {
-        const uint32_t slot = gt_before + (eq_before < need_eq ? eq_before : need_eq);
+        const uint32_t slot = gt_before + (eqb < need_eq ? eqb : need_eq);
         if (slot < (uint32_t)k) out[slot] = s0 + j;
         ++gt_before;
       } else if (key[j] == T) {
-        if (eq_before < need_eq && gt_before + eq_before < (uint32_t)k) out[gt_before + eq_before] = s0 + j;
-        ++eq_before;
+        if (eqb < need_eq && gt_before + eqb < (uint32_t)k) out[gt_before + eqb] = s0 + j;
+        ++eqb;
       }
     }
-    base_gt += total & 0xFFFFu;
-    base_eq += total >> 16;
+    base_gt += tot & 0xFFFFu;
+    base_eq += tot >> 16;
   }
 }
 
 cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scores, int64_t score_stride,
                         int max_seq_len, int topk, int32_t* topk_idx, cudaStream_t s) {
-  topk_kernel<<<nrows, kTopkThreads, 0, s>>>(m, row0, scores, score_stride, max_seq_len, topk, topk_idx);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  topk_kernel<<<nrows, kTopkThreads, kTopkSmem, s>>>(m, row0, scores, score_stride, max_seq_len, topk, topk_idx);
   count_launches(1);
   return cudaGetLastError();
 }
