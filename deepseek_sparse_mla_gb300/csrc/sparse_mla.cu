@@ -14,18 +14,18 @@
 // one CTA per SM).  A row cut between CTAs is finished by an LSE merge of the
 // pieces; a row inside one CTA is written directly.
 //
-// Per CTA (224 threads):
-//   warps 0-1  producers: TMA-load the row's 64 x 576 query (9 boxes of 64
+// Per CTA (16 warps):
+//   warps 0-7  producers: TMA-load the row's 64 x 576 query (9 boxes of 64
 //              heads x 64 columns) and gather each tile's 64 cached rows
 //              straight out of the paged pool with TMA gather4 (four 128-byte
 //              row pieces per instruction, 128-byte swizzle), two stages deep;
-//              each warp issues half of a tile's gathers, because one warp
-//              alone cannot issue TMA copies fast enough to fill HBM;
-//   warp 2     MMA issuer: S^T = K Q^T (M = 64 tokens, N = 64 heads, K = 576)
+//              warp w looks up and gathers entries 8w .. 8w+7 of each tile,
+//              because the TMA issue rate of one warp is far below HBM speed;
+//   warp 12    MMA issuer: S^T = K Q^T (M = 64 tokens, N = 64 heads, K = 576)
 //              into TMEM, then O^T += V^T P^T (M = 128 latent dims x 4,
 //              N = 64 heads, K = 64 tokens) with V read from the same gathered
 //              tile (MN-major) and P^T from shared memory;
-//   warps 3-6  softmax: per-head tile maxima with redux.sync, exp2 into bf16
+//   warps 8-11 softmax: per-head tile maxima with redux.sync, exp2 into bf16
 //              P^T rows (one 128-byte row per token, no transpose needed), a
 //              lazy rescale of the TMEM accumulator only when a head's running
 //              maximum grows by more than 2^8, and the epilogue.
@@ -49,8 +49,12 @@ constexpr int kQChunkBytes = kHeads * 128;
 constexpr int kQBytes = kChunks * kQChunkBytes;    // 72 KB
 constexpr int kPBytes = kTok * 128;                // P^T: 64 tokens x 64 heads bf16
 constexpr int kSmemBytes = kQBytes + 2 * kStageBytes + kPBytes + 1024;
-constexpr int kProducers = 2;                      // warps issuing the gathers (TMA issue is per-warp limited)
-constexpr int kThreads = 32 * (kProducers + 1 + 4);
+constexpr int kProducers = 8;                      // warps issuing the gathers (TMA issue is per-warp limited)
+constexpr int kSoftmaxWarp0 = 8;                   // warpgroup 2
+constexpr int kMmaWarp = 12;                       // first warp of warpgroup 3 (the other three idle)
+constexpr int kThreads = 512;
+// register split (sums to 61,440 of the 512 x 128 launched): producers / MMA 80, softmax 240
+constexpr uint32_t kRegsLow = 80, kRegsSoftmax = 240;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;                      // S^T of stage b at columns 64 b
 constexpr uint32_t kColO = 128;                    // O^T chunk k (dims 128k..) at columns 128 + 64 k
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
   __shared__ uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2];
   __shared__ uint64_t p_full, p_empty, q_full, q_empty, o_full, o_empty, mma_done;
-  __shared__ uint64_t tile_mask[2];
+  __shared__ __align__(8) uint8_t tile_mask8[2][8];   // entry validity, one byte per producer warp
   __shared__ float red[4][kHeads];
   __shared__ float mref[kHeads], alpha[kHeads], lfin[kHeads];
   __shared__ int rescale_tag;
@@ -107,7 +111,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&kv_full[b], kProducers);
+      mbar_init(&kv_full[b], kProducers);   // every producer warp arrives (with its own byte count)
       mbar_init(&kv_empty[b], 1);
       mbar_init(&s_full[b], 1);
       mbar_init(&s_empty[b], 4);
@@ -122,10 +126,14 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     rescale_tag = 0;
     fence_mbar_init();
   }
-  if (warp == kProducers) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  // rows a tile does not gather keep older finite data (zeros at first): their probability is 0
+  for (int i = threadIdx.x; i < 2 * kStageBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(sKV)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&kv_map);
     prefetch_tmap(&q_map);
@@ -137,28 +145,24 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
   if (warp < kProducers) {
     // ------------------------------------------------------------------ producers
-    // The physical slots of tile i+1 are looked up (index buffer -> page table) while tile i's
-    // gathers are in flight, so the two dependent global loads stay off the critical path.
+    // Warp w owns entries 8w .. 8w+7 of every tile (held by lanes 0..7): it looks up their physical
+    // slots one tile ahead, so the index-buffer and page-table loads stay off the critical path.
+    regs_dec<kRegsLow>();
     int q_loads = 0, cur_row = -1;
     int filled[2] = {0, 0};
-    auto lookup = [&](int u, int64_t (&sl)[2]) {
+    auto lookup = [&](int u) -> int64_t {
       const int r = u / T, j = u - r * T;
       int req, pos;
       row_info(a.m, r, req, pos);
-      const int32_t* idx = a.topk_idx + (int64_t)r * a.topk + (int64_t)j * kTok;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int t = lane + 32 * h;
-        const int e = (j * kTok + t < a.topk) ? idx[t] : -1;
-        sl[h] = (e >= 0 && e <= pos) ? token_slot(a.m, req, e, a.log2_page, a.num_pages) : -1;
-      }
+      const int t = j * kTok + 8 * warp + lane;
+      const int e = (lane < 8 && t < a.topk) ? a.topk_idx[(int64_t)r * a.topk + t] : -1;
+      return (e >= 0 && e <= pos) ? token_slot(a.m, req, e, a.log2_page, a.num_pages) : -1;
     };
-    int64_t nxt[2] = {-1, -1};
-    if (u0 < u1) lookup(u0, nxt);
+    int64_t nxt = u0 < u1 ? lookup(u0) : -1;
     for (int u = u0; u < u1; ++u) {
       const int i = u - u0, b = i & 1, n = i >> 1;
       const int r = u / T;
-      int64_t sl[2] = {nxt[0], nxt[1]};
+      const int64_t sl = nxt;
       if (n > 0 && !mbar_wait(&kv_empty[b], (n - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
       if (r != cur_row) {
         if (q_loads > 0 && !mbar_wait(&q_empty, (q_loads - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
@@ -169,113 +173,120 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         ++q_loads;
         cur_row = r;
       }
-      const uint32_t vb0 = __ballot_sync(0xffffffffu, sl[0] >= 0), vb1 = __ballot_sync(0xffffffffu, sl[1] >= 0);
-      const uint64_t mask = (uint64_t)vb0 | ((uint64_t)vb1 << 32);
-      if (mask != 0) {
-        // invalid entries re-read a valid row of the tile (finite data); their probability is 0
-        const int t0 = __ffsll((long long)mask) - 1;
-        const int64_t s0 = __shfl_sync(0xffffffffu, sl[0], t0 & 31), s1 = __shfl_sync(0xffffffffu, sl[1], t0 & 31);
-        const int64_t sub = t0 < 32 ? s0 : s1;
-        if (sl[0] < 0) sl[0] = sub;
-        if (sl[1] < 0) sl[1] = sub;
+      const uint32_t valid = __ballot_sync(0xffffffffu, sl >= 0) & 0xFFu;
+      // each group of 4 entries with a valid one is gathered; invalid entries repeat its first valid row
+      const int g = lane >= 18 ? 0 : lane / 9, c = lane % 9;
+      const uint32_t gbits = (valid >> (4 * g)) & 0xFu;
+      const int first = gbits ? 4 * g + __ffs(gbits) - 1 : 0;
+      const int64_t sub = __shfl_sync(0xffffffffu, sl, first);
+      int32_t y[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t v = __shfl_sync(0xffffffffu, sl, 4 * g + k);
+        y[k] = (int32_t)(v >= 0 ? v : sub);
       }
+      const uint32_t groups = ((valid & 0xFu) ? 1u : 0u) + ((valid >> 4) ? 1u : 0u);
       if (lane == 0) {
-        if (warp == 0) tile_mask[b] = mask;
-        mbar_arrive_expect_tx(&kv_full[b], mask ? (uint32_t)(kStageBytes / kProducers) : 0u);
+        tile_mask8[b][warp] = (uint8_t)valid;
+        mbar_arrive_expect_tx(&kv_full[b], groups * (uint32_t)(kChunks * 512));
       }
       __syncwarp();
       ++filled[b];
-      if (mask != 0) {
-        // this warp gathers entry groups 8w .. 8w+7 (4 entries each) for all 9 column chunks
+      if (lane < 18 && gbits) {
         uint8_t* stage = sKV + b * kStageBytes;
-        const int g = 8 * warp + (lane & 7);   // entries 4g .. 4g+3
-        const int hsel = g >> 3;               // held in sl[hsel] by lanes (4g .. 4g+3) % 32
-        int32_t y[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int src = (4 * g + k) & 31;
-          const int64_t v0 = __shfl_sync(0xffffffffu, sl[0], src), v1 = __shfl_sync(0xffffffffu, sl[1], src);
-          y[k] = (int32_t)(hsel ? v1 : v0);
-        }
-        for (int c = lane >> 3; c < kChunks; c += 4)
-          tma_gather4(stage + c * kChunkBytes + g * 4 * 128, &kv_map, c * 64, y[0], y[1], y[2], y[3], &kv_full[b]);
+        tma_gather4(stage + c * kChunkBytes + (2 * warp + g) * 512, &kv_map, c * 64, y[0], y[1], y[2], y[3], &kv_full[b]);
       }
-      if (u + 1 < u1) lookup(u + 1, nxt);
+      if (u + 1 < u1) nxt = lookup(u + 1);
     }
     // nothing may still be landing in shared memory when the CTA exits
     for (int b = 0; b < 2; ++b)
       if (filled[b] > 0) mbar_wait(&kv_full[b], (filled[b] - 1) & 1, a.err, kErrTmaTimeout, kPolls);
     if (q_loads > 0) mbar_wait(&q_full, (q_loads - 1) & 1, a.err, kErrTmaTimeout, kPolls);
-  } else if (warp == kProducers) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp >= kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer (warp 12; 13-15 idle)
+    regs_dec<kRegsLow>();
+    if (warp == kMmaWarp && lane == 0) {
       const uint32_t id_qk = idesc_f16(64, kHeads, true, true, false, false);
       const uint32_t id_pv = idesc_f16(128, kHeads, true, true, true, true);
       const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
       int q_loads = 0, seg = 0, prev_row = -1;
       bool o_init = false, ok = true;
-      auto pv = [&](int i) -> bool {
-        const int u = u0 + i, b = i & 1, r = u / T, j = u - r * T;
-        const bool seg_first = (u == u0) || j == 0;
-        const bool seg_last = (u == u1 - 1) || j == T - 1;
-        if (!mbar_wait(&p_full, i & 1, a.err, kErrMmaTimeout, kPolls)) return false;
-        if (seg_first) {
-          o_init = false;
-          if (seg > 0 && !mbar_wait(&o_empty, (seg - 1) & 1, a.err, kErrMmaTimeout, kPolls)) return false;
-        }
-        tc_fence_after();
-        if (tile_mask[b] != 0) {
-          const uint32_t stage = smem_u32(sKV + b * kStageBytes);
+      // PV of tile ip releases a stage and must not wait behind the QK of a later tile: issue
+      // whichever of QK(iq) / PV(ip) is ready, PV first.
+      const int ntiles = u1 - u0;
+      int iq = 0, ip = 0;
+      uint32_t idle = 0;
+      while (ok && ip < ntiles) {
+        bool progressed = false;
+        if (ip < iq) {
+          const int i = ip, u = u0 + i, b = i & 1, r = u / T, j = u - r * T;
+          const bool seg_first = (u == u0) || j == 0;
+          const bool seg_last = (u == u1 - 1) || j == T - 1;
+          if (mbar_test(&p_full, i & 1) && (!seg_first || seg == 0 || mbar_test(&o_empty, (seg - 1) & 1))) {
+            if (seg_first) o_init = false;
+            tc_fence_after();
+            if (*reinterpret_cast<volatile uint64_t*>(tile_mask8[b]) != 0) {
+              const uint32_t stage = smem_u32(sKV + b * kStageBytes);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
+              for (int k = 0; k < 4; ++k)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t da = smem_desc(stage + 2 * k * kChunkBytes + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
-              const uint64_t db = smem_desc(p_addr + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
-              mma_ss(tmem + kColO + 64 * k, da, db, id_pv, o_init || kk > 0);
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t da = smem_desc(stage + 2 * k * kChunkBytes + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
+                  const uint64_t db = smem_desc(p_addr + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
+                  mma_ss(tmem + kColO + 64 * k, da, db, id_pv, o_init || kk > 0);
+                }
+              o_init = true;
             }
-          o_init = true;
+            mma_commit(&kv_empty[b]);
+            mma_commit(&p_empty);
+            if (seg_last) {
+              mma_commit(&o_full);
+              ++seg;
+            }
+            ++ip;
+            progressed = true;
+          }
         }
-        mma_commit(&kv_empty[b]);
-        mma_commit(&p_empty);
-        if (seg_last) {
-          mma_commit(&o_full);
-          ++seg;
-        }
-        return true;
-      };
-      for (int u = u0; u < u1; ++u) {
-        const int i = u - u0, b = i & 1, n = i >> 1, r = u / T;
-        if (!mbar_wait(&kv_full[b], n & 1, a.err, kErrTmaTimeout, kPolls)) { ok = false; break; }
-        if (r != prev_row) {
-          if (!mbar_wait(&q_full, q_loads & 1, a.err, kErrTmaTimeout, kPolls)) { ok = false; break; }
-          ++q_loads;
-          prev_row = r;
-        }
-        if (n > 0 && !mbar_wait(&s_empty[b], (n - 1) & 1, a.err, kErrMmaTimeout, kPolls)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t stage = smem_u32(sKV + b * kStageBytes);
+        if (iq < ntiles && iq < ip + 2) {
+          const int i = iq, u = u0 + i, b = i & 1, n = i >> 1, r = u / T;
+          const bool need_q = r != prev_row;
+          if (mbar_test(&kv_full[b], n & 1) && (!need_q || mbar_test(&q_full, q_loads & 1)) &&
+              (n == 0 || mbar_test(&s_empty[b], (n - 1) & 1))) {
+            if (need_q) {
+              ++q_loads;
+              prev_row = r;
+            }
+            tc_fence_after();
+            const uint32_t stage = smem_u32(sKV + b * kStageBytes);
 #pragma unroll 4
-        for (int kk = 0; kk < kChunks * 4; ++kk) {
-          const int c = kk >> 2, off = (kk & 3) * 32;
-          mma_ss(tmem + kColS + 64 * b, smem_desc(stage + c * kChunkBytes + off, 16, 1024, kSwizzle128B),
-                 smem_desc(q_addr + c * kQChunkBytes + off, 16, 1024, kSwizzle128B), id_qk, kk > 0);
+            for (int kk = 0; kk < kChunks * 4; ++kk) {
+              const int c = kk >> 2, off = (kk & 3) * 32;
+              mma_ss(tmem + kColS + 64 * b, smem_desc(stage + c * kChunkBytes + off, 16, 1024, kSwizzle128B),
+                     smem_desc(q_addr + c * kQChunkBytes + off, 16, 1024, kSwizzle128B), id_qk, kk > 0);
+            }
+            mma_commit(&s_full[b]);
+            if (u == u1 - 1 || (u + 1) / T != r) mma_commit(&q_empty);
+            ++iq;
+            progressed = true;
+          }
         }
-        mma_commit(&s_full[b]);
-        if (u == u1 - 1 || (u + 1) / T != r) mma_commit(&q_empty);
-        if (i > 0 && !pv(i - 1)) { ok = false; break; }
+        if (progressed) idle = 0;
+        else if (++idle > (kPolls << 2)) {
+          atomicOr(a.err, kErrMmaTimeout);
+          ok = false;
+        }
       }
-      if (ok && u1 > u0) pv(u1 - u0 - 1);
       // every MMA issued here has finished before TMEM is released
       mma_commit(&mma_done);
       mbar_wait(&mma_done, 0, a.err, kErrMmaTimeout, kPolls);
     }
   } else {
-    // ------------------------------------------------------------------ softmax + epilogue
+    // ------------------------------------------------------------------ softmax + epilogue (warps 8-11)
+    regs_inc<kRegsSoftmax>();
     const int quarter = warp & 3;                       // TMEM lanes this warp may touch
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     const int tok = 16 * quarter + lane;                // S^T row held by this lane (lanes 0..15)
-    const int st = threadIdx.x - 32 * (kProducers + 1);  // 0..127
+    const int st = threadIdx.x - 32 * kSoftmaxWarp0;     // 0..127
     const int first_row = u0 / T;
     float l_acc[kHeads];
     int seg = 0;
@@ -298,7 +309,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[b]);
-      const uint64_t mask = tile_mask[b];
+      const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(tile_mask8[b]);
       const bool valid = lane < 16 && ((mask >> tok) & 1ull);
       float z[kHeads];
 #pragma unroll
@@ -306,26 +317,35 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         z[h] = valid ? __uint_as_float(s_lo[h]) * a.scale_log2 : -INFINITY;
         z[h + 32] = valid ? __uint_as_float(s_hi[h]) * a.scale_log2 : -INFINITY;
       }
+      // The running reference changes only when some head's tile maximum exceeds it by more than
+      // 2^kRescaleLog2; one predicate-OR barrier decides whether the exact per-head maxima are needed
+      // (always on a segment's first tile, which sets the reference).
+      bool need = seg_first;                             // mref was just reset by another thread
 #pragma unroll
-      for (int h = 0; h < kHeads; ++h) {
-        const float mx = warp_max_f32(z[h]);
-        if (lane == 0) red[quarter][h] = mx;
-      }
-      named_bar_sync(1, 128);
-      if (st < kHeads) {
-        const int h = st;
-        const float M = fmaxf(fmaxf(red[0][h], red[1][h]), fmaxf(red[2][h], red[3][h]));
-        const float old = mref[h];
-        float al = 1.f;
-        if (M > -INFINITY && (old == -INFINITY || M > old + kRescaleLog2)) {
-          al = old == -INFINITY ? 0.f : exp2f(old - M);
-          if (old != -INFINITY) rescale_tag = i + 1;
-          mref[h] = M;
+      for (int h = 0; h < kHeads; ++h) need |= z[h] > mref[h] + kRescaleLog2;
+      const bool resc = named_bar_or(1, 128, need);
+      if (resc) {
+#pragma unroll
+        for (int h = 0; h < kHeads; ++h) {
+          const float mx = warp_max_f32(z[h]);
+          if (lane == 0) red[quarter][h] = mx;
         }
-        alpha[h] = al;
+        named_bar_sync(1, 128);
+        if (st < kHeads) {
+          const int h = st;
+          const float M = fmaxf(fmaxf(red[0][h], red[1][h]), fmaxf(red[2][h], red[3][h]));
+          const float old = mref[h];
+          float al = 1.f;
+          if (M > -INFINITY && (old == -INFINITY || M > old + kRescaleLog2)) {
+            al = old == -INFINITY ? 0.f : exp2f(old - M);
+            if (old != -INFINITY) rescale_tag = i + 1;
+            mref[h] = M;
+          }
+          alpha[h] = al;
+        }
+        named_bar_sync(1, 128);
       }
-      named_bar_sync(1, 128);
-      const bool do_rescale = rescale_tag == i + 1;
+      const bool do_rescale = resc && rescale_tag == i + 1;
       uint32_t pk[32];
 #pragma unroll
       for (int h = 0; h < kHeads; h += 2) {
@@ -333,8 +353,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         const float p0 = z[h] == -INFINITY ? 0.f : exp2f(z[h] - m0);
         const float p1 = z[h + 1] == -INFINITY ? 0.f : exp2f(z[h + 1] - m1);
         const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        l_acc[h] = fmaf(l_acc[h], alpha[h], p0);          // the denominator keeps the fp32 probabilities
-        l_acc[h + 1] = fmaf(l_acc[h + 1], alpha[h + 1], p1);
+        l_acc[h] = fmaf(l_acc[h], resc ? alpha[h] : 1.f, p0);   // the denominator keeps the fp32 probabilities
+        l_acc[h + 1] = fmaf(l_acc[h + 1], resc ? alpha[h + 1] : 1.f, p1);
         pk[h >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
       }
       // P^T is free once the previous tile's PV has completed (which also settles O^T)
@@ -424,7 +444,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kProducers) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 // LSE merge of the pieces of rows that were cut between CTAs:

@@ -34,7 +34,7 @@
  *     cannot be checked on the host: kernels skip a slot, page id or index
  *     that falls outside its buffer rather than touching memory out of range.
  *   - bf16 is IEEE bfloat16; e4m3 is the OCP FP8 E4M3 format.
- *   - All pointers to 16-bit or 8-bit data must be 16-byte aligned.
+ *   - All pointers to 16-bit or 8-bit data, and cache.index_scales, must be 16-byte aligned.
  */
 #ifndef DSA_H_
 #define DSA_H_
