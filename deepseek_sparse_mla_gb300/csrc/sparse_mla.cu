@@ -25,10 +25,13 @@
 //              into TMEM, then O^T += V^T P^T (M = 128 latent dims x 4,
 //              N = 64 heads, K = 64 tokens) with V read from the same gathered
 //              tile (MN-major) and P^T from shared memory;
-//   warps 8-11 softmax: per-head tile maxima with redux.sync, exp2 into bf16
-//              P^T rows (one 128-byte row per token, no transpose needed), a
-//              lazy rescale of the TMEM accumulator only when a head's running
-//              maximum grows by more than 2^8, and the epilogue.
+//   warps 8-11 softmax: each thread holds 32 heads of one token (the M = 64
+//              accumulator fills 16 lanes per quarter; the second half of the
+//              lanes reads the other 32 columns), exp2 into bf16 P^T rows (one
+//              128-byte row per token, no transpose needed), a lazy rescale of
+//              the TMEM accumulator only when a head's running maximum grows by
+//              more than 2^8 (checked with one predicate-OR barrier per tile),
+//              and the epilogue.
 // Shared memory: Q 72 KB + 2 x 72 KB tiles + 8 KB P^T.  TMEM: 2 x 64 columns
 // for S^T and 4 x 64 columns for O^T.
 #include <mutex>
@@ -208,7 +211,13 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     if (warp == kMmaWarp && lane == 0) {
       const uint32_t id_qk = idesc_f16(64, kHeads, true, true, false, false);
       const uint32_t id_pv = idesc_f16(128, kHeads, true, true, true, true);
-      const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
+      // descriptors are built once; per MMA only the start-address field (bytes >> 4) advances
+      const uint64_t d_k0 = smem_desc(smem_u32(sKV), 16, 1024, kSwizzle128B);
+      const uint64_t d_q = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128B);
+      const uint64_t d_v0 = smem_desc(smem_u32(sKV), kChunkBytes, 1024, kSwizzle128B);
+      const uint64_t d_p = smem_desc(smem_u32(sP), kChunkBytes, 1024, kSwizzle128B);
+      const uint32_t hi = (uint32_t)(d_k0 >> 32);          // the same for all four descriptors
+      const uint32_t k_lo0 = (uint32_t)d_k0, q_lo0 = (uint32_t)d_q, v_lo0 = (uint32_t)d_v0, p_lo0 = (uint32_t)d_p;
       int q_loads = 0, seg = 0, prev_row = -1;
       bool o_init = false, ok = true;
       // PV of tile ip releases a stage and must not wait behind the QK of a later tile: issue
@@ -226,15 +235,25 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
             if (seg_first) o_init = false;
             tc_fence_after();
             if (*reinterpret_cast<volatile uint64_t*>(tile_mask8[b]) != 0) {
-              const uint32_t stage = smem_u32(sKV + b * kStageBytes);
+              const uint32_t v = opaque_u32(v_lo0 + (uint32_t)((b * kStageBytes) >> 4)), pl = opaque_u32(p_lo0);
+              const uint32_t dO = opaque_u32(tmem + kColO);
+              if (!o_init) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
+                for (int k = 0; k < 4; ++k) {
+                  mma_ss_lh<false>(dO + 64 * k, v + ((2 * k * kChunkBytes) >> 4), hi, pl, hi, id_pv);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                  const uint64_t da = smem_desc(stage + 2 * k * kChunkBytes + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
-                  const uint64_t db = smem_desc(p_addr + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
-                  mma_ss(tmem + kColO + 64 * k, da, db, id_pv, o_init || kk > 0);
+                  for (int kk = 1; kk < 4; ++kk)
+                    mma_ss_lh<true>(dO + 64 * k, v + ((2 * k * kChunkBytes + kk * 2048) >> 4), hi,
+                                    pl + ((kk * 2048) >> 4), hi, id_pv);
                 }
+              } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk)
+                    mma_ss_lh<true>(dO + 64 * k, v + ((2 * k * kChunkBytes + kk * 2048) >> 4), hi,
+                                    pl + ((kk * 2048) >> 4), hi, id_pv);
+              }
               o_init = true;
             }
             mma_commit(&kv_empty[b]);
@@ -257,12 +276,13 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
               prev_row = r;
             }
             tc_fence_after();
-            const uint32_t stage = smem_u32(sKV + b * kStageBytes);
-#pragma unroll 4
-            for (int kk = 0; kk < kChunks * 4; ++kk) {
+            const uint32_t kl = opaque_u32(k_lo0 + (uint32_t)((b * kStageBytes) >> 4)), ql = opaque_u32(q_lo0);
+            const uint32_t ds = tmem + kColS + 64 * b;
+            mma_ss_lh<false>(ds, kl, hi, ql, hi, id_qk);
+#pragma unroll
+            for (int kk = 1; kk < kChunks * 4; ++kk) {
               const int c = kk >> 2, off = (kk & 3) * 32;
-              mma_ss(tmem + kColS + 64 * b, smem_desc(stage + c * kChunkBytes + off, 16, 1024, kSwizzle128B),
-                     smem_desc(q_addr + c * kQChunkBytes + off, 16, 1024, kSwizzle128B), id_qk, kk > 0);
+              mma_ss_lh<true>(ds, kl + ((c * kChunkBytes + off) >> 4), hi, ql + ((c * kQChunkBytes + off) >> 4), hi, id_qk);
             }
             mma_commit(&s_full[b]);
             if (u == u1 - 1 || (u + 1) / T != r) mma_commit(&q_empty);
@@ -285,10 +305,13 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     regs_inc<kRegsSoftmax>();
     const int quarter = warp & 3;                       // TMEM lanes this warp may touch
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
-    const int tok = 16 * quarter + lane;                // S^T row held by this lane (lanes 0..15)
+    // S^T row (token) tok sits in TMEM lane 32 * quarter + lane % 16; lanes 0-15 take heads 0-31 of
+    // it and lanes 16-31 heads 32-63
+    const int tok = 16 * quarter + (lane & 15);
+    const int hh = 32 * (lane >> 4);
     const int st = threadIdx.x - 32 * kSoftmaxWarp0;     // 0..127
     const int first_row = u0 / T;
-    float l_acc[kHeads];
+    float l_acc[32];
     int seg = 0;
     for (int u = u0; u < u1; ++u) {
       const int i = u - u0, b = i & 1, n = i >> 1, r = u / T, j = u - r * T;
@@ -296,39 +319,37 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       const bool seg_last = (u == u1 - 1) || j == T - 1;
       if (seg_first) {
 #pragma unroll
-        for (int h = 0; h < kHeads; ++h) l_acc[h] = 0.f;
+        for (int h = 0; h < 32; ++h) l_acc[h] = 0.f;
         if (st < kHeads) mref[st] = -INFINITY;
       }
       if (!mbar_wait(&kv_full[b], n & 1, a.err, kErrTmaTimeout, kPolls)) break;
       if (!mbar_wait(&s_full[b], n & 1, a.err, kErrMmaTimeout, kPolls)) break;
       tc_fence_after();
-      uint32_t s_lo[32], s_hi[32];
-      tmem_ld32(tmem + lane_base + kColS + 64 * b, s_lo);
-      tmem_ld32(tmem + lane_base + kColS + 64 * b + 32, s_hi);
+      uint32_t sv[32];
+      tmem_ld16x2_32(tmem + lane_base + kColS + 64 * b, sv);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[b]);
       const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(tile_mask8[b]);
-      const bool valid = lane < 16 && ((mask >> tok) & 1ull);
-      float z[kHeads];
+      const bool valid = (mask >> tok) & 1ull;
+      float z[32];
 #pragma unroll
-      for (int h = 0; h < 32; ++h) {
-        z[h] = valid ? __uint_as_float(s_lo[h]) * a.scale_log2 : -INFINITY;
-        z[h + 32] = valid ? __uint_as_float(s_hi[h]) * a.scale_log2 : -INFINITY;
-      }
+      for (int h = 0; h < 32; ++h) z[h] = valid ? __uint_as_float(sv[h]) * a.scale_log2 : -INFINITY;
       // The running reference changes only when some head's tile maximum exceeds it by more than
       // 2^kRescaleLog2; one predicate-OR barrier decides whether the exact per-head maxima are needed
       // (always on a segment's first tile, which sets the reference).
       bool need = seg_first;                             // mref was just reset by another thread
 #pragma unroll
-      for (int h = 0; h < kHeads; ++h) need |= z[h] > mref[h] + kRescaleLog2;
+      for (int h = 0; h < 32; ++h) need |= z[h] > mref[hh + h] + kRescaleLog2;
       const bool resc = named_bar_or(1, 128, need);
       if (resc) {
 #pragma unroll
-        for (int h = 0; h < kHeads; ++h) {
-          const float mx = warp_max_f32(z[h]);
-          if (lane == 0) red[quarter][h] = mx;
+        for (int h = 0; h < 32; ++h) {
+          float mx = z[h];
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          if ((lane & 15) == 0) red[quarter][hh + h] = mx;
         }
         named_bar_sync(1, 128);
         if (st < kHeads) {
@@ -346,24 +367,23 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         named_bar_sync(1, 128);
       }
       const bool do_rescale = resc && rescale_tag == i + 1;
-      uint32_t pk[32];
+      uint32_t pk[16];
 #pragma unroll
-      for (int h = 0; h < kHeads; h += 2) {
-        const float m0 = mref[h], m1 = mref[h + 1];
-        const float p0 = z[h] == -INFINITY ? 0.f : exp2f(z[h] - m0);
-        const float p1 = z[h + 1] == -INFINITY ? 0.f : exp2f(z[h + 1] - m1);
+      for (int h = 0; h < 32; h += 2) {
+        const float m0 = mref[hh + h], m1 = mref[hh + h + 1];
+        const float p0 = z[h] == -INFINITY ? 0.f : ex2_approx(z[h] - m0);
+        const float p1 = z[h + 1] == -INFINITY ? 0.f : ex2_approx(z[h + 1] - m1);
         const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        l_acc[h] = fmaf(l_acc[h], resc ? alpha[h] : 1.f, p0);   // the denominator keeps the fp32 probabilities
-        l_acc[h + 1] = fmaf(l_acc[h + 1], resc ? alpha[h + 1] : 1.f, p1);
+        l_acc[h] = fmaf(l_acc[h], resc ? alpha[hh + h] : 1.f, p0);   // the denominator keeps the fp32 probabilities
+        l_acc[h + 1] = fmaf(l_acc[h + 1], resc ? alpha[hh + h + 1] : 1.f, p1);
         pk[h >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
       }
       // P^T is free once the previous tile's PV has completed (which also settles O^T)
       if (i > 0 && !mbar_wait(&p_empty, (i - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
-      if (lane < 16) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(sP + sw128_offset(tok, c)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      }
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(sP + sw128_offset(tok, (hh >> 3) + c)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       if (do_rescale) {
         tc_fence_after();
 #pragma unroll 1
@@ -387,11 +407,11 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
       if (seg_last) {
 #pragma unroll
-        for (int h = 0; h < kHeads; ++h) {
+        for (int h = 0; h < 32; ++h) {
           float v = l_acc[h];
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          if (lane == 0) red[quarter][h] = v;
+          for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if ((lane & 15) == 0) red[quarter][hh + h] = v;
         }
         named_bar_sync(1, 128);
         if (st < kHeads) lfin[st] = (red[0][st] + red[1][st]) + (red[2][st] + red[3][st]);
