@@ -79,11 +79,13 @@ struct MlaArgs {
 };
 
 __device__ __forceinline__ int unit_start(int c, int units, int ctas) {
+  if ((uint64_t)units * (uint64_t)ctas < (1ull << 32)) return (int)(((uint32_t)c * (uint32_t)units) / (uint32_t)ctas);
   return (int)(((int64_t)c * units) / ctas);
 }
 
 __device__ __forceinline__ int cta_of_unit(int u, int units, int ctas) {
-  int c = (int)(((int64_t)u * ctas) / units);
+  int c = (uint64_t)units * (uint64_t)ctas < (1ull << 32) ? (int)(((uint32_t)u * (uint32_t)ctas) / (uint32_t)units)
+                                                           : (int)(((int64_t)u * ctas) / units);
   while (c + 1 < ctas && unit_start(c + 1, units, ctas) <= u) ++c;
   while (c > 0 && unit_start(c, units, ctas) > u) --c;
   return c;
@@ -470,42 +472,85 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 // LSE merge of the pieces of rows that were cut between CTAs:
 //   out = sum_j e^{m_j - M} O_j / sum_j e^{m_j - M} l_j,  lse = M + ln sum_j e^{m_j - M} l_j.
 // Grid (row, group of 8 heads); thread = (head, 8 consecutive latent dims).
-__global__ void __launch_bounds__(512) mla_merge_kernel(MlaArgs a) {
+// LSE merge of the pieces of rows cut between CTAs.  CTA (row, 16 heads), thread (head, 16 dims);
+// the pieces are read two at a time with all loads of a pair in flight, and merged online across
+// pairs (the running maximum rescales what is already summed).  Launched as a programmatic
+// dependent of the attention kernel: the wait below orders every read after that grid's writes.
+constexpr int kMergeHeads = 16;
+__global__ void __launch_bounds__(512, 2) mla_merge_kernel(MlaArgs a) {
   const int r = blockIdx.x, tid = threadIdx.x;
-  const int h = blockIdx.y * 8 + (tid >> 6), d0 = (tid & 63) * 8;
+  const int h = blockIdx.y * kMergeHeads + (tid >> 5), d0 = (tid & 31) * 16;
   const int T = a.tiles;
-  const int c_first = cta_of_unit(r * T, a.units, a.ctas), c_last = cta_of_unit(r * T + T - 1, a.units, a.ctas);
-  if (c_first == c_last) return;    // written directly by the attention kernel
-  float M = -INFINITY;
-  for (int c = c_first; c <= c_last; ++c) {
-    const int slot = r == unit_start(c, a.units, a.ctas) / T ? 2 * c : 2 * c + 1;
-    M = fmaxf(M, a.part_ml[((int64_t)slot * kHeads + h) * 2]);
+  __shared__ int span[3];
+  if (tid == 0) {
+    // the pieces of row r: CTAs c_first .. c_last.  The first piece sits in its CTA's first-row slot
+    // only if that CTA's range starts in row r; every later piece starts its CTA's range.
+    const int cf = cta_of_unit(r * T, a.units, a.ctas);
+    span[0] = cf;
+    span[1] = cta_of_unit(r * T + T - 1, a.units, a.ctas);
+    span[2] = unit_start(cf, a.units, a.ctas) / T == r ? 2 * cf : 2 * cf + 1;
   }
-  float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int c = c_first; c <= c_last; ++c) {
-    const int slot = r == unit_start(c, a.units, a.ctas) / T ? 2 * c : 2 * c + 1;
-    const float mj = a.part_ml[((int64_t)slot * kHeads + h) * 2], lj = a.part_ml[((int64_t)slot * kHeads + h) * 2 + 1];
-    if (!(lj > 0.f)) continue;
-    const float wgt = expf(mj - M);
-    L = fmaf(wgt, lj, L);
-    const float4* o = reinterpret_cast<const float4*>(a.part_o + ((int64_t)slot * kHeads + h) * kLatent + d0);
-    const float4 x = o[0], y = o[1];
-    acc[0] = fmaf(wgt, x.x, acc[0]);
-    acc[1] = fmaf(wgt, x.y, acc[1]);
-    acc[2] = fmaf(wgt, x.z, acc[2]);
-    acc[3] = fmaf(wgt, x.w, acc[3]);
-    acc[4] = fmaf(wgt, y.x, acc[4]);
-    acc[5] = fmaf(wgt, y.y, acc[5]);
-    acc[6] = fmaf(wgt, y.z, acc[6]);
-    acc[7] = fmaf(wgt, y.w, acc[7]);
+  __syncthreads();
+  const int c_first = span[0], c_last = span[1], first_slot = span[2];
+  if (c_first == c_last) return;    // written directly by the attention kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int G = 2;
+  float M = -INFINITY, L = 0.f;
+  float acc[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+  for (int c0 = c_first; c0 <= c_last; c0 += G) {
+    float mj[G], lj[G];
+    float4 x[G][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int c = c0 + g;
+      mj[g] = -INFINITY;
+      lj[g] = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) x[g][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c <= c_last) {
+        const int slot = c == c_first ? first_slot : 2 * c;
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + ((int64_t)slot * kHeads + h) * 2));
+        mj[g] = ml.x;
+        lj[g] = ml.y;
+        const float4* o = reinterpret_cast<const float4*>(a.part_o + ((int64_t)slot * kHeads + h) * kLatent + d0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x[g][q] = __ldcg(o + q);
+      }
+    }
+    float Mn = M;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      if (lj[g] > 0.f) Mn = fmaxf(Mn, mj[g]);
+    if (Mn == -INFINITY) continue;
+    const float sc = M == -INFINITY ? 0.f : expf(M - Mn);
+    L *= sc;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[e] *= sc;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float wgt = lj[g] > 0.f ? expf(mj[g] - Mn) : 0.f;
+      L = fmaf(wgt, lj[g], L);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[4 * q] = fmaf(wgt, x[g][q].x, acc[4 * q]);
+        acc[4 * q + 1] = fmaf(wgt, x[g][q].y, acc[4 * q + 1]);
+        acc[4 * q + 2] = fmaf(wgt, x[g][q].z, acc[4 * q + 2]);
+        acc[4 * q + 3] = fmaf(wgt, x[g][q].w, acc[4 * q + 3]);
+      }
+    }
+    M = Mn;
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  uint4 v;
-  __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&v);
+  uint4 v[2];
+  __nv_bfloat162* xo = reinterpret_cast<__nv_bfloat162*>(v);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) x[e] = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-  *reinterpret_cast<uint4*>(a.out + ((int64_t)r * kHeads + h) * kLatent + d0) = v;
-  if (a.lse && (tid & 63) == 0) a.lse[(int64_t)r * kHeads + h] = L > 0.f ? M + logf(L) : -INFINITY;
+  for (int e = 0; e < 8; ++e) xo[e] = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+  uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)r * kHeads + h) * kLatent + d0);
+  dst[0] = v[0];
+  dst[1] = v[1];
+  if (a.lse && (tid & 31) == 0) a.lse[(int64_t)r * kHeads + h] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
 // ---------------------------------------------------------------------------
@@ -587,8 +632,20 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
   count_launches(1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mla_merge_kernel<<<dim3(num_rows, kHeads / 8), 512, 0, s>>>(a);
+  // the merge may be scheduled while the attention grid drains (it waits for that grid's writes)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_rows, kHeads / kMergeHeads);
+  cfg.blockDim = dim3(512);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mla_merge_kernel, a);
   count_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
