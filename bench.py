@@ -264,16 +264,24 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # distributed plumbing (replicas: no collective on the data path)
 # ---------------------------------------------------------------------------
-def dist_setup(n_gpus):
+def dist_setup(n_gpus, backend="nccl", device="cuda"):
+    """(rank, world) from the launcher's environment; joins the process group when world > 1.
+
+    Ranks never exchange data on the DSA path: each serves its own replica (its own requests and
+    caches).  The group only carries the barriers and the max-over-ranks of the timings."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     import torch
-    torch.cuda.set_device(local)
+    if device == "cuda":
+        torch.cuda.set_device(local)
     if world > 1:
         import torch.distributed as dist
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if backend == "nccl":
+            dist.init_process_group(backend, device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
     return rank, world
 
 
@@ -283,14 +291,30 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_workload(name: str, rank: int) -> wlm.Workload:
+    """Rank r's replica: the named workload's shape and recipe, drawn from its own seed (rank 0 is
+    the canonical workload), so ranks serve disjoint request sets of the same size."""
+    wl = wlm.FULL[name]()
+    if rank == 0:
+        return wl
+    return wlm.Workload(f"{wl.name}_replica{rank}", list(wl.seq_lens), list(wl.q_lens), wl.page_size, wl.key_format,
+                        wl.topk, wl.layers, wl.seed + 100000 * rank)
+
+
+def aggregate_rate(elapsed_ms_max: float, world: int, layers: int, steps: int) -> float:
+    """Whole-job layer-steps/s: every rank ran `steps` group steps of `layers` layers; the job
+    took as long as its slowest rank."""
+    return world * layers * steps / (elapsed_ms_max / 1e3)
 
 
 # ---------------------------------------------------------------------------
@@ -407,7 +431,7 @@ def main():
     import deepseek_sparse_mla_gb300 as dsa
     from deepseek_sparse_mla_gb300 import _lib
     rank, world = dist_setup(args.gpus)
-    wl = wlm.FULL[args.workload]()
+    wl = rank_workload(args.workload, rank)
     prob = DeviceProblem(wl)
     lib = _lib.load()
 
@@ -434,7 +458,7 @@ def main():
     barrier(world)
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world)
     ms_per_step = elapsed_ms / args.steps
-    value = world * wl.layers * args.steps / (elapsed_ms / 1e3)
+    value = aggregate_rate(elapsed_ms, world, wl.layers, args.steps)
 
     # ---- per-call breakdown (events between the library calls) --------------------------
     marks = Marks()
@@ -490,7 +514,7 @@ def main():
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    e2e = {"value": world * wl.layers * args.steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    e2e = {"value": aggregate_rate(e2e_ms, world, wl.layers, args.steps), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps}
 
     cpu = None

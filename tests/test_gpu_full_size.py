@@ -1,0 +1,105 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the benchmark times.
+
+Each workload is set up exactly as ``bench.py`` sets it up (every request's prefix resident in
+the paged caches, the step's new tokens appended, the same workspaces and the same calls), so
+the kernels run with the full grid, full score blocks and full split-k partition.  A few sampled
+requests are then re-drawn with the host generators and written over their slots, so that the
+float64 oracle can recompute their rows one by one from the same values: indexer scores over
+every visible position, the top-k set (swap tolerance at the k-th score), and the attention
+output and LSE on the oracle's own index set.
+"""
+import numpy as np
+import pytest
+
+import workloads as wlm
+from oracle import dsa_oracle as o
+from parity import check_attention, check_scores, check_topk
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(lib):
+    return lib
+
+
+def sampled_rows(wl: wlm.Workload):
+    """Rows checked against the oracle: the shortest and longest contexts, first and last rows,
+    and one seeded draw, so that ragged and maximal sizes are both covered."""
+    req, pos = o.row_positions(wl.seq_lens, wl.query_start_loc)
+    R = wl.num_rows
+    rng = np.random.default_rng(wl.seed + 77)
+    rows = {0, R - 1, int(np.argmin(pos)), int(np.argmax(pos)), int(rng.integers(0, R))}
+    return sorted(rows), req, pos
+
+
+def key_values(bits: np.ndarray, key_format: str) -> np.ndarray:
+    if key_format == "fp8":
+        codes, scales = o.quantize_index_keys(bits)
+        return o.e4m3_to_f64(codes) * scales.astype(np.float64)[:, None]
+    return o.bf16_to_f64(bits)
+
+
+@pytest.mark.parametrize("name", ["decode_b32_8k", "decode_b64_fp8_indexshare", "prefill_chunk_4096",
+                                  "verify_b8x4_240k"])
+def test_full_size_sampled_rows(name):
+    import torch
+    import bench
+    import deepseek_sparse_mla_gb300 as dsa
+    wl = wlm.FULL[name]()
+    prob = bench.DeviceProblem(wl)
+    # the step's append of the new tokens, as the benchmark step does it
+    for layer in range(wl.layers):
+        dsa.kv_append(prob.caches[layer], prob.new_c[layer], prob.new_r[layer], prob.slots,
+                      k_idx=prob.new_k if layer == 0 else None)
+    rows, req, pos = sampled_rows(wl)
+    host_lat, host_keys = {}, {}
+    for b in sorted({int(req[r]) for r in rows}):
+        L = int(wl.seq_lens[b])
+        slots = torch.from_numpy(wl.slots(b, np.arange(L)).astype(np.int64)).cuda()
+        host_keys[b] = wlm.request_index_keys(wl, b)
+        for layer in range(wl.layers):
+            lat = wlm.request_latent(wl, b, layer)
+            host_lat[(b, layer)] = lat
+            dsa.kv_append(prob.caches[layer], wlm.bits_to_torch(lat[:, :512], "cuda"),
+                          wlm.bits_to_torch(lat[:, 512:], "cuda"), slots,
+                          k_idx=wlm.bits_to_torch(host_keys[b], "cuda") if layer == 0 else None)
+    torch.cuda.synchronize()
+
+    # indexer + top-k as timed (score block in the workspace), then once more writing the scores out
+    idx = dsa.indexer_scores_topk(prob.caches[0], prob.batch, prob.q_idx, prob.w, wl.topk,
+                                  topk_idx=prob.topk_idx, workspace=prob.ws_idx).clone()
+    scores = torch.empty((wl.num_rows, wl.max_seq_len), dtype=torch.float32, device="cuda")
+    idx2 = dsa.indexer_scores_topk(prob.caches[0], prob.batch, prob.q_idx, prob.w, wl.topk, scores_out=scores,
+                                   workspace=prob.ws_idx)
+    assert torch.equal(idx, idx2), "the selection depends on where the scores are written"
+    g_idx = idx.cpu().numpy()
+    q_idx, w = wlm.indexer_queries(wl)
+    oracle_idx = {}
+    for r in rows:
+        b, p = int(req[r]), int(pos[r])
+        keys = key_values(host_keys[b][:p + 1], wl.key_format)
+        o_scores = o.index_scores(o.bf16_to_f64(q_idx[r]), w[r], keys)
+        check_scores(scores[r].cpu().numpy(), o_scores, p, wl.max_seq_len)
+        oracle_idx[r] = o.topk_select(o_scores, wl.topk)
+        check_topk(g_idx[r], oracle_idx[r], o_scores, p, wl.topk)
+    del scores
+
+    # attention on the oracle's index sets for the sampled rows, every layer of the group
+    idx_att = idx.clone()
+    for r in rows:
+        idx_att[r] = torch.from_numpy(oracle_idx[r]).cuda()
+    mla = dsa.sparse_mla_decode if wl.is_decode else dsa.sparse_mla_prefill
+    for layer in range(wl.layers):
+        mla(prob.caches[layer], prob.batch, prob.q[layer], idx_att, wl.scale, out=prob.out[layer],
+            lse=prob.lse[layer], workspace=prob.ws_mla)
+        torch.cuda.synchronize()
+        assert int(prob.ws_mla[:4].view(torch.int32).item()) == 0, "device status word set"
+        q = wlm.mla_queries(wl, layer)
+        out_bits = wlm.torch_to_bits(prob.out[layer][rows])
+        lse = prob.lse[layer][rows].cpu().numpy()
+        for n, r in enumerate(rows):
+            b, p = int(req[r]), int(pos[r])
+            sel = o.valid_selection(oracle_idx[r], p)
+            o_out, o_lse = o.attend(o.bf16_to_f64(q[r]), o.bf16_to_f64(host_lat[(b, layer)][sel]), wl.scale)
+            check_attention(o.bf16_to_f64(out_bits[n]), lse[n], o_out, o_lse)
