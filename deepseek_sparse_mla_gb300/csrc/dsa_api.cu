@@ -31,6 +31,9 @@ static dsa_status fail(dsa_status st, const char* fmt, ...) {
 
 static dsa_status ok() { return DSA_OK; }
 
+// Records a message for dsa_last_error() from the library's other translation units.
+dsa_status report_error(dsa_status st, const char* msg) { return fail(st, "%s", msg); }
+
 static dsa_status cuda_status(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return ok();
   return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));

@@ -45,6 +45,7 @@ MlaPlan plan_mla(int num_rows, int topk);
 
 // Counts every kernel launch the library issues (reported by dsa_kernel_launches).
 void count_launches(int n);
+dsa_status report_error(dsa_status st, const char* msg);
 
 // ---------------------------------------------------------------------------
 // launchers (defined next to their kernels)

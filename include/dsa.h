@@ -61,6 +61,7 @@ extern "C" {
 #define DSA_ROPE_DIM 64      /* k_R / q_rope width                               */
 #define DSA_ROW_DIM 576      /* one cached latent row: [c_KV(512) | k_R(64)]     */
 #define DSA_MAX_TOPK 8192    /* largest supported top-k budget                   */
+#define DSA_STATIC_SCRATCH_BYTES (16u << 20)  /* scratch of dsa_indexer_scores_topk_static */
 
 #define DSA_ABI_VERSION 1
 
@@ -194,6 +195,28 @@ DSA_API dsa_status dsa_kv_append(const dsa_cache* cache, const void* c_kv, const
 DSA_API dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_batch* batch, const void* q_idx,
                                    const float* w, int32_t topk, int32_t* topk_idx, float* scores_out,
                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dsa_indexer_scores_topk without a caller workspace.  The pages have no counterpart: this is
+ * a convenience of this library for callers that cannot allocate device memory per call (a
+ * serving loop whose memory was reserved and locked before it started, or host code without an
+ * allocator).  It computes exactly what dsa_indexer_scores_topk computes, with the same
+ * arguments apart from the workspace, and allocates nothing.
+ *   Scratch: a fixed device array of DSA_STATIC_SCRATCH_BYTES (16 MiB) inside the library, one
+ *     per device.  Shapes whose dsa_indexer_workspace_bytes(num_rows, max_seq_len, topk)
+ *     exceeds it return DSA_ERR_WORKSPACE before anything is launched (for example 32 rows of
+ *     120,000 keys or 64 rows of 60,000 keys fit; 64 rows of 131,072 keys do not).
+ *   Set-up: the first call on a device, made with that device current, looks the array up
+ *     (cudaGetSymbolAddress) and keeps its address; make that first call before capturing the
+ *     stream.  A failed look-up returns DSA_ERR_CUDA.
+ *   Zeroing: the call clears the array's status word on the stream before its launches; nothing
+ *     else in it needs to start at zero.
+ *   Concurrency: calls whose work overlaps on one device share the array and race; the caller
+ *     serialises them (one stream, or an event between streams).
+ */
+DSA_API dsa_status dsa_indexer_scores_topk_static(const dsa_cache* owner, const dsa_batch* batch, const void* q_idx,
+                                          const float* w, int32_t topk, int32_t* topk_idx, float* scores_out,
+                                          void* stream);
 
 /*
  * Sparse absorbed MLA over the selected positions, decode form: one query row
