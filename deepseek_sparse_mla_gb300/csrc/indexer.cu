@@ -5,25 +5,31 @@
 //
 // Rows are grouped by request (1 row in decode, up to 4 with e4m3 keys or 8
 // with bf16 keys otherwise); every key read from HBM serves the whole group.
-// One MMA computes D[key, (row, head)] for a tile of 128 keys:
-//   M = 128 keys, N = 32 heads x rows, K = 128, fp32 accumulators in TMEM,
+// One tile of 128 keys is one MMA chain D[key, (row, head, term)]:
+//   M = 128 keys, N = 32 heads x terms x rows, K = 128, fp32 accumulators in TMEM,
 // and the epilogue applies ReLU, the head weights, the key's scale and the
 // causal mask (masks precede any selection: "Making GLM-5.2 Sparse on TPUs",
 // "Make the sparsity unit match the memory unit").
 //
-// Per CTA (persistent, one per SM, 192 threads):
-//   warp 0     producer: looks up the key tile's pages and TMA-loads them into
-//              a ring of shared-memory stages (8 x 16 KB e4m3, 4 x 32 KB bf16),
-//              staging each key's fp32 scale beside it;
-//   warp 1     MMA issuer;
-//   warps 2-5  workers: per unit they load the group's queries into the B
-//              operand (128-byte swizzled, K-major); for e4m3 keys they convert
-//              each key row to f16 with cvt and store it straight into TMEM as
-//              the A operand (the MMA then reads A from TMEM, B from shared
-//              memory); and they run the epilogue of the previous tile.
-// e4m3 keys need f16 operands on both sides (one MMA kind per instruction):
-// every e4m3 value is exact in f16, and each (row, head) query vector is moved
-// into f16 range by an exact power of two that is folded into its head weight.
+// e4m3 keys run on the kind::f8f6f4 MMA with e4m3 on both sides: each (row,
+// head) query vector is scaled by an exact power of two and split into two
+// e4m3 terms q' = t1 + t2/16 that represent it exactly (query_exponent below),
+// so the two accumulators give q . k exactly up to fp32 rounding; bf16 keys
+// use kind::f16 with the bf16 queries as they are.
+//
+// Per CTA (persistent, one per SM, 416 threads), over one contiguous range of
+// the flattened (group, key tile) list:
+//   warps 0-2  producers, tiles round-robin: page lookups from a register
+//              window of the block table, TMA loads of the key pages into a
+//              ring of 16 KB (e4m3) or 32 KB (bf16) stages, and bulk copies of
+//              the keys' fp32 scales into a separate ring of scale slots;
+//   warp 3     MMA issuer; its commit frees the key stage;
+//   warp 4     B loader: each group's queries (split into e4m3 terms, or bf16)
+//              into the B operand, 128-byte swizzled, K-major;
+//   warps 5-12 two epilogue warpgroups taking alternate tiles; the one that
+//              reads a tile's scales frees its scale slot.
+// The key ring takes all shared memory the B operand does not need (10 stages
+// in decode), so enough bytes are in flight to cover HBM latency.
 #include <mutex>
 
 #include "dsa_internal.cuh"
@@ -37,9 +43,13 @@ namespace idx {
 constexpr int kTileKeys = 128;
 constexpr int kProducers = 3;                      // warps issuing the key copies (TMA issue is per-warp limited)
 constexpr int kThreads = 32 * (kProducers + 2 + 8);  // producers, MMA, B loader, two epilogue warpgroups
-constexpr int kBBytes = 65536;                      // up to 256 (row, head) query vectors of 128 bf16/f16
-constexpr int kRingBytes = 98304;                   // key stages: 6 x 16 KB e4m3 or 3 x 32 KB bf16
-constexpr int kSmemBytes = kBBytes + kRingBytes + 6 * 512 + 1024;
+constexpr int kBBytes = 65536;                      // B operand at most: 256 (row, head) query vectors
+// Dynamic shared memory: [B buffers | key-scale ring | key ring].  The B buffers take only what the
+// group size needs (16 KB in decode), and the key ring gets the rest, up to kMaxStages stages.
+constexpr int kSmemBytes = 200 * 1024;
+constexpr int kMaxStages = 12;
+constexpr int kScStages = 16;                       // key-scale ring (e4m3): 16 tiles x 128 fp32
+constexpr int kScRingBytes = kScStages * 128 * 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPolls = 1u << 22;
 constexpr int kMaxRows = 8;
@@ -145,7 +155,6 @@ template <bool kFp8>
 __global__ void __launch_bounds__(idx::kThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap key_map, const IdxArgs a) {
   using namespace idx;
-  constexpr int kStages = kFp8 ? 6 : 3;
   constexpr int kStageBytes = kFp8 ? 16384 : 32768;
   constexpr int kRowsMax = kFp8 ? 4 : 8;
   constexpr int kTerms = kFp8 ? 2 : 1;               // B rows per (row, head): e4m3 split terms
@@ -153,11 +162,17 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
   constexpr int kEpiWarp0 = kProducers + 2;           // two epilogue warpgroups take alternate tiles
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // carve-up (uniform across the CTA): B buffers sized for the group, then scales, then keys
+  const int n_cap = 32 * kTerms * a.rows_per_group;                // D buffer width (columns)
+  const int row_bytes = kFp8 ? 128 : 256;                           // one query vector in B
+  const int nB = n_cap * row_bytes <= kBBytes / 2 ? 2 : 1;         // B buffers (queries of one group each)
+  const int b_bytes = (n_cap * row_bytes + 1023) / 1024 * 1024;
+  const int kStages = min(kMaxStages, (kSmemBytes - 1024 - nB * b_bytes - kScRingBytes) / kStageBytes);
   uint8_t* sB = smem;
-  uint8_t* sRing = smem + kBBytes;
-  float* sScale = reinterpret_cast<float*>(sRing + kStages * kStageBytes);   // [kStages][128] staged by copies
+  float* sScale = reinterpret_cast<float*>(smem + nB * b_bytes);   // [kScStages][128], e4m3 keys only
+  uint8_t* sRing = smem + nB * b_bytes + kScRingBytes;
 
-  __shared__ uint64_t st_full[kStages], st_empty[kStages];
+  __shared__ uint64_t st_full[kMaxStages], st_empty[kMaxStages], sc_full[kScStages], sc_empty[kScStages];
   __shared__ uint64_t d_full[4], d_empty[4], b_full[2], b_empty[2];
   __shared__ uint64_t mma_done;
   __shared__ float wq_e[2][kMaxRows][32];   // each epilogue warpgroup's head weights for its current group
@@ -175,7 +190,11 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&st_full[s], 1);
-      mbar_init(&st_empty[s], kFp8 ? 2 : 1);       // the MMA (+ the epilogue that reads the scales)
+      mbar_init(&st_empty[s], 1);                  // the MMA's commit frees a key stage
+    }
+    for (int s = 0; s < kScStages; ++s) {
+      mbar_init(&sc_full[s], 1);
+      mbar_init(&sc_empty[s], 1);                  // the epilogue frees a scale slot once it has read it
     }
     for (int b = 0; b < 4; ++b) {
       mbar_init(&d_full[b], 1);
@@ -201,25 +220,26 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const int n_cap = 32 * kTerms * a.rows_per_group;                // D buffer width (columns)
   const int DD = min(4, 512 / n_cap);                               // D ring depth
-  const int row_bytes = kFp8 ? 128 : 256;                           // one query vector in B
-  const int nB = n_cap * row_bytes <= kBBytes / 2 ? 2 : 1;         // B buffers (queries of one group each)
-  const int b_bytes = kBBytes / nB;
 
+  // Producer warps take tiles round-robin and wait for a stage by phase parity.  A warp that has
+  // passed the wait for its previous tile j - nprod knows tile j - nprod - stages was released, so
+  // with nprod <= stages the barrier it now waits on is at most one phase behind and the parity
+  // cannot alias an older phase.  Warps beyond the stage count stay idle.
+  const int nprod = min(kProducers, kStages);
   if (warp < kProducers) {
     // ------------------------------------------------------------------ producers (tiles round-robin)
     // Each warp keeps a register window of 32 page ids (one per lane) and loads the next window
     // ahead of use, so page-table reads never sit between a free stage and its copy.
     const bool bulk_scales = kFp8 && a.box_rows >= 4;
-    const uint32_t tile_tx = (kFp8 ? 1u : 2u) * box_bytes + (bulk_scales ? (uint32_t)a.box_rows * 4u : 0u);
+    const uint32_t key_tx = (kFp8 ? 1u : 2u) * box_bytes;
     const bool windowed = loads_per_tile <= 32;
     TileCursor cur;
     cursor_init(cur, a, gcache, tcache, ngroups, tau0, tau1);
     int win_base = -1, win_req = -1, win_page = -1, nxt_page = -1;
     int last_tile = -1;
-    for (int i = 0; cur.valid(); ++i, cursor_next(cur, a, gcache, tcache)) {
-      if (i % kProducers != warp) continue;
+    for (int i = 0; warp < nprod && cur.valid(); ++i, cursor_next(cur, a, gcache, tcache)) {
+      if (i % nprod != warp) continue;
       const int s = i % kStages, n = i / kStages;
       const int req = cur.G.x, pos_last = cur.G.w + cur.G.z - 1;
       const int32_t* bt = a.m.block_table + (int64_t)req * a.m.block_table_stride;
@@ -241,18 +261,25 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
           nxt_page = l1 < a.m.block_table_stride ? bt[l1] : -1;
         }
       }
+      // the next window is read only by tiles that reach into it (a warp-uniform test), so a window
+      // that was just requested is not waited for by the tile that requested it
+      const bool reach_next = windowed && (((k0 + kTileKeys - 1) >> a.log2_page) >= win_base + 32);
       auto page_of = [&](int lp) -> int {      // called by all 32 lanes together
         if (windowed) {
           const int off = lp - win_base;
-          const int v0 = __shfl_sync(0xffffffffu, win_page, off & 31), v1 = __shfl_sync(0xffffffffu, nxt_page, off & 31);
+          const int v0 = __shfl_sync(0xffffffffu, win_page, off & 31);
+          int v1 = -1;
+          if (reach_next) v1 = __shfl_sync(0xffffffffu, nxt_page, off & 31);
           if (lp >= a.m.block_table_stride) return -1;
           return off < 32 ? v0 : v1;
         }
         return lp < a.m.block_table_stride ? bt[lp] : -1;
       };
       if (n > 0 && !mbar_wait(&st_empty[s], (n - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
+      const int sci = i % kScStages, scn = i / kScStages;
+      if (kFp8 && scn > 0 && !mbar_wait(&sc_empty[sci], (scn - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
       uint8_t* stage = sRing + s * kStageBytes;
-      float* sc = sScale + s * kTileKeys;
+      float* sc = sScale + sci * kTileKeys;
       // sub-box j holds keys k0 + j*box_rows ..; it is loaded when it starts at a visible key of a valid page
       uint32_t nvalid = 0;
       int my_page[4];
@@ -287,7 +314,10 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&st_full[s], nvalid * tile_tx);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&st_full[s], nvalid * key_tx);
+        if (kFp8) mbar_arrive_expect_tx(&sc_full[sci], bulk_scales ? nvalid * (uint32_t)a.box_rows * 4u : 0u);
+      }
       __syncwarp();
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -298,12 +328,15 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
         const int y = (page << a.log2_page) + (key & ((1 << a.log2_page) - 1));
         tma_load_2d(stage + j * box_bytes, &key_map, 0, y, &st_full[s]);
         if (!kFp8) tma_load_2d(stage + 16384 + j * box_bytes, &key_map, 64, y, &st_full[s]);
-        if (bulk_scales) bulk_load(sc + j * a.box_rows, a.key_scales + y, (uint32_t)a.box_rows * 4u, &st_full[s]);
+        if (bulk_scales) bulk_load(sc + j * a.box_rows, a.key_scales + y, (uint32_t)a.box_rows * 4u, &sc_full[sci]);
       }
       last_tile = i;
     }
     // drain: no copy of this warp may still be in flight at exit
-    if (last_tile >= 0) mbar_wait(&st_full[last_tile % kStages], (last_tile / kStages) & 1, a.err, kErrTmaTimeout, kPolls);
+    if (last_tile >= 0) {
+      mbar_wait(&st_full[last_tile % kStages], (last_tile / kStages) & 1, a.err, kErrTmaTimeout, kPolls);
+      if (kFp8) mbar_wait(&sc_full[last_tile % kScStages], (last_tile / kScStages) & 1, a.err, kErrTmaTimeout, kPolls);
+    }
   } else if (warp == kProducers) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -326,16 +359,17 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
           b_addr = smem_u32(sB + ub * b_bytes);
         }
         const int s = i % kStages, n = i / kStages, db = i % DD, nd = i / DD;
-        if (!mbar_wait(&st_full[s], n & 1, a.err, kErrTmaTimeout, kPolls)) { ok = false; break; }
-        if (nd > 0 && !mbar_wait(&d_empty[db], (nd - 1) & 1, a.err, kErrMmaTimeout, kPolls)) { ok = false; break; }
+        // the issuer paces the pipeline: poll without suspending (a suspended wait wakes late)
+        if (!mbar_spin(&st_full[s], n & 1, a.err, kErrTmaTimeout)) { ok = false; break; }
+        if (nd > 0 && !mbar_spin(&d_empty[db], (nd - 1) & 1, a.err, kErrMmaTimeout)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + db * (uint32_t)n_cap;
         const uint32_t stage = smem_u32(sRing + s * kStageBytes);
         if (kFp8) {
+          // one descriptor per operand and tile; K steps of 32 bytes advance the start address field
+          const uint64_t da = smem_desc(stage, 16, 1024, kSwizzle128B), dbq = smem_desc(b_addr, 16, 1024, kSwizzle128B);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss_f8(d, smem_desc(stage + kk * 32, 16, 1024, kSwizzle128B),
-                      smem_desc(b_addr + kk * 32, 16, 1024, kSwizzle128B), idesc, kk > 0);
+          for (int kk = 0; kk < 4; ++kk) mma_ss_f8(d, da + (uint64_t)(2 * kk), dbq + (uint64_t)(2 * kk), idesc, kk > 0);
         } else {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
@@ -432,7 +466,7 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
         named_bar_sync(2 + eg, 128);
       }
       if ((i & 1) == eg) {
-        const int s = i % kStages, n = i / kStages, db = i % DD, nd = i / DD;
+        const int db = i % DD, nd = i / DD;
         if (!mbar_wait(&d_full[db], nd & 1, a.err, kErrMmaTimeout, kPolls)) break;
         tc_fence_after();
         float score[kRowsMax];
@@ -463,11 +497,12 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&d_empty[db]);
         if (kFp8) {
-          // the tile's key scales sit beside its keys; the stage is refilled only after this read
-          if (!mbar_wait(&st_full[s], n & 1, a.err, kErrTmaTimeout, kPolls)) break;
-          const float ks = sScale[s * kTileKeys + key_local];
+          // the tile's key scales sit in their own ring slot, refilled only after this read
+          const int sci = i % kScStages, scn = i / kScStages;
+          if (!mbar_wait(&sc_full[sci], scn & 1, a.err, kErrTmaTimeout, kPolls)) break;
+          const float ks = sScale[sci * kTileKeys + key_local];
           named_bar_sync(4 + eg, 128);
-          if (et == 0) mbar_arrive(&st_empty[s]);
+          if (et == 0) mbar_arrive(&sc_empty[sci]);
 #pragma unroll
           for (int rr = 0; rr < kRowsMax; ++rr) score[rr] *= ks;
         }

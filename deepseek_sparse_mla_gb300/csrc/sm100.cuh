@@ -70,6 +70,19 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_wait, but polling with the non-suspending test: for the single thread whose progress
+// paces a pipeline (an MMA issuer), where the wake-up delay of a suspended wait is on the
+// critical path.  Bounded the same way.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code,
+                                          uint32_t max_polls = 1u << 25) {
+  uint32_t k = 0;
+  while (!mbar_test(bar, parity) && ++k < max_polls) {
+  }
+  if (k < max_polls) return true;
+  atomicOr(err, code);
+  return false;
+}
+
 // Poll until the phase with the given parity completes; false (and err |= code) after max_polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code,
                                           uint32_t max_polls = 1u << 24) {
