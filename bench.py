@@ -304,7 +304,7 @@ def max_over_ranks(x, world, device="cuda"):
 def rank_workload(name: str, rank: int) -> wlm.Workload:
     """Rank r's replica: the named workload's shape and recipe, drawn from its own seed (rank 0 is
     the canonical workload), so ranks serve disjoint request sets of the same size."""
-    wl = wlm.FULL[name]()
+    wl = (wlm.FULL[name] if name in wlm.FULL else wlm.PROFILE[name])()
     if rank == 0:
         return wl
     return wlm.Workload(f"{wl.name}_replica{rank}", list(wl.seq_lens), list(wl.q_lens), wl.page_size, wl.key_format,
@@ -387,7 +387,7 @@ def reference_main(args):
     if rank != 0:
         return
     import torch
-    wl = wlm.FULL[args.workload]()
+    wl = rank_workload(args.workload, 0)
     device = "cuda" if torch.cuda.is_available() else "cpu"
     q_idx, w = wlm.indexer_queries(wl)
     qs = [wlm.mla_queries(wl, l) for l in range(wl.layers)]
@@ -419,7 +419,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wlm.FULL))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wlm.FULL) + sorted(wlm.PROFILE))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-requests", type=int, default=64)
     args = ap.parse_args()

@@ -252,6 +252,17 @@ FULL = {
 }
 
 
+def profile_decode_b64_ctx16k_32k() -> Workload:
+    """The headline decode shape (64 rows, fp8 keys, top-k 2048) at 16K-32K contexts and one layer:
+    about 2 GB resident, small enough for a many-pass profiler capture of one launch."""
+    lens = _rng(4001, _TAG_LENS).integers(16384, 32768 + 1, 64)
+    return Workload("profile_decode_b64_ctx16k-32k_fp8", lens, [1] * 64, 64, "fp8", 2048, 1, 4001)
+
+
+# workloads that exist for profiler captures only (not parity or benchmark configurations)
+PROFILE = {"profile_decode_b64_ctx16k_32k": profile_decode_b64_ctx16k_32k}
+
+
 def reduced(name: str) -> Workload:
     """Same structure as the named workload at sizes a float64 oracle finishes in seconds.
 
