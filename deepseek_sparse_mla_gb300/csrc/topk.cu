@@ -8,12 +8,13 @@
 //
 // Scores are compared as order-preserving 32-bit keys.  Per row (one CTA of
 // 32 warps):
-//   1. radix select over a strided sample of 4096 keys gives the key a safety
+//   1. radix select over a strided sample of 4096 keys (read once into shared
+//      memory) gives the key a safety
 //      margin below the sample's k-th rank: a threshold that the true k-th
 //      key clears with high probability;
-//   2. each warp scans its contiguous share of the row and keeps the
-//      positions at or above the threshold, in order, in its own
-//      shared-memory segment;
+//   2. each warp scans its contiguous share of the row (sixteen coalesced loads
+//      in flight per lane) and keeps the positions at or above the
+//      threshold, in order, in its own shared-memory segment;
 //   3. if the segments hold at least k entries and none overflowed they hold
 //      the answer: radix select over the candidates finds the k-th key T and
 //      how many keys equal to T are taken (the smallest positions first), and
@@ -35,7 +36,9 @@ constexpr int kTopkThreads = 1024;
 constexpr int kWarps = kTopkThreads / 32;
 constexpr int kSample = 4096;
 constexpr int kSeg = 256;                                   // candidate capacity of one warp
-constexpr size_t kTopkSmem = (size_t)kWarps * kSeg * 8 + 2048 * 4;   // (key, position) segments + histogram
+constexpr int kScanUnroll = 16;                            // loads in flight per lane in the candidate scan
+// (key, position) segments + histogram + the sample's keys
+constexpr size_t kTopkSmem = (size_t)kWarps * kSeg * 8 + 2048 * 4 + (size_t)kSample * 4;
 
 // Block-wide exclusive scan of a 32-bit value; returns the exclusive prefix and the block total.
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_tot, uint32_t& total) {
@@ -92,29 +95,55 @@ __device__ void radix_select(Get get, int n, uint32_t k, uint32_t* hist, uint32_
       hist_add(hist, (key >> shift) & (nb - 1), i < n && (key & mask) == prefix);
     }
     __syncthreads();
-    if (tid < 32) {
-      // lane 0 owns the highest bins; find the bin where the count from the top reaches krem
-      const int per = nb / 32;
-      const int top = nb - 1 - tid * per;
-      uint32_t sum = 0;
-      for (int j = 0; j < per; ++j) sum += hist[top - j];
-      uint32_t inc = sum;
+    // find the bin where the count from the top reaches krem, in three short steps:
+    // every warp sums its slice of bins (warp 0 owns the highest), warp 0 finds the slice, and
+    // that slice's warp finds the bin
+    {
+      const int warp = tid >> 5, lane = tid & 31;
+      const int per = nb / kWarps, per_lane = per / 32;          // 64 and 2, or 32 and 1
+      const int top = nb - 1 - warp * per - lane * per_lane;      // this lane's highest bin
+      uint32_t mine = 0;
+      for (int j = 0; j < per_lane; ++j) mine += hist[top - j];
+      uint32_t wsum = mine;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
-        if (tid >= o) inc += t;
+      for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+      if (lane == 0) sh[8 + warp] = wsum;
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t c = sh[8 + lane];
+        uint32_t inc = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += t;
+        }
+        const uint32_t ex = inc - c;
+        if (ex < krem && krem <= inc) {
+          sh[2] = (uint32_t)lane;
+          sh[3] = krem - ex;
+        }
       }
-      const uint32_t ex = inc - sum;
-      if (ex < krem && krem <= inc) {
-        uint32_t c = ex;
-        for (int j = 0; j < per; ++j) {
-          const uint32_t h = hist[top - j];
-          if (c + h >= krem) {
-            sh[0] = (uint32_t)(top - j);
-            sh[1] = krem - c;
-            break;
+      __syncthreads();
+      if (warp == (int)sh[2]) {
+        const uint32_t kw = sh[3];
+        uint32_t inc = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += t;
+        }
+        const uint32_t ex = inc - mine;
+        if (ex < kw && kw <= inc) {
+          uint32_t c = ex;
+          for (int j = 0; j < per_lane; ++j) {
+            const uint32_t h = hist[top - j];
+            if (c + h >= kw) {
+              sh[0] = (uint32_t)(top - j);
+              sh[1] = kw - c;
+              break;
+            }
+            c += h;
           }
-          c += h;
         }
       }
     }
@@ -134,9 +163,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
   extern __shared__ uint64_t topk_smem[];
   uint64_t* seg = topk_smem;                                                  // [kWarps][kSeg] key << 32 | position
   uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem + kWarps * kSeg);    // [2048]
+  uint32_t* samp = hist + 2048;                                               // [kSample]
   __shared__ uint32_t warp_tot[33];
   __shared__ uint32_t cnt[kWarps], eq_before[kWarps], sel_before[kWarps];
-  __shared__ uint32_t sh[4];
+  __shared__ uint32_t sh[8 + kWarps];
   const int r = row0 + blockIdx.x;
   int b, pos;
   row_info(m, r, b, pos);
@@ -156,9 +186,16 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
   const int margin = 3 * (int)sqrtf((float)rank + 1.f) + 8;
   uint32_t t_low = 0;
   if (rank + margin < S) {
+    // the strided sample is read once (all loads in flight together) and selected in shared memory;
+    // S is either n (every position) or kSample = 2^12 (positions i * n / 2^12)
+#pragma unroll
+    for (int j = 0; j < kSample / kTopkThreads; ++j) {
+      const int i = tid + j * kTopkThreads;
+      if (i < S) samp[i] = order_key(sc[S == kSample ? (int)(((int64_t)i * n) >> 12) : i]);
+    }
+    __syncthreads();
     uint32_t T, eq;
-    radix_select([&](int i) { return order_key(sc[(int64_t)i * n / S]); }, S, (uint32_t)(rank + margin + 1), hist,
-                 sh, T, eq);
+    radix_select([&](int i) { return samp[i]; }, S, (uint32_t)(rank + margin + 1), hist, sh, T, eq);
     t_low = T;
   }
 
@@ -167,17 +204,27 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
   const int w0 = warp * per_warp, w1 = min(n, w0 + per_warp);
   uint32_t kept = 0;
   bool overflow = false;
-  for (int s0 = w0; s0 < w1; s0 += 32) {
-    const int s = s0 + lane;
-    const uint32_t key = s < w1 ? order_key(sc[s]) : 0u;
-    const bool take = s < w1 && key >= t_low;
-    const uint32_t ballot = __ballot_sync(0xffffffffu, take);
-    const uint32_t slot = kept + __popc(ballot & ((1u << lane) - 1u));
-    if (take) {
-      if (slot < (uint32_t)kSeg) seg[warp * kSeg + slot] = ((uint64_t)key << 32) | (uint32_t)s;
-      else overflow = true;
+  for (int c0 = w0; c0 < w1; c0 += 32 * kScanUnroll) {
+    // kScanUnroll coalesced loads in flight per lane, then kept in position order one 32-wide row at a time
+    float v[kScanUnroll];
+#pragma unroll
+    for (int j = 0; j < kScanUnroll; ++j) {
+      const int s = c0 + 32 * j + lane;
+      v[j] = s < w1 ? sc[s] : 0.f;
     }
-    kept += __popc(ballot);
+#pragma unroll
+    for (int j = 0; j < kScanUnroll; ++j) {
+      const int s = c0 + 32 * j + lane;
+      const uint32_t key = order_key(v[j]);
+      const bool take = s < w1 && key >= t_low;
+      const uint32_t ballot = __ballot_sync(0xffffffffu, take);
+      const uint32_t slot = kept + __popc(ballot & ((1u << lane) - 1u));
+      if (take) {
+        if (slot < (uint32_t)kSeg) seg[warp * kSeg + slot] = ((uint64_t)key << 32) | (uint32_t)s;
+        else overflow = true;
+      }
+      kept += __popc(ballot);
+    }
   }
   overflow = __any_sync(0xffffffffu, overflow);
   if (lane == 0) {
