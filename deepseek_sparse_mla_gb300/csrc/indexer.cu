@@ -17,17 +17,18 @@
 // so the two accumulators give q . k exactly up to fp32 rounding; bf16 keys
 // use kind::f16 with the bf16 queries as they are.
 //
-// Per CTA (persistent, one per SM, 416 threads), over one contiguous range of
+// Per CTA (persistent, one per SM, 448 threads), over one contiguous range of
 // the flattened (group, key tile) list:
 //   warps 0-2  producers, tiles round-robin: page lookups from a register
 //              window of the block table, TMA loads of the key pages into a
 //              ring of 16 KB (e4m3) or 32 KB (bf16) stages, and bulk copies of
 //              the keys' fp32 scales into a separate ring of scale slots;
-//   warp 3     MMA issuer; its commit frees the key stage;
-//   warp 4     B loader: each group's queries (split into e4m3 terms, or bf16)
+//   warps 3-4  MMA issuers, even and odd tiles; a commit frees the key stage;
+//   warp 5     B loader: each group's queries (split into e4m3 terms, or bf16)
 //              into the B operand, 128-byte swizzled, K-major;
-//   warps 5-12 two epilogue warpgroups taking alternate tiles; the one that
-//              reads a tile's scales frees its scale slot.
+//   warps 6-13 two epilogue warpgroups, even and odd tiles (fed by the
+//              matching issuer); the one that reads a tile's scales frees
+//              its scale slot.
 // The key ring takes all shared memory the B operand does not need (10 stages
 // in decode), so enough bytes are in flight to cover HBM latency.
 #include <mutex>
@@ -42,7 +43,8 @@ using namespace sm100;
 namespace idx {
 constexpr int kTileKeys = 128;
 constexpr int kProducers = 3;                      // warps issuing the key copies (TMA issue is per-warp limited)
-constexpr int kThreads = 32 * (kProducers + 2 + 8);  // producers, MMA, B loader, two epilogue warpgroups
+constexpr int kMmaWarps = 2;                       // MMA issuers: even and odd tiles
+constexpr int kThreads = 32 * (kProducers + kMmaWarps + 1 + 8);  // producers, MMA, B loader, two epilogue warpgroups
 constexpr int kBBytes = 65536;                      // B operand at most: 256 (row, head) query vectors
 // Dynamic shared memory: [B buffers | key-scale ring | key ring].  The B buffers take only what the
 // group size needs (16 KB in decode), and the key ring gets the rest, up to kMaxStages stages.
@@ -50,6 +52,7 @@ constexpr int kSmemBytes = 200 * 1024;
 constexpr int kMaxStages = 12;
 constexpr int kScStages = 16;                       // key-scale ring (e4m3): 16 tiles x 128 fp32
 constexpr int kScRingBytes = kScStages * 128 * 4;
+static_assert((kScStages & (kScStages - 1)) == 0 && kScStages >= kMaxStages + 4, "scale ring: power of two, deep");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPolls = 1u << 22;
 constexpr int kMaxRows = 8;
@@ -158,8 +161,8 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
   constexpr int kStageBytes = kFp8 ? 16384 : 32768;
   constexpr int kRowsMax = kFp8 ? 4 : 8;
   constexpr int kTerms = kFp8 ? 2 : 1;               // B rows per (row, head): e4m3 split terms
-  constexpr int kLoaderWarp = kProducers + 1;
-  constexpr int kEpiWarp0 = kProducers + 2;           // two epilogue warpgroups take alternate tiles
+  constexpr int kLoaderWarp = kProducers + kMmaWarps;
+  constexpr int kEpiWarp0 = kLoaderWarp + 1;           // two epilogue warpgroups take alternate tiles
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // carve-up (uniform across the CTA): B buffers sized for the group, then scales, then keys
@@ -167,14 +170,16 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
   const int row_bytes = kFp8 ? 128 : 256;                           // one query vector in B
   const int nB = n_cap * row_bytes <= kBBytes / 2 ? 2 : 1;         // B buffers (queries of one group each)
   const int b_bytes = (n_cap * row_bytes + 1023) / 1024 * 1024;
-  const int kStages = min(kMaxStages, (kSmemBytes - 1024 - nB * b_bytes - kScRingBytes) / kStageBytes);
+  // an even stage count: a stage's consecutive tiles then have the same parity, i.e. the same issuer
+  constexpr int kScBytes = kFp8 ? kScRingBytes : 0;                // bf16 keys carry no scales
+  const int kStages = min(kMaxStages, (kSmemBytes - 1024 - nB * b_bytes - kScBytes) / kStageBytes) & ~1;
   uint8_t* sB = smem;
   float* sScale = reinterpret_cast<float*>(smem + nB * b_bytes);   // [kScStages][128], e4m3 keys only
-  uint8_t* sRing = smem + nB * b_bytes + kScRingBytes;
+  uint8_t* sRing = smem + nB * b_bytes + kScBytes;
 
   __shared__ uint64_t st_full[kMaxStages], st_empty[kMaxStages], sc_full[kScStages], sc_empty[kScStages];
   __shared__ uint64_t d_full[4], d_empty[4], b_full[2], b_empty[2];
-  __shared__ uint64_t mma_done;
+  __shared__ uint64_t mma_done[kMmaWarps];
   __shared__ float wq_e[2][kMaxRows][32];   // each epilogue warpgroup's head weights for its current group
   __shared__ int4 gcache[kGroupCache];
   __shared__ int tcache[kGroupCache + 1];
@@ -202,9 +207,9 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&b_full[b], 1);
-      mbar_init(&b_empty[b], 1);
+      mbar_init(&b_empty[b], kMmaWarps);         // every issuer commits when it leaves a group
     }
-    mbar_init(&mma_done, 1);
+    for (int m = 0; m < kMmaWarps; ++m) mbar_init(&mma_done[m], 1);
     fence_mbar_init();
   }
   if (warp == kProducers) {
@@ -222,10 +227,11 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
   const uint32_t tmem = tmem_base;
   const int DD = min(4, 512 / n_cap);                               // D ring depth
 
-  // Producer warps take tiles round-robin and wait for a stage by phase parity.  A warp that has
-  // passed the wait for its previous tile j - nprod knows tile j - nprod - stages was released, so
-  // with nprod <= stages the barrier it now waits on is at most one phase behind and the parity
-  // cannot alias an older phase.  Warps beyond the stage count stay idle.
+  // Barriers are waited on by phase parity, so every waiter must be at most one phase behind the
+  // barrier it waits on.  Each stage is always refilled by the same producer warp (stage % nprod),
+  // which waited for that stage's previous release itself; each stage's consumers are one issuer
+  // (tile parity, stages even) that waits on its tiles in order; the D ring (depth 4 or 2) and the
+  // scale ring (16) are used by one epilogue warpgroup per parity, also in order.
   const int nprod = min(kProducers, kStages);
   if (warp < kProducers) {
     // ------------------------------------------------------------------ producers (tiles round-robin)
@@ -238,9 +244,12 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
     cursor_init(cur, a, gcache, tcache, ngroups, tau0, tau1);
     int win_base = -1, win_req = -1, win_page = -1, nxt_page = -1;
     int last_tile = -1;
-    for (int i = 0; warp < nprod && cur.valid(); ++i, cursor_next(cur, a, gcache, tcache)) {
-      if (i % nprod != warp) continue;
-      const int s = i % kStages, n = i / kStages;
+    // ring positions of tile i, stepped once per tile (no division on the issue path)
+    int s = 0, n = 0, sci = 0, scn = 0;
+    for (int i = 0; warp < nprod && cur.valid();
+         ++i, cursor_next(cur, a, gcache, tcache), s = s + 1 == kStages ? 0 : s + 1, n += s == 0,
+             sci = (sci + 1) & (kScStages - 1), scn += sci == 0) {
+      if (s % nprod != warp) continue;
       const int req = cur.G.x, pos_last = cur.G.w + cur.G.z - 1;
       const int32_t* bt = a.m.block_table + (int64_t)req * a.m.block_table_stride;
       const int k0 = cur.t * kTileKeys;
@@ -276,7 +285,6 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
         return lp < a.m.block_table_stride ? bt[lp] : -1;
       };
       if (n > 0 && !mbar_wait(&st_empty[s], (n - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
-      const int sci = i % kScStages, scn = i / kScStages;
       if (kFp8 && scn > 0 && !mbar_wait(&sc_empty[sci], (scn - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
       uint8_t* stage = sRing + s * kStageBytes;
       float* sc = sScale + sci * kTileKeys;
@@ -337,8 +345,11 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
       mbar_wait(&st_full[last_tile % kStages], (last_tile / kStages) & 1, a.err, kErrTmaTimeout, kPolls);
       if (kFp8) mbar_wait(&sc_full[last_tile % kScStages], (last_tile / kScStages) & 1, a.err, kErrTmaTimeout, kPolls);
     }
-  } else if (warp == kProducers) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp < kLoaderWarp) {
+    // ------------------------------------------------------------------ MMA issuers: warp m takes tiles i % 2 == m
+    // (one issuing thread cannot keep up with HBM at one small MMA chain per tile); each walks every
+    // tile to keep the group and ring positions, and commits its own barriers
+    const int mw = warp - kProducers;
     if (lane == 0) {
       TileCursor cur;
       cursor_init(cur, a, gcache, tcache, ngroups, tau0, tau1);
@@ -346,6 +357,7 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
       bool ok = true, new_group = true;
       uint32_t b_addr = 0, idesc = 0;
       int N = 0, ub = 0;
+      int s = 0, n = 0, db = 0, nd = 0;
       for (int i = 0; cur.valid() && ok; ++i) {
         if (new_group) {
           if (i > 0) {
@@ -358,30 +370,33 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
           if (!mbar_wait(&b_full[ub], (gcount / nB) & 1, a.err, kErrMmaTimeout, kPolls)) { ok = false; break; }
           b_addr = smem_u32(sB + ub * b_bytes);
         }
-        const int s = i % kStages, n = i / kStages, db = i % DD, nd = i / DD;
-        // the issuer paces the pipeline: poll without suspending (a suspended wait wakes late)
-        if (!mbar_spin(&st_full[s], n & 1, a.err, kErrTmaTimeout)) { ok = false; break; }
-        if (nd > 0 && !mbar_spin(&d_empty[db], (nd - 1) & 1, a.err, kErrMmaTimeout)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d = tmem + db * (uint32_t)n_cap;
-        const uint32_t stage = smem_u32(sRing + s * kStageBytes);
-        if (kFp8) {
-          // one descriptor per operand and tile; K steps of 32 bytes advance the start address field
-          const uint64_t da = smem_desc(stage, 16, 1024, kSwizzle128B), dbq = smem_desc(b_addr, 16, 1024, kSwizzle128B);
+        if ((i & 1) == mw) {
+          // the issuer paces the pipeline: poll without suspending (a suspended wait wakes late)
+          if (!mbar_spin(&st_full[s], n & 1, a.err, kErrTmaTimeout)) { ok = false; break; }
+          if (nd > 0 && !mbar_spin(&d_empty[db], (nd - 1) & 1, a.err, kErrMmaTimeout)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d = tmem + db * (uint32_t)n_cap;
+          const uint32_t stage = smem_u32(sRing + s * kStageBytes);
+          if (kFp8) {
+            // one descriptor per operand and tile; K steps of 32 bytes advance the start address field
+            const uint64_t da = smem_desc(stage, 16, 1024, kSwizzle128B), dbq = smem_desc(b_addr, 16, 1024, kSwizzle128B);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_ss_f8(d, da + (uint64_t)(2 * kk), dbq + (uint64_t)(2 * kk), idesc, kk > 0);
-        } else {
+            for (int kk = 0; kk < 4; ++kk) mma_ss_f8(d, da + (uint64_t)(2 * kk), dbq + (uint64_t)(2 * kk), idesc, kk > 0);
+          } else {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(d, smem_desc(stage + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B),
-                   smem_desc(b_addr + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B), idesc, kk > 0);
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(d, smem_desc(stage + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B),
+                     smem_desc(b_addr + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B), idesc, kk > 0);
+          }
+          mma_commit(&d_full[db]);
+          mma_commit(&st_empty[s]);
         }
-        mma_commit(&d_full[db]);
-        mma_commit(&st_empty[s]);
+        if (++s == kStages) { s = 0; ++n; }
+        if (++db == DD) { db = 0; ++nd; }
         new_group = cursor_next(cur, a, gcache, tcache);
       }
-      mma_commit(&mma_done);
-      mbar_wait(&mma_done, 0, a.err, kErrMmaTimeout, kPolls);
+      mma_commit(&mma_done[mw]);
+      mbar_wait(&mma_done[mw], 0, a.err, kErrMmaTimeout, kPolls);
     }
   } else if (warp == kLoaderWarp) {
     // ------------------------------------------------------------------ B loader: each group's queries
@@ -451,7 +466,9 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
     TileCursor cur;
     cursor_init(cur, a, gcache, tcache, ngroups, tau0, tau1);
     bool new_group = true;
-    for (int i = 0; cur.valid(); ++i) {
+    int db = 0, nd = 0, sci = 0, scn = 0;
+    for (int i = 0; cur.valid();
+         ++i, db = db + 1 == DD ? 0 : db + 1, nd += db == 0, sci = (sci + 1) & (kScStages - 1), scn += sci == 0) {
       if (new_group) {
         named_bar_sync(2 + eg, 128);                 // the previous group's weights are no longer read
         for (int p = et; p < 32 * cur.G.z; p += 128) {
@@ -466,7 +483,6 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
         named_bar_sync(2 + eg, 128);
       }
       if ((i & 1) == eg) {
-        const int db = i % DD, nd = i / DD;
         if (!mbar_wait(&d_full[db], nd & 1, a.err, kErrMmaTimeout, kPolls)) break;
         tc_fence_after();
         float score[kRowsMax];
@@ -498,7 +514,6 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
         if (lane == 0) mbar_arrive(&d_empty[db]);
         if (kFp8) {
           // the tile's key scales sit in their own ring slot, refilled only after this read
-          const int sci = i % kScStages, scn = i / kScStages;
           if (!mbar_wait(&sc_full[sci], scn & 1, a.err, kErrTmaTimeout, kPolls)) break;
           const float ks = sScale[sci * kTileKeys + key_local];
           named_bar_sync(4 + eg, 128);
