@@ -194,6 +194,136 @@ def kernel_traffic(call: str, files):
 
 
 # ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi samples every 200 ms; started before warm-up so its start-up never overlaps the
+    timed region, and only the samples taken inside [t_begin, t_end] are kept."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.t_begin = None
+        self.t_end = None
+
+    def mark_begin(self):
+        self.t_begin = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    def start(self):
+        import torch
+        ident = None
+        try:
+            ident = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+            if not ident.startswith("GPU-"):
+                ident = "GPU-" + ident
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")
+            ident = vis[torch.cuda.current_device()] if vis and vis[0] else "0"
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        import datetime
+        rows = []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:8]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t_begin is not None and self.t_begin - 0.25 <= r[0] <= (self.t_end or 1e30) + 0.25]
+        use = inside if inside else rows[-3:]
+        reasons = set()
+        for r in use:
+            for n, v in zip(names, r[3]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        sm = [r[1] for r in use]
+        mx = [r[2] for r in use]
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside),
+                "window": "timed region" if inside else "last samples before stop (timed region shorter than 200 ms)"}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: no collective on the data path)
+# ---------------------------------------------------------------------------
+def dist_setup(n_gpus, backend="nccl", device="cuda"):
+    """(rank, world) from the launcher's environment; joins the process group when world > 1.
+
+    Ranks never exchange data on the DSA path: each serves its own replica (its own requests and
+    caches).  The group only carries the barriers and the max-over-ranks of the timings."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    import torch
+    if device == "cuda":
+        torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        if backend == "nccl":
+            dist.init_process_group(backend, device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device="cuda"):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_workload(name: str, rank: int) -> wlm.Workload:
+    """Rank r's replica: the named workload's shape and recipe, drawn from its own seed (rank 0 is
+    the canonical workload), so ranks serve disjoint request sets of the same size."""
+    wl = (wlm.FULL[name] if name in wlm.FULL else wlm.PROFILE[name])()
+    if rank == 0:
+        return wl
+    return wlm.Workload(f"{wl.name}_replica{rank}", list(wl.seq_lens), list(wl.q_lens), wl.page_size, wl.key_format,
+                        wl.topk, wl.layers, wl.seed + 100000 * rank)
+
+
+def aggregate_rate(elapsed_ms_max: float, world: int, layers: int, steps: int) -> float:
+    """Whole-job layer-steps/s: every rank ran `steps` group steps of `layers` layers; the job
+    took as long as its slowest rank."""
+    return world * layers * steps / (elapsed_ms_max / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # the oracle as a CPU baseline (bounded sample)
 # ---------------------------------------------------------------------------
 def oracle_request_problem(wl, b, device):
