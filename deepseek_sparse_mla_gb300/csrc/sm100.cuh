@@ -216,6 +216,17 @@ __device__ __forceinline__ void tmem_ld16x2_32(uint32_t taddr, uint32_t (&r)[32]
       : "r"(taddr));
 }
 
+// As tmem_ld16x2_32 with 16 columns per half: thread t reads TMEM lane (32 * (warp % 4) + t % 16),
+// columns col .. col+15 for t < 16 and col+16 .. col+31 for t >= 16.
+__device__ __forceinline__ void tmem_ld16x2_16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15},"
+      " [%16], 16;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
 // 2^x with the hardware approximation (relative error near 2^-22; results below 2^-126 flush to 0).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

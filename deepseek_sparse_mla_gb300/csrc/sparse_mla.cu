@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
             progressed = true;
           }
         }
-        if (iq < ntiles && iq < ip + 2) {
+        if (iq < ntiles && iq < ip + 1) {
           const int i = iq, u = u0 + i, b = i & 1, n = i >> 1, r = u / T;
           const bool need_q = r != prev_row;
           if (mbar_test(&kv_full[b], n & 1) && (!need_q || mbar_test(&q_full, q_loads & 1)) &&
