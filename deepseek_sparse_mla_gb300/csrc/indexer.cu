@@ -29,8 +29,8 @@
 //   warps 6-13 two epilogue warpgroups, even and odd tiles (fed by the
 //              matching issuer); the one that reads a tile's scales frees
 //              its scale slot.
-// The key ring takes all shared memory the B operand does not need (10 stages
-// in decode), so enough bytes are in flight to cover HBM latency.
+// The key ring holds up to 6 stages: enough bytes in flight to cover HBM
+// latency, few enough not to congest the memory system.
 #include <mutex>
 
 #include "dsa_internal.cuh"
@@ -49,7 +49,9 @@ constexpr int kBBytes = 65536;                      // B operand at most: 256 (r
 // Dynamic shared memory: [B buffers | key-scale ring | key ring].  The B buffers take only what the
 // group size needs (16 KB in decode), and the key ring gets the rest, up to kMaxStages stages.
 constexpr int kSmemBytes = 200 * 1024;
-constexpr int kMaxStages = 12;
+// More key stages in flight than this only lengthen the memory system's queues: across 152 SMs,
+// 6 stages of 16 KB measured 3 % faster than 10 and 12 % faster than 4.
+constexpr int kMaxStages = 6;
 constexpr int kScStages = 16;                       // key-scale ring (e4m3): 16 tiles x 128 fp32
 constexpr int kScRingBytes = kScStages * 128 * 4;
 static_assert((kScStages & (kScStages - 1)) == 0 && kScStages >= kMaxStages + 4, "scale ring: power of two, deep");
