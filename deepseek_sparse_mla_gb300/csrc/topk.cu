@@ -32,13 +32,19 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The float whose order_key is k (k from order_key of a non-NaN float).
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 constexpr int kTopkThreads = 1024;
 constexpr int kWarps = kTopkThreads / 32;
 constexpr int kSample = 4096;
 constexpr int kSeg = 256;                                   // candidate capacity of one warp
 constexpr int kScanUnroll = 16;                            // loads in flight per lane in the candidate scan
+constexpr int kSampleBins = 4096;                           // the sample threshold's histogram: top 12 key bits
 // (key, position) segments + histogram + the sample's keys
-constexpr size_t kTopkSmem = (size_t)kWarps * kSeg * 8 + 2048 * 4 + (size_t)kSample * 4;
+constexpr size_t kTopkSmem = (size_t)kWarps * kSeg * 8 + kSampleBins * 4 + (size_t)kSample * 4;
 
 // Block-wide exclusive scan of a 32-bit value; returns the exclusive prefix and the block total.
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_tot, uint32_t& total) {
@@ -69,12 +75,64 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
   return ex;
 }
 
-// Histogram increment aggregated over the lanes of a warp that hit the same bin.
+// Histogram increment (shared-memory atomic; the inputs here spread over many bins).
 __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool active) {
-  const uint32_t act = __ballot_sync(0xffffffffu, active);
-  if (!active) return;
-  const uint32_t peers = __match_any_sync(act, bin);
-  if ((threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+  if (active) atomicAdd(&hist[bin], 1u);
+}
+
+// The bin where the count from the top of hist[0..nb) reaches krem (1 <= krem <= total), in three
+// short steps: every warp sums its slice of bins (warp 0 owns the highest), warp 0 finds the slice,
+// and that slice's warp finds the bin.  Leaves the bin in sh[0] and krem minus the count above it in
+// sh[1]; ends with a block barrier.  nb is 1024, 2048 or 4096.
+__device__ void find_bin_from_top(const uint32_t* hist, int nb, uint32_t krem, uint32_t* sh) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int per = nb / kWarps, per_lane = per / 32;          // bins per warp slice and per lane
+  const int top = nb - 1 - warp * per - lane * per_lane;      // this lane's highest bin
+  uint32_t mine = 0;
+  for (int j = 0; j < per_lane; ++j) mine += hist[top - j];
+  uint32_t wsum = mine;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  if (lane == 0) sh[8 + warp] = wsum;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t c = sh[8 + lane];
+    uint32_t inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    const uint32_t ex = inc - c;
+    if (ex < krem && krem <= inc) {
+      sh[2] = (uint32_t)lane;
+      sh[3] = krem - ex;
+    }
+  }
+  __syncthreads();
+  if (warp == (int)sh[2]) {
+    const uint32_t kw = sh[3];
+    uint32_t inc = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    const uint32_t ex = inc - mine;
+    if (ex < kw && kw <= inc) {
+      uint32_t c = ex;
+      for (int j = 0; j < per_lane; ++j) {
+        const uint32_t h = hist[top - j];
+        if (c + h >= kw) {
+          sh[0] = (uint32_t)(top - j);
+          sh[1] = kw - c;
+          break;
+        }
+        c += h;
+      }
+    }
+  }
+  __syncthreads();
 }
 
 // Radix select: the k-th largest of the keys produced by get(i), i < n (k <= n).  Returns T and
@@ -95,59 +153,7 @@ __device__ void radix_select(Get get, int n, uint32_t k, uint32_t* hist, uint32_
       hist_add(hist, (key >> shift) & (nb - 1), i < n && (key & mask) == prefix);
     }
     __syncthreads();
-    // find the bin where the count from the top reaches krem, in three short steps:
-    // every warp sums its slice of bins (warp 0 owns the highest), warp 0 finds the slice, and
-    // that slice's warp finds the bin
-    {
-      const int warp = tid >> 5, lane = tid & 31;
-      const int per = nb / kWarps, per_lane = per / 32;          // 64 and 2, or 32 and 1
-      const int top = nb - 1 - warp * per - lane * per_lane;      // this lane's highest bin
-      uint32_t mine = 0;
-      for (int j = 0; j < per_lane; ++j) mine += hist[top - j];
-      uint32_t wsum = mine;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-      if (lane == 0) sh[8 + warp] = wsum;
-      __syncthreads();
-      if (warp == 0) {
-        const uint32_t c = sh[8 + lane];
-        uint32_t inc = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
-          if (lane >= o) inc += t;
-        }
-        const uint32_t ex = inc - c;
-        if (ex < krem && krem <= inc) {
-          sh[2] = (uint32_t)lane;
-          sh[3] = krem - ex;
-        }
-      }
-      __syncthreads();
-      if (warp == (int)sh[2]) {
-        const uint32_t kw = sh[3];
-        uint32_t inc = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
-          if (lane >= o) inc += t;
-        }
-        const uint32_t ex = inc - mine;
-        if (ex < kw && kw <= inc) {
-          uint32_t c = ex;
-          for (int j = 0; j < per_lane; ++j) {
-            const uint32_t h = hist[top - j];
-            if (c + h >= kw) {
-              sh[0] = (uint32_t)(top - j);
-              sh[1] = kw - c;
-              break;
-            }
-            c += h;
-          }
-        }
-      }
-    }
-    __syncthreads();
+    find_bin_from_top(hist, nb, krem, sh);
     prefix |= sh[0] << shift;
     mask |= (uint32_t)(nb - 1) << shift;
     krem = sh[1];
@@ -162,8 +168,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
                                                             int32_t* __restrict__ topk_idx) {
   extern __shared__ uint64_t topk_smem[];
   uint64_t* seg = topk_smem;                                                  // [kWarps][kSeg] key << 32 | position
-  uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem + kWarps * kSeg);    // [2048]
-  uint32_t* samp = hist + 2048;                                               // [kSample]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem + kWarps * kSeg);    // [kSampleBins]
+  uint32_t* samp = hist + kSampleBins;                                        // [kSample]
   __shared__ uint32_t warp_tot[33];
   __shared__ uint32_t cnt[kWarps], eq_before[kWarps], sel_before[kWarps];
   __shared__ uint32_t sh[8 + kWarps];
@@ -193,37 +199,51 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
       const int i = tid + j * kTopkThreads;
       if (i < S) samp[i] = order_key(sc[S == kSample ? (int)(((int64_t)i * n) >> 12) : i]);
     }
+    // the threshold only has to sit at or below the (rank + margin + 1)-th sample key: the lower edge
+    // of the 12-bit bin that holds it (one histogram pass instead of an exact select)
+    for (int i = tid; i < kSampleBins; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
-    uint32_t T, eq;
-    radix_select([&](int i) { return samp[i]; }, S, (uint32_t)(rank + margin + 1), hist, sh, T, eq);
-    t_low = T;
+#pragma unroll
+    for (int j = 0; j < kSample / kTopkThreads; ++j) {
+      const int i = tid + j * kTopkThreads;
+      hist_add(hist, (i < S ? samp[i] : 0u) >> 20, i < S);
+    }
+    __syncthreads();
+    find_bin_from_top(hist, kSampleBins, (uint32_t)(rank + margin + 1), sh);
+    t_low = sh[0] << 20;
+    __syncthreads();
   }
 
   // ---- 2. each warp keeps its share's positions at or above the threshold, in order
+  // each warp scans a contiguous share with kScanUnroll coalesced loads in flight per lane; a score is
+  // kept when it is at least the threshold (compared as floats: the same order as the keys for
+  // non-NaN scores), and its key is formed only then
   const int per_warp = (n + kWarps - 1) / kWarps;
-  const int w0 = warp * per_warp, w1 = min(n, w0 + per_warp);
+  const int w0 = min(n, warp * per_warp), w1 = min(n, w0 + per_warp);
+  float t_low_f = t_low == 0u ? -INFINITY : key_to_float(t_low);   // no threshold: every position
+  if (t_low_f != t_low_f) t_low_f = -INFINITY;                        // a key below every finite score
+  const float thr = t_low_f;
   uint32_t kept = 0;
   bool overflow = false;
   for (int c0 = w0; c0 < w1; c0 += 32 * kScanUnroll) {
-    // kScanUnroll coalesced loads in flight per lane, then kept in position order one 32-wide row at a time
     float v[kScanUnroll];
 #pragma unroll
     for (int j = 0; j < kScanUnroll; ++j) {
       const int s = c0 + 32 * j + lane;
-      v[j] = s < w1 ? sc[s] : 0.f;
+      v[j] = s < w1 ? sc[s] : -INFINITY;
     }
 #pragma unroll
     for (int j = 0; j < kScanUnroll; ++j) {
-      const int s = c0 + 32 * j + lane;
-      const uint32_t key = order_key(v[j]);
-      const bool take = s < w1 && key >= t_low;
+      const bool take = v[j] >= thr && c0 + 32 * j + lane < w1;
       const uint32_t ballot = __ballot_sync(0xffffffffu, take);
-      const uint32_t slot = kept + __popc(ballot & ((1u << lane) - 1u));
-      if (take) {
-        if (slot < (uint32_t)kSeg) seg[warp * kSeg + slot] = ((uint64_t)key << 32) | (uint32_t)s;
-        else overflow = true;
+      if (ballot) {
+        if (take) {
+          const uint32_t slot = kept + __popc(ballot & ((1u << lane) - 1u));
+          if (slot < (uint32_t)kSeg) seg[warp * kSeg + slot] = ((uint64_t)order_key(v[j]) << 32) | (uint32_t)(c0 + 32 * j + lane);
+          else overflow = true;
+        }
+        kept += __popc(ballot);
       }
-      kept += __popc(ballot);
     }
   }
   overflow = __any_sync(0xffffffffu, overflow);
@@ -257,16 +277,23 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
     }
     __syncthreads();
     uint32_t T, need_eq;
-    radix_select(
-        [&](int i) {
-          int lo = 0, hi = kWarps - 1;   // warp whose segment holds candidate i
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (warp_tot[mid] <= (uint32_t)i) lo = mid; else hi = mid - 1;
-          }
-          return (uint32_t)(seg[lo * kSeg + (i - warp_tot[lo])] >> 32);
-        },
-        (int)total, (uint32_t)k, hist, sh, T, need_eq);
+    if (total <= (uint32_t)kSample) {
+      // the candidates' keys, packed into the (now free) sample array: one word per candidate per pass
+      for (uint32_t j = lane; j < kept; j += 32) samp[warp_tot[warp] + j] = (uint32_t)(seg[warp * kSeg + j] >> 32);
+      __syncthreads();
+      radix_select([&](int i) { return samp[i]; }, (int)total, (uint32_t)k, hist, sh, T, need_eq);
+    } else {
+      radix_select(
+          [&](int i) {
+            int lo = 0, hi = kWarps - 1;   // warp whose segment holds candidate i
+            while (lo < hi) {
+              const int mid = (lo + hi + 1) >> 1;
+              if (warp_tot[mid] <= (uint32_t)i) lo = mid; else hi = mid - 1;
+            }
+            return (uint32_t)(seg[lo * kSeg + (i - warp_tot[lo])] >> 32);
+          },
+          (int)total, (uint32_t)k, hist, sh, T, need_eq);
+    }
     // per-warp counts of keys > T and == T, then exclusive prefixes in warp (= position) order
     uint32_t gt = 0, eq = 0;
     for (uint32_t j = lane; j < kept; j += 32) {
