@@ -15,23 +15,26 @@
 // pieces; a row inside one CTA is written directly.
 //
 // Per CTA (16 warps):
-//   warps 0-7  producers: TMA-load the row's 64 x 576 query (9 boxes of 64
+//   warps 0-6  producers: TMA-load the row's 64 x 576 query (9 boxes of 64
 //              heads x 64 columns) and gather each tile's 64 cached rows
 //              straight out of the paged pool with TMA gather4 (four 128-byte
 //              row pieces per instruction, 128-byte swizzle), two stages deep;
-//              warp w looks up and gathers entries 8w .. 8w+7 of each tile,
-//              because the TMA issue rate of one warp is far below HBM speed;
-//   warp 12    MMA issuer: S^T = K Q^T (M = 64 tokens, N = 64 heads, K = 576)
+//              warp w looks up and gathers the tile's groups of four entries
+//              w, w + 7 (and w + 14), because the TMA issue rate of one warp
+//              is far below HBM speed;
+//   warp 7     MMA issuer: S^T = K Q^T (M = 64 tokens, N = 64 heads, K = 576)
 //              into TMEM, then O^T += V^T P^T (M = 128 latent dims x 4,
 //              N = 64 heads, K = 64 tokens) with V read from the same gathered
-//              tile (MN-major) and P^T from shared memory;
-//   warps 8-11 softmax: each thread holds 32 heads of one token (the M = 64
-//              accumulator fills 16 lanes per quarter; the second half of the
-//              lanes reads the other 32 columns), exp2 into bf16 P^T rows (one
-//              128-byte row per token, no transpose needed), a lazy rescale of
-//              the TMEM accumulator only when a head's running maximum grows by
-//              more than 2^8 (checked with one predicate-OR barrier per tile),
-//              and the epilogue.
+//              tile (MN-major) and P^T from shared memory; the next tile's QK
+//              goes out only after the current tile's PV;
+//   warps 8-15 softmax, two warpgroups of 32 heads each: a thread holds 16
+//              heads of one token (the M = 64 accumulator fills 16 lanes per
+//              quarter; the second half of the lanes reads the next 16
+//              columns), exp2 into bf16 P^T rows (one 128-byte row per token,
+//              no transpose needed), a lazy rescale of the TMEM accumulator
+//              only when a head's running maximum grows by more than 2^8
+//              (checked with one predicate-OR barrier per tile), and the
+//              epilogue.
 // Shared memory: Q 72 KB + 2 x 72 KB tiles + 8 KB P^T.  TMEM: 2 x 64 columns
 // for S^T and 4 x 64 columns for O^T.
 #include <mutex>
@@ -52,12 +55,13 @@ constexpr int kQChunkBytes = kHeads * 128;
 constexpr int kQBytes = kChunks * kQChunkBytes;    // 72 KB
 constexpr int kPBytes = kTok * 128;                // P^T: 64 tokens x 64 heads bf16
 constexpr int kSmemBytes = kQBytes + 2 * kStageBytes + kPBytes + 1024;
-constexpr int kProducers = 8;                      // warps issuing the gathers (TMA issue is per-warp limited)
-constexpr int kSoftmaxWarp0 = 8;                   // warpgroup 2
-constexpr int kMmaWarp = 12;                       // first warp of warpgroup 3 (the other three idle)
+constexpr int kProducers = 7;                      // warps issuing the gathers (TMA issue is per-warp limited)
+constexpr int kGroups = kTok / 4;                  // gather4 groups of a tile: group g is taken by warp g % 7
+constexpr int kMmaWarp = 7;                        // last warp of warpgroup 1
+constexpr int kSoftmaxWarp0 = 8;                   // warpgroups 2 and 3: heads 0-31 and heads 32-63
 constexpr int kThreads = 512;
-// register split (sums to 61,440 of the 512 x 128 launched): producers / MMA 80, softmax 240
-constexpr uint32_t kRegsLow = 80, kRegsSoftmax = 240;
+// register split (sums to 61,440 of the 512 x 128 launched): producers / MMA 80, softmax 160
+constexpr uint32_t kRegsLow = 80, kRegsSoftmax = 160;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;                      // S^T of stage b at columns 64 b
 constexpr uint32_t kColO = 128;                    // O^T chunk k (dims 128k..) at columns 128 + 64 k
@@ -103,10 +107,10 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
   __shared__ uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2];
   __shared__ uint64_t p_full, p_empty, q_full, q_empty, o_full, o_empty, mma_done;
-  __shared__ __align__(8) uint8_t tile_mask8[2][8];   // entry validity, one byte per producer warp
+  __shared__ __align__(16) uint8_t tile_mask4[2][kGroups];   // entry validity, 4 bits per gather4 group
   __shared__ float red[4][kHeads];
   __shared__ float mref[kHeads], alpha[kHeads], lfin[kHeads];
-  __shared__ int rescale_tag;
+  __shared__ int rescale_tag[2];
   __shared__ uint32_t tmem_base;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -119,16 +123,16 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       mbar_init(&kv_full[b], kProducers);   // every producer warp arrives (with its own byte count)
       mbar_init(&kv_empty[b], 1);
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_empty[b], 4);
+      mbar_init(&s_empty[b], 8);                 // every softmax warp
     }
-    mbar_init(&p_full, 1);
+    mbar_init(&p_full, 2);                       // both softmax warpgroups
     mbar_init(&p_empty, 1);
     mbar_init(&q_full, 1);
     mbar_init(&q_empty, 1);
     mbar_init(&o_full, 1);
-    mbar_init(&o_empty, 4);
+    mbar_init(&o_empty, 8);
     mbar_init(&mma_done, 1);
-    rescale_tag = 0;
+    rescale_tag[0] = rescale_tag[1] = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -147,20 +151,25 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-
+  // one register split per warpgroup, executed by all of its warps at one instruction: producers and
+  // the MMA issuer (warpgroups 0-1) give registers to the two softmax warpgroups
+  if (warp < kSoftmaxWarp0) {
+  regs_dec<kRegsLow>();
   if (warp < kProducers) {
     // ------------------------------------------------------------------ producers
-    // Warp w owns entries 8w .. 8w+7 of every tile (held by lanes 0..7): it looks up their physical
-    // slots one tile ahead, so the index-buffer and page-table loads stay off the critical path.
-    regs_dec<kRegsLow>();
+    // Warp w owns the tile's gather4 groups w, w + 7 (and w + 14): lane l < 4 ng looks up entry
+    // l % 4 of its group l / 4 one tile ahead, so the index-buffer and page-table loads stay off
+    // the critical path; lane l < 9 ng gathers 128-byte column chunk l % 9 of group l / 9.
+    const int ng = (kGroups - warp + kProducers - 1) / kProducers;   // groups of this warp (2 or 3)
     int q_loads = 0, cur_row = -1;
     int filled[2] = {0, 0};
     auto lookup = [&](int u) -> int64_t {
       const int r = u / T, j = u - r * T;
       int req, pos;
       row_info(a.m, r, req, pos);
-      const int t = j * kTok + 8 * warp + lane;
-      const int e = (lane < 8 && t < a.topk) ? a.topk_idx[(int64_t)r * a.topk + t] : -1;
+      const int g = warp + kProducers * (lane >> 2);
+      const int t = j * kTok + 4 * g + (lane & 3);
+      const int e = (lane < 4 * ng && t < a.topk) ? a.topk_idx[(int64_t)r * a.topk + t] : -1;
       return (e >= 0 && e <= pos) ? token_slot(a.m, req, e, a.log2_page, a.num_pages) : -1;
     };
     int64_t nxt = u0 < u1 ? lookup(u0) : -1;
@@ -178,28 +187,33 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         ++q_loads;
         cur_row = r;
       }
-      const uint32_t valid = __ballot_sync(0xffffffffu, sl >= 0) & 0xFFu;
-      // each group of 4 entries with a valid one is gathered; invalid entries repeat its first valid row
-      const int g = lane >= 18 ? 0 : lane / 9, c = lane % 9;
-      const uint32_t gbits = (valid >> (4 * g)) & 0xFu;
-      const int first = gbits ? 4 * g + __ffs(gbits) - 1 : 0;
+      const uint32_t valid = __ballot_sync(0xffffffffu, sl >= 0) & ((1u << (4 * ng)) - 1u);
+      // each group with a valid entry is gathered; its invalid entries repeat its first valid row
+      const int q = lane / 9 < ng ? lane / 9 : 0, c = lane % 9;
+      const uint32_t gbits = (valid >> (4 * q)) & 0xFu;
+      const int first = gbits ? 4 * q + __ffs(gbits) - 1 : 0;
       const int64_t sub = __shfl_sync(0xffffffffu, sl, first);
       int32_t y[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int64_t v = __shfl_sync(0xffffffffu, sl, 4 * g + k);
+        const int64_t v = __shfl_sync(0xffffffffu, sl, 4 * q + k);
         y[k] = (int32_t)(v >= 0 ? v : sub);
       }
-      const uint32_t groups = ((valid & 0xFu) ? 1u : 0u) + ((valid >> 4) ? 1u : 0u);
       if (lane == 0) {
-        tile_mask8[b][warp] = (uint8_t)valid;
+        uint32_t groups = 0;
+        for (int qq = 0; qq < ng; ++qq) {
+          const uint32_t gb = (valid >> (4 * qq)) & 0xFu;
+          tile_mask4[b][warp + kProducers * qq] = (uint8_t)gb;
+          groups += gb ? 1u : 0u;
+        }
         mbar_arrive_expect_tx(&kv_full[b], groups * (uint32_t)(kChunks * 512));
       }
       __syncwarp();
       ++filled[b];
-      if (lane < 18 && gbits) {
+      if (lane < 9 * ng && gbits) {
         uint8_t* stage = sKV + b * kStageBytes;
-        tma_gather4(stage + c * kChunkBytes + (2 * warp + g) * 512, &kv_map, c * 64, y[0], y[1], y[2], y[3], &kv_full[b]);
+        const int g = warp + kProducers * q;
+        tma_gather4(stage + c * kChunkBytes + g * 512, &kv_map, c * 64, y[0], y[1], y[2], y[3], &kv_full[b]);
       }
       if (u + 1 < u1) nxt = lookup(u + 1);
     }
@@ -207,10 +221,9 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     for (int b = 0; b < 2; ++b)
       if (filled[b] > 0) mbar_wait(&kv_full[b], (filled[b] - 1) & 1, a.err, kErrTmaTimeout, kPolls);
     if (q_loads > 0) mbar_wait(&q_full, (q_loads - 1) & 1, a.err, kErrTmaTimeout, kPolls);
-  } else if (warp >= kMmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer (warp 12; 13-15 idle)
-    regs_dec<kRegsLow>();
-    if (warp == kMmaWarp && lane == 0) {
+  } else {
+    // ------------------------------------------------------------------ MMA issuer (warp 7)
+    if (lane == 0) {
       const uint32_t id_qk = idesc_f16(64, kHeads, true, true, false, false);
       const uint32_t id_pv = idesc_f16(128, kHeads, true, true, true, true);
       // descriptors are built once; per MMA only the start-address field (bytes >> 4) advances
@@ -236,7 +249,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
           if (mbar_test(&p_full, i & 1) && (!seg_first || seg == 0 || mbar_test(&o_empty, (seg - 1) & 1))) {
             if (seg_first) o_init = false;
             tc_fence_after();
-            if (*reinterpret_cast<volatile uint64_t*>(tile_mask8[b]) != 0) {
+            const volatile uint64_t* tm = reinterpret_cast<const volatile uint64_t*>(tile_mask4[b]);
+            if ((tm[0] | tm[1]) != 0) {
               const uint32_t v = opaque_u32(v_lo0 + (uint32_t)((b * kStageBytes) >> 4)), pl = opaque_u32(p_lo0);
               const uint32_t dO = opaque_u32(tmem + kColO);
               if (!o_init) {
@@ -302,18 +316,24 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       mma_commit(&mma_done);
       mbar_wait(&mma_done, 0, a.err, kErrMmaTimeout, kPolls);
     }
+  }
   } else {
-    // ------------------------------------------------------------------ softmax + epilogue (warps 8-11)
     regs_inc<kRegsSoftmax>();
+    // ------------------------------------------------------------------ softmax + epilogue (warps 8-15)
+    // Warpgroup sg (0: warps 8-11, 1: warps 12-15) owns heads 32 sg .. 32 sg + 31: their running
+    // maxima, rescales, denominators and outputs.  S^T row (token) tok sits in TMEM lane
+    // 32 * quarter + lane % 16; a thread holds 16 of its warpgroup's heads for that token (lanes
+    // 0-15 the first 16 columns, lanes 16-31 the next 16).
+    const int sg = (warp - kSoftmaxWarp0) >> 2;
+    const int bar = 1 + sg;                              // named barrier of this warpgroup
     const int quarter = warp & 3;                       // TMEM lanes this warp may touch
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
-    // S^T row (token) tok sits in TMEM lane 32 * quarter + lane % 16; lanes 0-15 take heads 0-31 of
-    // it and lanes 16-31 heads 32-63
     const int tok = 16 * quarter + (lane & 15);
-    const int hh = 32 * (lane >> 4);
-    const int st = threadIdx.x - 32 * kSoftmaxWarp0;     // 0..127
+    const int h0 = 32 * sg;                             // first head of the warpgroup
+    const int hh = h0 + 16 * (lane >> 4);               // first head of this thread
+    const int st = threadIdx.x - 32 * (kSoftmaxWarp0 + 4 * sg);   // 0..127 within the warpgroup
     const int first_row = u0 / T;
-    float l_acc[32];
+    float l_acc[16];
     int seg = 0;
     for (int u = u0; u < u1; ++u) {
       const int i = u - u0, b = i & 1, n = i >> 1, r = u / T, j = u - r * T;
@@ -321,57 +341,56 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       const bool seg_last = (u == u1 - 1) || j == T - 1;
       if (seg_first) {
 #pragma unroll
-        for (int h = 0; h < 32; ++h) l_acc[h] = 0.f;
-        if (st < kHeads) mref[st] = -INFINITY;
+        for (int h = 0; h < 16; ++h) l_acc[h] = 0.f;
+        if (st < 32) mref[h0 + st] = -INFINITY;
       }
       if (!mbar_wait(&kv_full[b], n & 1, a.err, kErrTmaTimeout, kPolls)) break;
       if (!mbar_wait(&s_full[b], n & 1, a.err, kErrMmaTimeout, kPolls)) break;
       tc_fence_after();
-      uint32_t sv[32];
-      tmem_ld16x2_32(tmem + lane_base + kColS + 64 * b, sv);
+      uint32_t sv[16];
+      tmem_ld16x2_16(tmem + lane_base + kColS + 64 * b + h0, sv);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[b]);
-      const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(tile_mask8[b]);
-      const bool valid = (mask >> tok) & 1ull;
-      float z[32];
+      const bool valid = (tile_mask4[b][tok >> 2] >> (tok & 3)) & 1u;
+      float z[16];
 #pragma unroll
-      for (int h = 0; h < 32; ++h) z[h] = valid ? __uint_as_float(sv[h]) * a.scale_log2 : -INFINITY;
+      for (int h = 0; h < 16; ++h) z[h] = valid ? __uint_as_float(sv[h]) * a.scale_log2 : -INFINITY;
       // The running reference changes only when some head's tile maximum exceeds it by more than
       // 2^kRescaleLog2; one predicate-OR barrier decides whether the exact per-head maxima are needed
       // (always on a segment's first tile, which sets the reference).
       bool need = seg_first;                             // mref was just reset by another thread
 #pragma unroll
-      for (int h = 0; h < 32; ++h) need |= z[h] > mref[hh + h] + kRescaleLog2;
-      const bool resc = named_bar_or(1, 128, need);
+      for (int h = 0; h < 16; ++h) need |= z[h] > mref[hh + h] + kRescaleLog2;
+      const bool resc = named_bar_or(bar, 128, need);
       if (resc) {
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
+        for (int h = 0; h < 16; ++h) {
           float mx = z[h];
 #pragma unroll
           for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
           if ((lane & 15) == 0) red[quarter][hh + h] = mx;
         }
-        named_bar_sync(1, 128);
-        if (st < kHeads) {
-          const int h = st;
+        named_bar_sync(bar, 128);
+        if (st < 32) {
+          const int h = h0 + st;
           const float M = fmaxf(fmaxf(red[0][h], red[1][h]), fmaxf(red[2][h], red[3][h]));
           const float old = mref[h];
           float al = 1.f;
           if (M > -INFINITY && (old == -INFINITY || M > old + kRescaleLog2)) {
             al = old == -INFINITY ? 0.f : exp2f(old - M);
-            if (old != -INFINITY) rescale_tag = i + 1;
+            if (old != -INFINITY) rescale_tag[sg] = i + 1;
             mref[h] = M;
           }
           alpha[h] = al;
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(bar, 128);
       }
-      const bool do_rescale = resc && rescale_tag == i + 1;
-      uint32_t pk[16];
+      const bool do_rescale = resc && rescale_tag[sg] == i + 1;
+      uint32_t pk[8];
 #pragma unroll
-      for (int h = 0; h < 32; h += 2) {
+      for (int h = 0; h < 16; h += 2) {
         const float m0 = mref[hh + h], m1 = mref[hh + h + 1];
         const float p0 = z[h] == -INFINITY ? 0.f : ex2_approx(z[h] - m0);
         const float p1 = z[h + 1] == -INFINITY ? 0.f : ex2_approx(z[h + 1] - m1);
@@ -383,41 +402,39 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       // P^T is free once the previous tile's PV has completed (which also settles O^T)
       if (i > 0 && !mbar_wait(&p_empty, (i - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
         *reinterpret_cast<uint4*>(sP + sw128_offset(tok, (hh >> 3) + c)) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       if (do_rescale) {
         tc_fence_after();
 #pragma unroll 1
-        for (int k = 0; k < 4; ++k)
-#pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            uint32_t o[32];
-            const uint32_t addr = tmem + lane_base + kColO + 64 * k + 32 * half;
-            tmem_ld32(addr, o);
-            tmem_wait_ld();
+        for (int k = 0; k < 4; ++k) {
+          uint32_t o[32];
+          const uint32_t addr = tmem + lane_base + kColO + 64 * k + h0;
+          tmem_ld32(addr, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) o[jj] = __float_as_uint(__uint_as_float(o[jj]) * alpha[32 * half + jj]);
-            tmem_st32(addr, o);
-          }
+          for (int jj = 0; jj < 32; ++jj) o[jj] = __float_as_uint(__uint_as_float(o[jj]) * alpha[h0 + jj]);
+          tmem_st32(addr, o);
+        }
         tmem_wait_st();
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      named_bar_sync(1, 128);
+      named_bar_sync(bar, 128);
       if (st == 0) mbar_arrive(&p_full);
 
       if (seg_last) {
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
+        for (int h = 0; h < 16; ++h) {
           float v = l_acc[h];
 #pragma unroll
           for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
           if ((lane & 15) == 0) red[quarter][hh + h] = v;
         }
-        named_bar_sync(1, 128);
-        if (st < kHeads) lfin[st] = (red[0][st] + red[1][st]) + (red[2][st] + red[3][st]);
-        named_bar_sync(1, 128);
+        named_bar_sync(bar, 128);
+        if (st < 32) lfin[h0 + st] = (red[0][h0 + st] + red[1][h0 + st]) + (red[2][h0 + st] + red[3][h0 + st]);
+        named_bar_sync(bar, 128);
         if (!mbar_wait(&o_full, seg & 1, a.err, kErrMmaTimeout, kPolls)) break;
         tc_fence_after();
         const int seg_start = u0 > r * T ? u0 : r * T;
@@ -426,28 +443,25 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 #pragma unroll 1
         for (int k = 0; k < 4; ++k) {
           const int d = 128 * k + 32 * quarter + lane;
-#pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_base + kColO + 64 * k + 32 * half, o);
-            tmem_wait_ld();
-            if (whole) {
-              __nv_bfloat16* dst = a.out + (int64_t)r * kHeads * kLatent + d;
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_base + kColO + 64 * k + h0, o);
+          tmem_wait_ld();
+          if (whole) {
+            __nv_bfloat16* dst = a.out + (int64_t)r * kHeads * kLatent + d;
 #pragma unroll
-              for (int jj = 0; jj < 32; ++jj) {
-                const int h = 32 * half + jj;
-                const float L = lfin[h];
-                dst[(int64_t)h * kLatent] = __float2bfloat16_rn(L > 0.f ? __uint_as_float(o[jj]) / L : 0.f);
-              }
-            } else {
-              float* dst = a.part_o + (int64_t)slot * kHeads * kLatent + d;
-#pragma unroll
-              for (int jj = 0; jj < 32; ++jj) dst[(int64_t)(32 * half + jj) * kLatent] = __uint_as_float(o[jj]);
+            for (int jj = 0; jj < 32; ++jj) {
+              const int h = h0 + jj;
+              const float L = lfin[h];
+              dst[(int64_t)h * kLatent] = __float2bfloat16_rn(L > 0.f ? __uint_as_float(o[jj]) / L : 0.f);
             }
+          } else {
+            float* dst = a.part_o + (int64_t)slot * kHeads * kLatent + d;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) dst[(int64_t)(h0 + jj) * kLatent] = __uint_as_float(o[jj]);
           }
         }
-        if (st < kHeads) {
-          const int h = st;
+        if (st < 32) {
+          const int h = h0 + st;
           const float L = lfin[h];
           if (whole) {
             if (a.lse) a.lse[(int64_t)r * kHeads + h] = L > 0.f ? (mref[h] + log2f(L)) * 0.69314718055994530942f : -INFINITY;
