@@ -43,7 +43,6 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 static bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 IndexerPlan plan_indexer(int num_rows, int max_seq_len, int topk) {
-  (void)topk;
   IndexerPlan p;
   p.score_stride = ((int64_t)max_seq_len + 255) / 256 * 256;
   int64_t per_row = p.score_stride * (int64_t)sizeof(float);
@@ -53,7 +52,16 @@ IndexerPlan plan_indexer(int num_rows, int max_seq_len, int topk) {
   if (p.rows_per_block < 1) p.rows_per_block = 1;
   p.groups_offset = kWorkspaceHeader;
   p.scores_offset = p.groups_offset + ((size_t)(4 + 5 * p.rows_per_block + 1) * sizeof(int32_t) + 255) / 256 * 256;
-  p.workspace_bytes = p.scores_offset + (size_t)p.rows_per_block * (size_t)per_row;
+  size_t end = p.scores_offset + (size_t)p.rows_per_block * (size_t)per_row;
+  // top-k of rows longer than one chunk: one candidate list per chunk, at most kTopkMaxChunks chunks
+  int64_t chunk = (int64_t)16 * topk > kTopkChunkMin ? (int64_t)16 * topk : kTopkChunkMin;
+  if ((max_seq_len + chunk - 1) / chunk > kTopkMaxChunks) chunk = ((int64_t)max_seq_len + kTopkMaxChunks - 1) / kTopkMaxChunks;
+  chunk = (chunk + 1023) / 1024 * 1024;
+  p.topk_chunk = (int)chunk;
+  p.topk_chunks = max_seq_len > chunk ? (int)((max_seq_len + chunk - 1) / chunk) : 0;
+  p.cand_offset = (end + 255) / 256 * 256;
+  p.cand_cnt_offset = p.cand_offset + (size_t)p.rows_per_block * p.topk_chunks * kTopkChunkCap * sizeof(uint64_t);
+  p.workspace_bytes = p.cand_cnt_offset + (size_t)p.rows_per_block * p.topk_chunks * sizeof(uint32_t);
   return p;
 }
 
@@ -225,6 +233,11 @@ dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_batch* batc
   uint32_t* err = reinterpret_cast<uint32_t*>(ws);
   int32_t* groups = reinterpret_cast<int32_t*>(ws + plan.groups_offset);
   float* block = reinterpret_cast<float*>(ws + plan.scores_offset);
+  TopkChunks chunks;
+  chunks.chunk = plan.topk_chunk;
+  chunks.chunks = plan.topk_chunks;
+  chunks.cand = reinterpret_cast<uint64_t*>(ws + plan.cand_offset);
+  chunks.cnt = reinterpret_cast<uint32_t*>(ws + plan.cand_cnt_offset);
   cudaError_t e0 = cudaMemsetAsync(err, 0, sizeof(uint32_t), s);
   if (e0 != cudaSuccess) return cuda_status(e0, "workspace status reset");
   for (int row0 = 0; row0 < batch->num_rows; row0 += plan.rows_per_block) {
@@ -234,7 +247,7 @@ dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_batch* batc
     cudaError_t e = launch_indexer_scores(*owner, m, row0, n, batch->max_seq_len, q_idx, w, scores, stride,
                                           scores_out != nullptr, groups, err, s);
     if (e != cudaSuccess) return cuda_status(e, "indexer launch");
-    e = launch_topk(m, row0, n, scores, stride, batch->max_seq_len, topk, topk_idx, s);
+    e = launch_topk(m, row0, n, scores, stride, batch->max_seq_len, topk, topk_idx, chunks, s);
     if (e != cudaSuccess) return cuda_status(e, "top-k launch");
   }
   return ok();

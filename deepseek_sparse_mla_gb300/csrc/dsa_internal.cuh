@@ -22,6 +22,10 @@ constexpr int kMlaCtas = 152;
 // Upper bound on the fp32 score block the indexer materialises per launch group.
 constexpr size_t kScoreBlockBytes = size_t(256) << 20;
 constexpr size_t kWorkspaceHeader = 256;
+// Top-k of long rows: positions per chunk CTA (at least), and candidates one chunk may keep.
+constexpr int kTopkChunkMin = 32768;
+constexpr int kTopkChunkCap = 4096;
+constexpr int kTopkMaxChunks = 32;
 
 // ---------------------------------------------------------------------------
 // launch plans: shared by the *_workspace_bytes functions and the launches
@@ -31,6 +35,10 @@ struct IndexerPlan {
   int rows_per_block;     // rows scored and selected per pass
   size_t groups_offset;   // int32 scratch: 4 counts, rows_per_block int4 groups, rows_per_block + 1 tile offsets
   size_t scores_offset;   // fp32 score block [rows_per_block][score_stride]
+  int topk_chunk;         // rows longer than this are scanned for top-k candidates by one CTA per chunk
+  int topk_chunks;        // chunks of the longest row (0: no row is split)
+  size_t cand_offset;     // u64 candidate lists [rows_per_block][topk_chunks][kTopkChunkCap]
+  size_t cand_cnt_offset; // u32 candidate counts [rows_per_block][topk_chunks]
   size_t workspace_bytes;
 };
 IndexerPlan plan_indexer(int num_rows, int max_seq_len, int topk);
@@ -68,8 +76,13 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
                                   const void* q_idx, const float* w, float* scores, int64_t score_stride,
                                   bool fill_tail, int32_t* group_scratch, uint32_t* err, cudaStream_t s);
 
+struct TopkChunks {
+  int chunk = 0, chunks = 0;   // chunks == 0: every row is selected by one CTA
+  uint64_t* cand = nullptr;    // [nrows][chunks][kTopkChunkCap] (key << 32 | position)
+  uint32_t* cnt = nullptr;     // [nrows][chunks]; 0xFFFFFFFF marks an overflowed chunk
+};
 cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scores, int64_t score_stride,
-                        int max_seq_len, int topk, int32_t* topk_idx, cudaStream_t s);
+                        int max_seq_len, int topk, int32_t* topk_idx, const TopkChunks& ch, cudaStream_t s);
 
 cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows, const void* q,
                               const int32_t* topk_idx, int topk, float scale, void* out, float* lse,

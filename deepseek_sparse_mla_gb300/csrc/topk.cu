@@ -84,9 +84,10 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool acti
 // short steps: every warp sums its slice of bins (warp 0 owns the highest), warp 0 finds the slice,
 // and that slice's warp finds the bin.  Leaves the bin in sh[0] and krem minus the count above it in
 // sh[1]; ends with a block barrier.  nb is 1024, 2048 or 4096.
+template <int NW>
 __device__ void find_bin_from_top(const uint32_t* hist, int nb, uint32_t krem, uint32_t* sh) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int per = nb / kWarps, per_lane = per / 32;          // bins per warp slice and per lane
+  const int per = nb / NW, per_lane = per / 32;              // bins per warp slice and per lane
   const int top = nb - 1 - warp * per - lane * per_lane;      // this lane's highest bin
   uint32_t mine = 0;
   for (int j = 0; j < per_lane; ++j) mine += hist[top - j];
@@ -96,7 +97,7 @@ __device__ void find_bin_from_top(const uint32_t* hist, int nb, uint32_t krem, u
   if (lane == 0) sh[8 + warp] = wsum;
   __syncthreads();
   if (warp == 0) {
-    const uint32_t c = sh[8 + lane];
+    const uint32_t c = lane < NW ? sh[8 + lane] : 0u;
     uint32_t inc = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -153,7 +154,7 @@ __device__ void radix_select(Get get, int n, uint32_t k, uint32_t* hist, uint32_
       hist_add(hist, (key >> shift) & (nb - 1), i < n && (key & mask) == prefix);
     }
     __syncthreads();
-    find_bin_from_top(hist, nb, krem, sh);
+    find_bin_from_top<kWarps>(hist, nb, krem, sh);
     prefix |= sh[0] << shift;
     mask |= (uint32_t)(nb - 1) << shift;
     krem = sh[1];
@@ -163,68 +164,51 @@ __device__ void radix_select(Get get, int n, uint32_t k, uint32_t* hist, uint32_
   need_eq = krem;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0, const float* __restrict__ scores,
-                                                            int64_t stride, int max_seq_len, int k,
-                                                            int32_t* __restrict__ topk_idx) {
-  extern __shared__ uint64_t topk_smem[];
-  uint64_t* seg = topk_smem;                                                  // [kWarps][kSeg] key << 32 | position
-  uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem + kWarps * kSeg);    // [kSampleBins]
-  uint32_t* samp = hist + kSampleBins;                                        // [kSample]
-  __shared__ uint32_t warp_tot[33];
-  __shared__ uint32_t cnt[kWarps], eq_before[kWarps], sel_before[kWarps];
-  __shared__ uint32_t sh[8 + kWarps];
-  const int r = row0 + blockIdx.x;
-  int b, pos;
-  row_info(m, r, b, pos);
-  int n = pos + 1 > 0 ? pos + 1 : 0;
-  if (n > max_seq_len) n = max_seq_len;   // never read past the row's scores, whatever seq_lens says
-  int32_t* out = topk_idx + (int64_t)r * k;
-  const float* sc = scores + (int64_t)blockIdx.x * stride;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (n <= k) {
-    for (int i = tid; i < k; i += kTopkThreads) out[i] = i < n ? i : -1;
-    return;
-  }
-
-  // ---- 1. threshold: a key ranked a margin below k * S / n in a strided sample
+// Sample threshold of one row (scores sc[0..n), n > k): a key at or below the (rank + margin + 1)-th
+// largest key of a sample of S = min(n, 4096) scores, rank = k S / n (so the row's true k-th key
+// clears it with high probability): the lower edge of the 12-bit bin that holds that sample key.
+// A long row is sampled as 512 runs of 8 consecutive scores spread evenly over the row (one 32-byte
+// sector each, so the sample costs 16 KB of reads instead of a sector per score).
+// 0 when the sample is too small to cut anything.  Every CTA that asks for the same row gets the
+// same value.  The whole block calls it (NT threads); ends with a block barrier.
+template <int NT>
+__device__ uint32_t row_threshold(const float* sc, int n, int k, uint32_t* samp, uint32_t* hist, uint32_t* sh) {
+  const int tid = threadIdx.x;
   const int S = n < kSample ? n : kSample;
   const int rank = (int)(((int64_t)k * S) / n);
   const int margin = 3 * (int)sqrtf((float)rank + 1.f) + 8;
-  uint32_t t_low = 0;
-  if (rank + margin < S) {
-    // the strided sample is read once (all loads in flight together) and selected in shared memory;
-    // S is either n (every position) or kSample = 2^12 (positions i * n / 2^12)
+  if (rank + margin >= S) return 0u;
+  // the sample is read once (all loads in flight together); S is either n (every position) or
+  // kSample = 2^12: run i >> 3 starts at the 8-aligned position below (i >> 3) n / 2^9, and since
+  // n >= 2^12 the runs are disjoint and end inside the row
 #pragma unroll
-    for (int j = 0; j < kSample / kTopkThreads; ++j) {
-      const int i = tid + j * kTopkThreads;
-      if (i < S) samp[i] = order_key(sc[S == kSample ? (int)(((int64_t)i * n) >> 12) : i]);
-    }
-    // the threshold only has to sit at or below the (rank + margin + 1)-th sample key: the lower edge
-    // of the 12-bit bin that holds it (one histogram pass instead of an exact select)
-    for (int i = tid; i < kSampleBins; i += kTopkThreads) hist[i] = 0;
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < kSample / kTopkThreads; ++j) {
-      const int i = tid + j * kTopkThreads;
-      hist_add(hist, (i < S ? samp[i] : 0u) >> 20, i < S);
-    }
-    __syncthreads();
-    find_bin_from_top(hist, kSampleBins, (uint32_t)(rank + margin + 1), sh);
-    t_low = sh[0] << 20;
-    __syncthreads();
+  for (int j = 0; j < kSample / NT; ++j) {
+    const int i = tid + j * NT;
+    if (i < S) samp[i] = order_key(sc[S == kSample ? (int)((((int64_t)(i >> 3) * n) >> 9) & ~7ll) + (i & 7) : i]);
   }
+  for (int i = tid; i < kSampleBins; i += NT) hist[i] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kSample / NT; ++j) {
+    const int i = tid + j * NT;
+    hist_add(hist, (i < S ? samp[i] : 0u) >> 20, i < S);
+  }
+  __syncthreads();
+  find_bin_from_top<NT / 32>(hist, kSampleBins, (uint32_t)(rank + margin + 1), sh);
+  const uint32_t t = sh[0] << 20;
+  __syncthreads();
+  return t;
+}
 
-  // ---- 2. each warp keeps its share's positions at or above the threshold, in order
-  // each warp scans a contiguous share with kScanUnroll coalesced loads in flight per lane; a score is
-  // kept when it is at least the threshold (compared as floats: the same order as the keys for
-  // non-NaN scores), and its key is formed only then
-  const int per_warp = (n + kWarps - 1) / kWarps;
-  const int w0 = min(n, warp * per_warp), w1 = min(n, w0 + per_warp);
+// Scan positions [w0, w1) of sc and keep, in order, those whose score is at least the threshold
+// (compared as floats: the same order as the keys for non-NaN scores) in the warp's segment seg[0..cap):
+// (key << 32 | position).  Returns the number kept (more than cap means overflow).  One warp calls it.
+__device__ uint32_t scan_share(const float* sc, int w0, int w1, uint32_t t_low, uint64_t* seg, uint32_t cap) {
+  const int lane = threadIdx.x & 31;
   float t_low_f = t_low == 0u ? -INFINITY : key_to_float(t_low);   // no threshold: every position
   if (t_low_f != t_low_f) t_low_f = -INFINITY;                        // a key below every finite score
   const float thr = t_low_f;
   uint32_t kept = 0;
-  bool overflow = false;
   for (int c0 = w0; c0 < w1; c0 += 32 * kScanUnroll) {
     float v[kScanUnroll];
 #pragma unroll
@@ -239,29 +223,178 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
       if (ballot) {
         if (take) {
           const uint32_t slot = kept + __popc(ballot & ((1u << lane) - 1u));
-          if (slot < (uint32_t)kSeg) seg[warp * kSeg + slot] = ((uint64_t)order_key(v[j]) << 32) | (uint32_t)(c0 + 32 * j + lane);
-          else overflow = true;
+          if (slot < cap) seg[slot] = ((uint64_t)order_key(v[j]) << 32) | (uint32_t)(c0 + 32 * j + lane);
         }
         kept += __popc(ballot);
       }
     }
   }
-  overflow = __any_sync(0xffffffffu, overflow);
-  if (lane == 0) {
-    cnt[warp] = overflow ? 0xFFFFFFFFu : kept;
-    if (warp == 0) sh[2] = 0;
+  return kept;
+}
+
+// Rows longer than `chunk` are scanned by one CTA per chunk of positions: each computes the row's
+// threshold (the same in every chunk) and writes its candidates, in position order, to its slot of
+// cand (at most cap) with their count in cand_cnt (0xFFFFFFFF on overflow).  Shorter rows are left
+// to topk_kernel.
+constexpr int kChunkThreads = 512;
+constexpr int kChunkWarps = kChunkThreads / 32;
+constexpr size_t kChunkSmem = (size_t)kChunkWarps * kSeg * 8 + kSampleBins * 4 + (size_t)kSample * 4;
+static_assert(kChunkWarps * kSeg == kTopkChunkCap, "a chunk CTA holds exactly one candidate list");
+
+__global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(RowMeta m, int row0, const float* __restrict__ scores,
+                                                                   int64_t stride, int max_seq_len, int k, int chunk,
+                                                                   int chunks, int cap, uint64_t* __restrict__ cand,
+                                                                   uint32_t* __restrict__ cand_cnt) {
+  extern __shared__ uint64_t chunk_smem[];
+  uint64_t* seg = chunk_smem;                                                       // [16][kSeg]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(chunk_smem + kChunkWarps * kSeg);   // [kSampleBins]
+  uint32_t* samp = hist + kSampleBins;                                              // [kSample]
+  __shared__ uint32_t sh[8 + 32], wcnt[kChunkWarps];
+  // the select kernel may be scheduled now: it waits for this grid's results before reading them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int rl = blockIdx.y, r = row0 + rl, c = blockIdx.x;
+  int b, pos;
+  row_info(m, r, b, pos);
+  int n = pos + 1 > 0 ? pos + 1 : 0;
+  if (n > max_seq_len) n = max_seq_len;
+  if (n <= chunk) return;                                     // whole row in topk_kernel
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t* my_cnt = cand_cnt + (int64_t)rl * chunks + c;
+  const int c0 = c * chunk, c1 = min(n, c0 + chunk);
+  if (c0 >= n) {
+    if (tid == 0) *my_cnt = 0;
+    return;
   }
+  const float* sc = scores + (int64_t)rl * stride;
+  const uint32_t t_low = row_threshold<kChunkThreads>(sc, n, k, samp, hist, sh);
+  const int per_warp = (chunk + kChunkWarps - 1) / kChunkWarps;
+  const int w0 = min(c1, c0 + warp * per_warp), w1 = min(c1, w0 + per_warp);
+  const uint32_t kept = scan_share(sc, w0, w1, t_low, seg + warp * kSeg, kSeg);
+  if (lane == 0) wcnt[warp] = kept;
   __syncthreads();
-  if (tid < 32) {
-    const uint32_t c = cnt[tid];
-    const bool bad = __any_sync(0xffffffffu, c == 0xFFFFFFFFu);
-    uint32_t tot = bad ? 0 : c;
+  if (warp == 0) {
+    const uint32_t x = lane < kChunkWarps ? wcnt[lane] : 0u;
+    const bool bad = __any_sync(0xffffffffu, x > (uint32_t)kSeg);
+    uint32_t inc = x;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    if (tid == 0) sh[2] = bad ? 0u : tot;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (lane < kChunkWarps) sh[8 + lane] = inc - x;            // first output index of each warp
+    const uint32_t tot = __shfl_sync(0xffffffffu, inc, 31);
+    if (lane == 0) sh[0] = (bad || tot > (uint32_t)cap) ? 0xFFFFFFFFu : tot;
   }
   __syncthreads();
-  const uint32_t total = sh[2];
+  const uint32_t total = sh[0];
+  if (total != 0xFFFFFFFFu) {
+    uint64_t* dst = cand + ((int64_t)rl * chunks + c) * cap + sh[8 + warp];
+    for (uint32_t j = lane; j < kept; j += 32) dst[j] = seg[warp * kSeg + j];
+  }
+  if (tid == 0) *my_cnt = total;
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0, const float* __restrict__ scores,
+                                                            int64_t stride, int max_seq_len, int k,
+                                                            int32_t* __restrict__ topk_idx, int chunk, int chunks,
+                                                            int cap, const uint64_t* __restrict__ cand,
+                                                            const uint32_t* __restrict__ cand_cnt) {
+  extern __shared__ uint64_t topk_smem[];
+  uint64_t* seg = topk_smem;                                                  // [kWarps][kSeg] key << 32 | position
+  uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem + kWarps * kSeg);    // [kSampleBins]
+  uint32_t* samp = hist + kSampleBins;                                        // [kSample]
+  __shared__ uint32_t warp_tot[33];
+  __shared__ uint32_t cnt[kWarps], eq_before[kWarps], sel_before[kWarps];
+  __shared__ uint32_t sh[8 + kWarps];
+  const int r = row0 + blockIdx.x;
+  int b, pos;
+  row_info(m, r, b, pos);
+  int n = pos + 1 > 0 ? pos + 1 : 0;
+  if (n > max_seq_len) n = max_seq_len;   // never read past the row's scores, whatever seq_lens says
+  // Launched as a programmatic dependent of the chunk kernel, this grid may start before that one
+  // ends.  Rows the chunk kernel scans wait for its results before reading them; the others read
+  // only the scores (complete before the chunk kernel started) and wait just before they exit, so
+  // this grid never ends ahead of the chunk kernel.  (griddepcontrol.wait is a no-op in a plain launch.)
+  const auto wait_chunks = [] { asm volatile("griddepcontrol.wait;" ::: "memory"); };
+  int32_t* out = topk_idx + (int64_t)r * k;
+  const float* sc = scores + (int64_t)blockIdx.x * stride;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (n <= k) {
+    for (int i = tid; i < k; i += kTopkThreads) out[i] = i < n ? i : -1;
+    wait_chunks();
+    return;
+  }
+
+  uint32_t kept = 0, total = 0;
+  if (chunks > 0 && n > chunk) {
+    // ---- 1-2 (long rows). The chunk CTAs' candidate lists, concatenated in chunk (= position)
+    // order and dealt to the warps in equal contiguous shares.
+    const int nch = (n + chunk - 1) / chunk;                 // <= chunks <= 32
+    const uint32_t* rc = cand_cnt + (int64_t)blockIdx.x * chunks;
+    wait_chunks();
+    if (warp == 0) {
+      const uint32_t c = lane < nch ? rc[lane] : 0u;
+      const bool bad = __any_sync(0xffffffffu, c == 0xFFFFFFFFu);
+      uint32_t inc = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+      }
+      eq_before[lane] = bad ? 0u : inc - c;                  // first concatenated index of each chunk
+      const uint32_t tot = __shfl_sync(0xffffffffu, inc, 31);
+      if (lane == 0) sh[2] = (bad || tot > (uint32_t)(kWarps * kSeg)) ? 0u : tot;
+    }
+    __syncthreads();
+    total = sh[2];
+    if (total >= (uint32_t)k) {
+      const uint32_t per = (total + kWarps - 1) / kWarps;
+      const uint32_t i0 = min(total, warp * per), i1 = min(total, i0 + per);
+      kept = i1 - i0;
+      const uint64_t* rcand = cand + (int64_t)blockIdx.x * chunks * cap;
+      // per <= kSeg = 8 x 32: every lane issues its (at most 8) loads before storing any
+      uint64_t v[kSeg / 32];
+#pragma unroll
+      for (int j = 0; j < kSeg / 32; ++j) {
+        const uint32_t i = i0 + lane + 32 * j;
+        if (i < i1) {
+          int c = 0;
+          while (c + 1 < nch && eq_before[c + 1] <= i) ++c;
+          v[j] = rcand[(int64_t)c * cap + (i - eq_before[c])];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kSeg / 32; ++j)
+        if (i0 + lane + 32 * j < i1) seg[warp * kSeg + lane + 32 * j] = v[j];
+      if (lane == 0) cnt[warp] = kept;
+    }
+    __syncthreads();
+  } else {
+    // ---- 1. threshold: a key ranked a margin below k * S / n in a strided sample
+    const uint32_t t_low = row_threshold<kTopkThreads>(sc, n, k, samp, hist, sh);
+
+    // ---- 2. each warp keeps its share's positions at or above the threshold, in order
+    // each warp scans a contiguous share with kScanUnroll coalesced loads in flight per lane; a score
+    // is kept when it is at least the threshold, and its key is formed only then
+    const int per_warp = (n + kWarps - 1) / kWarps;
+    const int w0 = min(n, warp * per_warp), w1 = min(n, w0 + per_warp);
+    kept = scan_share(sc, w0, w1, t_low, seg + warp * kSeg, kSeg);
+    if (lane == 0) {
+      cnt[warp] = kept > (uint32_t)kSeg ? 0xFFFFFFFFu : kept;
+      if (warp == 0) sh[2] = 0;
+    }
+    __syncthreads();
+    if (tid < 32) {
+      const uint32_t c = cnt[tid];
+      const bool bad = __any_sync(0xffffffffu, c == 0xFFFFFFFFu);
+      uint32_t tot = bad ? 0 : c;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      if (tid == 0) sh[2] = bad ? 0u : tot;
+    }
+    __syncthreads();
+    total = sh[2];
+  }
 
   if (total >= (uint32_t)k) {
     // ---- 3a. exact k-th key among the candidates, then an ordered emission
@@ -348,6 +481,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
       out_at += __popc(sel_ballot);
       eq_seen += __popc(eq_ballot);
     }
+    wait_chunks();
     return;
   }
 
@@ -383,18 +517,41 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
     base_gt += tot & 0xFFFFu;
     base_eq += tot >> 16;
   }
+  wait_chunks();
 }
 
 cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scores, int64_t score_stride,
-                        int max_seq_len, int topk, int32_t* topk_idx, cudaStream_t s) {
+                        int max_seq_len, int topk, int32_t* topk_idx, const TopkChunks& ch, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkSmem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChunkSmem);
+    if (e != cudaSuccess) return e;
     configured = true;
   }
-  topk_kernel<<<nrows, kTopkThreads, kTopkSmem, s>>>(m, row0, scores, score_stride, max_seq_len, topk, topk_idx);
+  if (ch.chunks > 0) {
+    topk_chunk_kernel<<<dim3(ch.chunks, nrows), kChunkThreads, kChunkSmem, s>>>(
+        m, row0, scores, score_stride, max_seq_len, topk, ch.chunk, ch.chunks, kTopkChunkCap, ch.cand, ch.cnt);
+    count_launches(1);
+  }
+  // after the chunk kernel the select kernel is a programmatic dependent, so its launch and
+  // prologue overlap the chunk kernel's tail
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nrows);
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = kTopkSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = ch.chunks > 0 ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, m, row0, scores, score_stride, max_seq_len, topk, topk_idx,
+                                     ch.chunk, ch.chunks, (int)kTopkChunkCap, (const uint64_t*)ch.cand,
+                                     (const uint32_t*)ch.cnt);
   count_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -204,8 +204,8 @@ DSA_API dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_bat
  * arguments apart from the workspace, and allocates nothing.
  *   Scratch: a fixed device array of DSA_STATIC_SCRATCH_BYTES (16 MiB) inside the library, one
  *     per device.  Shapes whose dsa_indexer_workspace_bytes(num_rows, max_seq_len, topk)
- *     exceeds it return DSA_ERR_WORKSPACE before anything is launched (for example 32 rows of
- *     120,000 keys or 64 rows of 60,000 keys fit; 64 rows of 131,072 keys do not).
+ *     exceeds it return DSA_ERR_WORKSPACE before anything is launched (for example, with topk
+ *     2048, 32 rows of 90,000 keys or 64 rows of 40,000 keys fit; 64 rows of 131,072 keys do not).
  *   Set-up: the first call on a device, made with that device current, looks the array up
  *     (cudaGetSymbolAddress) and keeps its address; make that first call before capturing the
  *     stream.  A failed look-up returns DSA_ERR_CUDA.

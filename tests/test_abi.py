@@ -70,7 +70,8 @@ def test_workspace_sizes_depend_only_on_shape(lib):
     a = lib.dsa_indexer_workspace_bytes(64, 131072, 2048)
     assert a == lib.dsa_indexer_workspace_bytes(64, 131072, 2048) and a >= 64 * 131072 * 4
     big = lib.dsa_indexer_workspace_bytes(4096, 65536, 2048)
-    assert big <= (256 << 20) + 65536 * 4 + 4096          # score block is bounded, not R x L
+    # score block and top-k candidate lists (a quarter of it here) are bounded, not R x L
+    assert big <= (256 << 20) + (64 << 20) + 65536 * 4 + 4096 * 16
     # attention: two partial slots per persistent CTA, independent of the row count beyond one CTA per SM
     slot = 64 * (512 + 2) * 4
     assert lib.dsa_mla_workspace_bytes(64, 2048) == 256 + 2 * 152 * slot

@@ -218,3 +218,27 @@ def test_results_are_deterministic_across_calls():
     oa = gp.attention(1, a[0])
     ob = gp.attention(1, a[0])
     assert torch.equal(oa[0], ob[0]) and torch.equal(oa[1], ob[1])
+
+
+def test_long_rows_split_into_chunks():
+    """Rows longer than the top-k chunk (32,768 positions) are scanned by several CTAs whose candidate
+    lists are merged: rows just below, at and just above the boundary, and one spanning three chunks."""
+    wl = wlm.Workload("long_chunks", [70001, 32768, 32769, 40000], [1] * 4, 64, "fp8", 256, 1, 3010)
+    run_and_check(wl)
+
+
+def test_all_equal_scores_keep_the_first_positions():
+    """A zero indexer query gives every position the score 0: the tie rule (smaller position first)
+    fixes the selection exactly, and every candidate list overflows, so the full-row select runs."""
+    import torch
+    wl = wlm.Workload("ties", [5000, 40000, 300], [1] * 3, 64, "bf16", 2048, 1, 3011)
+    gp = GpuProblem(HostProblem(wl))
+    gp.append_step()
+    gp.q_idx.zero_()
+    idx, sc = gp.indexer()
+    torch.cuda.synchronize()
+    g_idx, g_sc = idx.cpu().numpy(), sc.cpu().numpy()
+    for r, L in enumerate(wl.seq_lens):
+        assert np.all(g_sc[r, :L] == 0.0)
+        want = np.arange(wl.topk, dtype=np.int32) if L > wl.topk else np.r_[np.arange(L), np.full(wl.topk - L, -1)]
+        assert np.array_equal(g_idx[r], want)
