@@ -482,7 +482,7 @@ def main():
     bytes_of = {"indexer": alg["indexer"], "attention": alg["attention"],
                 "append": (alg["append_owner"] + (wl.layers - 1) * alg["append_shared"]) / wl.layers}
     # each timed call, the kernels it launches and the sources they come from
-    files = {"indexer": (("indexer.cu", "topk.cu"), "indexer_scores_topk: indexer_groups_kernel + indexer_tc_kernel + topk_kernel"),
+    files = {"indexer": (("indexer.cu", "topk.cu"), "indexer_scores_topk: indexer_groups_kernel + indexer_tc_kernel + topk_chunk_kernel + topk_kernel"),
              "attention": (("sparse_mla.cu",), "sparse_mla_decode: sparse_mla_tc_kernel + mla_merge_kernel"),
              "append": (("kv_append.cu",), "kv_append: kv_append_kernel")}
     dom = max(share, key=share.get)

@@ -259,8 +259,16 @@ def profile_decode_b64_ctx16k_32k() -> Workload:
     return Workload("profile_decode_b64_ctx16k-32k_fp8", lens, [1] * 64, 64, "fp8", 2048, 1, 4001)
 
 
+def profile_decode_b24_ctx48k_96k() -> Workload:
+    """Long decode rows (24 rows of 48K-96K positions, fp8 keys, top-k 2048, one layer): the rows are
+    split into 2-3 top-k chunks, as in the headline shape; about 2.3 GB resident."""
+    lens = _rng(4002, _TAG_LENS).integers(49152, 98304 + 1, 24)
+    return Workload("profile_decode_b24_ctx48k-96k_fp8", lens, [1] * 24, 64, "fp8", 2048, 1, 4002)
+
+
 # workloads that exist for profiler captures only (not parity or benchmark configurations)
-PROFILE = {"profile_decode_b64_ctx16k_32k": profile_decode_b64_ctx16k_32k}
+PROFILE = {"profile_decode_b64_ctx16k_32k": profile_decode_b64_ctx16k_32k,
+           "profile_decode_b24_ctx48k_96k": profile_decode_b24_ctx48k_96k}
 
 
 def reduced(name: str) -> Workload:
