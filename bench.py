@@ -88,35 +88,58 @@ class DeviceProblem:
         self.ws_mla = torch.empty(dsa.mla_workspace_bytes(R, wl.topk), dtype=torch.uint8, device=device)
         torch.cuda.synchronize()
 
-    def step(self, marks=None):
-        """One DSA step of the layer group on the current stream."""
+    def step(self, marks=None, io=None):
+        """One DSA step of the layer group on the current stream.  io: the set of per-step inputs
+        and outputs to use (this object's own by default, or one made by io_set())."""
         import deepseek_sparse_mla_gb300 as dsa
         wl = self.wl
+        io = self if io is None else io
         mla = dsa.sparse_mla_decode if wl.is_decode else dsa.sparse_mla_prefill
         if marks is not None:
             marks.mark("append")
         for l in range(wl.layers):
-            dsa.kv_append(self.caches[l], self.new_c[l], self.new_r[l], self.slots,
-                          k_idx=self.new_k if l == 0 else None)
+            dsa.kv_append(self.caches[l], io.new_c[l], io.new_r[l], io.slots, k_idx=io.new_k if l == 0 else None)
         if marks is not None:
             marks.mark("indexer")
-        dsa.indexer_scores_topk(self.caches[0], self.batch, self.q_idx, self.w, wl.topk, topk_idx=self.topk_idx,
+        dsa.indexer_scores_topk(self.caches[0], io.batch, io.q_idx, io.w, wl.topk, topk_idx=self.topk_idx,
                                 workspace=self.ws_idx)
         for l in range(wl.layers):
             if marks is not None:
                 marks.mark("attention")
-            mla(self.caches[l], self.batch, self.q[l], self.topk_idx, wl.scale, out=self.out[l], lse=self.lse[l],
+            mla(self.caches[l], io.batch, io.q[l], self.topk_idx, wl.scale, out=io.out[l], lse=io.lse[l],
                 workspace=self.ws_mla)
         if marks is not None:
             marks.mark(None)
 
-    # per-step host<->device traffic of the end-to-end measurement
-    def step_inputs(self):
-        return (self.new_c + self.new_r + [self.new_k, self.slots, self.q_idx, self.w] + self.q +
-                [self.block_table, self.seq_lens] + ([self.qsl] if self.qsl is not None else []))
+    def io_set(self):
+        """A second set of the step's device inputs and outputs (same values), so that the copies of
+        one step can overlap the kernels of another."""
+        import types
+        import deepseek_sparse_mla_gb300 as dsa
+        c = lambda t: None if t is None else t.clone()   # noqa: E731
+        io = types.SimpleNamespace(new_c=[c(t) for t in self.new_c], new_r=[c(t) for t in self.new_r],
+                                   new_k=c(self.new_k), slots=c(self.slots), q_idx=c(self.q_idx), w=c(self.w),
+                                   q=[c(t) for t in self.q], block_table=c(self.block_table),
+                                   seq_lens=c(self.seq_lens), qsl=c(self.qsl),
+                                   out=[torch_empty_like(t) for t in self.out], lse=[torch_empty_like(t) for t in self.lse])
+        io.batch = dsa.Batch(io.block_table, io.seq_lens, io.qsl, num_rows=self.wl.num_rows,
+                             max_seq_len=self.wl.max_seq_len)
+        return io
 
-    def step_outputs(self):
-        return self.out + self.lse
+    # per-step host<->device traffic of the end-to-end measurement
+    def step_inputs(self, io=None):
+        io = self if io is None else io
+        return (io.new_c + io.new_r + [io.new_k, io.slots, io.q_idx, io.w] + io.q +
+                [io.block_table, io.seq_lens] + ([io.qsl] if io.qsl is not None else []))
+
+    def step_outputs(self, io=None):
+        io = self if io is None else io
+        return io.out + io.lse
+
+
+def torch_empty_like(t):
+    import torch
+    return torch.empty_like(t)
 
 
 class Marks:
@@ -180,13 +203,15 @@ def source_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_traffic(call: str, files):
-    """DRAM bytes per call from profiles/traffic.json, if it was captured on the current sources."""
+def kernel_traffic(call: str, files, workload: str):
+    """DRAM bytes per call from profiles/traffic.json, if it was captured (or scaled) for this workload
+    on the current sources."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
-            ent = json.load(f)[call]
-        if ent.get("source_sha256_16") != source_digest(files):
+            doc = json.load(f)
+        ent = doc[call]
+        if doc.get("workload") != workload or ent.get("source_sha256_16") != source_digest(files):
             return None
         return float(ent["dram_bytes_per_launch"])
     except Exception:
@@ -489,7 +514,7 @@ def main():
     achieved = bytes_of[dom] / (per_call[dom] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": files[dom][1], "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind,
-                "traffic": kernel_traffic(dom, files[dom][0]),
+                "traffic": kernel_traffic(dom, files[dom][0], wl.name),
                 "algorithmic_bytes_per_launch": bytes_of[dom]}
     kernels = {k: {"ms_per_call": per_call[k], "calls_per_step": calls[k], "share": share[k] / tot,
                    "algorithmic_GBps": bytes_of[k] / (per_call[k] * 1e-3) / 1e9,
@@ -497,28 +522,48 @@ def main():
     step_gbps = alg["step"] / (ms_per_step * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers ---------------------------
-    ins = prob.step_inputs()
-    outs = prob.step_outputs()
-    h_in = [t.cpu().pin_memory() for t in ins]
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    # Every step copies its inputs from pinned host memory and its outputs back.  Two sets of device
+    # inputs/outputs let a copy stream move step i+1's inputs and step i-1's outputs while step i's
+    # kernels run (the usual double buffering of a serving loop); a step starts only after its own
+    # inputs have landed, and a set is refilled only after the step that used it and its read-back.
+    ios = [prob, prob.io_set()]
+    h_in = [t.cpu().pin_memory() for t in prob.step_inputs()]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in prob.step_outputs()]
     h2d = int(sum(t.numel() * t.element_size() for t in h_in))
     d2h = int(sum(t.numel() * t.element_size() for t in h_out))
+    comp, copy = torch.cuda.current_stream(), torch.cuda.Stream()
+    ready = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def e2e_step():
-        for d, h in zip(ins, h_in):
-            d.copy_(h, non_blocking=True)
-        prob.step()
-        for h, d in zip(h_out, outs):
-            h.copy_(d, non_blocking=True)
+    def e2e_run(n):
+        copy.wait_stream(comp)
+        with torch.cuda.stream(copy):
+            for d, h in zip(prob.step_inputs(ios[0]), h_in):
+                d.copy_(h, non_blocking=True)
+            ready[0].record(copy)
+        for i in range(n):
+            s = i & 1
+            comp.wait_event(ready[s])
+            prob.step(io=ios[s])
+            done[s].record(comp)
+            with torch.cuda.stream(copy):
+                if i + 1 < n:
+                    if i >= 1:
+                        copy.wait_event(done[s ^ 1])          # step i-1 is done with the other set
+                    for d, h in zip(prob.step_inputs(ios[s ^ 1]), h_in):
+                        d.copy_(h, non_blocking=True)
+                    ready[s ^ 1].record(copy)
+                copy.wait_event(done[s])
+                for h, d in zip(h_out, prob.step_outputs(ios[s])):
+                    h.copy_(d, non_blocking=True)
+        comp.wait_stream(copy)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    e2e_run(args.warmup)
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps)
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
