@@ -53,6 +53,34 @@ MlaPlan plan_mla(int num_rows, int topk);
 
 // Counts every kernel launch the library issues (reported by dsa_kernel_launches).
 void count_launches(int n);
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched as a programmatic
+// dependent of the kernel before it in the stream, so that its launch and its prologue overlap that
+// kernel's tail.  Each kernel keeps one contract: every CTA calls pdl_wait() (which returns once
+// the preceding grid has completed and its writes are visible) before it reads any input memory
+// or exits, and calls pdl_trigger() (if at all: without it the next grid starts when this one
+// completes) only after its own pdl_wait().  A grid can then start only when its predecessor has
+// passed its wait, so every grid before that predecessor has completed; a grid completes only
+// after its predecessor has.  (Both are no-ops in a plain launch.)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 dsa_status report_error(dsa_status st, const char* msg);
 
 // ---------------------------------------------------------------------------

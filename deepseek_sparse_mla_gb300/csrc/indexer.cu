@@ -190,9 +190,6 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t box_bytes = (uint32_t)a.box_rows * 128u;
   const int loads_per_tile = kTileKeys / a.box_rows;
-  const int ngroups = a.counts[0], total_tiles = a.counts[1];
-  const int tau0 = (int)(((int64_t)blockIdx.x * total_tiles) / gridDim.x);
-  const int tau1 = (int)(((int64_t)(blockIdx.x + 1) * total_tiles) / gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -219,6 +216,12 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) prefetch_tmap(&key_map);
+  // the group table and every input are complete past this point (programmatic dependent launch)
+  pdl_wait();
+  pdl_trigger();
+  const int ngroups = a.counts[0], total_tiles = a.counts[1];
+  const int tau0 = (int)(((int64_t)blockIdx.x * total_tiles) / gridDim.x);
+  const int tau1 = (int)(((int64_t)(blockIdx.x + 1) * total_tiles) / gridDim.x);
   for (int g = threadIdx.x; g <= kGroupCache; g += blockDim.x) {
     if (g < kGroupCache) gcache[g] = g < ngroups ? a.groups[g] : make_int4(0, 0, 0, 0);
     tcache[g] = g <= ngroups ? a.tile_start[g] : total_tiles;
@@ -546,6 +549,8 @@ __global__ void __launch_bounds__(1024) indexer_groups_kernel(RowMeta m, int row
                                                               int32_t* tile_start, int32_t* counts) {
   __shared__ int carry, warp_tot[33];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  pdl_wait();
+  pdl_trigger();
   // number of groups: in decode one per row; otherwise walk the requests
   int ngroups = 0;
   if (m.query_start_loc == nullptr) {
@@ -616,6 +621,8 @@ __global__ void __launch_bounds__(1024) indexer_groups_kernel(RowMeta m, int row
 
 // -inf for the positions of a caller-visible score row that no tile covered (s beyond the row's last tile).
 __global__ void indexer_fill_tail_kernel(RowMeta m, int row0, float* scores, int64_t stride, int max_seq_len) {
+  pdl_wait();
+  pdl_trigger();
   const int r = row0 + blockIdx.y;
   int b, pos;
   row_info(m, r, b, pos);
@@ -698,8 +705,10 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
   int4* groups = reinterpret_cast<int4*>(group_scratch + 4);
   int32_t* tile_start = group_scratch + 4 + 4 * nrows;
   const int rg = indexer_rows_per_group(c, decode);
-  indexer_groups_kernel<<<1, 1024, 0, s>>>(m, row0, nrows, rg, groups, tile_start, counts);
+  cudaError_t e = launch_pdl(indexer_groups_kernel, dim3(1), dim3(1024), 0, s, m, row0, nrows, rg, groups, tile_start,
+                             counts);
   count_launches(1);
+  if (e != cudaSuccess) return e;
 
   IdxArgs a;
   a.m = m;
@@ -720,16 +729,16 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
   a.max_seq_len = max_seq_len;
   a.err = err;
   const int grid = g_sm_count;
-  if (fp8)
-    indexer_tc_kernel<true><<<grid, idx::kThreads, idx::kSmemBytes, s>>>(map, a);
-  else
-    indexer_tc_kernel<false><<<grid, idx::kThreads, idx::kSmemBytes, s>>>(map, a);
+  e = fp8 ? launch_pdl(indexer_tc_kernel<true>, dim3(grid), dim3(idx::kThreads), idx::kSmemBytes, s, map, a)
+          : launch_pdl(indexer_tc_kernel<false>, dim3(grid), dim3(idx::kThreads), idx::kSmemBytes, s, map, a);
   count_launches(1);
-  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaGetLastError();
   if (e != cudaSuccess || !fill_tail) return e;
   dim3 fgrid((max_seq_len + 255) / 256 < 64 ? (max_seq_len + 255) / 256 : 64, nrows);
-  indexer_fill_tail_kernel<<<fgrid, 256, 0, s>>>(m, row0, scores, score_stride, max_seq_len);
+  e = launch_pdl(indexer_fill_tail_kernel, fgrid, dim3(256), 0, s, m, row0, scores, score_stride, max_seq_len);
   count_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     const int64_t* __restrict__ slot_mapping, int num_tokens) {
   const int t = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
   if (t >= num_tokens) return;
   const int64_t slot = slot_mapping[t];
   if (slot < 0 || slot >= total_slots) return;
@@ -67,11 +69,13 @@ cudaError_t launch_kv_append(const dsa_cache& c, const void* c_kv, const void* k
                              int num_tokens, cudaStream_t s) {
   const int threads = 256, per_block = threads / 32;
   const int blocks = (num_tokens + per_block - 1) / per_block;
-  kv_append_kernel<<<blocks, threads, 0, s>>>(
-      static_cast<uint4*>(c.latent), (int64_t)c.num_pages * c.page_size, static_cast<uint8_t*>(c.index_keys),
-      c.index_scales, c.key_format, static_cast<const uint4*>(c_kv), static_cast<const uint4*>(k_rope),
-      static_cast<const uint8_t*>(k_idx), k_idx_format, k_idx_scales, slot_mapping, num_tokens);
+  cudaError_t e = launch_pdl(
+      kv_append_kernel, dim3(blocks), dim3(threads), 0, s, static_cast<uint4*>(c.latent),
+      (int64_t)c.num_pages * c.page_size, static_cast<uint8_t*>(c.index_keys), c.index_scales, c.key_format,
+      static_cast<const uint4*>(c_kv), static_cast<const uint4*>(k_rope), static_cast<const uint8_t*>(k_idx),
+      k_idx_format, k_idx_scales, slot_mapping, num_tokens);
   count_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -250,8 +250,8 @@ __global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(RowMeta m, in
   uint32_t* hist = reinterpret_cast<uint32_t*>(chunk_smem + kChunkWarps * kSeg);   // [kSampleBins]
   uint32_t* samp = hist + kSampleBins;                                              // [kSample]
   __shared__ uint32_t sh[8 + 32], wcnt[kChunkWarps];
-  // the select kernel may be scheduled now: it waits for this grid's results before reading them
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_wait();
+  pdl_trigger();   // the select kernel may start: it waits for this grid before reading its lists
   const int rl = blockIdx.y, r = row0 + rl, c = blockIdx.x;
   int b, pos;
   row_info(m, r, b, pos);
@@ -311,11 +311,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
   row_info(m, r, b, pos);
   int n = pos + 1 > 0 ? pos + 1 : 0;
   if (n > max_seq_len) n = max_seq_len;   // never read past the row's scores, whatever seq_lens says
-  // Launched as a programmatic dependent of the chunk kernel, this grid may start before that one
-  // ends.  Rows the chunk kernel scans wait for its results before reading them; the others read
-  // only the scores (complete before the chunk kernel started) and wait just before they exit, so
-  // this grid never ends ahead of the chunk kernel.  (griddepcontrol.wait is a no-op in a plain launch.)
-  const auto wait_chunks = [] { asm volatile("griddepcontrol.wait;" ::: "memory"); };
+  // A programmatic dependent of the chunk kernel (or, when no row is split, of the indexer), this
+  // grid may start before that one ends.  Rows the chunk kernel scans wait for its results before
+  // reading them.  With a chunk kernel, the other rows read only the scores, which are complete
+  // once it has started (it waits for the indexer before it triggers this launch), and wait just
+  // before they exit, so that this grid never completes ahead of its predecessor.  Without one,
+  // every row waits first.  Every CTA triggers the next launch after its wait.
+  const auto wait_chunks = [] {
+    pdl_wait();
+    pdl_trigger();
+  };
+  if (chunks == 0) wait_chunks();
   int32_t* out = topk_idx + (int64_t)r * k;
   const float* sc = scores + (int64_t)blockIdx.x * stride;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -546,7 +552,7 @@ cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scor
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = ch.chunks > 0 ? 1 : 0;
+  cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, m, row0, scores, score_stride, max_seq_len, topk, topk_idx,
                                      ch.chunk, ch.chunks, (int)kTopkChunkCap, (const uint64_t*)ch.cand,
                                      (const uint32_t*)ch.cnt);
