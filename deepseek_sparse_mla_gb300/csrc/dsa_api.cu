@@ -238,8 +238,7 @@ dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_batch* batc
   chunks.chunks = plan.topk_chunks;
   chunks.cand = reinterpret_cast<uint64_t*>(ws + plan.cand_offset);
   chunks.cnt = reinterpret_cast<uint32_t*>(ws + plan.cand_cnt_offset);
-  cudaError_t e0 = cudaMemsetAsync(err, 0, sizeof(uint32_t), s);
-  if (e0 != cudaSuccess) return cuda_status(e0, "workspace status reset");
+  // the status word is cleared on the device by the first row block's group-table kernel
   for (int row0 = 0; row0 < batch->num_rows; row0 += plan.rows_per_block) {
     int n = batch->num_rows - row0 < plan.rows_per_block ? batch->num_rows - row0 : plan.rows_per_block;
     float* scores = scores_out ? scores_out + (int64_t)row0 * batch->max_seq_len : block;

@@ -546,11 +546,14 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
 // Row groups of rows [row0, row0 + nrows): consecutive rows of one request, at most `rg` per group,
 // each with its count of 128-key tiles, and the exclusive prefix of those counts (one CTA).
 __global__ void __launch_bounds__(1024) indexer_groups_kernel(RowMeta m, int row0, int nrows, int rg, int4* groups,
-                                                              int32_t* tile_start, int32_t* counts) {
+                                                              int32_t* tile_start, int32_t* counts, uint32_t* status) {
   __shared__ int carry, warp_tot[33];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   pdl_wait();
   pdl_trigger();
+  // the call's status word starts at zero: the indexer kernels set bits only after their own wait
+  // on this grid (status is null after the call's first row block)
+  if (status != nullptr && tid == 0) *status = 0u;
   // number of groups: in decode one per row; otherwise walk the requests
   int ngroups = 0;
   if (m.query_start_loc == nullptr) {
@@ -706,7 +709,7 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
   int32_t* tile_start = group_scratch + 4 + 4 * nrows;
   const int rg = indexer_rows_per_group(c, decode);
   cudaError_t e = launch_pdl(indexer_groups_kernel, dim3(1), dim3(1024), 0, s, m, row0, nrows, rg, groups, tile_start,
-                             counts);
+                             counts, row0 == 0 ? err : (uint32_t*)nullptr);
   count_launches(1);
   if (e != cudaSuccess) return e;
 

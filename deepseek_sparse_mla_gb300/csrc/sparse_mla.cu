@@ -79,7 +79,8 @@ struct MlaArgs {
   float* lse;
   float* part_o;                  // [2 * ctas][64][512]
   float* part_ml;                 // [2 * ctas][64][2]
-  uint32_t* err;
+  uint32_t* cta_err;              // [ctas]: each CTA's timeout bits (zeroed by the CTA itself)
+  uint32_t* err;                  // the call's status word: the OR of cta_err, written by the merge
 };
 
 __device__ __forceinline__ int unit_start(int c, int units, int ctas) {
@@ -116,6 +117,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
   const int T = a.tiles;
+  uint32_t* const err = a.cta_err + cta;
   const int u0 = unit_start(cta, a.units, a.ctas), u1 = unit_start(cta + 1, a.units, a.ctas);
 
   if (threadIdx.x == 0) {
@@ -151,6 +153,9 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
   // dependent launch: the prologue above overlaps the previous kernel).  No early trigger: the merge
   // kernel launched while this grid still runs made each call about 5 us slower.
   pdl_wait();
+  // this CTA's timeout bits: cleared after the wait (the previous call's merge has read them) and
+  // before the barrier below, after which a bounded wait may set them
+  if (threadIdx.x == 0) *err = 0u;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -181,9 +186,9 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       const int i = u - u0, b = i & 1, n = i >> 1;
       const int r = u / T;
       const int64_t sl = nxt;
-      if (n > 0 && !mbar_wait(&kv_empty[b], (n - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
+      if (n > 0 && !mbar_wait(&kv_empty[b], (n - 1) & 1, err, kErrMmaTimeout, kPolls)) break;
       if (r != cur_row) {
-        if (q_loads > 0 && !mbar_wait(&q_empty, (q_loads - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
+        if (q_loads > 0 && !mbar_wait(&q_empty, (q_loads - 1) & 1, err, kErrMmaTimeout, kPolls)) break;
         if (warp == 0 && lane == 0) {
           mbar_arrive_expect_tx(&q_full, kQBytes);
           for (int c = 0; c < kChunks; ++c) tma_load_2d(sQ + c * kQChunkBytes, &q_map, c * 64, r * kHeads, &q_full);
@@ -223,8 +228,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     }
     // nothing may still be landing in shared memory when the CTA exits
     for (int b = 0; b < 2; ++b)
-      if (filled[b] > 0) mbar_wait(&kv_full[b], (filled[b] - 1) & 1, a.err, kErrTmaTimeout, kPolls);
-    if (q_loads > 0) mbar_wait(&q_full, (q_loads - 1) & 1, a.err, kErrTmaTimeout, kPolls);
+      if (filled[b] > 0) mbar_wait(&kv_full[b], (filled[b] - 1) & 1, err, kErrTmaTimeout, kPolls);
+    if (q_loads > 0) mbar_wait(&q_full, (q_loads - 1) & 1, err, kErrTmaTimeout, kPolls);
   } else {
     // ------------------------------------------------------------------ MMA issuer (warp 7)
     if (lane == 0) {
@@ -312,13 +317,13 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         }
         if (progressed) idle = 0;
         else if (++idle > (kPolls << 2)) {
-          atomicOr(a.err, kErrMmaTimeout);
+          atomicOr(err, kErrMmaTimeout);
           ok = false;
         }
       }
       // every MMA issued here has finished before TMEM is released
       mma_commit(&mma_done);
-      mbar_wait(&mma_done, 0, a.err, kErrMmaTimeout, kPolls);
+      mbar_wait(&mma_done, 0, err, kErrMmaTimeout, kPolls);
     }
   }
   } else {
@@ -348,8 +353,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         for (int h = 0; h < 16; ++h) l_acc[h] = 0.f;
         if (st < 32) mref[h0 + st] = -INFINITY;
       }
-      if (!mbar_wait(&kv_full[b], n & 1, a.err, kErrTmaTimeout, kPolls)) break;
-      if (!mbar_wait(&s_full[b], n & 1, a.err, kErrMmaTimeout, kPolls)) break;
+      if (!mbar_wait(&kv_full[b], n & 1, err, kErrTmaTimeout, kPolls)) break;
+      if (!mbar_wait(&s_full[b], n & 1, err, kErrMmaTimeout, kPolls)) break;
       tc_fence_after();
       uint32_t sv[16];
       tmem_ld16x2_16(tmem + lane_base + kColS + 64 * b + h0, sv);
@@ -404,7 +409,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         pk[h >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
       }
       // P^T is free once the previous tile's PV has completed (which also settles O^T)
-      if (i > 0 && !mbar_wait(&p_empty, (i - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
+      if (i > 0 && !mbar_wait(&p_empty, (i - 1) & 1, err, kErrMmaTimeout, kPolls)) break;
 #pragma unroll
       for (int c = 0; c < 2; ++c)
         *reinterpret_cast<uint4*>(sP + sw128_offset(tok, (hh >> 3) + c)) =
@@ -439,7 +444,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         named_bar_sync(bar, 128);
         if (st < 32) lfin[h0 + st] = (red[0][h0 + st] + red[1][h0 + st]) + (red[2][h0 + st] + red[3][h0 + st]);
         named_bar_sync(bar, 128);
-        if (!mbar_wait(&o_full, seg & 1, a.err, kErrMmaTimeout, kPolls)) break;
+        if (!mbar_wait(&o_full, seg & 1, err, kErrMmaTimeout, kPolls)) break;
         tc_fence_after();
         const int seg_start = u0 > r * T ? u0 : r * T;
         const bool whole = seg_start == r * T && j == T - 1;
@@ -511,6 +516,14 @@ __global__ void __launch_bounds__(512, 2) mla_merge_kernel(MlaArgs a) {
   const int c_first = span[0], c_last = span[1], first_slot = span[2];
   pdl_wait();
   pdl_trigger();
+  if (blockIdx.x == 0 && blockIdx.y == 0 && tid < 32) {
+    // the call's status word: the OR of the attention CTAs' timeout bits (no host reset needed)
+    uint32_t bits = 0;
+    for (int c = tid; c < a.ctas; c += 32) bits |= __ldcg(a.cta_err + c);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o);
+    if (tid == 0) *a.err = bits;
+  }
   if (c_first == c_last) return;    // written directly by the attention kernel
   constexpr int G = 2;
   float M = -INFINITY, L = 0.f;
@@ -611,7 +624,9 @@ MlaPlan plan_mla(int num_rows, int topk) {
   p.units = (int64_t)num_rows * p.tiles > INT32_MAX ? INT32_MAX : num_rows * p.tiles;
   p.ctas = p.units < kMlaCtas ? p.units : kMlaCtas;
   if (p.ctas < 1) p.ctas = 1;
-  p.workspace_bytes = kWorkspaceHeader + (size_t)2 * p.ctas * kHeads * (kLatent + 2) * sizeof(float);
+  p.cta_err_offset = kWorkspaceHeader;
+  p.part_offset = p.cta_err_offset + ((size_t)p.ctas * sizeof(uint32_t) + 255) / 256 * 256;
+  p.workspace_bytes = p.part_offset + (size_t)2 * p.ctas * kHeads * (kLatent + 2) * sizeof(float);
   return p;
 }
 
@@ -629,8 +644,7 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
   if (!g_kv_maps.get(c.latent, (uint64_t)c.num_pages * c.page_size, 1, &kv_map)) return cudaErrorInvalidValue;
   if (!g_q_maps.get(q, (uint64_t)num_rows * kHeads, 64, &q_map)) return cudaErrorInvalidValue;
   uint32_t* err = static_cast<uint32_t*>(workspace);
-  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(uint32_t), s);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
   MlaArgs a;
   a.m = m;
   a.topk_idx = topk_idx;
@@ -643,8 +657,9 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
-  a.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeader);
+  a.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.part_offset);
   a.part_ml = a.part_o + (size_t)2 * plan.ctas * kHeads * kLatent;
+  a.cta_err = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + plan.cta_err_offset);
   a.err = err;
   e = launch_pdl(sparse_mla_tc_kernel, dim3(plan.ctas), dim3(mla::kThreads), mla::kSmemBytes, s, kv_map, q_map, a);
   count_launches(1);

@@ -10,9 +10,9 @@
 // address with cudaGetSymbolAddress and keeps it for later calls on that device.  Make that
 // first call before capturing the stream into a graph.
 //
-// Zeroing: only the status word must be zero when the kernels start; the call clears it on the
-// stream before launching, as the workspace entry point does.  The group table and the score
-// block are fully written before they are read.
+// Zeroing: only the status word must start at zero; the call's first kernel clears it on the
+// device, as in the workspace entry point.  The group table, the score block and the top-k
+// candidate lists are fully written before they are read.
 //
 // Concurrency: there is one array per device.  Two calls whose work overlaps on the device
 // (different streams, or different host threads) share it and race; serialise them.

@@ -209,8 +209,8 @@ DSA_API dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_bat
  *   Set-up: the first call on a device, made with that device current, looks the array up
  *     (cudaGetSymbolAddress) and keeps its address; make that first call before capturing the
  *     stream.  A failed look-up returns DSA_ERR_CUDA.
- *   Zeroing: the call clears the array's status word on the stream before its launches; nothing
- *     else in it needs to start at zero.
+ *   Zeroing: the call's first kernel clears the array's status word; nothing else in it needs
+ *     to start at zero.
  *   Concurrency: calls whose work overlaps on one device share the array and race; the caller
  *     serialises them (one stream, or an event between streams).
  */

@@ -72,11 +72,12 @@ def test_workspace_sizes_depend_only_on_shape(lib):
     big = lib.dsa_indexer_workspace_bytes(4096, 65536, 2048)
     # score block and top-k candidate lists (a quarter of it here) are bounded, not R x L
     assert big <= (256 << 20) + (64 << 20) + 65536 * 4 + 4096 * 16
-    # attention: two partial slots per persistent CTA, independent of the row count beyond one CTA per SM
+    # attention: a timeout word and two partial slots per persistent CTA, independent of the row count
+    # beyond one CTA per SM
     slot = 64 * (512 + 2) * 4
-    assert lib.dsa_mla_workspace_bytes(64, 2048) == 256 + 2 * 152 * slot
+    assert lib.dsa_mla_workspace_bytes(64, 2048) == 256 + 768 + 2 * 152 * slot      # 152 words: 608 -> 768 bytes
     assert lib.dsa_mla_workspace_bytes(4096, 2048) == lib.dsa_mla_workspace_bytes(100000, 2048)
-    assert lib.dsa_mla_workspace_bytes(2, 128) == 256 + 2 * 4 * slot          # 2 rows x 2 tiles -> 4 CTAs
+    assert lib.dsa_mla_workspace_bytes(2, 128) == 256 + 256 + 2 * 4 * slot    # 2 rows x 2 tiles -> 4 CTAs
     assert lib.dsa_indexer_workspace_bytes(1, 0, 2048) == 0
 
 
