@@ -46,7 +46,8 @@ IndexerPlan plan_indexer(int num_rows, int max_seq_len, int topk);
 struct MlaPlan {
   int tiles;              // 64-entry tiles per row of the index buffer
   int units;              // rows x tiles, split into one contiguous range per CTA
-  int ctas;               // persistent CTAs (at most one per SM)
+  int ctas;               // persistent CTAs of the unit split (at most one per SM)
+  int split;              // > 1: pieces per row, one cluster of `split` CTAs per row (few rows)
   size_t cta_err_offset;  // u32 timeout bits per CTA, after the 256-byte header (status word first)
   size_t part_offset;     // two (64 x 512 + 64 x 2) fp32 partial slots per CTA
   size_t workspace_bytes;

@@ -9,10 +9,14 @@
 // unabsorbed 192 + 64 width; "Carry sparse reads through prefill": online
 // softmax over the selected entries).
 //
-// Work: the rows' index buffers are cut into tiles of 64 entries; the
+// Work: the rows' index buffers are cut into tiles of 64 entries.  With few
+// rows (2 R <= 152) each row is cut into S = 2, 4 or 8 equal pieces taken by
+// the S CTAs of one thread-block cluster: each CTA leaves its unnormalised O^T
+// in its shared memory, and after a cluster barrier each CTA merges 64 / S
+// heads from all pieces through distributed shared memory.  Otherwise the
 // (row, tile) units are split into one contiguous range per CTA (persistent,
-// one CTA per SM).  A row cut between CTAs is finished by an LSE merge of the
-// pieces; a row inside one CTA is written directly.
+// one CTA per SM); a row cut between CTAs is finished by an LSE merge of the
+// pieces in a second kernel, and a row inside one CTA is written directly.
 //
 // Per CTA (16 warps):
 //   warps 0-6  producers: TMA-load the row's 64 x 576 query (9 boxes of 64
@@ -73,6 +77,7 @@ struct MlaArgs {
   RowMeta m;
   const int32_t* topk_idx;
   int topk, tiles, units, ctas;
+  int split;                      // > 1: cluster mode, pieces per row (= cluster size); 1: unit split
   int log2_page, num_pages;
   float scale_log2;               // softmax scale * log2(e)
   __nv_bfloat16* out;
@@ -118,7 +123,10 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
   const int cta = blockIdx.x;
   const int T = a.tiles;
   uint32_t* const err = a.cta_err + cta;
-  const int u0 = unit_start(cta, a.units, a.ctas), u1 = unit_start(cta + 1, a.units, a.ctas);
+  const int split = a.split;
+  // cluster mode: piece cta % split of row cta / split; otherwise a contiguous range of units
+  const int u0 = split > 1 ? (cta / split) * T + (cta % split) * T / split : unit_start(cta, a.units, a.ctas);
+  const int u1 = split > 1 ? (cta / split) * T + (cta % split + 1) * T / split : unit_start(cta + 1, a.units, a.ctas);
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -449,6 +457,9 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         const int seg_start = u0 > r * T ? u0 : r * T;
         const bool whole = seg_start == r * T && j == T - 1;
         const int slot = r == first_row ? 2 * cta : 2 * cta + 1;
+        // a piece without valid entries never initialised its accumulator (its l is 0 for every head,
+        // and positive for every head otherwise): it contributes zeros, not TMEM contents
+        const bool has_valid = lfin[h0] > 0.f;
 #pragma unroll 1
         for (int k = 0; k < 4; ++k) {
           const int d = 128 * k + 32 * quarter + lane;
@@ -463,10 +474,16 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
               const float L = lfin[h];
               dst[(int64_t)h * kLatent] = __float2bfloat16_rn(L > 0.f ? __uint_as_float(o[jj]) / L : 0.f);
             }
+          } else if (split > 1) {
+            // cluster mode: the piece stays in this CTA's (now idle) gather stages, [64 heads][512] fp32,
+            // with its m (mref, log2 units) and l (lfin) beside it
+            float* sO = reinterpret_cast<float*>(sKV) + d;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) sO[(h0 + jj) * kLatent] = has_valid ? __uint_as_float(o[jj]) : 0.f;
           } else {
             float* dst = a.part_o + (int64_t)slot * kHeads * kLatent + d;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) dst[(int64_t)(h0 + jj) * kLatent] = __uint_as_float(o[jj]);
+            for (int jj = 0; jj < 32; ++jj) dst[(int64_t)(h0 + jj) * kLatent] = has_valid ? __uint_as_float(o[jj]) : 0.f;
           }
         }
         if (st < 32) {
@@ -474,7 +491,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
           const float L = lfin[h];
           if (whole) {
             if (a.lse) a.lse[(int64_t)r * kHeads + h] = L > 0.f ? (mref[h] + log2f(L)) * 0.69314718055994530942f : -INFINITY;
-          } else {
+          } else if (split == 1) {
             a.part_ml[((int64_t)slot * kHeads + h) * 2] = L > 0.f ? mref[h] * 0.69314718055994530942f : -INFINITY;
             a.part_ml[((int64_t)slot * kHeads + h) * 2 + 1] = L;
           }
@@ -489,6 +506,50 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (split > 1) {
+    // ---- cluster merge: CTA q of the row's cluster writes heads [q HS, q HS + HS), HS = 64 / split:
+    //   out = sum_p w_p O_p,  w_p = 2^{m_p - M} / L,  L = sum_p 2^{m_p - M} l_p,  lse = (M + log2 L) ln 2.
+    cluster_sync();                     // every piece's O, m and l are in its CTA's shared memory
+    const int r = u0 / T, q = cta % split, HS = kHeads / split, hs0 = q * HS;
+    float* wts = reinterpret_cast<float*>(sP);          // [split][HS]
+    if (threadIdx.x < HS) {
+      const int h = hs0 + threadIdx.x;
+      float M = -INFINITY, L = 0.f;
+      for (int p = 0; p < split; ++p) {
+        const float l = ld_cluster_f32(cluster_map(&lfin[h], p)), m = ld_cluster_f32(cluster_map(&mref[h], p));
+        if (l > 0.f) {
+          const float Mn = fmaxf(M, m);
+          L = L * exp2f(M - Mn) + l * exp2f(m - Mn);   // M = -inf: L is 0 and so is the product
+          M = Mn;
+        }
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (int p = 0; p < split; ++p) {
+        const float l = ld_cluster_f32(cluster_map(&lfin[h], p)), m = ld_cluster_f32(cluster_map(&mref[h], p));
+        wts[p * HS + threadIdx.x] = l > 0.f ? exp2f(m - M) * inv : 0.f;
+      }
+      if (a.lse) a.lse[(int64_t)r * kHeads + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < HS * (kLatent / 4); i += kThreads) {
+      const int hl = i / (kLatent / 4), d = 4 * (i % (kLatent / 4)), h = hs0 + hl;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int p = 0; p < split; ++p) {
+        const float w = wts[p * HS + hl];
+        const float4 x = ld_cluster_v4(cluster_map(sKV, p) + (uint32_t)((h * kLatent + d) * 4));
+        acc.x = fmaf(w, x.x, acc.x);
+        acc.y = fmaf(w, x.y, acc.y);
+        acc.z = fmaf(w, x.z, acc.z);
+        acc.w = fmaf(w, x.w, acc.w);
+      }
+      uint2 v;
+      __nv_bfloat162* xo = reinterpret_cast<__nv_bfloat162*>(&v);
+      xo[0] = __floats2bfloat162_rn(acc.x, acc.y);
+      xo[1] = __floats2bfloat162_rn(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(a.out + ((int64_t)r * kHeads + h) * kLatent + d) = v;
+    }
+    cluster_sync();                     // no CTA leaves while a peer may still read its shared memory
+  }
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -516,14 +577,6 @@ __global__ void __launch_bounds__(512, 2) mla_merge_kernel(MlaArgs a) {
   const int c_first = span[0], c_last = span[1], first_slot = span[2];
   pdl_wait();
   pdl_trigger();
-  if (blockIdx.x == 0 && blockIdx.y == 0 && tid < 32) {
-    // the call's status word: the OR of the attention CTAs' timeout bits (no host reset needed)
-    uint32_t bits = 0;
-    for (int c = tid; c < a.ctas; c += 32) bits |= __ldcg(a.cta_err + c);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o);
-    if (tid == 0) *a.err = bits;
-  }
   if (c_first == c_last) return;    // written directly by the attention kernel
   constexpr int G = 2;
   float M = -INFINITY, L = 0.f;
@@ -584,6 +637,18 @@ __global__ void __launch_bounds__(512, 2) mla_merge_kernel(MlaArgs a) {
   if (a.lse && (tid & 31) == 0) a.lse[(int64_t)r * kHeads + h] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
+// The call's status word: the OR of the attention CTAs' timeout bits (one warp, the call's last
+// kernel; no host reset needed).
+__global__ void __launch_bounds__(32) mla_status_kernel(MlaArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  uint32_t bits = 0;
+  for (int c = threadIdx.x; c < a.ctas; c += 32) bits |= __ldcg(a.cta_err + c);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o);
+  if (threadIdx.x == 0) *a.err = bits;
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -624,6 +689,10 @@ MlaPlan plan_mla(int num_rows, int topk) {
   p.units = (int64_t)num_rows * p.tiles > INT32_MAX ? INT32_MAX : num_rows * p.tiles;
   p.ctas = p.units < kMlaCtas ? p.units : kMlaCtas;
   if (p.ctas < 1) p.ctas = 1;
+  // few rows: S pieces per row in clusters of S (the largest power of two <= 8 with S R <= 152 and
+  // S <= tiles); the workspace below is sized for the unit split either way
+  p.split = 1;
+  while (p.split < 8 && (int64_t)2 * p.split * num_rows <= kMlaCtas && 2 * p.split <= p.tiles) p.split *= 2;
   p.cta_err_offset = kWorkspaceHeader;
   p.part_offset = p.cta_err_offset + ((size_t)p.ctas * sizeof(uint32_t) + 255) / 256 * 256;
   p.workspace_bytes = p.part_offset + (size_t)2 * p.ctas * kHeads * (kLatent + 2) * sizeof(float);
@@ -651,7 +720,8 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
   a.topk = topk;
   a.tiles = plan.tiles;
   a.units = plan.units;
-  a.ctas = plan.ctas;
+  a.ctas = plan.split > 1 ? num_rows * plan.split : plan.ctas;
+  a.split = plan.split;
   a.log2_page = ilog2(c.page_size);
   a.num_pages = c.num_pages;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -661,23 +731,34 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
   a.part_ml = a.part_o + (size_t)2 * plan.ctas * kHeads * kLatent;
   a.cta_err = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + plan.cta_err_offset);
   a.err = err;
-  e = launch_pdl(sparse_mla_tc_kernel, dim3(plan.ctas), dim3(mla::kThreads), mla::kSmemBytes, s, kv_map, q_map, a);
+  {
+    cudaLaunchConfig_t c = {};
+    c.gridDim = dim3(a.ctas);
+    c.blockDim = dim3(mla::kThreads);
+    c.dynamicSmemBytes = mla::kSmemBytes;
+    c.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = (unsigned)plan.split;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    c.attrs = at;
+    c.numAttrs = plan.split > 1 ? 2 : 1;
+    e = cudaLaunchKernelEx(&c, sparse_mla_tc_kernel, kv_map, q_map, a);
+  }
   count_launches(1);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // the merge may be scheduled while the attention grid drains (it waits for that grid's writes)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_rows, kHeads / kMergeHeads);
-  cfg.blockDim = dim3(512);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mla_merge_kernel, a);
+  if (plan.split == 1) {
+    // the merge may be scheduled while the attention grid drains (it waits for that grid's writes)
+    e = launch_pdl(mla_merge_kernel, dim3(num_rows, kHeads / kMergeHeads), dim3(512), 0, s, a);
+    count_launches(1);
+    if (e != cudaSuccess) return e;
+  }
+  e = launch_pdl(mla_status_kernel, dim3(1), dim3(32), 0, s, a);
   count_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
