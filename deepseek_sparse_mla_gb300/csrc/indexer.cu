@@ -339,8 +339,8 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
         if (page < 0) continue;
         const int key = k0 + j * a.box_rows;
         const int y = (page << a.log2_page) + (key & ((1 << a.log2_page) - 1));
-        tma_load_2d(stage + j * box_bytes, &key_map, 0, y, &st_full[s]);
-        if (!kFp8) tma_load_2d(stage + 16384 + j * box_bytes, &key_map, 64, y, &st_full[s]);
+        tma_load_2d_hint(stage + j * box_bytes, &key_map, 0, y, &st_full[s], l2_evict_first());
+        if (!kFp8) tma_load_2d_hint(stage + 16384 + j * box_bytes, &key_map, 64, y, &st_full[s], l2_evict_first());
         if (bulk_scales) bulk_load(sc + j * a.box_rows, a.key_scales + y, (uint32_t)a.box_rows * 4u, &sc_full[sci]);
       }
       last_tile = i;

@@ -230,7 +230,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       if (lane < 9 * ng && gbits) {
         uint8_t* stage = sKV + b * kStageBytes;
         const int g = warp + kProducers * q;
-        tma_gather4(stage + c * kChunkBytes + g * 512, &kv_map, c * 64, y[0], y[1], y[2], y[3], &kv_full[b]);
+        tma_gather4_hint(stage + c * kChunkBytes + g * 512, &kv_map, c * 64, y[0], y[1], y[2], y[3], &kv_full[b],
+                         l2_evict_first());
       }
       if (u + 1 < u1) nxt = lookup(u + 1);
     }
