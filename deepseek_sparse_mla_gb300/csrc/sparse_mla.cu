@@ -11,9 +11,10 @@
 //
 // Work: the rows' index buffers are cut into tiles of 64 entries.  With few
 // rows (2 R <= 152) each row is cut into S = 2, 4 or 8 equal pieces taken by
-// the S CTAs of one thread-block cluster: each CTA leaves its unnormalised O^T
-// in its shared memory, and after a cluster barrier each CTA merges 64 / S
-// heads from all pieces through distributed shared memory.  Otherwise the
+// the S CTAs of one thread-block cluster: after a cluster barrier each CTA
+// pushes its unnormalised O^T and (m, l) into the shared memory of the CTA
+// that owns each head (distributed shared memory), and each CTA merges its
+// 64 / S heads locally.  Otherwise the
 // (row, tile) units are split into one contiguous range per CTA (persistent,
 // one CTA per SM); a row cut between CTAs is finished by an LSE merge of the
 // pieces in a second kernel, and a row inside one CTA is written directly.
@@ -99,6 +100,31 @@ __device__ __forceinline__ int cta_of_unit(int u, int units, int ctas) {
   while (c + 1 < ctas && unit_start(c + 1, units, ctas) <= u) ++c;
   while (c > 0 && unit_start(c, units, ctas) > u) --c;
   return c;
+}
+
+// Cluster merge, push side: a softmax thread's latent dims d = 128 k + (this thread's offset in
+// `rows`) of the 32 heads h0 .. h0 + 31, read from TMEM (O^T at `src` + 64 k) and stored into the
+// shared memory of each head's owner CTA (head h belongs to CTA h / HS), at row h % HS of the
+// block `rows` (this piece's block, mapped into the owner's window).
+template <int HS>
+__device__ __forceinline__ void push_piece(uint32_t src, const float* rows, int h0, bool has_valid) {
+  constexpr int kOwners = 32 / HS;
+  uint32_t ob[kOwners];
+#pragma unroll
+  for (int i = 0; i < kOwners; ++i) ob[i] = cluster_map(rows, (uint32_t)(h0 / HS + i));
+  tc_fence_after();
+#pragma unroll 1
+  for (int k = 0; k < 4; ++k) {
+    uint32_t o[32];
+    tmem_ld32(src + 64 * k, o);
+    tmem_wait_ld();
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const uint32_t dst = ob[jj / HS] + (uint32_t)(((jj % HS) * kLatent + 128 * k) * 4);
+      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(has_valid ? __uint_as_float(o[jj]) : 0.f)
+                   : "memory");
+    }
+  }
 }
 
 __global__ void __launch_bounds__(mla::kThreads, 1)
@@ -476,11 +502,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
               dst[(int64_t)h * kLatent] = __float2bfloat16_rn(L > 0.f ? __uint_as_float(o[jj]) / L : 0.f);
             }
           } else if (split > 1) {
-            // cluster mode: the piece stays in this CTA's (now idle) gather stages, [64 heads][512] fp32,
-            // with its m (mref, log2 units) and l (lfin) beside it
-            float* sO = reinterpret_cast<float*>(sKV) + d;
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) sO[(h0 + jj) * kLatent] = has_valid ? __uint_as_float(o[jj]) : 0.f;
+            // cluster mode: the piece stays in TMEM, with its m (mref, log2 units) and l (lfin) in
+            // shared memory, until the cluster merge below
           } else {
             float* dst = a.part_o + (int64_t)slot * kHeads * kLatent + d;
 #pragma unroll
@@ -508,16 +531,38 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (split > 1) {
-    // ---- cluster merge: CTA q of the row's cluster writes heads [q HS, q HS + HS), HS = 64 / split:
+    // ---- cluster merge.  CTA q of the row's cluster owns heads [q HS, q HS + HS), HS = 64 / split:
     //   out = sum_p w_p O_p,  w_p = 2^{m_p - M} / L,  L = sum_p 2^{m_p - M} l_p,  lse = (M + log2 L) ln 2.
-    cluster_sync();                     // every piece's O, m and l are in its CTA's shared memory
+    // Each CTA pushes every head of its piece into the owner's shared memory (remote stores, no
+    // round trips): O into [split][HS][512] fp32 in the gather stages, (m, l) into [split][HS][2] in
+    // the P^T buffer; then every CTA merges its heads from local shared memory.
     const int r = u0 / T, q = cta % split, HS = kHeads / split, hs0 = q * HS;
-    float* wts = reinterpret_cast<float*>(sP);          // [split][HS]
+    float* buf = reinterpret_cast<float*>(sKV);
+    float* mlb = reinterpret_cast<float*>(sP);
+    float* wts = mlb + 2 * kHeads;                       // [split][HS]
+    cluster_sync();                     // every CTA of the cluster is done with its gather stages
+    if (warp >= kSoftmaxWarp0) {
+      const int sg = (warp - kSoftmaxWarp0) >> 2, quarter = warp & 3, h0 = 32 * sg;
+      const int st = threadIdx.x - 32 * (kSoftmaxWarp0 + 4 * sg);
+      const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+      const bool has_valid = lfin[h0] > 0.f;   // a piece without valid entries never set its accumulator
+      const uint32_t src = tmem + lane_base + kColO + h0;
+      const float* my_rows = buf + (q * HS) * kLatent + 32 * quarter + lane;
+      if (HS == 32) push_piece<32>(src, my_rows, h0, has_valid);
+      else if (HS == 16) push_piece<16>(src, my_rows, h0, has_valid);
+      else push_piece<8>(src, my_rows, h0, has_valid);
+      if (st < 32) {
+        const int h = h0 + st, owner = h / HS;
+        const uint32_t dst = cluster_map(mlb + 2 * (q * HS + (h - owner * HS)), owner);
+        asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(dst), "f"(mref[h]), "f"(lfin[h]) : "memory");
+      }
+    }
+    cluster_sync();                     // every piece of this CTA's heads is in its shared memory
     if (threadIdx.x < HS) {
       const int h = hs0 + threadIdx.x;
       float M = -INFINITY, L = 0.f;
       for (int p = 0; p < split; ++p) {
-        const float l = ld_cluster_f32(cluster_map(&lfin[h], p)), m = ld_cluster_f32(cluster_map(&mref[h], p));
+        const float m = mlb[2 * (p * HS + threadIdx.x)], l = mlb[2 * (p * HS + threadIdx.x) + 1];
         if (l > 0.f) {
           const float Mn = fmaxf(M, m);
           L = L * exp2f(M - Mn) + l * exp2f(m - Mn);   // M = -inf: L is 0 and so is the product
@@ -526,18 +571,18 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       }
       const float inv = L > 0.f ? 1.f / L : 0.f;
       for (int p = 0; p < split; ++p) {
-        const float l = ld_cluster_f32(cluster_map(&lfin[h], p)), m = ld_cluster_f32(cluster_map(&mref[h], p));
+        const float m = mlb[2 * (p * HS + threadIdx.x)], l = mlb[2 * (p * HS + threadIdx.x) + 1];
         wts[p * HS + threadIdx.x] = l > 0.f ? exp2f(m - M) * inv : 0.f;
       }
       if (a.lse) a.lse[(int64_t)r * kHeads + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < HS * (kLatent / 4); i += kThreads) {
-      const int hl = i / (kLatent / 4), d = 4 * (i % (kLatent / 4)), h = hs0 + hl;
+      const int hl = i / (kLatent / 4), d = 4 * (i % (kLatent / 4));
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int p = 0; p < split; ++p) {
         const float w = wts[p * HS + hl];
-        const float4 x = ld_cluster_v4(cluster_map(sKV, p) + (uint32_t)((h * kLatent + d) * 4));
+        const float4 x = *reinterpret_cast<const float4*>(buf + (p * HS + hl) * kLatent + d);
         acc.x = fmaf(w, x.x, acc.x);
         acc.y = fmaf(w, x.y, acc.y);
         acc.z = fmaf(w, x.z, acc.z);
@@ -547,9 +592,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       __nv_bfloat162* xo = reinterpret_cast<__nv_bfloat162*>(&v);
       xo[0] = __floats2bfloat162_rn(acc.x, acc.y);
       xo[1] = __floats2bfloat162_rn(acc.z, acc.w);
-      *reinterpret_cast<uint2*>(a.out + ((int64_t)r * kHeads + h) * kLatent + d) = v;
+      *reinterpret_cast<uint2*>(a.out + ((int64_t)r * kHeads + hs0 + hl) * kLatent + d) = v;
     }
-    cluster_sync();                     // no CTA leaves while a peer may still read its shared memory
   }
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
