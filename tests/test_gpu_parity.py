@@ -242,3 +242,10 @@ def test_all_equal_scores_keep_the_first_positions():
         assert np.all(g_sc[r, :L] == 0.0)
         want = np.arange(wl.topk, dtype=np.int32) if L > wl.topk else np.r_[np.arange(L), np.full(wl.topk - L, -1)]
         assert np.array_equal(g_idx[r], want)
+
+
+def test_e4m3_scales_of_small_pages():
+    """Pages of 16 and 32 keys put 8 or 4 pages' scales into each 128-key tile (two or one gathers of
+    four page rows), with ragged lengths that leave part of the last group without a page."""
+    run_and_check(wlm.Workload("fp8_p16", [700, 1500, 333], [1, 1, 1], 16, "fp8", 256, 1, 3012))
+    run_and_check(wlm.Workload("fp8_p32", [1111, 2050], [1, 1], 32, "fp8", 512, 1, 3013))
