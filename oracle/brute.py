@@ -94,3 +94,23 @@ def attention(q_heads: list, rows: list, scale: float, d_latent: int) -> tuple[l
         outs.append(out)
         lses.append(m + math.log(l))
     return outs, lses
+
+
+def page_select(scores: list, page_size: int, budget: int) -> tuple[list, list]:
+    """Page-granular selection by loops over the visible scores of one row (index = position).
+
+    A page's score is the largest score among its positions; pages are ranked by (score descending,
+    page ascending) and the first `budget` kept (all when fewer).  Returns (kept pages ascending,
+    their positions ascending)."""
+    n = len(scores)
+    pages = []
+    for pg in range((n + page_size - 1) // page_size):
+        best = None
+        for s in range(pg * page_size, min(n, (pg + 1) * page_size)):
+            if best is None or scores[s] > best:
+                best = scores[s]
+        pages.append((best, pg))
+    ranked = sorted(pages, key=lambda t: (-t[0], t[1]))
+    kept = sorted(pg for _, pg in ranked[:budget])
+    positions = [s for pg in kept for s in range(pg * page_size, min(n, (pg + 1) * page_size))]
+    return kept, positions

@@ -40,6 +40,12 @@ Definitions (R query rows, B requests, P page size):
   Inference Path", "MLA Projections and KV State" and "Sparse MLA Attention");
   entries outside ``0 .. pos`` (including -1 padding) are skipped, and a row
   with no valid entry gets out = 0, lse = -inf;
+* page-granular selection -- a page's score is the largest I over its visible
+  tokens (masks before the maximum), the page budget keeps the best pages
+  (ties: smaller page), and attention reads every visible token of a kept page
+  ("Making GLM-5.2 Sparse on TPUs", "Make the sparsity unit match the memory
+  unit": a page ranked by its highest legal token score; "Stream indexer scores
+  over live context": only page scores reach HBM);
 * IndexShare -- layers marked shared reuse the index buffer of the nearest
   preceding full (owner) layer ("vLLM Inference Path", "DSA Indexer";
   "Serving GLM-5.2-504B on 8x RTX PRO 6000 GPUs", "Root cause: a missing
@@ -247,6 +253,65 @@ def indexer_topk(cache: PagedCache, block_table, seq_lens, query_start_loc, q_id
         all_scores.append(s)
         idx.append(topk_select(s, topk))
     return np.stack(idx), all_scores
+
+
+# ---------------------------------------------------------------------------
+# page-granular selection ("Making GLM-5.2 Sparse on TPUs", "Make the sparsity unit match the
+# memory unit" and "Stream indexer scores over live context")
+# ---------------------------------------------------------------------------
+def page_scores(scores, page_size: int) -> np.ndarray:
+    """Score of each logical page of a row: the largest I over the page's visible tokens.
+
+    `scores` holds I over the visible positions 0..pos only, so the causal / valid-length mask is
+    applied before the maximum (an invisible token cannot promote its page).  Returns one value per
+    page 0 .. pos // P (the pages holding at least one visible token)."""
+    scores = np.asarray(scores, dtype=np.float64)
+    n_pages = -(-scores.shape[0] // page_size)
+    out = np.empty(n_pages, dtype=np.float64)
+    for pg in range(n_pages):
+        out[pg] = scores[pg * page_size:(pg + 1) * page_size].max()
+    return out
+
+
+def page_topk_select(pscores, page_budget: int) -> np.ndarray:
+    """The page_budget pages with the largest page score (ties: smaller page first), or every page
+    when there are at most page_budget; sorted ascending, padded with -1 (the token rule of
+    topk_select, applied to pages)."""
+    return topk_select(pscores, page_budget)
+
+
+def pages_to_positions(pages, page_size: int, pos: int) -> np.ndarray:
+    """The visible positions (<= pos) of the selected pages, ascending, padded with -1 to
+    len(pages) * page_size: attention reads every visible token of a selected page."""
+    out = np.full(len(pages) * page_size, -1, dtype=np.int32)
+    at = 0
+    for pg in sorted(int(x) for x in pages if x >= 0):
+        for s in range(pg * page_size, (pg + 1) * page_size):
+            if s <= pos:
+                out[at] = s
+                at += 1
+    return out
+
+
+def page_indexer_topk(cache: PagedCache, block_table, seq_lens, query_start_loc, q_idx_bits, w,
+                      page_budget: int, rows=None):
+    """Page-granular selection for every (or the listed) query row: token scores, page scores
+    (maximum over visible tokens), the page_budget best pages and their visible positions.
+
+    Returns (pages [n_rows, page_budget] int32, positions [n_rows, page_budget * P] int32,
+    page scores: list of float64 arrays, token scores: list of float64 arrays)."""
+    P = cache.page_size
+    idx, t_scores = indexer_topk(cache, block_table, seq_lens, query_start_loc, q_idx_bits, w, 1, rows)
+    _, pos = row_positions(seq_lens, query_start_loc)
+    rows = range(len(pos)) if rows is None else rows
+    pages, positions, p_scores = [], [], []
+    for r, s in zip(rows, t_scores):
+        ps = page_scores(s, P)
+        sel = page_topk_select(ps, page_budget)
+        p_scores.append(ps)
+        pages.append(sel)
+        positions.append(pages_to_positions(sel, P, int(pos[r])))
+    return np.stack(pages), np.stack(positions), p_scores, t_scores
 
 
 # ---------------------------------------------------------------------------

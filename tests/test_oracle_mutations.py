@@ -122,3 +122,40 @@ def _attend_variant(q, rows, scale, dl, rope=True, shift=0, transpose=False):
 def test_attention_mutants_are_caught(tiny_case, monkeypatch, name):
     monkeypatch.setattr(o, "attend", ATTEND_MUTANTS[name])
     assert not _attention_ok(tiny_case)
+
+
+def _pages_ok():
+    """The page-selection pins: brute force over a few shapes with ties between pages."""
+    for n, P, budget in [(17, 4, 2), (64, 8, 3), (100, 16, 7), (37, 8, 2)]:
+        rng = np.random.default_rng(n * 7 + P)
+        scores = rng.standard_normal(n)
+        scores[rng.integers(0, n, max(1, n // 5))] = 0.5
+        pages = o.page_topk_select(o.page_scores(scores, P), budget)
+        positions = o.pages_to_positions(pages, P, n - 1)
+        want_pages, want_pos = brute.page_select([float(x) for x in scores], P, budget)
+        if [int(x) for x in pages if x >= 0] != want_pages or [int(x) for x in positions if x >= 0] != want_pos:
+            return False
+    return True
+
+
+PAGE_MUTANTS = {
+    # the page score as the sum, the mean or the first token of the page instead of the maximum
+    "page_sum": ("page_scores", lambda s, P: np.array([np.sum(s[i:i + P]) for i in range(0, len(s), P)])),
+    "page_mean": ("page_scores", lambda s, P: np.array([np.mean(s[i:i + P]) for i in range(0, len(s), P)])),
+    "page_first": ("page_scores", lambda s, P: np.asarray(s, float)[::P].copy()),
+    # a page index off by one when expanding to positions
+    "expand_shifted": ("pages_to_positions", lambda pages, P, pos: np.array(
+        [s for pg in sorted(int(x) for x in pages if x >= 0) for s in range((pg + 1) * P, (pg + 2) * P) if s <= pos]
+        + [-1] * len(pages) * P, dtype=np.int32)[:len(pages) * P]),
+}
+
+
+def test_unmutated_page_selection_passes():
+    assert _pages_ok()
+
+
+@pytest.mark.parametrize("name", sorted(PAGE_MUTANTS))
+def test_page_mutants_are_caught(monkeypatch, name):
+    fn, bad = PAGE_MUTANTS[name]
+    monkeypatch.setattr(o, fn, bad)
+    assert not _pages_ok()
