@@ -24,7 +24,7 @@ INDEX_HEADS, INDEX_DIM, HEADS, LATENT_DIM, ROPE_DIM, ROW_DIM = 32, 128, 64, 512,
 DEFAULT_SCALE = 1.0 / 16.0     # 1/sqrt(192 + 64)
 _FORMATS = {"bf16": KEY_BF16, "fp8": KEY_FP8_E4M3, None: KEY_BF16}
 
-__all__ = ["LayerCache", "Batch", "kv_append", "indexer_scores_topk", "sparse_mla_decode", "sparse_mla_prefill",
+__all__ = ["LayerCache", "Batch", "kv_append", "indexer_scores_topk", "indexer_page_topk", "sparse_mla_decode", "sparse_mla_prefill",
            "cache_bytes", "indexer_workspace_bytes", "mla_workspace_bytes", "DsaError", "DEFAULT_SCALE"]
 
 
@@ -104,6 +104,10 @@ def indexer_workspace_bytes(num_rows: int, max_seq_len: int, topk: int) -> int:
     return int(_lib.load().dsa_indexer_workspace_bytes(num_rows, max_seq_len, topk))
 
 
+def indexer_page_workspace_bytes(num_rows: int, max_seq_len: int, page_size: int, page_budget: int) -> int:
+    return int(_lib.load().dsa_indexer_page_workspace_bytes(num_rows, max_seq_len, page_size, page_budget))
+
+
 def mla_workspace_bytes(num_rows: int, topk: int) -> int:
     return int(_lib.load().dsa_mla_workspace_bytes(num_rows, topk))
 
@@ -150,6 +154,33 @@ def indexer_scores_topk(owner: LayerCache, batch: Batch, q_idx, w, topk: int, to
                                                    _ptr(topk_idx), _ptr(scores_out), _ptr(workspace),
                                                    workspace.numel() * workspace.element_size(), _stream(stream)))
     return topk_idx
+
+
+def indexer_page_topk(owner: LayerCache, batch: Batch, q_idx, w, page_budget: int, page_idx=None, token_idx=None,
+                      expand=True, page_scores_out=None, workspace=None, stream=None):
+    """Page-granular selection: page scores (max over visible tokens), the page budget, and (unless
+    expand is False) the selected pages' positions.  Returns (page_idx [R, page_budget],
+    token_idx [R, page_budget * page_size] or None)."""
+    R, P = batch.num_rows, owner.page_size
+    _need(q_idx, torch.bfloat16, (R, INDEX_HEADS, INDEX_DIM), "q_idx")
+    _need(w, torch.float32, (R, INDEX_HEADS), "w")
+    if page_idx is None:
+        page_idx = torch.empty((R, page_budget), dtype=torch.int32, device=q_idx.device)
+    _need(page_idx, torch.int32, (R, page_budget), "page_idx")
+    if expand and token_idx is None:
+        token_idx = torch.empty((R, page_budget * P), dtype=torch.int32, device=q_idx.device)
+    if token_idx is not None:
+        _need(token_idx, torch.int32, (R, page_budget * P), "token_idx")
+    if page_scores_out is not None:
+        _need(page_scores_out, torch.float32, (R, -(-batch.max_seq_len // P)), "page_scores_out")
+    if workspace is None:
+        workspace = _workspace(indexer_page_workspace_bytes(R, batch.max_seq_len, P, page_budget), q_idx.device)
+    c, b = owner.struct(), batch.struct()
+    _lib.check(_lib.load().dsa_indexer_page_topk(ctypes.byref(c), ctypes.byref(b), _ptr(q_idx), _ptr(w), page_budget,
+                                                 _ptr(page_idx), _ptr(token_idx), _ptr(page_scores_out),
+                                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                                 _stream(stream)))
+    return page_idx, token_idx
 
 
 def _sparse_mla(fn, layer, batch, q, topk_idx, scale, out, lse, workspace, stream):

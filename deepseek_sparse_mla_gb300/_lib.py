@@ -19,7 +19,7 @@ KEY_BF16, KEY_FP8_E4M3 = 0, 1
 # every entry point include/dsa.h declares
 EXPORTS = ("dsa_abi_version", "dsa_last_error", "dsa_kernel_launches", "dsa_cache_bytes", "dsa_indexer_workspace_bytes",
            "dsa_mla_workspace_bytes", "dsa_kv_append", "dsa_indexer_scores_topk", "dsa_indexer_scores_topk_static",
-           "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill")
+           "dsa_indexer_page_workspace_bytes", "dsa_indexer_page_topk", "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill")
 
 
 class DsaCache(ctypes.Structure):
@@ -71,6 +71,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_indexer_scores_topk_static.restype = I32
     lib.dsa_indexer_scores_topk_static.argtypes = [ctypes.POINTER(DsaCache), ctypes.POINTER(DsaBatch), P, P, I32, P,
                                                    P, P]
+    lib.dsa_indexer_page_workspace_bytes.restype = SZ
+    lib.dsa_indexer_page_workspace_bytes.argtypes = [I32, I32, I32, I32]
+    lib.dsa_indexer_page_topk.restype = I32
+    lib.dsa_indexer_page_topk.argtypes = [ctypes.POINTER(DsaCache), ctypes.POINTER(DsaBatch), P, P, I32, P, P, P, P,
+                                          SZ, P]
     for name in ("dsa_sparse_mla_decode", "dsa_sparse_mla_prefill"):
         fn = getattr(lib, name)
         fn.restype = I32

@@ -252,6 +252,69 @@ dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_batch* batc
   return ok();
 }
 
+size_t dsa_indexer_page_workspace_bytes(int32_t num_rows, int32_t max_seq_len, int32_t page_size, int32_t page_budget) {
+  if (num_rows < 0 || max_seq_len <= 0 || page_size <= 0 || page_budget < 1) return 0;
+  const int max_pages = (int)(((int64_t)max_seq_len + page_size - 1) / page_size);
+  return plan_indexer(num_rows > 0 ? num_rows : 1, max_pages, page_budget).workspace_bytes;
+}
+
+dsa_status dsa_indexer_page_topk(const dsa_cache* owner, const dsa_batch* batch, const void* q_idx, const float* w,
+                                 int32_t page_budget, int32_t* page_idx, int32_t* token_idx, float* page_scores_out,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  dsa_status st = check_cache(owner, true);
+  if (st != DSA_OK) return st;
+  st = check_batch(batch, false);
+  if (st != DSA_OK) return st;
+  const int P = owner->page_size;
+  if (P > 128)
+    return fail(DSA_ERR_UNSUPPORTED, "page-granular selection needs pages of at most 128 keys (got %d)", P);
+  if (page_budget < 1 || page_budget > DSA_MAX_TOPK)
+    return fail(DSA_ERR_INVALID_ARG, "page_budget must be in 1..%d (got %d)", DSA_MAX_TOPK, page_budget);
+  if (token_idx && (int64_t)page_budget * P > DSA_MAX_TOPK)
+    return fail(DSA_ERR_INVALID_ARG, "page_budget * page_size = %lld positions exceeds DSA_MAX_TOPK (%d)",
+                (long long)page_budget * P, DSA_MAX_TOPK);
+  if (!q_idx || !w || !page_idx) return fail(DSA_ERR_INVALID_ARG, "q_idx / w / page_idx is NULL");
+  if (!aligned16(q_idx)) return fail(DSA_ERR_INVALID_ARG, "q_idx is not 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(w) & 3u) || (reinterpret_cast<uintptr_t>(page_idx) & 3u) ||
+      (reinterpret_cast<uintptr_t>(token_idx) & 3u) || (reinterpret_cast<uintptr_t>(page_scores_out) & 3u))
+    return fail(DSA_ERR_INVALID_ARG, "w / page_idx / token_idx / page_scores_out is not 4-byte aligned");
+  if (batch->num_rows == 0) return ok();
+  const int log2p = ilog2(P);
+  const int max_pages = (int)(((int64_t)batch->max_seq_len + P - 1) / P);
+  IndexerPlan plan = plan_indexer(batch->num_rows, max_pages, page_budget);
+  if (!workspace || workspace_bytes < plan.workspace_bytes)
+    return fail(DSA_ERR_WORKSPACE,
+                "workspace of %zu bytes is smaller than the %zu bytes dsa_indexer_page_workspace_bytes requires",
+                workspace_bytes, plan.workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(DSA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  RowMeta m = row_meta(batch, batch->query_start_loc == nullptr);
+  cudaStream_t s = (cudaStream_t)stream;
+  char* ws = static_cast<char*>(workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+  int32_t* groups = reinterpret_cast<int32_t*>(ws + plan.groups_offset);
+  float* block = reinterpret_cast<float*>(ws + plan.scores_offset);
+  TopkChunks chunks;
+  chunks.chunk = plan.topk_chunk;
+  chunks.chunks = plan.topk_chunks;
+  chunks.cand = reinterpret_cast<uint64_t*>(ws + plan.cand_offset);
+  chunks.cnt = reinterpret_cast<uint32_t*>(ws + plan.cand_cnt_offset);
+  for (int row0 = 0; row0 < batch->num_rows; row0 += plan.rows_per_block) {
+    int n = batch->num_rows - row0 < plan.rows_per_block ? batch->num_rows - row0 : plan.rows_per_block;
+    float* scores = page_scores_out ? page_scores_out + (int64_t)row0 * max_pages : block;
+    int64_t stride = page_scores_out ? (int64_t)max_pages : plan.score_stride;
+    cudaError_t e = launch_indexer_scores(*owner, m, row0, n, batch->max_seq_len, q_idx, w, scores, stride,
+                                          page_scores_out != nullptr, groups, err, s, log2p);
+    if (e != cudaSuccess) return cuda_status(e, "indexer launch");
+    e = launch_topk(m, row0, n, scores, stride, max_pages, page_budget, page_idx, chunks, s, log2p);
+    if (e != cudaSuccess) return cuda_status(e, "page top-k launch");
+    if (token_idx) {
+      e = launch_page_expand(m, row0, n, page_idx, page_budget, log2p, token_idx, s);
+      if (e != cudaSuccess) return cuda_status(e, "page expansion launch");
+    }
+  }
+  return ok();
+}
+
 dsa_status dsa_sparse_mla_decode(const dsa_cache* layer, const dsa_batch* batch, const void* q, const int32_t* topk_idx,
                                  int32_t topk, float scale, void* out, float* lse, void* workspace,
                                  size_t workspace_bytes, void* stream) {

@@ -103,17 +103,23 @@ struct RowMeta {
 
 // Scores of rows [row0, row0 + nrows) into scores[(r - row0) * score_stride + s].  group_scratch holds
 // 4 + 5 * nrows + 1 ints; err is the device status word; fill_tail writes -inf past each row's last key tile.
+// page_log2 >= 0: page mode, one score per page of 2^page_log2 keys (pages of at most 128 keys)
 cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0, int nrows, int max_seq_len,
                                   const void* q_idx, const float* w, float* scores, int64_t score_stride,
-                                  bool fill_tail, int32_t* group_scratch, uint32_t* err, cudaStream_t s);
+                                  bool fill_tail, int32_t* group_scratch, uint32_t* err, cudaStream_t s,
+                                  int page_log2 = -1);
 
 struct TopkChunks {
   int chunk = 0, chunks = 0;   // chunks == 0: every row is selected by one CTA
   uint64_t* cand = nullptr;    // [nrows][chunks][kTopkChunkCap] (key << 32 | position)
   uint32_t* cnt = nullptr;     // [nrows][chunks]; 0xFFFFFFFF marks an overflowed chunk
 };
+// unit_shift > 0: the scores are page scores, a row's visible units are pages 0 .. pos >> unit_shift
 cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scores, int64_t score_stride,
-                        int max_seq_len, int topk, int32_t* topk_idx, const TopkChunks& ch, cudaStream_t s);
+                        int max_seq_len, int topk, int32_t* topk_idx, const TopkChunks& ch, cudaStream_t s,
+                        int unit_shift = 0);
+cudaError_t launch_page_expand(const RowMeta& m, int row0, int nrows, const int32_t* page_idx, int kp, int page_log2,
+                               int32_t* token_idx, cudaStream_t s);
 
 cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows, const void* q,
                               const int32_t* topk_idx, int topk, float scale, void* out, float* lse,

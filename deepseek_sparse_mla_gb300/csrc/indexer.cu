@@ -76,6 +76,8 @@ struct IdxArgs {
   float* scores;
   int64_t stride;
   int max_seq_len;
+  int page_log2;                 // >= 0: write page scores (max over a page's visible keys), pages of 2^page_log2
+  int max_pages;                 // page-score columns per row (page mode)
   uint32_t* err;
 };
 
@@ -183,6 +185,7 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
   __shared__ uint64_t d_full[4], d_empty[4], b_full[2], b_empty[2];
   __shared__ uint64_t mma_done[kMmaWarps];
   __shared__ float wq_e[2][kMaxRows][32];   // each epilogue warpgroup's head weights for its current group
+  __shared__ float pmax[2][4];              // page mode, pages over 32 keys: each warp's maximum
   __shared__ int4 gcache[kGroupCache];
   __shared__ int tcache[kGroupCache + 1];
   __shared__ uint32_t tmem_base;
@@ -527,11 +530,41 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
           for (int rr = 0; rr < kRowsMax; ++rr) score[rr] *= ks;
         }
         const int skey = cur.t * kTileKeys + key_local;
-        if (skey < a.max_seq_len) {
+        if (a.page_log2 < 0) {
+          if (skey < a.max_seq_len) {
 #pragma unroll
-          for (int rr = 0; rr < kRowsMax; ++rr)
-            if (rr < cur.G.z)
-              a.scores[(int64_t)(cur.G.y + rr - a.row0) * a.stride + skey] = skey <= cur.G.w + rr ? score[rr] : -INFINITY;
+            for (int rr = 0; rr < kRowsMax; ++rr)
+              if (rr < cur.G.z)
+                a.scores[(int64_t)(cur.G.y + rr - a.row0) * a.stride + skey] = skey <= cur.G.w + rr ? score[rr] : -INFINITY;
+          }
+        } else {
+          // page mode ("Make the sparsity unit match the memory unit"; "Stream indexer scores over live
+          // context"): a page's score is the largest score among its visible keys (the mask comes first),
+          // and only page scores are written.  Pages of up to 128 keys lie inside one 128-key tile.
+          const int lp = a.page_log2, P = 1 << lp;
+#pragma unroll
+          for (int rr = 0; rr < kRowsMax; ++rr) {
+            if (rr < cur.G.z) {                          // uniform across the warpgroup
+              float v = skey <= cur.G.w + rr ? score[rr] : -INFINITY;
+              for (int o = 1; o < P && o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+              float* dst = a.scores + (int64_t)(cur.G.y + rr - a.row0) * a.stride;
+              if (P <= 32) {
+                const int page = skey >> lp;
+                if ((lane & (P - 1)) == 0 && page < a.max_pages) dst[page] = v;
+              } else {
+                if (lane == 0) pmax[eg][quarter] = v;
+                named_bar_sync(6 + eg, 128);
+                if (et < 128 / P) {                      // 64 keys: quarters 0-1 and 2-3; 128 keys: all four
+                  const int per = P / 32;
+                  float m = pmax[eg][et * per];
+                  for (int qq = 1; qq < per; ++qq) m = fmaxf(m, pmax[eg][et * per + qq]);
+                  const int page = ((cur.t * kTileKeys) >> lp) + et;
+                  if (page < a.max_pages) dst[page] = m;
+                }
+                named_bar_sync(6 + eg, 128);             // pmax is free for the next row
+              }
+            }
+          }
         }
       }
       new_group = cursor_next(cur, a, gcache, tcache);
@@ -623,14 +656,17 @@ __global__ void __launch_bounds__(1024) indexer_groups_kernel(RowMeta m, int row
 }
 
 // -inf for the positions of a caller-visible score row that no tile covered (s beyond the row's last tile).
-__global__ void indexer_fill_tail_kernel(RowMeta m, int row0, float* scores, int64_t stride, int max_seq_len) {
+// -inf beyond what the indexer wrote for each row (its last 128-key tile), in units of 2^unit_log2
+// keys (1: token scores; a page: page scores), up to max_units columns.
+__global__ void indexer_fill_tail_kernel(RowMeta m, int row0, float* scores, int64_t stride, int max_units,
+                                         int unit_log2) {
   pdl_wait();
   pdl_trigger();
   const int r = row0 + blockIdx.y;
   int b, pos;
   row_info(m, r, b, pos);
-  const int start = pos < 0 ? 0 : (pos / 128 + 1) * 128;
-  for (int s = start + blockIdx.x * blockDim.x + threadIdx.x; s < max_seq_len; s += gridDim.x * blockDim.x)
+  const int start = pos < 0 ? 0 : ((pos / 128 + 1) * 128) >> unit_log2;
+  for (int s = start + blockIdx.x * blockDim.x + threadIdx.x; s < max_units; s += gridDim.x * blockDim.x)
     scores[(int64_t)blockIdx.y * stride + s] = -INFINITY;
 }
 
@@ -680,7 +716,8 @@ static int indexer_rows_per_group(const dsa_cache& c, bool decode) {
 
 cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0, int nrows, int max_seq_len,
                                   const void* q_idx, const float* w, float* scores, int64_t score_stride,
-                                  bool fill_tail, int32_t* group_scratch, uint32_t* err, cudaStream_t s) {
+                                  bool fill_tail, int32_t* group_scratch, uint32_t* err, cudaStream_t s,
+                                  int page_log2) {
   const bool fp8 = c.key_format == DSA_KEY_FP8_E4M3;
   const bool decode = m.query_start_loc == nullptr;
   static bool configured[2] = {false, false};
@@ -730,6 +767,8 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
   a.scores = scores;
   a.stride = score_stride;
   a.max_seq_len = max_seq_len;
+  a.page_log2 = page_log2;
+  a.max_pages = page_log2 >= 0 ? (max_seq_len + (1 << page_log2) - 1) >> page_log2 : 0;
   a.err = err;
   const int grid = g_sm_count;
   e = fp8 ? launch_pdl(indexer_tc_kernel<true>, dim3(grid), dim3(idx::kThreads), idx::kSmemBytes, s, map, a)
@@ -738,8 +777,10 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess || !fill_tail) return e;
-  dim3 fgrid((max_seq_len + 255) / 256 < 64 ? (max_seq_len + 255) / 256 : 64, nrows);
-  e = launch_pdl(indexer_fill_tail_kernel, fgrid, dim3(256), 0, s, m, row0, scores, score_stride, max_seq_len);
+  const int units = page_log2 >= 0 ? a.max_pages : max_seq_len;
+  dim3 fgrid((units + 255) / 256 < 64 ? (units + 255) / 256 : 64, nrows);
+  e = launch_pdl(indexer_fill_tail_kernel, fgrid, dim3(256), 0, s, m, row0, scores, score_stride, units,
+                 page_log2 >= 0 ? page_log2 : 0);
   count_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

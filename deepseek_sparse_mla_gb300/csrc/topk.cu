@@ -244,7 +244,7 @@ static_assert(kChunkWarps * kSeg == kTopkChunkCap, "a chunk CTA holds exactly on
 __global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(RowMeta m, int row0, const float* __restrict__ scores,
                                                                    int64_t stride, int max_seq_len, int k, int chunk,
                                                                    int chunks, int cap, uint64_t* __restrict__ cand,
-                                                                   uint32_t* __restrict__ cand_cnt) {
+                                                                   uint32_t* __restrict__ cand_cnt, int unit_shift) {
   extern __shared__ uint64_t chunk_smem[];
   uint64_t* seg = chunk_smem;                                                       // [16][kSeg]
   uint32_t* hist = reinterpret_cast<uint32_t*>(chunk_smem + kChunkWarps * kSeg);   // [kSampleBins]
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(RowMeta m, in
   const int rl = blockIdx.y, r = row0 + rl, c = blockIdx.x;
   int b, pos;
   row_info(m, r, b, pos);
-  int n = pos + 1 > 0 ? pos + 1 : 0;
+  int n = pos >= 0 ? (pos >> unit_shift) + 1 : 0;          // visible units (positions, or pages)
   if (n > max_seq_len) n = max_seq_len;
   if (n <= chunk) return;                                     // whole row in topk_kernel
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -294,11 +294,12 @@ __global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(RowMeta m, in
   if (tid == 0) *my_cnt = total;
 }
 
+// Units are positions (unit_shift 0) or pages of 2^unit_shift positions, ranked by their page score.
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0, const float* __restrict__ scores,
                                                             int64_t stride, int max_seq_len, int k,
                                                             int32_t* __restrict__ topk_idx, int chunk, int chunks,
                                                             int cap, const uint64_t* __restrict__ cand,
-                                                            const uint32_t* __restrict__ cand_cnt) {
+                                                            const uint32_t* __restrict__ cand_cnt, int unit_shift) {
   extern __shared__ uint64_t topk_smem[];
   uint64_t* seg = topk_smem;                                                  // [kWarps][kSeg] key << 32 | position
   uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem + kWarps * kSeg);    // [kSampleBins]
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
   const int r = row0 + blockIdx.x;
   int b, pos;
   row_info(m, r, b, pos);
-  int n = pos + 1 > 0 ? pos + 1 : 0;
+  int n = pos >= 0 ? (pos >> unit_shift) + 1 : 0;   // visible units (positions, or pages)
   if (n > max_seq_len) n = max_seq_len;   // never read past the row's scores, whatever seq_lens says
   // A programmatic dependent of the chunk kernel (or, when no row is split, of the indexer), this
   // grid may start before that one ends.  Rows the chunk kernel scans wait for its results before
@@ -527,7 +528,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
 }
 
 cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scores, int64_t score_stride,
-                        int max_seq_len, int topk, int32_t* topk_idx, const TopkChunks& ch, cudaStream_t s) {
+                        int max_seq_len, int topk, int32_t* topk_idx, const TopkChunks& ch, cudaStream_t s,
+                        int unit_shift) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkSmem);
@@ -537,9 +539,11 @@ cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scor
     configured = true;
   }
   if (ch.chunks > 0) {
-    topk_chunk_kernel<<<dim3(ch.chunks, nrows), kChunkThreads, kChunkSmem, s>>>(
-        m, row0, scores, score_stride, max_seq_len, topk, ch.chunk, ch.chunks, kTopkChunkCap, ch.cand, ch.cnt);
+    cudaError_t e = launch_pdl(topk_chunk_kernel, dim3(ch.chunks, nrows), dim3(kChunkThreads), kChunkSmem, s, m, row0,
+                               scores, score_stride, max_seq_len, topk, ch.chunk, ch.chunks, (int)kTopkChunkCap,
+                               ch.cand, ch.cnt, unit_shift);
     count_launches(1);
+    if (e != cudaSuccess) return e;
   }
   // after the chunk kernel the select kernel is a programmatic dependent, so its launch and
   // prologue overlap the chunk kernel's tail
@@ -555,7 +559,37 @@ cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scor
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, m, row0, scores, score_stride, max_seq_len, topk, topk_idx,
                                      ch.chunk, ch.chunks, (int)kTopkChunkCap, (const uint64_t*)ch.cand,
-                                     (const uint32_t*)ch.cnt);
+                                     (const uint32_t*)ch.cnt, unit_shift);
+  count_launches(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// The positions of the selected pages ("Make the sparsity unit match the memory unit": attention
+// reads every visible token of a kept page): token_idx[r][j P + t] = page_idx[r][j] P + t when that
+// is a visible position, else -1.  Pages are ascending and only a row's last page can be partly
+// visible, so the result is ascending with its -1 entries at the end.
+__global__ void __launch_bounds__(256) page_expand_kernel(RowMeta m, int row0, const int32_t* __restrict__ page_idx,
+                                                          int kp, int page_log2, int32_t* __restrict__ token_idx) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = row0 + blockIdx.x;
+  int b, pos;
+  row_info(m, r, b, pos);
+  const int n = kp << page_log2;
+  const int32_t* pr = page_idx + (int64_t)r * kp;
+  int32_t* out = token_idx + (int64_t)r * n;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int pg = pr[i >> page_log2];
+    const int s = (pg << page_log2) + (i & ((1 << page_log2) - 1));
+    out[i] = (pg >= 0 && s <= pos) ? s : -1;
+  }
+}
+
+cudaError_t launch_page_expand(const RowMeta& m, int row0, int nrows, const int32_t* page_idx, int kp, int page_log2,
+                               int32_t* token_idx, cudaStream_t s) {
+  cudaError_t e = launch_pdl(page_expand_kernel, dim3(nrows), dim3(256), 0, s, m, row0, page_idx, kp, page_log2,
+                             token_idx);
   count_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

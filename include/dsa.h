@@ -197,6 +197,39 @@ DSA_API dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_bat
                                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Scratch bytes dsa_indexer_page_topk needs for num_rows rows of up to max_seq_len keys, pages of
+ * page_size keys and budget page_budget (shape only, like dsa_indexer_workspace_bytes).
+ */
+DSA_API size_t dsa_indexer_page_workspace_bytes(int32_t num_rows, int32_t max_seq_len, int32_t page_size,
+                                                int32_t page_budget);
+
+/*
+ * Page-granular selection: the indexer scores pooled into page scores, and a page budget.
+ * ("Making GLM-5.2 Sparse on TPUs", "Make the sparsity unit match the memory unit": rank each page
+ * by its highest legal token score, masks before the maximum; "Stream indexer scores over live
+ * context": masks and page maxima on chip, only page scores reach HBM.)
+ *   S(r, p) = max over visible s (0 <= s <= pos(r)) in logical page p of I(r, s), I as in
+ *             dsa_indexer_scores_topk; pages 0 .. pos(r) / page_size.
+ *   page_idx[r]  = the page_budget pages with the largest S (ties: smaller page), sorted ascending;
+ *                  every such page when there are at most page_budget; padded with -1.
+ *   token_idx[r] = the visible positions of those pages, ascending, padded with -1 to
+ *                  page_budget * page_size: an index buffer for dsa_sparse_mla_decode / _prefill
+ *                  with topk = page_budget * page_size.  Optional (NULL to skip).
+ *   owner          cache of the indexer-owning layer; page_size <= 128 (DSA_ERR_UNSUPPORTED otherwise).
+ *   page_budget    1..DSA_MAX_TOPK; with token_idx, page_budget * page_size <= DSA_MAX_TOPK.
+ *   page_idx       device int32 [num_rows, page_budget] (output).
+ *   token_idx      device int32 [num_rows, page_budget * page_size] (output) or NULL.
+ *   page_scores_out optional device fp32 [num_rows, ceil(max_seq_len / page_size)]: S, -inf beyond
+ *                  the row's last page; NULL to skip.
+ *   workspace      device scratch of at least dsa_indexer_page_workspace_bytes(...) bytes, 256-byte
+ *                  aligned; its first word is the device status word, as for dsa_indexer_scores_topk.
+ * The library has no page counterpart of the static-scratch entry point.
+ */
+DSA_API dsa_status dsa_indexer_page_topk(const dsa_cache* owner, const dsa_batch* batch, const void* q_idx,
+                                         const float* w, int32_t page_budget, int32_t* page_idx, int32_t* token_idx,
+                                         float* page_scores_out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * dsa_indexer_scores_topk without a caller workspace.  The pages have no counterpart: this is
  * a convenience of this library for callers that cannot allocate device memory per call (a
  * serving loop whose memory was reserved and locked before it started, or host code without an

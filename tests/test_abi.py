@@ -137,3 +137,29 @@ def test_sparse_mla_rejects_bad_arguments(lib):
     # prefill needs query_start_loc
     assert lib.dsa_sparse_mla_prefill(ctypes.byref(c), ctypes.byref(_batch(rows=2)), P(A), P(A), 128, 0.0625, P(A),
                                       None, P(A), ws, None) == INVALID
+
+
+def test_page_topk_rejects_bad_arguments(lib):
+    P = ctypes.c_void_p
+    b = _batch()
+    ws = lib.dsa_indexer_page_workspace_bytes(2, 300, 64, 4)
+    args = lambda kp, tok, wsb: (P(A), P(A), kp, P(A), tok, None, P(A), wsb, None)   # noqa: E731
+    c = _cache()
+    assert lib.dsa_indexer_page_topk(ctypes.byref(c), ctypes.byref(b), *args(0, P(A), ws)) == INVALID
+    assert lib.dsa_indexer_page_topk(ctypes.byref(c), ctypes.byref(b), *args(200, P(A), ws)) == INVALID
+    assert "DSA_MAX_TOPK" in _err(lib)                       # 200 pages x 64 positions > 8192
+    assert lib.dsa_indexer_page_topk(ctypes.byref(c), ctypes.byref(b), *args(4, P(A), ws - 1)) == WORKSPACE
+    big = _cache(P=256)
+    assert lib.dsa_indexer_page_topk(ctypes.byref(big), ctypes.byref(b), *args(4, P(A), ws)) == UNSUPPORTED
+    shared = _cache(keys=0, scales=0)
+    assert lib.dsa_indexer_page_topk(ctypes.byref(shared), ctypes.byref(b), *args(4, P(A), ws)) == INVALID
+    assert lib.dsa_indexer_page_topk(ctypes.byref(c), ctypes.byref(b), P(A), P(A), 4, None, None, None, P(A), ws,
+                                     None) == INVALID                          # page_idx is required
+
+
+def test_page_workspace_holds_page_scores_not_token_scores(lib):
+    # 64 rows of 131,072 keys: token scores need 32 MiB, page scores of 64-key pages 0.5 MiB
+    tok = lib.dsa_indexer_workspace_bytes(64, 131072, 2048)
+    page = lib.dsa_indexer_page_workspace_bytes(64, 131072, 64, 32)
+    assert tok >= 64 * 131072 * 4 and page < 64 * 2048 * 4 + (1 << 16)
+    assert lib.dsa_indexer_page_workspace_bytes(0, 100, 64, 4) > 0 and lib.dsa_indexer_page_workspace_bytes(4, 0, 64, 4) == 0
