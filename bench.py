@@ -46,10 +46,10 @@ class DeviceProblem:
     prefix (drawn on the device with torch's seeded generator and appended through the
     library), and the step's inputs (new tokens, queries, metadata) are on the device."""
 
-    def __init__(self, wl: wlm.Workload, device="cuda"):
+    def __init__(self, wl: wlm.Workload, device="cuda", selection="token"):
         import torch
         import deepseek_sparse_mla_gb300 as dsa
-        self.wl, self.dev = wl, device
+        self.wl, self.dev, self.selection = wl, device, selection
         B, R, layers = wl.num_requests, wl.num_rows, wl.layers
         self.caches = [dsa.LayerCache(wl.num_pages, wl.page_size, wl.key_format if l == 0 else None, device)
                        for l in range(layers)]
@@ -86,6 +86,14 @@ class DeviceProblem:
         self.ws_idx = torch.empty(dsa.indexer_workspace_bytes(R, wl.max_seq_len, wl.topk), dtype=torch.uint8,
                                   device=device)
         self.ws_mla = torch.empty(dsa.mla_workspace_bytes(R, wl.topk), dtype=torch.uint8, device=device)
+        if selection == "page":
+            # page-granular selection: topk / page_size pages, expanded into the same-size index buffer
+            self.page_budget = wl.topk // wl.page_size
+            assert self.page_budget * wl.page_size == wl.topk, "the token budget must be whole pages"
+            self.page_idx = torch.empty((R, self.page_budget), dtype=torch.int32, device=device)
+            self.ws_page = torch.empty(dsa.indexer_page_workspace_bytes(R, wl.max_seq_len, wl.page_size,
+                                                                        self.page_budget),
+                                       dtype=torch.uint8, device=device)
         torch.cuda.synchronize()
 
     def step(self, marks=None, io=None):
@@ -101,8 +109,12 @@ class DeviceProblem:
             dsa.kv_append(self.caches[l], io.new_c[l], io.new_r[l], io.slots, k_idx=io.new_k if l == 0 else None)
         if marks is not None:
             marks.mark("indexer")
-        dsa.indexer_scores_topk(self.caches[0], io.batch, io.q_idx, io.w, wl.topk, topk_idx=self.topk_idx,
-                                workspace=self.ws_idx)
+        if self.selection == "page":
+            dsa.indexer_page_topk(self.caches[0], io.batch, io.q_idx, io.w, self.page_budget, page_idx=self.page_idx,
+                                  token_idx=self.topk_idx, workspace=self.ws_page)
+        else:
+            dsa.indexer_scores_topk(self.caches[0], io.batch, io.q_idx, io.w, wl.topk, topk_idx=self.topk_idx,
+                                    workspace=self.ws_idx)
         for l in range(wl.layers):
             if marks is not None:
                 marks.mark("attention")
@@ -482,6 +494,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wlm.FULL) + sorted(wlm.PROFILE))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--selection", choices=["token", "page"], default="token",
+                    help="token top-k (the method's selection), or page-granular selection of topk / page_size pages")
     ap.add_argument("--cpu-sample-requests", type=int, default=64)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -493,7 +507,8 @@ def main():
     from deepseek_sparse_mla_gb300 import _lib
     rank, world = dist_setup(args.gpus)
     wl = rank_workload(args.workload, rank)
-    prob = DeviceProblem(wl)
+    prob = DeviceProblem(wl, selection=args.selection)
+    page_mode = args.selection == "page"
     lib = _lib.load()
 
     # ---- device-resident timing --------------------------------------------------------
@@ -537,14 +552,18 @@ def main():
     bytes_of = {"indexer": alg["indexer"], "attention": alg["attention"],
                 "append": (alg["append_owner"] + (wl.layers - 1) * alg["append_shared"]) / wl.layers}
     # each timed call, the kernels it launches and the sources they come from
-    files = {"indexer": (("indexer.cu", "topk.cu"), "indexer_scores_topk: indexer_groups_kernel + indexer_tc_kernel + topk_chunk_kernel + topk_kernel"),
-             "attention": (("sparse_mla.cu",), "sparse_mla_decode: sparse_mla_tc_kernel + mla_merge_kernel"),
+    files = {"indexer": (("indexer.cu", "topk.cu"),
+                         "indexer_page_topk: indexer_groups_kernel + indexer_tc_kernel (page scores) + topk_kernel + "
+                         "page_expand_kernel" if page_mode else
+                         "indexer_scores_topk: indexer_groups_kernel + indexer_tc_kernel + topk_chunk_kernel + topk_kernel"),
+             "attention": (("sparse_mla.cu",), "sparse_mla_decode: sparse_mla_tc_kernel (clusters merge in shared memory; "
+                                               "mla_merge_kernel when rows are cut between CTAs) + mla_status_kernel"),
              "append": (("kv_append.cu",), "kv_append: kv_append_kernel")}
     dom = max(share, key=share.get)
     achieved = bytes_of[dom] / (per_call[dom] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": files[dom][1], "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind,
-                "traffic": kernel_traffic(dom, files[dom][0], wl.name),
+                "traffic": kernel_traffic(dom, files[dom][0], wl.name + (" (page selection)" if page_mode else "")),
                 "algorithmic_bytes_per_launch": bytes_of[dom]}
     kernels = {k: {"ms_per_call": per_call[k], "calls_per_step": calls[k], "share": share[k] / tot,
                    "algorithmic_GBps": bytes_of[k] / (per_call[k] * 1e-3) / 1e9,
@@ -615,6 +634,8 @@ def main():
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": wl.name, **{k: v for k, v in summary.items() if k != "workload"},
+                           "selection": ("page budget: %d pages of %d positions" % (prob.page_budget, wl.page_size)
+                                         if page_mode else "token top-k"),
                            "l2": "no flush: each step reads %.0f MB (> 129 MB L2)" % (alg["step"] / 1e6),
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,

@@ -252,10 +252,34 @@ dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_batch* batc
   return ok();
 }
 
+// Page mode workspace: the indexer plan over units of min(P, 32) keys (its score block holds the
+// units' maxima) and, for pages of more than 32 keys, a page-score block after it.
+namespace {
+struct PagePlan {
+  IndexerPlan ix;
+  int max_units, max_pages;
+  bool pooled;
+  int64_t page_stride;
+  size_t pages_offset, workspace_bytes;
+};
+PagePlan plan_pages(int num_rows, int max_seq_len, int page_size, int page_budget) {
+  PagePlan p;
+  const int unit = page_size < 32 ? page_size : 32;
+  p.max_units = (int)(((int64_t)max_seq_len + unit - 1) / unit);
+  p.max_pages = (int)(((int64_t)max_seq_len + page_size - 1) / page_size);
+  p.pooled = page_size > 32;
+  p.ix = plan_indexer(num_rows, p.max_units, page_budget);
+  p.page_stride = ((int64_t)p.max_pages + 255) / 256 * 256;
+  p.pages_offset = (p.ix.workspace_bytes + 255) / 256 * 256;
+  p.workspace_bytes = p.pooled ? p.pages_offset + (size_t)p.ix.rows_per_block * p.page_stride * sizeof(float)
+                               : p.ix.workspace_bytes;
+  return p;
+}
+}  // namespace
+
 size_t dsa_indexer_page_workspace_bytes(int32_t num_rows, int32_t max_seq_len, int32_t page_size, int32_t page_budget) {
   if (num_rows < 0 || max_seq_len <= 0 || page_size <= 0 || page_budget < 1) return 0;
-  const int max_pages = (int)(((int64_t)max_seq_len + page_size - 1) / page_size);
-  return plan_indexer(num_rows > 0 ? num_rows : 1, max_pages, page_budget).workspace_bytes;
+  return plan_pages(num_rows > 0 ? num_rows : 1, max_seq_len, page_size, page_budget).workspace_bytes;
 }
 
 dsa_status dsa_indexer_page_topk(const dsa_cache* owner, const dsa_batch* batch, const void* q_idx, const float* w,
@@ -280,12 +304,13 @@ dsa_status dsa_indexer_page_topk(const dsa_cache* owner, const dsa_batch* batch,
     return fail(DSA_ERR_INVALID_ARG, "w / page_idx / token_idx / page_scores_out is not 4-byte aligned");
   if (batch->num_rows == 0) return ok();
   const int log2p = ilog2(P);
-  const int max_pages = (int)(((int64_t)batch->max_seq_len + P - 1) / P);
-  IndexerPlan plan = plan_indexer(batch->num_rows, max_pages, page_budget);
-  if (!workspace || workspace_bytes < plan.workspace_bytes)
+  const PagePlan pp = plan_pages(batch->num_rows, batch->max_seq_len, P, page_budget);
+  const IndexerPlan& plan = pp.ix;
+  const int max_pages = pp.max_pages;
+  if (!workspace || workspace_bytes < pp.workspace_bytes)
     return fail(DSA_ERR_WORKSPACE,
                 "workspace of %zu bytes is smaller than the %zu bytes dsa_indexer_page_workspace_bytes requires",
-                workspace_bytes, plan.workspace_bytes);
+                workspace_bytes, pp.workspace_bytes);
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(DSA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
   RowMeta m = row_meta(batch, batch->query_start_loc == nullptr);
   cudaStream_t s = (cudaStream_t)stream;
@@ -293,6 +318,7 @@ dsa_status dsa_indexer_page_topk(const dsa_cache* owner, const dsa_batch* batch,
   uint32_t* err = reinterpret_cast<uint32_t*>(ws);
   int32_t* groups = reinterpret_cast<int32_t*>(ws + plan.groups_offset);
   float* block = reinterpret_cast<float*>(ws + plan.scores_offset);
+  float* page_block = reinterpret_cast<float*>(ws + pp.pages_offset);
   TopkChunks chunks;
   chunks.chunk = plan.topk_chunk;
   chunks.chunks = plan.topk_chunks;
@@ -300,12 +326,20 @@ dsa_status dsa_indexer_page_topk(const dsa_cache* owner, const dsa_batch* batch,
   chunks.cnt = reinterpret_cast<uint32_t*>(ws + plan.cand_cnt_offset);
   for (int row0 = 0; row0 < batch->num_rows; row0 += plan.rows_per_block) {
     int n = batch->num_rows - row0 < plan.rows_per_block ? batch->num_rows - row0 : plan.rows_per_block;
-    float* scores = page_scores_out ? page_scores_out + (int64_t)row0 * max_pages : block;
-    int64_t stride = page_scores_out ? (int64_t)max_pages : plan.score_stride;
-    cudaError_t e = launch_indexer_scores(*owner, m, row0, n, batch->max_seq_len, q_idx, w, scores, stride,
-                                          page_scores_out != nullptr, groups, err, s, log2p);
+    // pages of up to 32 keys: the indexer writes page scores itself (into page_scores_out if given);
+    // larger pages: it writes 32-key unit maxima into the workspace, pooled into page scores next
+    float* pages = page_scores_out ? page_scores_out + (int64_t)row0 * max_pages : (pp.pooled ? page_block : block);
+    int64_t page_stride = page_scores_out ? (int64_t)max_pages : (pp.pooled ? pp.page_stride : plan.score_stride);
+    float* units = pp.pooled ? block : pages;
+    int64_t unit_stride = pp.pooled ? plan.score_stride : page_stride;
+    cudaError_t e = launch_indexer_scores(*owner, m, row0, n, batch->max_seq_len, q_idx, w, units, unit_stride,
+                                          !pp.pooled && page_scores_out != nullptr, groups, err, s, log2p);
     if (e != cudaSuccess) return cuda_status(e, "indexer launch");
-    e = launch_topk(m, row0, n, scores, stride, max_pages, page_budget, page_idx, chunks, s, log2p);
+    if (pp.pooled) {
+      e = launch_page_pool(m, row0, n, units, unit_stride, log2p, pages, page_stride, max_pages, s);
+      if (e != cudaSuccess) return cuda_status(e, "page pooling launch");
+    }
+    e = launch_topk(m, row0, n, pages, page_stride, max_pages, page_budget, page_idx, chunks, s, log2p);
     if (e != cudaSuccess) return cuda_status(e, "page top-k launch");
     if (token_idx) {
       e = launch_page_expand(m, row0, n, page_idx, page_budget, log2p, token_idx, s);

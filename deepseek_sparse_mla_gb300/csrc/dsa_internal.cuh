@@ -103,7 +103,8 @@ struct RowMeta {
 
 // Scores of rows [row0, row0 + nrows) into scores[(r - row0) * score_stride + s].  group_scratch holds
 // 4 + 5 * nrows + 1 ints; err is the device status word; fill_tail writes -inf past each row's last key tile.
-// page_log2 >= 0: page mode, one score per page of 2^page_log2 keys (pages of at most 128 keys)
+// page_log2 >= 0: page mode, one score per unit of 2^min(page_log2, 5) keys: the page itself for pages of
+// up to 32 keys, else a part that launch_page_pool combines (pages of at most 128 keys)
 cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0, int nrows, int max_seq_len,
                                   const void* q_idx, const float* w, float* scores, int64_t score_stride,
                                   bool fill_tail, int32_t* group_scratch, uint32_t* err, cudaStream_t s,
@@ -118,6 +119,8 @@ struct TopkChunks {
 cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scores, int64_t score_stride,
                         int max_seq_len, int topk, int32_t* topk_idx, const TopkChunks& ch, cudaStream_t s,
                         int unit_shift = 0);
+cudaError_t launch_page_pool(const RowMeta& m, int row0, int nrows, const float* units, int64_t unit_stride,
+                             int page_log2, float* pages, int64_t page_stride, int max_pages, cudaStream_t s);
 cudaError_t launch_page_expand(const RowMeta& m, int row0, int nrows, const int32_t* page_idx, int kp, int page_log2,
                                int32_t* token_idx, cudaStream_t s);
 

@@ -76,8 +76,8 @@ struct IdxArgs {
   float* scores;
   int64_t stride;
   int max_seq_len;
-  int page_log2;                 // >= 0: write page scores (max over a page's visible keys), pages of 2^page_log2
-  int max_pages;                 // page-score columns per row (page mode)
+  int page_log2;                 // >= 0: page mode, write maxima over units of 2^min(page_log2, 5) visible keys
+  int max_pages;                 // unit columns per row (page mode)
   uint32_t* err;
 };
 
@@ -185,7 +185,6 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
   __shared__ uint64_t d_full[4], d_empty[4], b_full[2], b_empty[2];
   __shared__ uint64_t mma_done[kMmaWarps];
   __shared__ float wq_e[2][kMaxRows][32];   // each epilogue warpgroup's head weights for its current group
-  __shared__ float pmax[2][4];              // page mode, pages over 32 keys: each warp's maximum
   __shared__ int4 gcache[kGroupCache];
   __shared__ int tcache[kGroupCache + 1];
   __shared__ uint32_t tmem_base;
@@ -539,30 +538,19 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
           }
         } else {
           // page mode ("Make the sparsity unit match the memory unit"; "Stream indexer scores over live
-          // context"): a page's score is the largest score among its visible keys (the mask comes first),
-          // and only page scores are written.  Pages of up to 128 keys lie inside one 128-key tile.
-          const int lp = a.page_log2, P = 1 << lp;
+          // context"): the largest visible score (the mask comes first) of each unit of U = min(P, 32) keys,
+          // reduced within the warp.  Pages of up to 32 keys are whole units; larger pages (at most 128
+          // keys: one tile) are pooled from their units by a small kernel afterwards, since a page then
+          // spans the keys of several warps and a barrier per tile to combine them costs more.
+          const int lu = a.page_log2 < 5 ? a.page_log2 : 5, U = 1 << lu;
 #pragma unroll
           for (int rr = 0; rr < kRowsMax; ++rr) {
             if (rr < cur.G.z) {                          // uniform across the warpgroup
               float v = skey <= cur.G.w + rr ? score[rr] : -INFINITY;
-              for (int o = 1; o < P && o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-              float* dst = a.scores + (int64_t)(cur.G.y + rr - a.row0) * a.stride;
-              if (P <= 32) {
-                const int page = skey >> lp;
-                if ((lane & (P - 1)) == 0 && page < a.max_pages) dst[page] = v;
-              } else {
-                if (lane == 0) pmax[eg][quarter] = v;
-                named_bar_sync(6 + eg, 128);
-                if (et < 128 / P) {                      // 64 keys: quarters 0-1 and 2-3; 128 keys: all four
-                  const int per = P / 32;
-                  float m = pmax[eg][et * per];
-                  for (int qq = 1; qq < per; ++qq) m = fmaxf(m, pmax[eg][et * per + qq]);
-                  const int page = ((cur.t * kTileKeys) >> lp) + et;
-                  if (page < a.max_pages) dst[page] = m;
-                }
-                named_bar_sync(6 + eg, 128);             // pmax is free for the next row
-              }
+              for (int o = 1; o < U; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+              const int unit = skey >> lu;
+              if ((lane & (U - 1)) == 0 && unit < a.max_pages)
+                a.scores[(int64_t)(cur.G.y + rr - a.row0) * a.stride + unit] = v;
             }
           }
         }
@@ -657,7 +645,7 @@ __global__ void __launch_bounds__(1024) indexer_groups_kernel(RowMeta m, int row
 
 // -inf for the positions of a caller-visible score row that no tile covered (s beyond the row's last tile).
 // -inf beyond what the indexer wrote for each row (its last 128-key tile), in units of 2^unit_log2
-// keys (1: token scores; a page: page scores), up to max_units columns.
+// keys (1: token scores; page mode: the units of at most 32 keys it pools), up to max_units columns.
 __global__ void indexer_fill_tail_kernel(RowMeta m, int row0, float* scores, int64_t stride, int max_units,
                                          int unit_log2) {
   pdl_wait();
@@ -668,6 +656,37 @@ __global__ void indexer_fill_tail_kernel(RowMeta m, int row0, float* scores, int
   const int start = pos < 0 ? 0 : ((pos / 128 + 1) * 128) >> unit_log2;
   for (int s = start + blockIdx.x * blockDim.x + threadIdx.x; s < max_units; s += gridDim.x * blockDim.x)
     scores[(int64_t)blockIdx.y * stride + s] = -INFINITY;
+}
+
+// Page scores of pages larger than 32 keys from the indexer's 32-key unit maxima:
+//   pages[r][p] = max_j units[r][p * pool + j] for the row's pages p <= pos / P, -inf for p < max_pages beyond.
+__global__ void __launch_bounds__(256) page_pool_kernel(RowMeta m, int row0, const float* __restrict__ units,
+                                                        int64_t unit_stride, int pool_log2, int page_log2,
+                                                        float* __restrict__ pages, int64_t page_stride, int max_pages) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = row0 + blockIdx.y;
+  int b, pos;
+  row_info(m, r, b, pos);
+  const int n = pos >= 0 ? (pos >> page_log2) + 1 : 0;
+  const float* u = units + (int64_t)blockIdx.y * unit_stride;
+  float* out = pages + (int64_t)blockIdx.y * page_stride;
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < max_pages; p += gridDim.x * blockDim.x) {
+    float v = -INFINITY;
+    if (p < n)
+      for (int j = 0; j < (1 << pool_log2); ++j) v = fmaxf(v, u[((int64_t)p << pool_log2) + j]);
+    out[p] = v;
+  }
+}
+
+cudaError_t launch_page_pool(const RowMeta& m, int row0, int nrows, const float* units, int64_t unit_stride,
+                             int page_log2, float* pages, int64_t page_stride, int max_pages, cudaStream_t s) {
+  dim3 grid((max_pages + 255) / 256 < 16 ? (max_pages + 255) / 256 : 16, nrows);
+  cudaError_t e = launch_pdl(page_pool_kernel, grid, dim3(256), 0, s, m, row0, units, unit_stride, page_log2 - 5,
+                             page_log2, pages, page_stride, max_pages);
+  count_launches(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
@@ -768,7 +787,8 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
   a.stride = score_stride;
   a.max_seq_len = max_seq_len;
   a.page_log2 = page_log2;
-  a.max_pages = page_log2 >= 0 ? (max_seq_len + (1 << page_log2) - 1) >> page_log2 : 0;
+  const int unit_log2 = page_log2 < 5 ? page_log2 : 5;
+  a.max_pages = page_log2 >= 0 ? (max_seq_len + (1 << unit_log2) - 1) >> unit_log2 : 0;
   a.err = err;
   const int grid = g_sm_count;
   e = fp8 ? launch_pdl(indexer_tc_kernel<true>, dim3(grid), dim3(idx::kThreads), idx::kSmemBytes, s, map, a)
@@ -780,7 +800,7 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
   const int units = page_log2 >= 0 ? a.max_pages : max_seq_len;
   dim3 fgrid((units + 255) / 256 < 64 ? (units + 255) / 256 : 64, nrows);
   e = launch_pdl(indexer_fill_tail_kernel, fgrid, dim3(256), 0, s, m, row0, scores, score_stride, units,
-                 page_log2 >= 0 ? page_log2 : 0);
+                 page_log2 >= 0 ? unit_log2 : 0);
   count_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -158,8 +158,10 @@ def test_page_topk_rejects_bad_arguments(lib):
 
 
 def test_page_workspace_holds_page_scores_not_token_scores(lib):
-    # 64 rows of 131,072 keys: token scores need 32 MiB, page scores of 64-key pages 0.5 MiB
+    # 64 rows of 131,072 keys: token scores need 32 MiB; 64-key pages need 32-key unit maxima (1 MiB)
+    # and the page scores pooled from them (0.5 MiB); 32-key pages only their page scores
     tok = lib.dsa_indexer_workspace_bytes(64, 131072, 2048)
     page = lib.dsa_indexer_page_workspace_bytes(64, 131072, 64, 32)
-    assert tok >= 64 * 131072 * 4 and page < 64 * 2048 * 4 + (1 << 16)
+    assert tok >= 64 * 131072 * 4 and page < 64 * (4096 + 2048) * 4 + (1 << 16)
+    assert lib.dsa_indexer_page_workspace_bytes(64, 131072, 32, 64) < 64 * 4096 * 4 + (1 << 16)
     assert lib.dsa_indexer_page_workspace_bytes(0, 100, 64, 4) > 0 and lib.dsa_indexer_page_workspace_bytes(4, 0, 64, 4) == 0
