@@ -5,8 +5,9 @@ the paged caches, the step's new tokens appended, the same workspaces and the sa
 the kernels run with the full grid, full score blocks and full split-k partition.  A few sampled
 requests are then re-drawn with the host generators and written over their slots, so that the
 float64 oracle can recompute their rows one by one from the same values: indexer scores over
-every visible position, the top-k set (swap tolerance at the k-th score), and the attention
-output and LSE on the oracle's own index set.
+every visible position, the top-k set (swap tolerance at the k-th score), the page-granular
+selection (page scores, the page set, its expansion), and the attention output and LSE on the
+oracle's own index set.
 """
 import numpy as np
 import pytest
@@ -84,6 +85,23 @@ def test_full_size_sampled_rows(name):
         oracle_idx[r] = o.topk_select(o_scores, wl.topk)
         check_topk(g_idx[r], oracle_idx[r], o_scores, p, wl.topk)
     del scores
+
+    # page-granular selection with a budget of topk / page_size pages, on the same rows
+    P = wl.page_size
+    budget = wl.topk // P
+    n_pages = -(-wl.max_seq_len // P)
+    pscores = torch.empty((wl.num_rows, n_pages), dtype=torch.float32, device="cuda")
+    page_idx, token_idx = dsa.indexer_page_topk(prob.caches[0], prob.batch, prob.q_idx, prob.w, budget,
+                                                page_scores_out=pscores)
+    g_pages, g_tok, g_ps = page_idx.cpu().numpy(), token_idx.cpu().numpy(), pscores.cpu().numpy()
+    for r in rows:
+        p = int(pos[r])
+        keys = key_values(host_keys[int(req[r])][:p + 1], wl.key_format)
+        o_ps = o.page_scores(o.index_scores(o.bf16_to_f64(q_idx[r]), w[r], keys), P)
+        check_scores(g_ps[r], o_ps, p // P, n_pages)
+        check_topk(g_pages[r], o.page_topk_select(o_ps, budget), o_ps, p // P, budget)
+        assert np.array_equal(g_tok[r], o.pages_to_positions(g_pages[r], P, p))
+    del pscores
 
     # attention on the oracle's index sets for the sampled rows, every layer of the group
     idx_att = idx.clone()
