@@ -46,6 +46,13 @@ Definitions (R query rows, B requests, P page size):
   ("Making GLM-5.2 Sparse on TPUs", "Make the sparsity unit match the memory
   unit": a page ranked by its highest legal token score; "Stream indexer scores
   over live context": only page scores reach HBM);
+* decode context parallelism -- a request's tokens are interleaved over the
+  ranks (token s on rank s mod N); each rank selects the top-k of its own
+  positions, the candidates are exchanged, the top-k of their union is the
+  selection, each rank attends over its share of it and the pieces are
+  LSE-merged ("Serving GLM-5.2-504B on 8x RTX PRO 6000 GPUs", "Reaching 240K
+  context with DCP": KV sharded along the sequence, each rank's indexer scores
+  1/N of the keys; the interleave is the reading taken here);
 * IndexShare -- layers marked shared reuse the index buffer of the nearest
   preceding full (owner) layer ("vLLM Inference Path", "DSA Indexer";
   "Serving GLM-5.2-504B on 8x RTX PRO 6000 GPUs", "Root cause: a missing
@@ -312,6 +319,49 @@ def page_indexer_topk(cache: PagedCache, block_table, seq_lens, query_start_loc,
         pages.append(sel)
         positions.append(pages_to_positions(sel, P, int(pos[r])))
     return np.stack(pages), np.stack(positions), p_scores, t_scores
+
+
+# ---------------------------------------------------------------------------
+# decode context parallelism ("Serving GLM-5.2-504B on 8x RTX PRO 6000 GPUs", "Reaching 240K
+# context with DCP": the KV is sharded along the sequence across the ranks, so each rank's indexer
+# scores only its share of the keys)
+# ---------------------------------------------------------------------------
+def dcp_local_positions(L: int, rank: int, world: int) -> np.ndarray:
+    """Global positions of a request's first L tokens held by `rank`: s = rank, rank + world, ...
+    (interleaved by token; local position s // world)."""
+    return np.arange(rank, L, world, dtype=np.int64)
+
+
+def dcp_select(scores, k: int, world: int):
+    """The DCP selection of one decode row from its token scores over 0..pos, step by step:
+    each rank keeps the top-k of its own positions (local order = global order restricted to the
+    rank), the ranks exchange their (score, position) candidates, and every rank takes the top-k of
+    the union (larger score first, smaller position on ties).  Returns (global selection ascending,
+    -1 padded, as topk_select; per-rank candidate lists)."""
+    scores = np.asarray(scores, dtype=np.float64)
+    cand = []
+    for rank in range(world):
+        pos = dcp_local_positions(len(scores), rank, world)
+        local = topk_select(scores[pos], k)
+        cand.append([(scores[pos[i]], int(pos[i])) for i in local if i >= 0])
+    union = [c for lst in cand for c in lst]
+    union.sort(key=lambda c: (-c[0], c[1]))
+    chosen = sorted(p for _, p in union[:k])
+    out = np.full(k, -1, dtype=np.int32)
+    out[:len(chosen)] = chosen
+    return out, cand
+
+
+def dcp_attend(q_row, rows_of, selection, world: int, scale: float, d_latent: int = 512):
+    """Attention of one decode row over a selection whose positions are split between the ranks
+    that hold them: each rank attends over its own positions, and the partial results are combined
+    by the LSE merge.  rows_of(positions) returns the cached rows of global positions."""
+    sel = np.asarray([s for s in selection if s >= 0], dtype=np.int64)
+    parts = []
+    for rank in range(world):
+        mine = sel[sel % world == rank]
+        parts.append(attend(q_row, rows_of(mine), scale, d_latent))
+    return lse_merge(parts)
 
 
 # ---------------------------------------------------------------------------

@@ -159,3 +159,25 @@ def test_page_mutants_are_caught(monkeypatch, name):
     fn, bad = PAGE_MUTANTS[name]
     monkeypatch.setattr(o, fn, bad)
     assert not _pages_ok()
+
+
+def test_dcp_share_of_k_mutant_is_caught(monkeypatch):
+    """Keeping only k / world candidates per rank (a plausible shortcut) loses selections whenever the
+    top scores cluster on one rank: the DCP pin against the single-device top-k must fail."""
+    def share_of_k(scores, k, world):
+        scores = np.asarray(scores, float)
+        union = []
+        for rank in range(world):
+            pos = o.dcp_local_positions(len(scores), rank, world)
+            local = o.topk_select(scores[pos], max(1, k // world))
+            union += [(scores[pos[i]], int(pos[i])) for i in local if i >= 0]
+        union.sort(key=lambda c: (-c[0], c[1]))
+        out = np.full(k, -1, np.int32)
+        chosen = sorted(p for _, p in union[:k])
+        out[:len(chosen)] = chosen
+        return out, None
+    monkeypatch.setattr(o, "dcp_select", share_of_k)
+    world, k, n = 4, 16, 400
+    scores = np.random.default_rng(5).uniform(0, 1, n)
+    scores[np.arange(0, 4 * k, world)] += 10.0
+    assert not np.array_equal(o.dcp_select(scores, k, world)[0], o.topk_select(scores, k))
