@@ -486,6 +486,89 @@ def reference_main(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# decode context parallelism: one rank's device work
+# ---------------------------------------------------------------------------
+def dcp_main(args):
+    """One rank's side of the decode step under context parallelism over `world` ranks, on one GPU.
+
+    Rank 0 holds every request's interleaved share (ceil(L / world) tokens) in its own caches and
+    runs: append, the indexer and top-k over its keys, dcp_candidates, dcp_select, and per layer the
+    sparse MLA over its share plus dcp_merge.  The two all-gathers cross GPUs in a deployment; here
+    each is stood in by a device copy of the same bytes (every rank's slot holds this rank's tensor,
+    candidate positions relabelled to that rank's interleave), so the line measures the rank's
+    kernels without the exchanges.  Every request's new token is appended on this rank (the worst
+    case)."""
+    import torch
+    import deepseek_sparse_mla_gb300 as dsa
+    from deepseek_sparse_mla_gb300 import _lib
+    W = args.dcp
+    full = rank_workload(args.workload, 0)
+    lens = [-(-L // W) for L in full.seq_lens]
+    wl = wlm.Workload(f"{full.name}_dcp{W}_rank0", lens, [1] * len(lens), full.page_size, full.key_format, full.topk,
+                      full.layers, full.seed + 7000 + W)
+    prob = DeviceProblem(wl)
+    R, k = wl.num_rows, wl.topk
+    dev = "cuda"
+    scores = torch.empty((R, wl.max_seq_len), dtype=torch.float32, device=dev)
+    cs = torch.empty((R, k), dtype=torch.float32, device=dev)
+    cp = torch.empty((R, k), dtype=torch.int32, device=dev)
+    gidx = torch.empty((R, k), dtype=torch.int32, device=dev)
+    lidx = torch.empty((R, k), dtype=torch.int32, device=dev)
+    rel = torch.arange(W, dtype=torch.int32, device=dev).view(W, 1, 1)
+    merged = [torch.empty((R, 64, 512), dtype=torch.bfloat16, device=dev) for _ in range(wl.layers)]
+    merged_lse = [torch.empty((R, 64), dtype=torch.float32, device=dev) for _ in range(wl.layers)]
+
+    def step(marks=None):
+        m = marks.mark if marks is not None else (lambda name: None)
+        m("append")
+        for l in range(wl.layers):
+            dsa.kv_append(prob.caches[l], prob.new_c[l], prob.new_r[l], prob.slots, k_idx=prob.new_k if l == 0 else None)
+        m("indexer")
+        dsa.indexer_scores_topk(prob.caches[0], prob.batch, prob.q_idx, prob.w, k, topk_idx=prob.topk_idx,
+                                scores_out=scores, workspace=prob.ws_idx)
+        m("dcp_select")
+        dsa.dcp_candidates(scores, prob.topk_idx, 0, W, cand_scores=cs, cand_pos=cp)
+        all_s = cs.unsqueeze(0).expand(W, R, k).contiguous()                    # exchange 1 stand-in
+        all_p = torch.where(cp.unsqueeze(0) >= 0, cp.unsqueeze(0) + rel, cp.unsqueeze(0)).contiguous()
+        dsa.dcp_select(all_s, all_p, 0, global_idx=gidx, local_idx=lidx)
+        for l in range(wl.layers):
+            m("attention")
+            dsa.sparse_mla_decode(prob.caches[l], prob.batch, prob.q[l], lidx, wl.scale, out=prob.out[l],
+                                  lse=prob.lse[l], workspace=prob.ws_mla)
+            m("merge")
+            outs = prob.out[l].unsqueeze(0).expand(W, R, 64, 512).contiguous()  # exchange 2 stand-in
+            lses = prob.lse[l].unsqueeze(0).expand(W, R, 64).contiguous()
+            dsa.dcp_merge(outs, lses, out=merged[l], lse=merged_lse[l])
+        m(None)
+
+    lib = _lib.load()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    launches0 = lib.dsa_kernel_launches()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    launches = int(lib.dsa_kernel_launches() - launches0)
+    ms = t0.elapsed_time(t1) / args.steps
+    marks = Marks()
+    for _ in range(max(3, min(args.steps, 20))):
+        step(marks)
+        torch.cuda.synchronize()
+        marks.collect()
+    spans = {n: float(np.sum(v)) / max(3, min(args.steps, 20)) for n, v in marks.spans.items()}
+    line = {"metric": f"DCP rank decode layer-steps/s (world {W}, exchanges stood in by local copies)",
+            "value": wl.layers / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": full.name, "world": W, "rank_share": wl.summary()},
+            "ms_per_step_by_phase": spans, "gpu_launches": launches}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -497,10 +580,14 @@ def main():
     ap.add_argument("--selection", choices=["token", "page"], default="token",
                     help="token top-k (the method's selection), or page-granular selection of topk / page_size pages")
     ap.add_argument("--cpu-sample-requests", type=int, default=64)
+    ap.add_argument("--dcp", type=int, default=0,
+                    help="time one rank's device work of decode context parallelism over this many ranks")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         return reference_main(args)
+    if args.dcp:
+        return dcp_main(args)
 
     import torch
     import deepseek_sparse_mla_gb300 as dsa

@@ -25,7 +25,8 @@ DEFAULT_SCALE = 1.0 / 16.0     # 1/sqrt(192 + 64)
 _FORMATS = {"bf16": KEY_BF16, "fp8": KEY_FP8_E4M3, None: KEY_BF16}
 
 __all__ = ["LayerCache", "Batch", "kv_append", "indexer_scores_topk", "indexer_page_topk", "sparse_mla_decode", "sparse_mla_prefill",
-           "cache_bytes", "indexer_workspace_bytes", "mla_workspace_bytes", "DsaError", "DEFAULT_SCALE"]
+           "cache_bytes", "indexer_workspace_bytes", "mla_workspace_bytes", "DsaError", "DEFAULT_SCALE",
+           "dcp_candidates", "dcp_select", "dcp_merge"]
 
 
 def _ptr(t):
@@ -213,3 +214,55 @@ def sparse_mla_prefill(layer: LayerCache, batch: Batch, q, topk_idx, scale: floa
                        workspace=None, stream=None):
     """Sparse absorbed MLA for extend/prefill/verify rows (causal per row); returns (out, lse)."""
     return _sparse_mla(_lib.load().dsa_sparse_mla_prefill, layer, batch, q, topk_idx, scale, out, lse, workspace, stream)
+
+
+def dcp_candidates(local_scores, local_idx, rank: int, world: int, cand_scores=None, cand_pos=None, stream=None):
+    """Decode context parallelism, step 1: this rank's local top-k as (score, global position)
+    candidates.  local_scores [R, S] fp32 (the indexer's scores_out), local_idx [R, topk] int32.
+    Returns (cand_scores [R, topk] fp32, cand_pos [R, topk] int32)."""
+    R, topk = local_idx.shape
+    _need(local_idx, torch.int32, (R, topk), "local_idx")
+    _need(local_scores, torch.float32, (R, local_scores.shape[1]), "local_scores")
+    if cand_scores is None:
+        cand_scores = torch.empty((R, topk), dtype=torch.float32, device=local_idx.device)
+    if cand_pos is None:
+        cand_pos = torch.empty((R, topk), dtype=torch.int32, device=local_idx.device)
+    _need(cand_scores, torch.float32, (R, topk), "cand_scores")
+    _need(cand_pos, torch.int32, (R, topk), "cand_pos")
+    _lib.check(_lib.load().dsa_dcp_candidates(_ptr(local_scores), int(local_scores.shape[1]), _ptr(local_idx), topk, R,
+                                              rank, world, _ptr(cand_scores), _ptr(cand_pos), _stream(stream)))
+    return cand_scores, cand_pos
+
+
+def dcp_select(all_scores, all_pos, rank: int, global_idx=None, local_idx=None, stream=None):
+    """Step 2, after the candidate all-gather: all_scores / all_pos [world, R, topk].  Returns
+    (global_idx [R, topk], local_idx [R, topk]): the row's top-k as global positions (ascending) and
+    this rank's index buffer for sparse_mla_decode (-1 where another rank holds the position)."""
+    world, R, topk = all_scores.shape
+    _need(all_scores, torch.float32, (world, R, topk), "all_scores")
+    _need(all_pos, torch.int32, (world, R, topk), "all_pos")
+    if global_idx is None:
+        global_idx = torch.empty((R, topk), dtype=torch.int32, device=all_pos.device)
+    if local_idx is None:
+        local_idx = torch.empty((R, topk), dtype=torch.int32, device=all_pos.device)
+    _need(global_idx, torch.int32, (R, topk), "global_idx")
+    _need(local_idx, torch.int32, (R, topk), "local_idx")
+    _lib.check(_lib.load().dsa_dcp_select(_ptr(all_scores), _ptr(all_pos), world, R, topk, rank, _ptr(global_idx),
+                                          _ptr(local_idx), _stream(stream)))
+    return global_idx, local_idx
+
+
+def dcp_merge(outs, lses, out=None, lse=None, stream=None):
+    """Step 3, after the out/lse all-gather: outs [world, R, 64, 512] bf16, lses [world, R, 64]
+    fp32.  Returns (out [R, 64, 512] bf16, lse [R, 64] fp32): the LSE merge of the ranks' parts."""
+    world, R = outs.shape[0], outs.shape[1]
+    _need(outs, torch.bfloat16, (world, R, HEADS, LATENT_DIM), "outs")
+    _need(lses, torch.float32, (world, R, HEADS), "lses")
+    if out is None:
+        out = torch.empty((R, HEADS, LATENT_DIM), dtype=torch.bfloat16, device=outs.device)
+    if lse is None:
+        lse = torch.empty((R, HEADS), dtype=torch.float32, device=outs.device)
+    _need(out, torch.bfloat16, (R, HEADS, LATENT_DIM), "out")
+    _need(lse, torch.float32, (R, HEADS), "lse")
+    _lib.check(_lib.load().dsa_dcp_merge(_ptr(outs), _ptr(lses), world, R, _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse

@@ -361,4 +361,53 @@ dsa_status dsa_sparse_mla_prefill(const dsa_cache* layer, const dsa_batch* batch
   return sparse_mla_common(layer, batch, q, topk_idx, topk, scale, out, lse, workspace, workspace_bytes, stream, false);
 }
 
+
+// ---------------------------------------------------------------- decode context parallelism
+static dsa_status check_dcp(int32_t world, int32_t rank, int32_t num_rows, int32_t topk) {
+  if (world < 1 || world > 8) return fail(DSA_ERR_UNSUPPORTED, "dcp: world %d outside 1..8", world);
+  if (rank < 0 || rank >= world) return fail(DSA_ERR_INVALID_ARG, "dcp: rank %d outside 0..%d", rank, world - 1);
+  if (num_rows < 0) return fail(DSA_ERR_INVALID_ARG, "dcp: num_rows %d < 0", num_rows);
+  if (topk < 1 || topk > DSA_MAX_TOPK) return fail(DSA_ERR_INVALID_ARG, "dcp: topk %d outside 1..%d", topk, DSA_MAX_TOPK);
+  if ((int64_t)world * topk > 16384)
+    return fail(DSA_ERR_UNSUPPORTED, "dcp: world * topk = %d exceeds 16384", world * topk);
+  return ok();
+}
+
+dsa_status dsa_dcp_candidates(const float* local_scores, int64_t score_stride, const int32_t* local_idx, int32_t topk,
+                              int32_t num_rows, int32_t rank, int32_t world, float* cand_scores, int32_t* cand_pos,
+                              void* stream) {
+  dsa_status st = check_dcp(world, rank, num_rows, topk);
+  if (st != DSA_OK) return st;
+  if (num_rows == 0) return ok();
+  if (!local_scores || !local_idx || !cand_scores || !cand_pos) return fail(DSA_ERR_INVALID_ARG, "dcp_candidates: NULL pointer");
+  if (score_stride < 1) return fail(DSA_ERR_INVALID_ARG, "dcp_candidates: score_stride %lld < 1", (long long)score_stride);
+  if ((int64_t)world * score_stride > INT32_MAX)
+    return fail(DSA_ERR_UNSUPPORTED, "dcp_candidates: global positions overflow int32");
+  cudaError_t e = launch_dcp_candidates(local_scores, score_stride, local_idx, topk, num_rows, rank, world, cand_scores,
+                                        cand_pos, static_cast<cudaStream_t>(stream));
+  return cuda_status(e, "dcp candidates launch");
+}
+
+dsa_status dsa_dcp_select(const float* cand_scores, const int32_t* cand_pos, int32_t world, int32_t num_rows,
+                          int32_t topk, int32_t rank, int32_t* global_idx, int32_t* local_idx, void* stream) {
+  dsa_status st = check_dcp(world, rank, num_rows, topk);
+  if (st != DSA_OK) return st;
+  if (num_rows == 0) return ok();
+  if (!cand_scores || !cand_pos || !global_idx || !local_idx) return fail(DSA_ERR_INVALID_ARG, "dcp_select: NULL pointer");
+  cudaError_t e = launch_dcp_select(cand_scores, cand_pos, world, num_rows, topk, rank, global_idx, local_idx,
+                                    static_cast<cudaStream_t>(stream));
+  return cuda_status(e, "dcp select launch");
+}
+
+dsa_status dsa_dcp_merge(const void* outs, const float* lses, int32_t world, int32_t num_rows, void* out, float* lse,
+                         void* stream) {
+  if (world < 1 || world > 8) return fail(DSA_ERR_UNSUPPORTED, "dcp_merge: world %d outside 1..8", world);
+  if (num_rows < 0) return fail(DSA_ERR_INVALID_ARG, "dcp_merge: num_rows %d < 0", num_rows);
+  if (num_rows == 0) return ok();
+  if (!outs || !lses || !out) return fail(DSA_ERR_INVALID_ARG, "dcp_merge: NULL pointer");
+  if (!aligned16(outs) || !aligned16(out)) return fail(DSA_ERR_INVALID_ARG, "dcp_merge: outs/out not 16-byte aligned");
+  cudaError_t e = launch_dcp_merge(outs, lses, world, num_rows, out, lse, static_cast<cudaStream_t>(stream));
+  return cuda_status(e, "dcp merge launch");
+}
+
 }  // extern "C"

@@ -285,6 +285,57 @@ DSA_API dsa_status dsa_sparse_mla_prefill(const dsa_cache* layer, const dsa_batc
                                   const int32_t* topk_idx, int32_t topk, float scale, void* out, float* lse,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Decode context parallelism: the device steps around the two exchanges.
+ * ("Serving GLM-5.2-504B on 8x RTX PRO 6000 GPUs", "Reaching 240K context with DCP": the KV is
+ * sharded along the sequence across the ranks, each rank scoring only its share of the keys.)
+ * Token s of a request lives on rank s mod world at local position s / world; each rank holds
+ * its share of every request in its own cache and runs dsa_indexer_scores_topk over it (decode
+ * rows only: the local row sees all of its rank's keys).  Then, per rank:
+ *   dsa_dcp_candidates  local top-k -> (score, global position) candidates;
+ *   all-gather of the candidates (the caller's collective) into [world][num_rows][topk];
+ *   dsa_dcp_select      the global top-k (identical on every rank) and this rank's local index
+ *                       buffer for dsa_sparse_mla_decode;
+ *   dsa_sparse_mla_decode over the local cache with that buffer (out and lse required);
+ *   all-gather of out and lse into [world][...];
+ *   dsa_dcp_merge       the LSE merge: the single-device attention over the global selection.
+ * world is 1..8 and world * topk <= 16384 (DSA_ERR_UNSUPPORTED otherwise); num_rows 0 is a no-op.
+ * No workspace; nothing is allocated.  Errors as for the other entry points.
+ */
+
+/*
+ *   local_scores  device fp32 [num_rows, score_stride]: the rank's indexer scores (scores_out of
+ *                 dsa_indexer_scores_topk, whose row stride is the batch's max_seq_len).
+ *   local_idx     device int32 [num_rows, topk]: the rank's local top-k (-1 padded).
+ *   cand_scores   device fp32 [num_rows, topk] (output): local_scores at local_idx, -inf for -1.
+ *   cand_pos      device int32 [num_rows, topk] (output): local_idx * world + rank, -1 for -1.
+ */
+DSA_API dsa_status dsa_dcp_candidates(const float* local_scores, int64_t score_stride, const int32_t* local_idx,
+                                      int32_t topk, int32_t num_rows, int32_t rank, int32_t world,
+                                      float* cand_scores, int32_t* cand_pos, void* stream);
+
+/*
+ *   cand_scores, cand_pos  device [world, num_rows, topk]: every rank's candidates, rank-major.
+ *   global_idx  device int32 [num_rows, topk] (output): the topk candidates with the largest score
+ *               (ties: smaller global position), sorted ascending, -1 padded when fewer exist;
+ *               equal to dsa_indexer_scores_topk's selection over the unsharded row.
+ *   local_idx   device int32 [num_rows, topk] (output): global_idx[i] / world where
+ *               global_idx[i] mod world == rank, else -1 (same slots as global_idx).
+ */
+DSA_API dsa_status dsa_dcp_select(const float* cand_scores, const int32_t* cand_pos, int32_t world,
+                                  int32_t num_rows, int32_t topk, int32_t rank, int32_t* global_idx,
+                                  int32_t* local_idx, void* stream);
+
+/*
+ *   outs   device bf16 [world, num_rows, 64, 512], 16-byte aligned: every rank's out.
+ *   lses   device fp32 [world, num_rows, 64]: every rank's lse (-inf: that rank selected nothing).
+ *   out    device bf16 [num_rows, 64, 512] (output), 16-byte aligned:
+ *          sum_w exp(lse_w - M) out_w / sum_w exp(lse_w - M), M = max_w lse_w; 0 if all are -inf.
+ *   lse    optional device fp32 [num_rows, 64] (output): M + ln sum_w exp(lse_w - M), or -inf.
+ */
+DSA_API dsa_status dsa_dcp_merge(const void* outs, const float* lses, int32_t world, int32_t num_rows, void* out,
+                                 float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -165,3 +165,26 @@ def test_page_workspace_holds_page_scores_not_token_scores(lib):
     assert tok >= 64 * 131072 * 4 and page < 64 * (4096 + 2048) * 4 + (1 << 16)
     assert lib.dsa_indexer_page_workspace_bytes(64, 131072, 32, 64) < 64 * 4096 * 4 + (1 << 16)
     assert lib.dsa_indexer_page_workspace_bytes(0, 100, 64, 4) > 0 and lib.dsa_indexer_page_workspace_bytes(4, 0, 64, 4) == 0
+
+
+def test_dcp_entry_points_reject_bad_arguments(lib):
+    P = ctypes.c_void_p
+    # dsa_dcp_candidates(scores, stride, local_idx, topk, rows, rank, world, cand_scores, cand_pos, stream)
+    assert lib.dsa_dcp_candidates(P(A), 4096, P(A), 2048, 4, 0, 9, P(A), P(A), None) == UNSUPPORTED   # world > 8
+    assert lib.dsa_dcp_candidates(P(A), 4096, P(A), 2048, 4, 0, 0, P(A), P(A), None) == UNSUPPORTED   # world 0
+    assert lib.dsa_dcp_candidates(P(A), 4096, P(A), 2048, 4, 2, 2, P(A), P(A), None) == INVALID       # rank >= world
+    assert lib.dsa_dcp_candidates(P(A), 4096, P(A), 4096, 4, 0, 8, P(A), P(A), None) == UNSUPPORTED   # 8 x 4096 > 16384
+    assert lib.dsa_dcp_candidates(P(A), 4096, P(A), 9000, 4, 0, 1, P(A), P(A), None) == INVALID       # topk > 8192
+    assert lib.dsa_dcp_candidates(None, 4096, P(A), 2048, 4, 0, 2, P(A), P(A), None) == INVALID
+    assert lib.dsa_dcp_candidates(P(A), 0, P(A), 2048, 4, 0, 2, P(A), P(A), None) == INVALID
+    assert lib.dsa_dcp_candidates(P(A), 1 << 30, P(A), 2048, 4, 0, 4, P(A), P(A), None) == UNSUPPORTED  # int32 positions
+    assert lib.dsa_dcp_candidates(None, 4096, None, 2048, 0, 0, 2, None, None, None) == 0             # no rows: no-op
+    # dsa_dcp_select(cand_scores, cand_pos, world, rows, topk, rank, global_idx, local_idx, stream)
+    assert lib.dsa_dcp_select(P(A), P(A), 8, 4, 2049, 0, P(A), P(A), None) == UNSUPPORTED
+    assert lib.dsa_dcp_select(P(A), None, 2, 4, 2048, 0, P(A), P(A), None) == INVALID
+    assert lib.dsa_dcp_select(P(A), P(A), 2, -1, 2048, 0, P(A), P(A), None) == INVALID
+    # dsa_dcp_merge(outs, lses, world, rows, out, lse, stream)
+    assert lib.dsa_dcp_merge(P(A), P(A), 9, 4, P(A), None, None) == UNSUPPORTED
+    assert lib.dsa_dcp_merge(P(A + 8), P(A), 2, 4, P(A), None, None) == INVALID                        # unaligned outs
+    assert lib.dsa_dcp_merge(P(A), None, 2, 4, P(A), None, None) == INVALID
+    assert lib.dsa_dcp_merge(None, None, 2, 0, None, None, None) == 0
