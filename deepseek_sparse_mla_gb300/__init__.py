@@ -184,7 +184,7 @@ def indexer_page_topk(owner: LayerCache, batch: Batch, q_idx, w, page_budget: in
     return page_idx, token_idx
 
 
-def _sparse_mla(fn, layer, batch, q, topk_idx, scale, out, lse, workspace, stream):
+def _sparse_mla(fn, layer, batch, q, topk_idx, scale, out, lse, workspace, stream, row_counts=None):
     R = batch.num_rows
     _need(q, torch.bfloat16, (R, HEADS, ROW_DIM), "q")
     if topk_idx is None:
@@ -199,15 +199,24 @@ def _sparse_mla(fn, layer, batch, q, topk_idx, scale, out, lse, workspace, strea
     if workspace is None:
         workspace = _workspace(mla_workspace_bytes(R, topk), q.device)
     c, b = layer.struct(), batch.struct()
-    _lib.check(fn(ctypes.byref(c), ctypes.byref(b), _ptr(q), _ptr(topk_idx), topk, float(scale), _ptr(out), _ptr(lse),
-                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    if row_counts is None:
+        _lib.check(fn(ctypes.byref(c), ctypes.byref(b), _ptr(q), _ptr(topk_idx), topk, float(scale), _ptr(out),
+                      _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    else:
+        _need(row_counts, torch.int32, (R,), "row_counts")
+        _lib.check(_lib.load().dsa_sparse_mla_decode_ragged(
+            ctypes.byref(c), ctypes.byref(b), _ptr(q), _ptr(topk_idx), topk, _ptr(row_counts), float(scale), _ptr(out),
+            _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse
 
 
 def sparse_mla_decode(layer: LayerCache, batch: Batch, q, topk_idx, scale: float = DEFAULT_SCALE, out=None, lse=None,
-                      workspace=None, stream=None):
-    """Sparse absorbed MLA for decode rows (one per request); returns (out [R,64,512] bf16, lse)."""
-    return _sparse_mla(_lib.load().dsa_sparse_mla_decode, layer, batch, q, topk_idx, scale, out, lse, workspace, stream)
+                      workspace=None, stream=None, row_counts=None):
+    """Sparse absorbed MLA for decode rows (one per request); returns (out [R,64,512] bf16, lse).
+    row_counts (optional int32 [R]): row r's valid entries lead its buffer and entries from
+    row_counts[r] on are -1; the call then spends time only on those leading entries."""
+    return _sparse_mla(_lib.load().dsa_sparse_mla_decode, layer, batch, q, topk_idx, scale, out, lse, workspace, stream,
+                       row_counts)
 
 
 def sparse_mla_prefill(layer: LayerCache, batch: Batch, q, topk_idx, scale: float = DEFAULT_SCALE, out=None, lse=None,
@@ -234,22 +243,24 @@ def dcp_candidates(local_scores, local_idx, rank: int, world: int, cand_scores=N
     return cand_scores, cand_pos
 
 
-def dcp_select(all_scores, all_pos, rank: int, global_idx=None, local_idx=None, stream=None):
+def dcp_select(all_scores, all_pos, rank: int, global_idx=None, local_idx=None, local_count=None, stream=None):
     """Step 2, after the candidate all-gather: all_scores / all_pos [world, R, topk].  Returns
-    (global_idx [R, topk], local_idx [R, topk]): the row's top-k as global positions (ascending) and
-    this rank's index buffer for sparse_mla_decode (-1 where another rank holds the position)."""
+    (global_idx [R, topk], local_idx [R, topk], local_count [R]): the row's top-k as global positions
+    (ascending), this rank's share of it as local positions (ascending, compacted to the front of
+    the row, -1 after), and the share's size; local_idx and local_count feed sparse_mla_decode."""
     world, R, topk = all_scores.shape
     _need(all_scores, torch.float32, (world, R, topk), "all_scores")
     _need(all_pos, torch.int32, (world, R, topk), "all_pos")
-    if global_idx is None:
-        global_idx = torch.empty((R, topk), dtype=torch.int32, device=all_pos.device)
-    if local_idx is None:
-        local_idx = torch.empty((R, topk), dtype=torch.int32, device=all_pos.device)
+    dev = all_pos.device
+    global_idx = torch.empty((R, topk), dtype=torch.int32, device=dev) if global_idx is None else global_idx
+    local_idx = torch.empty((R, topk), dtype=torch.int32, device=dev) if local_idx is None else local_idx
+    local_count = torch.empty((R,), dtype=torch.int32, device=dev) if local_count is None else local_count
     _need(global_idx, torch.int32, (R, topk), "global_idx")
     _need(local_idx, torch.int32, (R, topk), "local_idx")
+    _need(local_count, torch.int32, (R,), "local_count")
     _lib.check(_lib.load().dsa_dcp_select(_ptr(all_scores), _ptr(all_pos), world, R, topk, rank, _ptr(global_idx),
-                                          _ptr(local_idx), _stream(stream)))
-    return global_idx, local_idx
+                                          _ptr(local_idx), _ptr(local_count), _stream(stream)))
+    return global_idx, local_idx, local_count
 
 
 def dcp_merge(outs, lses, out=None, lse=None, stream=None):

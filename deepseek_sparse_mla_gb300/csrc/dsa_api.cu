@@ -119,7 +119,8 @@ static RowMeta row_meta(const dsa_batch* b, bool decode) {
 
 static dsa_status sparse_mla_common(const dsa_cache* layer, const dsa_batch* batch, const void* q,
                                     const int32_t* topk_idx, int32_t topk, float scale, void* out, float* lse,
-                                    void* workspace, size_t workspace_bytes, void* stream, bool decode) {
+                                    void* workspace, size_t workspace_bytes, void* stream, bool decode,
+                                    const int32_t* row_counts = nullptr) {
   dsa_status st = check_cache(layer, false);
   if (st != DSA_OK) return st;
   st = check_batch(batch, !decode);
@@ -141,7 +142,7 @@ static dsa_status sparse_mla_common(const dsa_cache* layer, const dsa_batch* bat
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(DSA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
   RowMeta m = row_meta(batch, decode);
   cudaError_t e = launch_sparse_mla(*layer, m, batch->num_rows, q, topk_idx, topk, scale, out, lse, workspace, plan,
-                                    (cudaStream_t)stream);
+                                    (cudaStream_t)stream, row_counts);
   return cuda_status(e, "sparse MLA launch");
 }
 
@@ -355,6 +356,14 @@ dsa_status dsa_sparse_mla_decode(const dsa_cache* layer, const dsa_batch* batch,
   return sparse_mla_common(layer, batch, q, topk_idx, topk, scale, out, lse, workspace, workspace_bytes, stream, true);
 }
 
+dsa_status dsa_sparse_mla_decode_ragged(const dsa_cache* layer, const dsa_batch* batch, const void* q,
+                                        const int32_t* topk_idx, int32_t topk, const int32_t* row_counts, float scale,
+                                        void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!row_counts) return fail(DSA_ERR_INVALID_ARG, "row_counts is NULL");
+  return sparse_mla_common(layer, batch, q, topk_idx, topk, scale, out, lse, workspace, workspace_bytes, stream, true,
+                           row_counts);
+}
+
 dsa_status dsa_sparse_mla_prefill(const dsa_cache* layer, const dsa_batch* batch, const void* q, const int32_t* topk_idx,
                                   int32_t topk, float scale, void* out, float* lse, void* workspace,
                                   size_t workspace_bytes, void* stream) {
@@ -389,13 +398,14 @@ dsa_status dsa_dcp_candidates(const float* local_scores, int64_t score_stride, c
 }
 
 dsa_status dsa_dcp_select(const float* cand_scores, const int32_t* cand_pos, int32_t world, int32_t num_rows,
-                          int32_t topk, int32_t rank, int32_t* global_idx, int32_t* local_idx, void* stream) {
+                          int32_t topk, int32_t rank, int32_t* global_idx, int32_t* local_idx, int32_t* local_count,
+                          void* stream) {
   dsa_status st = check_dcp(world, rank, num_rows, topk);
   if (st != DSA_OK) return st;
   if (num_rows == 0) return ok();
   if (!cand_scores || !cand_pos || !global_idx || !local_idx) return fail(DSA_ERR_INVALID_ARG, "dcp_select: NULL pointer");
   cudaError_t e = launch_dcp_select(cand_scores, cand_pos, world, num_rows, topk, rank, global_idx, local_idx,
-                                    static_cast<cudaStream_t>(stream));
+                                    local_count, static_cast<cudaStream_t>(stream));
   return cuda_status(e, "dcp select launch");
 }
 

@@ -126,12 +126,13 @@ cudaError_t launch_page_expand(const RowMeta& m, int row0, int nrows, const int3
 
 cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows, const void* q,
                               const int32_t* topk_idx, int topk, float scale, void* out, float* lse,
-                              void* workspace, const MlaPlan& plan, cudaStream_t s);
+                              void* workspace, const MlaPlan& plan, cudaStream_t s,
+                              const int32_t* row_count = nullptr);
 
 cudaError_t launch_dcp_candidates(const float* local_scores, int64_t stride, const int32_t* local_idx, int k, int rows,
                                   int rank, int world, float* cand_score, int32_t* cand_pos, cudaStream_t s);
 cudaError_t launch_dcp_select(const float* cand_score, const int32_t* cand_pos, int world, int rows, int k, int rank,
-                              int32_t* global_idx, int32_t* local_idx, cudaStream_t s);
+                              int32_t* global_idx, int32_t* local_idx, int32_t* local_count, cudaStream_t s);
 cudaError_t launch_dcp_merge(const void* outs, const float* lses, int world, int rows, void* out, float* lse,
                              cudaStream_t s);
 

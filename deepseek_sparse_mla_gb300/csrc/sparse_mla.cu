@@ -77,6 +77,7 @@ constexpr uint32_t kPolls = 1u << 22;
 struct MlaArgs {
   RowMeta m;
   const int32_t* topk_idx;
+  const int32_t* row_count;       // optional [rows]: valid entries lead each row (cluster mode uses it)
   int topk, tiles, units, ctas;
   int split;                      // > 1: cluster mode, pieces per row (= cluster size); 1: unit split
   int log2_page, num_pages;
@@ -151,8 +152,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
   uint32_t* const err = a.cta_err + cta;
   const int split = a.split;
   // cluster mode: piece cta % split of row cta / split; otherwise a contiguous range of units
-  const int u0 = split > 1 ? (cta / split) * T + (cta % split) * T / split : unit_start(cta, a.units, a.ctas);
-  const int u1 = split > 1 ? (cta / split) * T + (cta % split + 1) * T / split : unit_start(cta + 1, a.units, a.ctas);
+  int u0 = split > 1 ? (cta / split) * T + (cta % split) * T / split : unit_start(cta, a.units, a.ctas);
+  int u1 = split > 1 ? (cta / split) * T + (cta % split + 1) * T / split : unit_start(cta + 1, a.units, a.ctas);
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -187,6 +188,16 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
   // dependent launch: the prologue above overlaps the previous kernel).  No early trigger: the merge
   // kernel launched while this grid still runs made each call about 5 us slower.
   pdl_wait();
+  // With row counts (cluster mode only) a row spans only the tiles that hold its first row_count
+  // entries, at least one per piece; entries past the count are -1 by contract, so the unit split,
+  // which ignores the counts, gives the same result.  The counts are read after the wait; the
+  // ranges without them are known before it (computing them only after the wait cost 6 us a call).
+  if (split > 1 && a.row_count) {
+    const int c = a.row_count[cta / split];
+    const int Tr = c < 0 ? split : min(T, max(split, (c + kTok - 1) / kTok));
+    u0 = (cta / split) * T + (cta % split) * Tr / split;
+    u1 = (cta / split) * T + (cta % split + 1) * Tr / split;
+  }
   // this CTA's timeout bits: cleared after the wait (the previous call's merge has read them) and
   // before the barrier below, after which a bounded wait may set them
   if (threadIdx.x == 0) *err = 0u;
@@ -746,7 +757,7 @@ MlaPlan plan_mla(int num_rows, int topk) {
 
 cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows, const void* q,
                               const int32_t* topk_idx, int topk, float scale, void* out, float* lse,
-                              void* workspace, const MlaPlan& plan, cudaStream_t s) {
+                              void* workspace, const MlaPlan& plan, cudaStream_t s, const int32_t* row_count) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -762,6 +773,7 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
   MlaArgs a;
   a.m = m;
   a.topk_idx = topk_idx;
+  a.row_count = row_count;
   a.topk = topk;
   a.tiles = plan.tiles;
   a.units = plan.units;

@@ -10,7 +10,8 @@ its local positions.  A decode step on one rank is:
   1. ``indexer_scores_topk`` over the local cache (its local top-k and scores);
   2. ``dcp_candidates`` -> all-gather -> ``dcp_select``: the top-k of the union of every rank's
      local top-k, which holds the whole row's top-k, so the selection equals the single-device one;
-  3. ``sparse_mla_decode`` over the local cache with this rank's share of that selection;
+  3. ``sparse_mla_decode`` over the local cache with this rank's share of that selection (a
+     compacted buffer with its per-row sizes, so the rank's attention covers only its share);
   4. all-gather of out / lse -> ``dcp_merge`` (LSE merge): the single-device attention.
 
 The two all-gathers are the only exchanges.  ``gather`` is any callable that maps this rank's
@@ -72,7 +73,7 @@ class DcpDecode:
     def select(self, owner, batch, q_idx, w, topk: int):
         """Indexer over the local cache, candidate exchange, global top-k.  batch describes the
         local cache (decode rows: seq_lens are the local lengths, max_seq_len their bound).
-        Returns (global_idx, local_idx), both [R, topk] int32."""
+        Returns (global_idx [R, topk], local_idx [R, topk], local_count [R]), int32."""
         if self.world * topk > 16384:
             raise ValueError(f"world * topk = {self.world * topk} exceeds 16384")
         R = batch.num_rows
@@ -81,10 +82,10 @@ class DcpDecode:
         cand_s, cand_p = self.ops.dcp_candidates(scores, local_top, self.rank, self.world)
         return self.ops.dcp_select(self.gather(cand_s), self.gather(cand_p), self.rank)
 
-    def attend(self, layer, batch, q, local_idx, scale: float = DEFAULT_SCALE):
+    def attend(self, layer, batch, q, local_idx, local_count=None, scale: float = DEFAULT_SCALE):
         """Local sparse MLA over this rank's share of the selection, out/lse exchange, LSE merge.
         Returns (out [R, 64, 512] bf16, lse [R, 64] fp32), identical on every rank."""
         R = batch.num_rows
         lse = torch.empty((R, HEADS), dtype=torch.float32, device=q.device)
-        out, lse = self.ops.sparse_mla_decode(layer, batch, q, local_idx, scale, lse=lse)
+        out, lse = self.ops.sparse_mla_decode(layer, batch, q, local_idx, scale, lse=lse, row_counts=local_count)
         return self.ops.dcp_merge(self.gather(out), self.gather(lse))

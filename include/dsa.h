@@ -276,6 +276,20 @@ DSA_API dsa_status dsa_sparse_mla_decode(const dsa_cache* layer, const dsa_batch
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * dsa_sparse_mla_decode over index buffers whose valid entries lead each row: row r's entries at
+ * and past row_counts[r] must be -1 (the caller guarantees it; they are skipped as usual).  The
+ * result is dsa_sparse_mla_decode's on the same buffer; the call only spends less time on rows with
+ * few entries, since each row's work covers its first row_counts[r] entries rather than all topk.
+ * (Used for a rank's share of a DCP selection, which holds about topk / world entries.)
+ *   row_counts  device int32 [num_rows], written before the call on the same stream (for example by
+ *               dsa_dcp_select); NULL is rejected.  Other arguments as for dsa_sparse_mla_decode.
+ */
+DSA_API dsa_status dsa_sparse_mla_decode_ragged(const dsa_cache* layer, const dsa_batch* batch, const void* q,
+                                        const int32_t* topk_idx, int32_t topk, const int32_t* row_counts,
+                                        float scale, void* out, float* lse, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
+/*
  * Same operation for extend/prefill/verify batches: several query rows per request, causal per
  * row (row i of request b sees positions 0..L_b - q_len_b + i; query_start_loc is required).
  * ("Making GLM-5.2 Sparse on TPUs", "Carry sparse reads through prefill" and "Pack requests and
@@ -294,9 +308,10 @@ DSA_API dsa_status dsa_sparse_mla_prefill(const dsa_cache* layer, const dsa_batc
  * rows only: the local row sees all of its rank's keys).  Then, per rank:
  *   dsa_dcp_candidates  local top-k -> (score, global position) candidates;
  *   all-gather of the candidates (the caller's collective) into [world][num_rows][topk];
- *   dsa_dcp_select      the global top-k (identical on every rank) and this rank's local index
- *                       buffer for dsa_sparse_mla_decode;
- *   dsa_sparse_mla_decode over the local cache with that buffer (out and lse required);
+ *   dsa_dcp_select      the global top-k (identical on every rank), this rank's share of it as a
+ *                       compacted local index buffer, and the share's size per row;
+ *   dsa_sparse_mla_decode_ragged over the local cache with that buffer and those sizes (out and
+ *                       lse required): each rank's attention covers only its share;
  *   all-gather of out and lse into [world][...];
  *   dsa_dcp_merge       the LSE merge: the single-device attention over the global selection.
  * world is 1..8 and world * topk <= 16384 (DSA_ERR_UNSUPPORTED otherwise); num_rows 0 is a no-op.
@@ -319,12 +334,15 @@ DSA_API dsa_status dsa_dcp_candidates(const float* local_scores, int64_t score_s
  *   global_idx  device int32 [num_rows, topk] (output): the topk candidates with the largest score
  *               (ties: smaller global position), sorted ascending, -1 padded when fewer exist;
  *               equal to dsa_indexer_scores_topk's selection over the unsharded row.
- *   local_idx   device int32 [num_rows, topk] (output): global_idx[i] / world where
- *               global_idx[i] mod world == rank, else -1 (same slots as global_idx).
+ *   local_idx   device int32 [num_rows, topk] (output): this rank's share of global_idx (positions p
+ *               with p mod world == rank) as local positions p / world, ascending, in the first
+ *               local_count[r] slots of row r, -1 after them: an index buffer for
+ *               dsa_sparse_mla_decode_ragged (or dsa_sparse_mla_decode) over the rank's cache.
+ *   local_count optional device int32 [num_rows] (output): the size of this rank's share; NULL to skip.
  */
 DSA_API dsa_status dsa_dcp_select(const float* cand_scores, const int32_t* cand_pos, int32_t world,
                                   int32_t num_rows, int32_t topk, int32_t rank, int32_t* global_idx,
-                                  int32_t* local_idx, void* stream);
+                                  int32_t* local_idx, int32_t* local_count, void* stream);
 
 /*
  *   outs   device bf16 [world, num_rows, 64, 512], 16-byte aligned: every rank's out.

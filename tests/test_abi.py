@@ -179,10 +179,15 @@ def test_dcp_entry_points_reject_bad_arguments(lib):
     assert lib.dsa_dcp_candidates(P(A), 0, P(A), 2048, 4, 0, 2, P(A), P(A), None) == INVALID
     assert lib.dsa_dcp_candidates(P(A), 1 << 30, P(A), 2048, 4, 0, 4, P(A), P(A), None) == UNSUPPORTED  # int32 positions
     assert lib.dsa_dcp_candidates(None, 4096, None, 2048, 0, 0, 2, None, None, None) == 0             # no rows: no-op
-    # dsa_dcp_select(cand_scores, cand_pos, world, rows, topk, rank, global_idx, local_idx, stream)
-    assert lib.dsa_dcp_select(P(A), P(A), 8, 4, 2049, 0, P(A), P(A), None) == UNSUPPORTED
-    assert lib.dsa_dcp_select(P(A), None, 2, 4, 2048, 0, P(A), P(A), None) == INVALID
-    assert lib.dsa_dcp_select(P(A), P(A), 2, -1, 2048, 0, P(A), P(A), None) == INVALID
+    # dsa_dcp_select(cand_scores, cand_pos, world, rows, topk, rank, global_idx, local_idx, local_count, stream)
+    assert lib.dsa_dcp_select(P(A), P(A), 8, 4, 2049, 0, P(A), P(A), None, None) == UNSUPPORTED
+    assert lib.dsa_dcp_select(P(A), None, 2, 4, 2048, 0, P(A), P(A), None, None) == INVALID
+    assert lib.dsa_dcp_select(P(A), P(A), 2, -1, 2048, 0, P(A), P(A), None, None) == INVALID
+    # the ragged attention call needs its row counts
+    b = _batch(B=2, rows=2, L=300)
+    c = _cache(fmt=0)
+    assert lib.dsa_sparse_mla_decode_ragged(ctypes.byref(c), ctypes.byref(b), P(A), P(A), 128, None, 0.0625, P(A),
+                                            None, P(A), 1 << 30, None) == INVALID
     # dsa_dcp_merge(outs, lses, world, rows, out, lse, stream)
     assert lib.dsa_dcp_merge(P(A), P(A), 9, 4, P(A), None, None) == UNSUPPORTED
     assert lib.dsa_dcp_merge(P(A + 8), P(A), 2, 4, P(A), None, None) == INVALID                        # unaligned outs

@@ -62,10 +62,16 @@ def _fake_ops(rank, world):
             cand = sorted((-float(s), int(p)) for s, p in zip(all_s[:, r].flatten(), all_p[:, r].flatten()) if p >= 0)
             chosen = sorted(p for _, p in cand[:k])
             g[r, :len(chosen)] = torch.tensor(chosen, dtype=torch.int32)
-        mine = (g >= 0) & (g % world == rank)
-        return g, torch.where(mine, g // world, torch.tensor(-1, dtype=torch.int32))
+        li = torch.full_like(g, -1)
+        cnt = torch.zeros(g.shape[0], dtype=torch.int32)
+        for r in range(g.shape[0]):
+            mine = [int(p) // world for p in g[r] if p >= 0 and p % world == rank]
+            li[r, :len(mine)] = torch.tensor(mine, dtype=torch.int32)
+            cnt[r] = len(mine)
+        return g, li, cnt
 
-    def sparse_mla_decode(layer, batch, q, local_idx, scale, lse=None):
+    def sparse_mla_decode(layer, batch, q, local_idx, scale, lse=None, row_counts=None):
+        assert row_counts is not None and bool(torch.all(local_idx[torch.arange(local_idx.shape[1]) >= row_counts[:, None]] == -1))
         outs, lses = [], []
         for b in range(batch.num_rows):
             sel = local_idx[b][local_idx[b] >= 0].numpy()
@@ -96,8 +102,8 @@ def _rank_main(rank, world, port, out_dir):
     cache = {"scores": [s[p] for s, p in zip(scores, share)], "rows": [r[p] for r, p in zip(rows, share)]}
     batch = SimpleNamespace(num_rows=len(L_ROWS), max_seq_len=max(len(p) for p in share))
     step = dcp.DcpDecode(rank, world, ops=_fake_ops(rank, world))
-    g, li = step.select(cache, batch, torch.zeros(1), None, TOPK)
-    out, lse = step.attend(cache, batch, torch.from_numpy(q), li, SCALE)
+    g, li, cnt = step.select(cache, batch, torch.zeros(1), None, TOPK)
+    out, lse = step.attend(cache, batch, torch.from_numpy(q), li, cnt, SCALE)
     np.savez(os.path.join(out_dir, f"rank{rank}.npz"), g=g.numpy(), li=li.numpy(), out=out.numpy(), lse=lse.numpy())
     dist.destroy_process_group()
 
@@ -114,8 +120,8 @@ def test_dcp_decode_on_gloo_ranks(tmp_path, world):
         want_out, want_lse = o.attend(q[b], rows[b][sel], SCALE, DL)
         for r, x in enumerate(res):
             assert np.array_equal(x["g"][b], want), f"rank {r} row {b}: selection"
-            mine = (want >= 0) & (want % world == r)
-            assert np.array_equal(x["li"][b][mine], want[mine] // world) and np.all(x["li"][b][~mine] == -1)
+            mine = want[(want >= 0) & (want % world == r)] // world
+            assert np.array_equal(x["li"][b][:len(mine)], mine) and np.all(x["li"][b][len(mine):] == -1)
             assert np.allclose(x["out"][b], want_out, atol=1e-12) and np.allclose(x["lse"][b], want_lse, atol=1e-12)
 
 
