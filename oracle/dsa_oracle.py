@@ -62,7 +62,16 @@ Definitions (R query rows, B requests, P page size):
   division.  The pages name "FP8 e4m3 keys with FP32 scales" ("GLM-5.2 on
   vLLM Ascend", section 7) without fixing the scale rule: amax/448 is the
   reading taken here.  The e4m3 format is the OCP 8-bit floating point
-  specification's E4M3 (bias 7, no infinities, S.1111.111 = NaN, max 448).
+  specification's E4M3 (bias 7, no infinities, S.1111.111 = NaN, max 448);
+* packed 8-bit latent cache (SFA C8) -- the 512 c_KV values of a token are
+  stored as e4m3 codes with one float32 scale per token, by the same rule as
+  the fp8 index keys (``scale = amax / 448``, 1 if amax = 0, ``code =
+  e4m3(x / scale)``); k_R stays bf16; attention runs over ``code * scale``
+  exactly ("GLM-5.2 on vLLM Ascend", "Quantization and Hardware Branches": SFA
+  C8 packs the main latent KV and uses the quantized sparse-attention operator,
+  while the non-RoPE / RoPE split is preserved; "vLLM Inference Path", "MLA
+  Projections and KV State": an explicit FP8 KV setting narrows the main MLA
+  cache).  The per-token amax / 448 rule and bf16 k_R are the readings taken.
 """
 from __future__ import annotations
 
@@ -123,6 +132,12 @@ def f32_to_e4m3(x) -> np.ndarray:
     return code.astype(np.uint8)
 
 
+def quantize_latent(c_kv_bits) -> tuple[np.ndarray, np.ndarray]:
+    """bf16 c_KV rows [T, 512] -> (e4m3 codes [T, 512], float32 scales [T]): the packed 8-bit latent
+    cache, one scale per token by the same amax / 448 rule as the fp8 index keys."""
+    return quantize_index_keys(c_kv_bits)
+
+
 def quantize_index_keys(bits) -> tuple[np.ndarray, np.ndarray]:
     """bf16 index keys [T, 128] -> (e4m3 codes [T, 128], float32 scales [T]).
 
@@ -144,10 +159,20 @@ class PagedCache:
     indexer-owning layer, index-key pages [N_pg, P, 128] (bf16, or e4m3 codes
     with float32 scales [N_pg, P]).  Unwritten slots hold 0."""
 
-    def __init__(self, num_pages: int, page_size: int, key_format: str | None, d_latent=512, d_rope=64, d_index=128):
+    def __init__(self, num_pages: int, page_size: int, key_format: str | None, d_latent=512, d_rope=64, d_index=128,
+                 latent_format: str = "bf16"):
         self.num_pages, self.page_size, self.key_format = num_pages, page_size, key_format
         self.d_latent, self.d_rope, self.d_index = d_latent, d_rope, d_index
+        self.latent_format = latent_format
         self.latent = np.zeros((num_pages, page_size, d_latent + d_rope), dtype=np.uint16)
+        self.latent_codes = self.latent_scales = None
+        if latent_format == "e4m3":
+            # packed 8-bit latent: c_KV as e4m3 codes + a float32 scale per token; k_R stays in
+            # the bf16 array's last 64 columns (its c_KV columns stay 0)
+            self.latent_codes = np.zeros((num_pages, page_size, d_latent), dtype=np.uint8)
+            self.latent_scales = np.zeros((num_pages, page_size), dtype=np.float32)
+        elif latent_format != "bf16":
+            raise ValueError(latent_format)
         self.index_keys = None
         self.index_scales = None
         if key_format == "bf16":
@@ -166,7 +191,12 @@ class PagedCache:
         stored as given codes + scales (pre-quantised input)."""
         slot = np.asarray(slot_mapping, dtype=np.int64)
         pg, off = slot // self.page_size, slot % self.page_size
-        self.latent[pg, off, :self.d_latent] = c_kv_bits
+        if self.latent_format == "e4m3":
+            codes, scales = quantize_latent(c_kv_bits)
+            self.latent_codes[pg, off] = codes
+            self.latent_scales[pg, off] = scales
+        else:
+            self.latent[pg, off, :self.d_latent] = c_kv_bits
         self.latent[pg, off, self.d_latent:] = k_rope_bits
         if self.key_format is None:
             return
@@ -186,9 +216,14 @@ class PagedCache:
         return pages, positions % self.page_size
 
     def latent_rows(self, block_row, positions) -> np.ndarray:
-        """[n, 576] float64 cached rows [c_KV | k_R] at logical positions of one request."""
+        """[n, 576] float64 cached rows [c_KV | k_R] at logical positions of one request (an e4m3
+        c_KV is its code times the token's scale)."""
         pg, off = self.slots(block_row, positions)
-        return bf16_to_f64(self.latent[pg, off])
+        rows = bf16_to_f64(self.latent[pg, off])
+        if self.latent_format == "e4m3":
+            rows[:, :self.d_latent] = (e4m3_to_f64(self.latent_codes[pg, off]) *
+                                       self.latent_scales[pg, off].astype(np.float64)[:, None])
+        return rows
 
     def index_key_rows(self, block_row, positions) -> np.ndarray:
         """[n, 128] float64 index keys: the bf16 value, or e4m3 value times the token's scale."""

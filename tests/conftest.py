@@ -43,7 +43,7 @@ class TinyCase:
     """Random tiny DSA problem with its own widths; builds an oracle cache."""
 
     def __init__(self, seed, seq_lens, q_lens, page_size, key_format="bf16",
-                 n_idx_heads=2, d_index=4, n_heads=2, d_latent=6, d_rope=3, spare=3):
+                 n_idx_heads=2, d_index=4, n_heads=2, d_latent=6, d_rope=3, spare=3, latent_format="bf16"):
         import workloads as wlm
         from oracle import dsa_oracle as o
         rng = np.random.default_rng(seed)
@@ -68,7 +68,8 @@ class TinyCase:
         self.q_idx = wlm.bf16_bits(rng.standard_normal((R, n_idx_heads, d_index)).astype(np.float32))
         self.w = (rng.standard_normal((R, n_idx_heads)) / np.sqrt(n_idx_heads)).astype(np.float32)
         self.q = wlm.bf16_bits(rng.standard_normal((R, n_heads, d_latent + d_rope)).astype(np.float32))
-        self.cache = o.PagedCache(self.num_pages, page_size, key_format, d_latent, d_rope, d_index)
+        self.cache = o.PagedCache(self.num_pages, page_size, key_format, d_latent, d_rope, d_index,
+                                  latent_format=latent_format)
         for b, L in enumerate(seq_lens):
             slots = self.slots(b, np.arange(L))
             self.cache.append(self.latent[b][:, :d_latent], self.latent[b][:, d_latent:], slots,

@@ -181,3 +181,43 @@ def test_dcp_share_of_k_mutant_is_caught(monkeypatch):
     scores = np.random.default_rng(5).uniform(0, 1, n)
     scores[np.arange(0, 4 * k, world)] += 10.0
     assert not np.array_equal(o.dcp_select(scores, k, world)[0], o.topk_select(scores, k))
+
+
+C8_MUTANTS = {
+    # an int8-style scale, the scale applied twice, k_R quantised along with c_KV
+    "scale_amax_over_127": lambda bits: (lambda x, s: (o.f32_to_e4m3((x / s[:, None]).astype(np.float32)), s))(
+        o.bf16_to_f64(bits).astype(np.float32),
+        np.where(np.abs(o.bf16_to_f64(bits)).max(-1) > 0, np.abs(o.bf16_to_f64(bits)).max(-1) / 127.0, 1.0).astype(np.float32)),
+    "no_scale": lambda bits: (o.f32_to_e4m3(o.bf16_to_f64(bits).astype(np.float32)),
+                              np.ones(bits.shape[0], np.float32)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(C8_MUTANTS))
+def test_c8_quantizer_mutants_are_caught(monkeypatch, name):
+    import test_oracle_c8 as pins
+    monkeypatch.setattr(o, "quantize_latent", C8_MUTANTS[name])
+    with pytest.raises(AssertionError):
+        pins.test_latent_quantizer_matches_exhaustive_nearest_code()
+    with pytest.raises(AssertionError):
+        pins.test_c8_attention_matches_brute_force()
+
+
+def test_c8_rope_quantised_mutant_is_caught(monkeypatch):
+    """k_R pushed through the c_KV quantizer as well: the stored rope columns change."""
+    import test_oracle_c8 as pins
+    real_append = o.PagedCache.append
+
+    def append(self, c_kv_bits, k_rope_bits, slot_mapping, **kw):
+        if self.latent_format == "e4m3":
+            codes, scales = o.quantize_latent(k_rope_bits)
+            k_rope_bits = wlm_bits(o.e4m3_to_f64(codes) * scales.astype(np.float64)[:, None])
+        return real_append(self, c_kv_bits, k_rope_bits, slot_mapping, **kw)
+
+    def wlm_bits(v):
+        import workloads as wlm
+        return wlm.bf16_bits(v.astype(np.float32))
+
+    monkeypatch.setattr(o.PagedCache, "append", append)
+    with pytest.raises(AssertionError):
+        pins.test_rope_columns_are_stored_untouched()
