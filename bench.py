@@ -51,7 +51,8 @@ class DeviceProblem:
         import deepseek_sparse_mla_gb300 as dsa
         self.wl, self.dev, self.selection = wl, device, selection
         B, R, layers = wl.num_requests, wl.num_rows, wl.layers
-        self.caches = [dsa.LayerCache(wl.num_pages, wl.page_size, wl.key_format if l == 0 else None, device)
+        self.caches = [dsa.LayerCache(wl.num_pages, wl.page_size, wl.key_format if l == 0 else None, device,
+                                      latent_format=wl.latent_format)
                        for l in range(layers)]
         self.block_table = torch.from_numpy(wl.block_table).to(device)
         self.seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=device)
@@ -215,14 +216,16 @@ def algorithmic_bytes(wl: wlm.Workload) -> dict:
     selected = np.minimum(k, pos + 1).sum()
     keys = sum(wl.seq_lens) * wl.key_bytes_per_token()
     indexer = keys + R * 32 * 128 * 2 + R * 32 * 4 + R * k * 4
-    attention = selected * 1152 + R * 64 * 576 * 2 + R * 64 * 512 * 2 + R * 64 * 4 + R * k * 4
+    # one cached latent row: 1152 bytes of bf16, or a packed 8-bit row of 640 bytes and its 4-byte scale
+    row = 1152 if wl.latent_format == "bf16" else 640 + 4
+    attention = selected * row + R * 64 * 576 * 2 + R * 64 * 512 * 2 + R * 64 * 4 + R * k * 4
     key_in = 256
     key_out = wl.key_bytes_per_token()
-    append_owner = R * (1152 * 2 + key_in + key_out)
-    append_shared = R * 1152 * 2
+    append_owner = R * (1152 + row + key_in + key_out)
+    append_shared = R * (1152 + row)
     return {"indexer": float(indexer), "attention": float(attention), "append_owner": float(append_owner),
             "append_shared": float(append_shared), "index_key_bytes": float(keys),
-            "gather_bytes_per_layer": float(selected * 1152),
+            "gather_bytes_per_layer": float(selected * row),
             "step": float(indexer + wl.layers * attention + append_owner + (wl.layers - 1) * append_shared)}
 
 
@@ -407,7 +410,8 @@ def oracle_request_problem(wl, b, device):
     for l in range(wl.layers):
         lat = wlm.torch_to_bits(wlm.request_latent_device(wl, b, l, device))
         keys = wlm.torch_to_bits(wlm.request_index_keys_device(wl, b, device)) if l == 0 else None
-        c = o.PagedCache(pages, P, wl.key_format if l == 0 else None)
+        c = o.PagedCache(pages, P, wl.key_format if l == 0 else None,
+                         latent_format="e4m3" if wl.latent_format == "fp8" else "bf16")
         c.append(lat[:L - q, :512], lat[:L - q, 512:], slots[:L - q],
                  k_idx_bits=None if keys is None else keys[:L - q])
         caches.append((c, lat[L - q:], None if keys is None else keys[L - q:]))
@@ -592,6 +596,8 @@ def main():
     ap.add_argument("--selection", choices=["token", "page"], default="token",
                     help="token top-k (the method's selection), or page-granular selection of topk / page_size pages")
     ap.add_argument("--cpu-sample-requests", type=int, default=64)
+    ap.add_argument("--latent", choices=["bf16", "fp8"], default="bf16",
+                    help="latent cache format: bf16, or packed 8-bit (e4m3 c_KV with a scale per token, bf16 k_R)")
     ap.add_argument("--dcp", type=int, default=0,
                     help="time one rank's device work of decode context parallelism over this many ranks")
     args = ap.parse_args()
@@ -606,6 +612,9 @@ def main():
     from deepseek_sparse_mla_gb300 import _lib
     rank, world = dist_setup(args.gpus)
     wl = rank_workload(args.workload, rank)
+    if args.latent != "bf16":
+        import dataclasses
+        wl = dataclasses.replace(wl, name=f"{wl.name}_latent_{args.latent}", latent_format=args.latent)
     prob = DeviceProblem(wl, selection=args.selection)
     page_mode = args.selection == "page"
     lib = _lib.load()

@@ -23,6 +23,7 @@ from ._lib import DsaError, KEY_BF16, KEY_FP8_E4M3  # noqa: F401
 INDEX_HEADS, INDEX_DIM, HEADS, LATENT_DIM, ROPE_DIM, ROW_DIM = 32, 128, 64, 512, 64, 576
 DEFAULT_SCALE = 1.0 / 16.0     # 1/sqrt(192 + 64)
 _FORMATS = {"bf16": KEY_BF16, "fp8": KEY_FP8_E4M3, None: KEY_BF16}
+_LATENT_FORMATS = {"bf16": _lib.LATENT_BF16, "fp8": _lib.LATENT_E4M3}
 
 __all__ = ["LayerCache", "Batch", "kv_append", "indexer_scores_topk", "indexer_page_topk", "sparse_mla_decode", "sparse_mla_prefill",
            "cache_bytes", "indexer_workspace_bytes", "mla_workspace_bytes", "DsaError", "DEFAULT_SCALE",
@@ -52,14 +53,27 @@ def _need(t, dtype, shape, name):
 class LayerCache:
     """One layer's paged caches (device tensors owned by this object).
 
-    latent [num_pages, page_size, 576] bf16; for an indexer-owning layer also
+    latent [num_pages, page_size, 576] bf16 (or, with latent_format "fp8", packed 8-bit rows
+    [num_pages, page_size, 640] uint8 = 512 e4m3 codes of c_KV + k_R as 64 bf16, with latent_scales
+    [num_pages, page_size] fp32); for an indexer-owning layer also
     index_keys [num_pages, page_size, 128] (bf16, or uint8 e4m3 codes) and, for
     e4m3, index_scales [num_pages, page_size] fp32.  key_format None makes an
     IndexShare layer that holds only latent pages."""
 
-    def __init__(self, num_pages: int, page_size: int, key_format: str | None = None, device="cuda"):
+    def __init__(self, num_pages: int, page_size: int, key_format: str | None = None, device="cuda",
+                 latent_format: str = "bf16"):
         self.num_pages, self.page_size, self.key_format = int(num_pages), int(page_size), key_format
-        self.latent = torch.zeros((num_pages, page_size, ROW_DIM), dtype=torch.bfloat16, device=device)
+        self.latent_format = latent_format
+        self.latent_scales = None
+        if latent_format == "bf16":
+            self.latent = torch.zeros((num_pages, page_size, ROW_DIM), dtype=torch.bfloat16, device=device)
+        elif latent_format == "fp8":
+            # packed 8-bit rows: [512 e4m3 codes of c_KV | k_R as 64 bf16] = 640 bytes, a scale per slot
+            self.latent = torch.zeros((num_pages, page_size, LATENT_DIM + 2 * ROPE_DIM), dtype=torch.uint8,
+                                      device=device)
+            self.latent_scales = torch.zeros((num_pages, page_size), dtype=torch.float32, device=device)
+        else:
+            raise ValueError(f"latent_format {latent_format!r}")
         self.index_keys = self.index_scales = None
         if key_format == "bf16":
             self.index_keys = torch.zeros((num_pages, page_size, INDEX_DIM), dtype=torch.bfloat16, device=device)
@@ -72,7 +86,8 @@ class LayerCache:
     def struct(self) -> _lib.DsaCache:
         return _lib.DsaCache(self.latent.data_ptr(), 0 if self.index_keys is None else self.index_keys.data_ptr(),
                              0 if self.index_scales is None else self.index_scales.data_ptr(), self.num_pages,
-                             self.page_size, _FORMATS[self.key_format])
+                             self.page_size, _FORMATS[self.key_format], _LATENT_FORMATS[self.latent_format],
+                             0 if self.latent_scales is None else self.latent_scales.data_ptr())
 
 
 class Batch:
@@ -97,8 +112,9 @@ class Batch:
                              self.num_requests, self.num_rows, self.max_seq_len, int(self.block_table.shape[1]))
 
 
-def cache_bytes(num_pages: int, page_size: int, key_format: str | None, owner: bool) -> int:
-    return int(_lib.load().dsa_cache_bytes(num_pages, page_size, _FORMATS[key_format], int(owner)))
+def cache_bytes(num_pages: int, page_size: int, key_format: str | None, owner: bool, latent_format: str = "bf16") -> int:
+    return int(_lib.load().dsa_cache_bytes(num_pages, page_size, _FORMATS[key_format], int(owner),
+                                           _LATENT_FORMATS[latent_format]))
 
 
 def indexer_workspace_bytes(num_rows: int, max_seq_len: int, topk: int) -> int:

@@ -15,6 +15,7 @@ DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE, DSA_ERR_CUD
 STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_INVALID_ARG", -2: "DSA_ERR_UNSUPPORTED", -3: "DSA_ERR_WORKSPACE",
                 -4: "DSA_ERR_CUDA"}
 KEY_BF16, KEY_FP8_E4M3 = 0, 1
+LATENT_BF16, LATENT_E4M3 = 0, 1
 
 # every entry point include/dsa.h declares
 EXPORTS = ("dsa_abi_version", "dsa_last_error", "dsa_kernel_launches", "dsa_cache_bytes", "dsa_indexer_workspace_bytes",
@@ -25,7 +26,8 @@ EXPORTS = ("dsa_abi_version", "dsa_last_error", "dsa_kernel_launches", "dsa_cach
 
 class DsaCache(ctypes.Structure):
     _fields_ = [("latent", ctypes.c_void_p), ("index_keys", ctypes.c_void_p), ("index_scales", ctypes.c_void_p),
-                ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32), ("key_format", ctypes.c_int32)]
+                ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32), ("key_format", ctypes.c_int32),
+                ("latent_format", ctypes.c_int32), ("latent_scales", ctypes.c_void_p)]
 
 
 class DsaBatch(ctypes.Structure):
@@ -59,7 +61,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_kernel_launches.restype = ctypes.c_uint64
     lib.dsa_kernel_launches.argtypes = []
     lib.dsa_cache_bytes.restype = SZ
-    lib.dsa_cache_bytes.argtypes = [I32, I32, I32, I32]
+    lib.dsa_cache_bytes.argtypes = [I32, I32, I32, I32, I32]
     lib.dsa_indexer_workspace_bytes.restype = SZ
     lib.dsa_indexer_workspace_bytes.argtypes = [I32, I32, I32]
     lib.dsa_mla_workspace_bytes.restype = SZ

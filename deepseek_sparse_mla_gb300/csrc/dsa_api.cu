@@ -74,6 +74,14 @@ static dsa_status check_cache(const dsa_cache* c, bool need_keys) {
     return fail(DSA_ERR_INVALID_ARG, "cache.page_size must be a power of two in 1..1024 (got %d)", c->page_size);
   if ((int64_t)c->num_pages * c->page_size > (int64_t)INT32_MAX)
     return fail(DSA_ERR_UNSUPPORTED, "cache holds more than 2^31 slots");
+  if (c->latent_format != DSA_LATENT_BF16 && c->latent_format != DSA_LATENT_E4M3)
+    return fail(DSA_ERR_INVALID_ARG, "cache.latent_format %d is not a dsa_latent_format", c->latent_format);
+  if (c->latent_format == DSA_LATENT_E4M3 && !c->latent_scales)
+    return fail(DSA_ERR_INVALID_ARG, "an e4m3 latent cache needs cache.latent_scales");
+  if (c->latent_format == DSA_LATENT_BF16 && c->latent_scales)
+    return fail(DSA_ERR_INVALID_ARG, "a bf16 latent cache takes no cache.latent_scales (layouts are not interchangeable)");
+  if (c->latent_scales && (reinterpret_cast<uintptr_t>(c->latent_scales) & 15u))
+    return fail(DSA_ERR_INVALID_ARG, "cache.latent_scales is not 16-byte aligned");
   if (c->index_keys) {
     if (c->key_format != DSA_KEY_BF16 && c->key_format != DSA_KEY_FP8_E4M3)
       return fail(DSA_ERR_INVALID_ARG, "cache.key_format %d is not a dsa_key_format", c->key_format);
@@ -158,10 +166,14 @@ const char* dsa_last_error(void) { return g_last_error.c_str(); }
 
 uint64_t dsa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
-size_t dsa_cache_bytes(int32_t num_pages, int32_t page_size, int32_t key_format, int32_t owner) {
+size_t dsa_cache_bytes(int32_t num_pages, int32_t page_size, int32_t key_format, int32_t owner,
+                       int32_t latent_format) {
   if (num_pages <= 0 || page_size <= 0) return 0;
   size_t slots = (size_t)num_pages * (size_t)page_size;
-  size_t bytes = slots * kRow * 2;
+  size_t bytes;
+  if (latent_format == DSA_LATENT_BF16) bytes = slots * kRow * 2;
+  else if (latent_format == DSA_LATENT_E4M3) bytes = slots * (kLatent + kRope * 2 + sizeof(float));
+  else return 0;
   if (owner) {
     if (key_format == DSA_KEY_BF16) bytes += slots * kIndexDim * 2;
     else if (key_format == DSA_KEY_FP8_E4M3) bytes += slots * (kIndexDim + sizeof(float));

@@ -4,15 +4,17 @@
 // "Making GLM-5.2 Sparse on TPUs", "Append new KV without moving the resident
 // cache": the cost must scale with the new rows, never with the resident pool,
 // and every other slot keeps its contents.  Here one warp owns one new token
-// and moves its 1152-byte latent row with 16-byte stores straight into its
-// slot; nothing else in the pool is read or written.
+// and moves its 1152-byte latent row (or its packed 8-bit 640-byte row and
+// scale) with 16-byte stores straight into its slot; nothing else in the pool
+// is read or written.
 #include "dsa_internal.cuh"
 
 namespace dsa {
 
 __global__ void __launch_bounds__(256) kv_append_kernel(
     uint4* __restrict__ latent, int64_t total_slots, uint8_t* __restrict__ index_keys, float* __restrict__ index_scales,
-    int cache_key_format, const uint4* __restrict__ c_kv, const uint4* __restrict__ k_rope,
+    int cache_key_format, int latent_format, float* __restrict__ latent_scales, const uint4* __restrict__ c_kv,
+    const uint4* __restrict__ k_rope,
     const uint8_t* __restrict__ k_idx, int k_idx_format, const float* __restrict__ k_idx_scales,
     const int64_t* __restrict__ slot_mapping, int num_tokens) {
   const int t = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
@@ -23,12 +25,44 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
   const int64_t slot = slot_mapping[t];
   if (slot < 0 || slot >= total_slots) return;
 
-  // latent row [c_KV(512) | k_R(64)] bf16 = 64 + 8 chunks of 16 bytes, copied bit-exactly
   constexpr int kChunksC = kLatent * 2 / 16, kChunksR = kRope * 2 / 16;
-  uint4* dst = latent + slot * (kChunksC + kChunksR);
   const uint4* src_c = c_kv + (int64_t)t * kChunksC;
   const uint4* src_r = k_rope + (int64_t)t * kChunksR;
-  for (int i = lane; i < kChunksC + kChunksR; i += 32) dst[i] = i < kChunksC ? src_c[i] : src_r[i - kChunksC];
+  if (latent_format == DSA_LATENT_BF16) {
+    // latent row [c_KV(512) | k_R(64)] bf16 = 64 + 8 chunks of 16 bytes, copied bit-exactly
+    uint4* dst = latent + slot * (kChunksC + kChunksR);
+    for (int i = lane; i < kChunksC + kChunksR; i += 32) dst[i] = i < kChunksC ? src_c[i] : src_r[i - kChunksC];
+  } else {
+    // packed 8-bit row [c_KV as 512 e4m3 codes | k_R as 64 bf16] = 32 + 8 chunks of 16 bytes; the
+    // codes by the index keys' rule (scale = amax / 448, or 1 if amax = 0; rne_satfinite(x / scale))
+    uint4* dst = latent + slot * (kLatent / 16 + kChunksR);
+    float x[16];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint4 v = src_c[2 * lane + q];
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[8 * q + 2 * e] = __low2float(b2[e]);
+        x[8 * q + 2 * e + 1] = __high2float(b2[e]);
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(__fdiv_rn(x[i], scale), __NV_SATFINITE, __NV_E4M3);
+      packed[i >> 2] |= (uint32_t)c << (8 * (i & 3));
+    }
+    dst[lane] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    if (lane < kChunksR) dst[kLatent / 16 + lane] = src_r[lane];
+    if (lane == 0) latent_scales[slot] = scale;
+  }
 
   if (index_keys == nullptr) return;
   if (cache_key_format == DSA_KEY_BF16) {             // 256 bytes per key, copied
@@ -72,7 +106,7 @@ cudaError_t launch_kv_append(const dsa_cache& c, const void* c_kv, const void* k
   cudaError_t e = launch_pdl(
       kv_append_kernel, dim3(blocks), dim3(threads), 0, s, static_cast<uint4*>(c.latent),
       (int64_t)c.num_pages * c.page_size, static_cast<uint8_t*>(c.index_keys), c.index_scales, c.key_format,
-      static_cast<const uint4*>(c_kv), static_cast<const uint4*>(k_rope), static_cast<const uint8_t*>(k_idx),
+      c.latent_format, c.latent_scales, static_cast<const uint4*>(c_kv), static_cast<const uint4*>(k_rope), static_cast<const uint8_t*>(k_idx),
       k_idx_format, k_idx_scales, slot_mapping, num_tokens);
   count_launches(1);
   if (e != cudaSuccess) return e;

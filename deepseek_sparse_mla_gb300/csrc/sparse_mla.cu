@@ -128,9 +128,21 @@ __device__ __forceinline__ void push_piece(uint32_t src, const float* rows, int 
   }
 }
 
+// fp16 bits of 2^e for -24 <= e <= 15 (subnormal below -14)
+__device__ __forceinline__ uint16_t half_pow2_bits(int e) {
+  return e >= -14 ? (uint16_t)((e + 15) << 10) : (uint16_t)(1u << (e + 24));
+}
+
+// kC8: the latent pool holds packed 8-bit rows [c_KV as 512 e4m3 codes | k_R as 64 bf16] (640 bytes)
+// and a scale per slot.  Each producer warp gathers its groups' rows as five 128-byte pieces into the
+// slots the first five chunks of those groups would take, waits for the tile's gathers, and expands them in place
+// into the tile's usual swizzled 576-wide layout in fp16: c_KV = code * scale, k_R converted.  The
+// query row is converted to fp16 in place once it lands, P^T is written in fp16, and both MMAs take
+// fp16 operands (kind::f16 with A and B of one type).
+template <bool kC8>
 __global__ void __launch_bounds__(mla::kThreads, 1)
     sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
-                         const MlaArgs a) {
+                         const MlaArgs a, const float* __restrict__ latent_scales) {
   using namespace mla;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -140,6 +152,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
   __shared__ uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2];
   __shared__ uint64_t p_full, p_empty, q_full, q_empty, o_full, o_empty, mma_done;
+  __shared__ uint64_t cv_full[2], q_conv;   // packed 8-bit latent only: gathers landed, query converted
   __shared__ __align__(16) uint8_t tile_mask4[2][kGroups];   // entry validity, 4 bits per gather4 group
   __shared__ float red[4][kHeads];
   __shared__ float mref[kHeads], alpha[kHeads], lfin[kHeads];
@@ -169,6 +182,10 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     mbar_init(&o_full, 1);
     mbar_init(&o_empty, 8);
     mbar_init(&mma_done, 1);
+    if (kC8) {
+      for (int b = 0; b < 2; ++b) mbar_init(&cv_full[b], kProducers);   // every producer warp's gathers
+      mbar_init(&q_conv, kProducers);                                    // every producer warp
+    }
     rescale_tag[0] = rescale_tag[1] = 0;
     fence_mbar_init();
   }
@@ -226,12 +243,82 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       const int e = (lane < 4 * ng && t < a.topk) ? a.topk_idx[(int64_t)r * a.topk + t] : -1;
       return (e >= 0 && e <= pos) ? token_slot(a.m, req, e, a.log2_page, a.num_pages) : -1;
     };
+    constexpr int kPieces = kC8 ? 5 : kChunks;        // 128-byte pieces gathered per row
+    // the scale of a looked-up entry (packed 8-bit latent; 0 where the entry is invalid)
+    auto scale_of = [&](int64_t slot) -> float { return (kC8 && slot >= 0) ? __ldg(latent_scales + slot) : 0.f; };
+    // packed 8-bit latent: expand this warp's groups of tile ip (landed in stage ip & 1) in place
+    auto convert = [&](int ip, uint32_t vmask, float scl) -> bool {
+      const int bp = ip & 1;
+      if (!mbar_wait(&cv_full[bp], (ip >> 1) & 1, err, kErrTmaTimeout, kPolls)) return false;
+      uint8_t* stage = sKV + bp * kStageBytes;
+      const int rl = lane >> 3, j = lane & 7;
+      for (int qg = 0; qg < ng; ++qg) {
+        const float sc = __shfl_sync(0xffffffffu, scl, 4 * qg + rl);
+        if (((vmask >> (4 * qg)) & 0xFu) == 0u) continue;          // not gathered (uniform in the warp)
+        const int t = 4 * (warp + kProducers * qg) + rl;          // this lane's row of the tile
+        uint8_t* row = stage + t * 128;
+        const int sw = t & 7;                                      // 128-byte swizzle of the row
+        uint4 in[5];
+#pragma unroll
+        for (int pc = 0; pc < 5; ++pc) in[pc] = *reinterpret_cast<const uint4*>(row + pc * kChunkBytes + ((j ^ sw) << 4));
+        __syncwarp();                                              // the group's pieces are read before any write
+        // sc = m 2^e with m in [1, 2): code * m stays below 896, then the exact power of two
+        const uint32_t sb = __float_as_uint(sc);
+        const int e = sc > 0.f ? (int)((sb >> 23) & 0xFFu) - 127 : 0;
+        const __half2 m2 = __float2half2_rn(sc > 0.f ? __uint_as_float((sb & 0x807FFFFFu) | 0x3F800000u) : 0.f);
+        const uint16_t pb = half_pow2_bits(e < -24 ? -24 : (e > 15 ? 15 : e));
+        const __half2 p2 = __halves2half2(__ushort_as_half(pb), __ushort_as_half(pb));
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) {
+          const uint32_t w4[4] = {in[pc].x, in[pc].y, in[pc].z, in[pc].w};
+          uint32_t h[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[k >> 1] >> (16 * (k & 1))), __NV_E4M3);
+            __half2 v = __hmul2(__hmul2(*reinterpret_cast<const __half2*>(&hr), m2), p2);
+            h[k] = *reinterpret_cast<const uint32_t*>(&v);
+          }
+          // dims 128 pc + 16 j .. + 15: chunk 2 pc + j / 4, units 2 (j % 4) and 2 (j % 4) + 1
+          uint8_t* dst = row + (2 * pc + (j >> 2)) * kChunkBytes;
+          const int u0 = 2 * (j & 3);
+          *reinterpret_cast<uint4*>(dst + ((u0 ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(dst + (((u0 + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+        {
+          const uint32_t w4[4] = {in[4].x, in[4].y, in[4].z, in[4].w};   // k_R dims 8 j .. 8 j + 7, bf16
+          uint32_t h[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __half2 v = __float22half2_rn(__bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[k])));
+            h[k] = *reinterpret_cast<const uint32_t*>(&v);
+          }
+          *reinterpret_cast<uint4*>(row + 8 * kChunkBytes + ((j ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+        __syncwarp();
+      }
+      fence_proxy_async_smem();                                    // generic writes before the MMA's reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&kv_full[bp]);
+      return true;
+    };
     int64_t nxt = u0 < u1 ? lookup(u0) : -1;
+    float nxt_sc = 0.f;
+    if constexpr (kC8) nxt_sc = scale_of(nxt);
+    uint32_t prev_valid = 0;
+    float prev_sc = 0.f;
+    bool ok = true;
     for (int u = u0; u < u1; ++u) {
       const int i = u - u0, b = i & 1, n = i >> 1;
       const int r = u / T;
       const int64_t sl = nxt;
+      const float cur_sc = nxt_sc;
+      // packed 8-bit latent: the previous tile is expanded first (the MMA needs it before it can
+      // release the query of a finished row or the stage this tile reuses)
+      if constexpr (kC8) {
+        if (i > 0 && !(ok = convert(i - 1, prev_valid, prev_sc))) break;
+      }
       if (n > 0 && !mbar_wait(&kv_empty[b], (n - 1) & 1, err, kErrMmaTimeout, kPolls)) break;
+      bool new_q = false;
       if (r != cur_row) {
         if (q_loads > 0 && !mbar_wait(&q_empty, (q_loads - 1) & 1, err, kErrMmaTimeout, kPolls)) break;
         if (warp == 0 && lane == 0) {
@@ -240,10 +327,11 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         }
         ++q_loads;
         cur_row = r;
+        new_q = true;
       }
       const uint32_t valid = __ballot_sync(0xffffffffu, sl >= 0) & ((1u << (4 * ng)) - 1u);
       // each group with a valid entry is gathered; its invalid entries repeat its first valid row
-      const int q = lane / 9 < ng ? lane / 9 : 0, c = lane % 9;
+      const int q = lane / kPieces < ng ? lane / kPieces : 0, c = lane % kPieces;
       const uint32_t gbits = (valid >> (4 * q)) & 0xFu;
       const int first = gbits ? 4 * q + __ffs(gbits) - 1 : 0;
       const int64_t sub = __shfl_sync(0xffffffffu, sl, first);
@@ -253,6 +341,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         const int64_t v = __shfl_sync(0xffffffffu, sl, 4 * q + k);
         y[k] = (int32_t)(v >= 0 ? v : sub);
       }
+      uint64_t* land = kC8 ? &cv_full[b] : &kv_full[b];
       if (lane == 0) {
         uint32_t groups = 0;
         for (int qq = 0; qq < ng; ++qq) {
@@ -260,27 +349,57 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
           tile_mask4[b][warp + kProducers * qq] = (uint8_t)gb;
           groups += gb ? 1u : 0u;
         }
-        mbar_arrive_expect_tx(&kv_full[b], groups * (uint32_t)(kChunks * 512));
+        mbar_arrive_expect_tx(land, groups * (uint32_t)(kPieces * 512));
       }
       __syncwarp();
       ++filled[b];
-      if (lane < 9 * ng && gbits) {
+      if (lane < kPieces * ng && gbits) {
         uint8_t* stage = sKV + b * kStageBytes;
         const int g = warp + kProducers * q;
-        tma_gather4_hint(stage + c * kChunkBytes + g * 512, &kv_map, c * 64, y[0], y[1], y[2], y[3], &kv_full[b],
+        tma_gather4_hint(stage + c * kChunkBytes + g * 512, &kv_map, c * 64, y[0], y[1], y[2], y[3], land,
                          l2_evict_first());
       }
-      if (u + 1 < u1) nxt = lookup(u + 1);
+      if constexpr (kC8) {
+       if (new_q) {
+        // the query row in fp16, in place (same swizzled layout, same element width)
+        if (!mbar_wait(&q_full, (q_loads - 1) & 1, err, kErrTmaTimeout, kPolls)) break;
+        for (int k = warp * 32 + lane; k < kQBytes / 16; k += kProducers * 32) {
+          uint4 v = reinterpret_cast<const uint4*>(sQ)[k];
+          uint32_t* w4 = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __half2 h = __float22half2_rn(__bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e])));
+            w4[e] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          reinterpret_cast<uint4*>(sQ)[k] = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_conv);
+       }
+        prev_valid = valid;
+        prev_sc = cur_sc;
+      }
+      if (u + 1 < u1) {
+        nxt = lookup(u + 1);
+        if constexpr (kC8) nxt_sc = scale_of(nxt);
+      }
+      if constexpr (kC8) {
+        if (u + 1 == u1) ok = convert(i, prev_valid, prev_sc);   // the last tile
+      }
     }
     // nothing may still be landing in shared memory when the CTA exits
     for (int b = 0; b < 2; ++b)
-      if (filled[b] > 0) mbar_wait(&kv_full[b], (filled[b] - 1) & 1, err, kErrTmaTimeout, kPolls);
+      if (filled[b] > 0)
+        mbar_wait(kC8 ? &cv_full[b] : &kv_full[b], (filled[b] - 1) & 1, err, kErrTmaTimeout, kPolls);
     if (q_loads > 0) mbar_wait(&q_full, (q_loads - 1) & 1, err, kErrTmaTimeout, kPolls);
+    (void)ok;
   } else {
     // ------------------------------------------------------------------ MMA issuer (warp 7)
     if (lane == 0) {
-      const uint32_t id_qk = idesc_f16(64, kHeads, true, true, false, false);
-      const uint32_t id_pv = idesc_f16(128, kHeads, true, true, true, true);
+      // bf16 operands, or fp16 ones for the packed 8-bit latent (the expanded tile, Q and P^T)
+      const uint32_t id_qk = idesc_f16(64, kHeads, !kC8, !kC8, false, false);
+      const uint32_t id_pv = idesc_f16(128, kHeads, !kC8, !kC8, true, true);
       // descriptors are built once; per MMA only the start-address field (bytes >> 4) advances
       const uint64_t d_k0 = smem_desc(smem_u32(sKV), 16, 1024, kSwizzle128B);
       const uint64_t d_q = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128B);
@@ -340,7 +459,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         if (iq < ntiles && iq < ip + 1) {
           const int i = iq, u = u0 + i, b = i & 1, n = i >> 1, r = u / T;
           const bool need_q = r != prev_row;
-          if (mbar_test(&kv_full[b], n & 1) && (!need_q || mbar_test(&q_full, q_loads & 1)) &&
+          if (mbar_test(&kv_full[b], n & 1) && (!need_q || mbar_test(kC8 ? &q_conv : &q_full, q_loads & 1)) &&
               (n == 0 || mbar_test(&s_empty[b], (n - 1) & 1))) {
             if (need_q) {
               ++q_loads;
@@ -449,10 +568,17 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         const float m0 = mref[hh + h], m1 = mref[hh + h + 1];
         const float p0 = z[h] == -INFINITY ? 0.f : ex2_approx(z[h] - m0);
         const float p1 = z[h + 1] == -INFINITY ? 0.f : ex2_approx(z[h + 1] - m1);
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+        uint32_t pb;
+        if (kC8) {
+          const __half2 v = __floats2half2_rn(p0, p1);
+          pb = *reinterpret_cast<const uint32_t*>(&v);
+        } else {
+          const __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
+          pb = *reinterpret_cast<const uint32_t*>(&v);
+        }
         l_acc[h] = fmaf(l_acc[h], resc ? alpha[hh + h] : 1.f, p0);   // the denominator keeps the fp32 probabilities
         l_acc[h + 1] = fmaf(l_acc[h + 1], resc ? alpha[hh + h + 1] : 1.f, p1);
-        pk[h >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+        pk[h >> 1] = pb;
       }
       // P^T is free once the previous tile's PV has completed (which also settles O^T)
       if (i > 0 && !mbar_wait(&p_empty, (i - 1) & 1, err, kErrMmaTimeout, kPolls)) break;
@@ -719,8 +845,8 @@ struct MapCache {
   MapKey key[16] = {};
   CUtensorMap map[16];
   int next = 0;
-  // 2-D bf16 tensor [rows, 576] with 1152-byte rows, box {64 columns, box_rows}
-  bool get(const void* ptr, uint64_t rows, uint32_t box_rows, CUtensorMap* out) {
+  // 2-D 16-bit tensor [rows, cols] with 2 cols-byte rows, box {64 columns, box_rows}
+  bool get(const void* ptr, uint64_t rows, uint32_t box_rows, CUtensorMap* out, uint64_t cols = kRow) {
     std::lock_guard<std::mutex> g(mu);
     for (int i = 0; i < 16; ++i)
       if (key[i] == MapKey{ptr, rows} && key[i].ptr) {
@@ -728,7 +854,7 @@ struct MapCache {
         return true;
       }
     CUtensorMap m;
-    if (!encode_2d(&m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kRow, rows, kRow * 2, 64, box_rows)) return false;
+    if (!encode_2d(&m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, rows, cols * 2, 64, box_rows)) return false;
     key[next] = MapKey{ptr, rows};
     map[next] = m;
     next = (next + 1) % 16;
@@ -736,7 +862,7 @@ struct MapCache {
     return true;
   }
 };
-MapCache g_kv_maps, g_q_maps;
+MapCache g_kv_maps, g_kv8_maps, g_q_maps;   // bf16 latent rows, packed 8-bit latent rows (640 bytes), queries
 }  // namespace
 
 MlaPlan plan_mla(int num_rows, int topk) {
@@ -760,13 +886,20 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
                               void* workspace, const MlaPlan& plan, cudaStream_t s, const int32_t* row_count) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          mla::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(sparse_mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  const bool c8 = c.latent_format == DSA_LATENT_E4M3;
+  const float* ls = c8 ? c.latent_scales : nullptr;
   CUtensorMap kv_map, q_map;
-  if (!g_kv_maps.get(c.latent, (uint64_t)c.num_pages * c.page_size, 1, &kv_map)) return cudaErrorInvalidValue;
+  // a packed 8-bit row is 640 bytes: 320 16-bit columns, gathered as five 64-column pieces
+  if (!(c8 ? g_kv8_maps.get(c.latent, (uint64_t)c.num_pages * c.page_size, 1, &kv_map, 320)
+           : g_kv_maps.get(c.latent, (uint64_t)c.num_pages * c.page_size, 1, &kv_map)))
+    return cudaErrorInvalidValue;
   if (!g_q_maps.get(q, (uint64_t)num_rows * kHeads, 64, &q_map)) return cudaErrorInvalidValue;
   uint32_t* err = static_cast<uint32_t*>(workspace);
   cudaError_t e = cudaSuccess;
@@ -774,6 +907,7 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
   a.m = m;
   a.topk_idx = topk_idx;
   a.row_count = row_count;
+
   a.topk = topk;
   a.tiles = plan.tiles;
   a.units = plan.units;
@@ -803,7 +937,8 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
     at[1].val.clusterDim.z = 1;
     c.attrs = at;
     c.numAttrs = plan.split > 1 ? 2 : 1;
-    e = cudaLaunchKernelEx(&c, sparse_mla_tc_kernel, kv_map, q_map, a);
+    e = c8 ? cudaLaunchKernelEx(&c, sparse_mla_tc_kernel<true>, kv_map, q_map, a, ls)
+           : cudaLaunchKernelEx(&c, sparse_mla_tc_kernel<false>, kv_map, q_map, a, ls);
   }
   count_launches(1);
   if (e != cudaSuccess) return e;

@@ -63,7 +63,7 @@ extern "C" {
 #define DSA_MAX_TOPK 8192    /* largest supported top-k budget                   */
 #define DSA_STATIC_SCRATCH_BYTES (16u << 20)  /* scratch of dsa_indexer_scores_topk_static */
 
-#define DSA_ABI_VERSION 1
+#define DSA_ABI_VERSION 2
 
 typedef enum {
   DSA_OK = 0,
@@ -78,9 +78,21 @@ typedef enum {
   DSA_KEY_FP8_E4M3 = 1  /* index keys stored as e4m3 codes [.., 128] + fp32 scale per token */
 } dsa_key_format;
 
+typedef enum {
+  DSA_LATENT_BF16 = 0,  /* latent rows [c_KV(512) | k_R(64)] bf16: 1152 bytes per token              */
+  DSA_LATENT_E4M3 = 1   /* packed 8-bit latent: [c_KV as 512 e4m3 codes | k_R as 64 bf16] = 640 bytes
+                           per token, plus an fp32 scale per token (c_KV = code * scale)            */
+} dsa_latent_format;
+
 /*
  * One layer's paged caches (caller-owned device memory).
- *   latent       [num_pages, page_size, 576] bf16: row = [c_KV(0..511) | k_R(512..575)].
+ *   latent       DSA_LATENT_BF16: [num_pages, page_size, 576] bf16, row = [c_KV(0..511) | k_R(512..575)].
+ *                DSA_LATENT_E4M3 (SFA C8, "GLM-5.2 on vLLM Ascend", "Quantization and Hardware
+ *                Branches": the main latent KV packed to 8 bits, the RoPE part kept apart):
+ *                [num_pages, page_size, 640] bytes, row = [512 e4m3 codes of c_KV | k_R as 64 bf16].
+ *   latent_scales [num_pages, page_size] fp32, DSA_LATENT_E4M3 only: c_KV = code * scale, with
+ *                scale = amax(c_KV) / 448 per token (1 if amax = 0) as written by dsa_kv_append;
+ *                NULL otherwise.
  *   index_keys   [num_pages, page_size, 128] bf16 or e4m3 codes; only on a layer that owns
  *                an indexer.  NULL on an IndexShare (shared) layer, which keeps only its
  *                latent pages and reuses the owner's index buffer.
@@ -95,8 +107,10 @@ typedef struct {
   void* index_keys;
   float* index_scales;
   int32_t num_pages;
-  int32_t page_size;  /* power of two, 1..1024 */
-  int32_t key_format; /* dsa_key_format of index_keys */
+  int32_t page_size;     /* power of two, 1..1024 */
+  int32_t key_format;    /* dsa_key_format of index_keys */
+  int32_t latent_format; /* dsa_latent_format of latent */
+  float* latent_scales;
 } dsa_cache;
 
 /*
@@ -139,7 +153,8 @@ DSA_API uint64_t dsa_kernel_launches(void);
  * them out of admission left memory unbudgeted ("Making GLM-5.2 Sparse on TPUs", "Use
  * independent oracles and test the tests").  Returns 0 for invalid arguments.
  */
-DSA_API size_t dsa_cache_bytes(int32_t num_pages, int32_t page_size, int32_t key_format, int32_t owner);
+DSA_API size_t dsa_cache_bytes(int32_t num_pages, int32_t page_size, int32_t key_format, int32_t owner,
+                               int32_t latent_format);
 
 /*
  * Scratch bytes dsa_indexer_scores_topk needs for num_rows rows of up to max_seq_len keys

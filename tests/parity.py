@@ -37,7 +37,8 @@ class HostProblem:
         self.qsl = wl.query_start_loc
         self.caches = []
         for layer in range(wl.layers):
-            c = o.PagedCache(wl.num_pages, wl.page_size, wl.key_format if layer == 0 else None)
+            c = o.PagedCache(wl.num_pages, wl.page_size, wl.key_format if layer == 0 else None,
+                             latent_format="e4m3" if wl.latent_format == "fp8" else "bf16")
             for b in range(wl.num_requests):
                 c.append(self.latent[layer][b][:, :512], self.latent[layer][b][:, 512:], wl.slots(b, np.arange(L[b])),
                          k_idx_bits=self.keys[b] if layer == 0 else None)
@@ -78,7 +79,8 @@ class GpuProblem:
         import deepseek_sparse_mla_gb300 as dsa
         self.hp, self.wl, self.dev = hp, hp.wl, device
         wl = self.wl
-        self.caches = [dsa.LayerCache(wl.num_pages, wl.page_size, wl.key_format if layer == 0 else None, device)
+        self.caches = [dsa.LayerCache(wl.num_pages, wl.page_size, wl.key_format if layer == 0 else None, device,
+                                      latent_format=wl.latent_format)
                        for layer in range(wl.layers)]
         decode = wl.is_decode
         self.batch = dsa.Batch(torch.from_numpy(wl.block_table).to(device),
@@ -142,7 +144,14 @@ def check_cache_bytes(gp: GpuProblem, hp: HostProblem):
     import torch
     for layer in range(hp.wl.layers):
         g, h = gp.caches[layer], hp.caches[layer]
-        assert np.array_equal(wlm.torch_to_bits(g.latent), h.latent), f"latent pages differ (layer {layer})"
+        if h.latent_format == "e4m3":
+            lat = g.latent.cpu().numpy()                                  # [N, P, 640] bytes
+            assert np.array_equal(lat[..., :512], h.latent_codes), f"latent codes differ (layer {layer})"
+            assert np.array_equal(lat[..., 512:].copy().view(np.uint16), h.latent[..., 512:]), f"k_R differs (layer {layer})"
+            assert np.array_equal(g.latent_scales.cpu().numpy().view(np.uint32), h.latent_scales.view(np.uint32)), \
+                f"latent scales differ (layer {layer})"
+        else:
+            assert np.array_equal(wlm.torch_to_bits(g.latent), h.latent), f"latent pages differ (layer {layer})"
         if h.index_keys is not None:
             gk = g.index_keys.cpu().numpy() if g.index_keys.dtype == torch.uint8 else wlm.torch_to_bits(g.index_keys)
             assert np.array_equal(gk, h.index_keys), "index-key pages differ"

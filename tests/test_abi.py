@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in declared():
         assert hasattr(lib, n), n
     assert set(declared()) == set(_lib.EXPORTS)
-    assert lib.dsa_abi_version() == 1
+    assert lib.dsa_abi_version() == 2
 
 
 def test_missing_library_fails_loudly(tmp_path):
@@ -60,10 +60,14 @@ def _err(lib):
 def test_cache_bytes_counts_index_keys_and_scales(lib):
     pages, P = 1000, 64
     latent = pages * P * 576 * 2
-    assert lib.dsa_cache_bytes(pages, P, 1, 1) == latent + pages * P * (128 + 4)
-    assert lib.dsa_cache_bytes(pages, P, 0, 1) == latent + pages * P * 256
-    assert lib.dsa_cache_bytes(pages, P, 1, 0) == latent
-    assert lib.dsa_cache_bytes(0, P, 1, 1) == 0 and lib.dsa_cache_bytes(pages, P, 7, 1) == 0
+    assert lib.dsa_cache_bytes(pages, P, 1, 1, 0) == latent + pages * P * (128 + 4)
+    assert lib.dsa_cache_bytes(pages, P, 0, 1, 0) == latent + pages * P * 256
+    assert lib.dsa_cache_bytes(pages, P, 1, 0, 0) == latent
+    assert lib.dsa_cache_bytes(0, P, 1, 1, 0) == 0 and lib.dsa_cache_bytes(pages, P, 7, 1, 0) == 0
+    # packed 8-bit latent: 512 codes + 128 bytes of k_R + a 4-byte scale per slot
+    assert lib.dsa_cache_bytes(pages, P, 1, 0, 1) == pages * P * (512 + 128 + 4)
+    assert lib.dsa_cache_bytes(pages, P, 1, 1, 1) == pages * P * (512 + 128 + 4 + 128 + 4)
+    assert lib.dsa_cache_bytes(pages, P, 1, 1, 5) == 0
 
 
 def test_workspace_sizes_depend_only_on_shape(lib):
@@ -193,3 +197,20 @@ def test_dcp_entry_points_reject_bad_arguments(lib):
     assert lib.dsa_dcp_merge(P(A + 8), P(A), 2, 4, P(A), None, None) == INVALID                        # unaligned outs
     assert lib.dsa_dcp_merge(P(A), None, 2, 4, P(A), None, None) == INVALID
     assert lib.dsa_dcp_merge(None, None, 2, 0, None, None, None) == 0
+
+
+def test_latent_format_is_checked(lib):
+    from deepseek_sparse_mla_gb300._lib import DsaCache
+    P = ctypes.c_void_p
+    b = _batch(B=2, rows=2, L=300)
+    ws = lib.dsa_mla_workspace_bytes(2, 128)
+
+    def call(cache):
+        return lib.dsa_sparse_mla_decode(ctypes.byref(cache), ctypes.byref(b), P(A), P(A), 128, 0.0625, P(A), None,
+                                         P(A), ws, None)
+
+    assert call(DsaCache(A, 0, 0, 16, 64, 0, 1, 0)) == INVALID          # e4m3 latent without its scales
+    assert "latent_scales" in _err(lib)
+    assert call(DsaCache(A, 0, 0, 16, 64, 0, 0, A)) == INVALID          # scales on a bf16 latent
+    assert call(DsaCache(A, 0, 0, 16, 64, 0, 3, A)) == INVALID          # not a latent format
+    assert call(DsaCache(A, 0, 0, 16, 64, 0, 1, A + 4)) == INVALID      # unaligned scales

@@ -54,6 +54,7 @@ class Workload:
     spare_frac: float = 0.01
     block_table: np.ndarray = field(default=None, repr=False)
     num_pages: int = 0
+    latent_format: str = "bf16"   # "bf16", or "fp8": packed 8-bit latent (e4m3 c_KV + scale, bf16 k_R)
 
     def __post_init__(self):
         self.seq_lens = [int(x) for x in self.seq_lens]
@@ -114,7 +115,7 @@ class Workload:
         return {"workload": self.name, "requests": self.num_requests, "rows": self.num_rows,
                 "seq_lens": f"{min(self.seq_lens)}..{max(self.seq_lens)} (sum {sum(self.seq_lens)})",
                 "page_size": self.page_size, "index_keys": self.key_format, "topk": self.topk,
-                "layers": self.layers}
+                "layers": self.layers, "latent": self.latent_format}
 
 
 def make_page_table(seq_lens, page_size, seed, spare_frac=0.01):
