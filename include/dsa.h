@@ -277,7 +277,10 @@ DSA_API dsa_status dsa_indexer_scores_topk_static(const dsa_cache* owner, const 
  *     z_s = scale * (q[r,h,0:512] . c_KV[s] + q[r,h,512:576] . k_R[s]),
  *     out[r,h,:] = sum_s softmax(z)_s c_KV[s]   (bf16),   lse[r,h] = ln sum_s exp(z_s)  (fp32).
  *   A row with no valid entry gets out = 0 and lse = -inf.
- *   layer     this layer's cache (only latent is read; index_keys may be NULL).
+ *   layer     this layer's cache (only latent, and latent_scales for a packed 8-bit latent, is read;
+ *             index_keys may be NULL).  With DSA_LATENT_E4M3, c_KV[s] = code * scale[s]: the kernel
+ *             expands each gathered row to fp16 on chip (c_KV and k_R must lie within fp16 range)
+ *             and runs the products in fp16 with fp32 accumulation.
  *   q         device bf16 [num_rows, 64, 576]: [q_latent (W^UK absorbed) | q_rope] per head.
  *   topk_idx  device int32 [num_rows, topk]: the owner layer's index buffer.  IndexShare layers
  *             pass the owner's buffer; NULL is rejected ("GLM-5.2 on vLLM Ascend", "Failure and
