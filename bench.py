@@ -106,8 +106,8 @@ class DeviceProblem:
         mla = dsa.sparse_mla_decode if wl.is_decode else dsa.sparse_mla_prefill
         if marks is not None:
             marks.mark("append")
-        for l in range(wl.layers):
-            dsa.kv_append(self.caches[l], io.new_c[l], io.new_r[l], io.slots, k_idx=io.new_k if l == 0 else None)
+        dsa.kv_append_layers(self.caches, io.new_c, io.new_r, io.slots,
+                             k_idx=[io.new_k] + [None] * (wl.layers - 1))
         if marks is not None:
             marks.mark("indexer")
         if self.selection == "page":
@@ -532,8 +532,8 @@ def dcp_main(args):
     def step(marks=None):
         m = marks.mark if marks is not None else (lambda name: None)
         m("append")
-        for l in range(wl.layers):
-            dsa.kv_append(prob.caches[l], prob.new_c[l], prob.new_r[l], prob.slots, k_idx=prob.new_k if l == 0 else None)
+        dsa.kv_append_layers(prob.caches, prob.new_c, prob.new_r, prob.slots,
+                             k_idx=[prob.new_k] + [None] * (wl.layers - 1))
         m("indexer")
         dsa.indexer_scores_topk(prob.caches[0], prob.batch, prob.q_idx, prob.w, k, topk_idx=prob.topk_idx,
                                 scores_out=scores, workspace=prob.ws_idx)
@@ -666,7 +666,7 @@ def main():
                          "indexer_scores_topk: indexer_groups_kernel + indexer_tc_kernel + topk_chunk_kernel + topk_kernel"),
              "attention": (("sparse_mla.cu",), "sparse_mla_decode: sparse_mla_tc_kernel (clusters merge in shared memory; "
                                                "mla_merge_kernel when rows are cut between CTAs) + mla_status_kernel"),
-             "append": (("kv_append.cu",), "kv_append: kv_append_kernel")}
+             "append": (("kv_append.cu",), "kv_append_layers: kv_append_kernel (every layer in one launch)")}
     dom = max(share, key=share.get)
     achieved = bytes_of[dom] / (per_call[dom] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": files[dom][1], "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -25,7 +25,7 @@ DEFAULT_SCALE = 1.0 / 16.0     # 1/sqrt(192 + 64)
 _FORMATS = {"bf16": KEY_BF16, "fp8": KEY_FP8_E4M3, None: KEY_BF16}
 _LATENT_FORMATS = {"bf16": _lib.LATENT_BF16, "fp8": _lib.LATENT_E4M3}
 
-__all__ = ["LayerCache", "Batch", "kv_append", "indexer_scores_topk", "indexer_page_topk", "sparse_mla_decode", "sparse_mla_prefill",
+__all__ = ["LayerCache", "Batch", "kv_append", "kv_append_layers", "indexer_scores_topk", "indexer_page_topk", "sparse_mla_decode", "sparse_mla_prefill",
            "cache_bytes", "indexer_workspace_bytes", "mla_workspace_bytes", "DsaError", "DEFAULT_SCALE",
            "dcp_candidates", "dcp_select", "dcp_merge"]
 
@@ -150,6 +150,26 @@ def kv_append(cache: LayerCache, c_kv, k_rope, slot_mapping, k_idx=None, k_idx_s
     c = cache.struct()
     _lib.check(_lib.load().dsa_kv_append(ctypes.byref(c), _ptr(c_kv), _ptr(k_rope), _ptr(k_idx), fmt,
                                          _ptr(k_idx_scales), _ptr(slot_mapping), T, _stream(stream)))
+
+
+def kv_append_layers(caches, c_kv, k_rope, slot_mapping, k_idx=None, stream=None):
+    """kv_append for several layers in one launch: the same T tokens and slots in every layer,
+    c_kv[l] / k_rope[l] per layer, k_idx[l] (bf16) on the layers that own index keys, else None."""
+    n = len(caches)
+    T = int(slot_mapping.shape[0])
+    _need(slot_mapping, torch.int64, (T,), "slot_mapping")
+    k_idx = [None] * n if k_idx is None else list(k_idx)
+    if not (len(c_kv) == len(k_rope) == len(k_idx) == n):
+        raise ValueError("one c_kv, k_rope and k_idx entry per layer")
+    for l in range(n):
+        _need(c_kv[l], torch.bfloat16, (T, LATENT_DIM), f"c_kv[{l}]")
+        _need(k_rope[l], torch.bfloat16, (T, ROPE_DIM), f"k_rope[{l}]")
+        if k_idx[l] is not None:
+            _need(k_idx[l], torch.bfloat16, (T, INDEX_DIM), f"k_idx[{l}]")
+    structs = (_lib.DsaCache * n)(*[c.struct() for c in caches])
+    ptrs = lambda ts: (ctypes.c_void_p * n)(*[None if t is None else t.data_ptr() for t in ts])   # noqa: E731
+    _lib.check(_lib.load().dsa_kv_append_layers(structs, n, ptrs(c_kv), ptrs(k_rope), ptrs(k_idx), KEY_BF16, None,
+                                                _ptr(slot_mapping), T, _stream(stream)))
 
 
 def indexer_scores_topk(owner: LayerCache, batch: Batch, q_idx, w, topk: int, topk_idx=None, scores_out=None,

@@ -21,7 +21,8 @@ LATENT_BF16, LATENT_E4M3 = 0, 1
 EXPORTS = ("dsa_abi_version", "dsa_last_error", "dsa_kernel_launches", "dsa_cache_bytes", "dsa_indexer_workspace_bytes",
            "dsa_mla_workspace_bytes", "dsa_kv_append", "dsa_indexer_scores_topk", "dsa_indexer_scores_topk_static",
            "dsa_indexer_page_workspace_bytes", "dsa_indexer_page_topk", "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill",
-           "dsa_dcp_candidates", "dsa_dcp_select", "dsa_dcp_merge", "dsa_sparse_mla_decode_ragged")
+           "dsa_dcp_candidates", "dsa_dcp_select", "dsa_dcp_merge", "dsa_sparse_mla_decode_ragged",
+           "dsa_kv_append_layers")
 
 
 class DsaCache(ctypes.Structure):
@@ -83,6 +84,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = I32
         fn.argtypes = [ctypes.POINTER(DsaCache), ctypes.POINTER(DsaBatch), P, P, I32, ctypes.c_float, P, P, P, SZ, P]
+    lib.dsa_kv_append_layers.restype = I32
+    lib.dsa_kv_append_layers.argtypes = [ctypes.POINTER(DsaCache), I32, P, P, P, I32, P, P, I32, P]
     lib.dsa_dcp_candidates.restype = I32
     lib.dsa_dcp_candidates.argtypes = [P, ctypes.c_int64, P, I32, I32, I32, I32, P, P, P]
     lib.dsa_dcp_select.restype = I32

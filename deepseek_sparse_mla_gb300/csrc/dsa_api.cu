@@ -192,16 +192,12 @@ size_t dsa_mla_workspace_bytes(int32_t num_rows, int32_t topk) {
   return plan_mla(num_rows > 0 ? num_rows : 1, topk).workspace_bytes;
 }
 
-dsa_status dsa_kv_append(const dsa_cache* cache, const void* c_kv, const void* k_rope, const void* k_idx,
-                         int32_t k_idx_format, const float* k_idx_scales, const int64_t* slot_mapping,
-                         int32_t num_tokens, void* stream) {
+static dsa_status check_append_layer(const dsa_cache* cache, const void* c_kv, const void* k_rope, const void* k_idx,
+                                     int32_t k_idx_format, const float* k_idx_scales) {
   dsa_status st = check_cache(cache, false);
   if (st != DSA_OK) return st;
-  if (num_tokens < 0) return fail(DSA_ERR_INVALID_ARG, "num_tokens is negative");
-  if (num_tokens == 0) return ok();
-  if (!c_kv || !k_rope || !slot_mapping) return fail(DSA_ERR_INVALID_ARG, "c_kv / k_rope / slot_mapping is NULL");
+  if (!c_kv || !k_rope) return fail(DSA_ERR_INVALID_ARG, "c_kv / k_rope is NULL");
   if (!aligned16(c_kv) || !aligned16(k_rope)) return fail(DSA_ERR_INVALID_ARG, "c_kv / k_rope is not 16-byte aligned");
-  if (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) return fail(DSA_ERR_INVALID_ARG, "slot_mapping is not 8-byte aligned");
   if (cache->index_keys) {
     if (!k_idx) return fail(DSA_ERR_INVALID_ARG, "this layer owns an indexer cache: k_idx is required");
     if (!aligned16(k_idx)) return fail(DSA_ERR_INVALID_ARG, "k_idx is not 16-byte aligned");
@@ -216,8 +212,42 @@ dsa_status dsa_kv_append(const dsa_cache* cache, const void* c_kv, const void* k
   } else if (k_idx) {
     return fail(DSA_ERR_INVALID_ARG, "k_idx given for a layer without an indexer cache (cache.index_keys is NULL)");
   }
-  cudaError_t e = launch_kv_append(*cache, c_kv, k_rope, cache->index_keys ? k_idx : nullptr, k_idx_format, k_idx_scales,
-                                   slot_mapping, num_tokens, (cudaStream_t)stream);
+  return ok();
+}
+
+dsa_status dsa_kv_append(const dsa_cache* cache, const void* c_kv, const void* k_rope, const void* k_idx,
+                         int32_t k_idx_format, const float* k_idx_scales, const int64_t* slot_mapping,
+                         int32_t num_tokens, void* stream) {
+  return dsa_kv_append_layers(cache, 1, &c_kv, &k_rope, &k_idx, k_idx_format, &k_idx_scales, slot_mapping, num_tokens,
+                              stream);
+}
+
+dsa_status dsa_kv_append_layers(const dsa_cache* caches, int32_t num_layers, const void* const* c_kv,
+                                const void* const* k_rope, const void* const* k_idx, int32_t k_idx_format,
+                                const float* const* k_idx_scales, const int64_t* slot_mapping, int32_t num_tokens,
+                                void* stream) {
+  if (!caches || !c_kv || !k_rope) return fail(DSA_ERR_INVALID_ARG, "caches / c_kv / k_rope is NULL");
+  if (num_layers < 1 || num_layers > kMaxAppendLayers)
+    return fail(DSA_ERR_UNSUPPORTED, "num_layers %d outside 1..%d", num_layers, kMaxAppendLayers);
+  if (num_tokens < 0) return fail(DSA_ERR_INVALID_ARG, "num_tokens is negative");
+  for (int l = 0; l < num_layers; ++l) {
+    dsa_status st = check_cache(&caches[l], false);
+    if (st != DSA_OK) return st;
+  }
+  if (num_tokens == 0) return ok();                  // a no-op once the caches are valid
+  AppendArgs args = {};
+  for (int l = 0; l < num_layers; ++l) {
+    const void* ki = k_idx ? k_idx[l] : nullptr;
+    const float* ks = k_idx_scales ? k_idx_scales[l] : nullptr;
+    dsa_status st = check_append_layer(&caches[l], c_kv[l], k_rope[l], ki, k_idx_format, ks);
+    if (st != DSA_OK) return num_layers > 1 ? fail(st, "layer %d: %s", l, dsa_last_error()) : st;
+    args.layer[l] = append_layer(caches[l], c_kv[l], k_rope[l], caches[l].index_keys ? ki : nullptr, k_idx_format, ks);
+  }
+  if (!slot_mapping) return fail(DSA_ERR_INVALID_ARG, "slot_mapping is NULL");
+  if (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) return fail(DSA_ERR_INVALID_ARG, "slot_mapping is not 8-byte aligned");
+  args.slot_mapping = slot_mapping;
+  args.num_tokens = num_tokens;
+  cudaError_t e = launch_kv_append(args, num_layers, (cudaStream_t)stream);
   return cuda_status(e, "kv append launch");
 }
 

@@ -89,9 +89,29 @@ dsa_status report_error(dsa_status st, const char* msg);
 // ---------------------------------------------------------------------------
 // launchers (defined next to their kernels)
 // ---------------------------------------------------------------------------
-cudaError_t launch_kv_append(const dsa_cache& c, const void* c_kv, const void* k_rope, const void* k_idx,
-                             int k_idx_format, const float* k_idx_scales, const int64_t* slot_mapping,
-                             int num_tokens, cudaStream_t s);
+// one layer's side of an append (device pointers; k_idx NULL for a layer without index keys)
+struct AppendLayer {
+  uint4* latent;
+  int64_t total_slots;
+  uint8_t* index_keys;
+  float* index_scales;
+  float* latent_scales;
+  int key_format, latent_format;
+  const uint4* c_kv;
+  const uint4* k_rope;
+  const uint8_t* k_idx;
+  int k_idx_format;
+  const float* k_idx_scales;
+};
+constexpr int kMaxAppendLayers = 16;
+struct AppendArgs {
+  AppendLayer layer[kMaxAppendLayers];
+  const int64_t* slot_mapping;
+  int num_tokens;
+};
+AppendLayer append_layer(const dsa_cache& c, const void* c_kv, const void* k_rope, const void* k_idx, int k_idx_format,
+                         const float* k_idx_scales);
+cudaError_t launch_kv_append(const AppendArgs& a, int num_layers, cudaStream_t s);
 
 struct RowMeta {
   const int32_t* block_table;

@@ -11,31 +11,29 @@
 
 namespace dsa {
 
-__global__ void __launch_bounds__(256) kv_append_kernel(
-    uint4* __restrict__ latent, int64_t total_slots, uint8_t* __restrict__ index_keys, float* __restrict__ index_scales,
-    int cache_key_format, int latent_format, float* __restrict__ latent_scales, const uint4* __restrict__ c_kv,
-    const uint4* __restrict__ k_rope,
-    const uint8_t* __restrict__ k_idx, int k_idx_format, const float* __restrict__ k_idx_scales,
-    const int64_t* __restrict__ slot_mapping, int num_tokens) {
+// blockIdx.y = layer: one launch appends the step's tokens to every layer's caches (the tokens and
+// their slots are the same in every layer of a step; each layer brings its own rows and keys)
+__global__ void __launch_bounds__(256) kv_append_kernel(const AppendArgs a) {
+  const AppendLayer& L = a.layer[blockIdx.y];
   const int t = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   pdl_wait();
   pdl_trigger();
-  if (t >= num_tokens) return;
-  const int64_t slot = slot_mapping[t];
-  if (slot < 0 || slot >= total_slots) return;
+  if (t >= a.num_tokens) return;
+  const int64_t slot = a.slot_mapping[t];
+  if (slot < 0 || slot >= L.total_slots) return;
 
   constexpr int kChunksC = kLatent * 2 / 16, kChunksR = kRope * 2 / 16;
-  const uint4* src_c = c_kv + (int64_t)t * kChunksC;
-  const uint4* src_r = k_rope + (int64_t)t * kChunksR;
-  if (latent_format == DSA_LATENT_BF16) {
+  const uint4* src_c = L.c_kv + (int64_t)t * kChunksC;
+  const uint4* src_r = L.k_rope + (int64_t)t * kChunksR;
+  if (L.latent_format == DSA_LATENT_BF16) {
     // latent row [c_KV(512) | k_R(64)] bf16 = 64 + 8 chunks of 16 bytes, copied bit-exactly
-    uint4* dst = latent + slot * (kChunksC + kChunksR);
+    uint4* dst = L.latent + slot * (kChunksC + kChunksR);
     for (int i = lane; i < kChunksC + kChunksR; i += 32) dst[i] = i < kChunksC ? src_c[i] : src_r[i - kChunksC];
   } else {
     // packed 8-bit row [c_KV as 512 e4m3 codes | k_R as 64 bf16] = 32 + 8 chunks of 16 bytes; the
     // codes by the index keys' rule (scale = amax / 448, or 1 if amax = 0; rne_satfinite(x / scale))
-    uint4* dst = latent + slot * (kLatent / 16 + kChunksR);
+    uint4* dst = L.latent + slot * (kLatent / 16 + kChunksR);
     float x[16];
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
@@ -61,28 +59,28 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     }
     dst[lane] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     if (lane < kChunksR) dst[kLatent / 16 + lane] = src_r[lane];
-    if (lane == 0) latent_scales[slot] = scale;
+    if (lane == 0) L.latent_scales[slot] = scale;
   }
 
-  if (index_keys == nullptr) return;
-  if (cache_key_format == DSA_KEY_BF16) {             // 256 bytes per key, copied
+  if (L.index_keys == nullptr) return;
+  if (L.key_format == DSA_KEY_BF16) {                 // 256 bytes per key, copied
     if (lane < 16)
-      reinterpret_cast<uint4*>(index_keys)[slot * 16 + lane] = reinterpret_cast<const uint4*>(k_idx)[(int64_t)t * 16 + lane];
+      reinterpret_cast<uint4*>(L.index_keys)[slot * 16 + lane] = reinterpret_cast<const uint4*>(L.k_idx)[(int64_t)t * 16 + lane];
     return;
   }
-  if (k_idx_format == DSA_KEY_FP8_E4M3) {             // pre-quantised: 128 code bytes + scale, copied
+  if (L.k_idx_format == DSA_KEY_FP8_E4M3) {           // pre-quantised: 128 code bytes + scale, copied
     if (lane < 8)
-      reinterpret_cast<uint4*>(index_keys)[slot * 8 + lane] = reinterpret_cast<const uint4*>(k_idx)[(int64_t)t * 8 + lane];
-    if (lane == 0) index_scales[slot] = k_idx_scales[t];
+      reinterpret_cast<uint4*>(L.index_keys)[slot * 8 + lane] = reinterpret_cast<const uint4*>(L.k_idx)[(int64_t)t * 8 + lane];
+    if (lane == 0) L.index_scales[slot] = L.k_idx_scales[t];
     return;
   }
   // quantise a bf16 key into e4m3: scale = amax / 448 (1 if amax = 0), code = rne_satfinite(x / scale)
-  const uint2 raw = reinterpret_cast<const uint2*>(k_idx)[(int64_t)t * 32 + lane];   // 4 bf16 per lane
+  const uint2 raw = reinterpret_cast<const uint2*>(L.k_idx)[(int64_t)t * 32 + lane];   // 4 bf16 per lane
   float x[4];
   {
-    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-    x[0] = __low2float(a); x[1] = __high2float(a); x[2] = __low2float(b); x[3] = __high2float(b);
+    const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+    const __nv_bfloat162 q = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+    x[0] = __low2float(p); x[1] = __high2float(p); x[2] = __low2float(q); x[3] = __high2float(q);
   }
   float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
@@ -94,20 +92,32 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(__fdiv_rn(x[i], scale), __NV_SATFINITE, __NV_E4M3);
     packed |= (uint32_t)c << (8 * i);
   }
-  reinterpret_cast<uint32_t*>(index_keys)[slot * 32 + lane] = packed;
-  if (lane == 0) index_scales[slot] = scale;
+  reinterpret_cast<uint32_t*>(L.index_keys)[slot * 32 + lane] = packed;
+  if (lane == 0) L.index_scales[slot] = scale;
 }
 
-cudaError_t launch_kv_append(const dsa_cache& c, const void* c_kv, const void* k_rope, const void* k_idx,
-                             int k_idx_format, const float* k_idx_scales, const int64_t* slot_mapping,
-                             int num_tokens, cudaStream_t s) {
+AppendLayer append_layer(const dsa_cache& c, const void* c_kv, const void* k_rope, const void* k_idx, int k_idx_format,
+                         const float* k_idx_scales) {
+  AppendLayer L;
+  L.latent = static_cast<uint4*>(c.latent);
+  L.total_slots = (int64_t)c.num_pages * c.page_size;
+  L.index_keys = static_cast<uint8_t*>(c.index_keys);
+  L.index_scales = c.index_scales;
+  L.latent_scales = c.latent_scales;
+  L.key_format = c.key_format;
+  L.latent_format = c.latent_format;
+  L.c_kv = static_cast<const uint4*>(c_kv);
+  L.k_rope = static_cast<const uint4*>(k_rope);
+  L.k_idx = static_cast<const uint8_t*>(k_idx);
+  L.k_idx_format = k_idx_format;
+  L.k_idx_scales = k_idx_scales;
+  return L;
+}
+
+cudaError_t launch_kv_append(const AppendArgs& a, int num_layers, cudaStream_t s) {
   const int threads = 256, per_block = threads / 32;
-  const int blocks = (num_tokens + per_block - 1) / per_block;
-  cudaError_t e = launch_pdl(
-      kv_append_kernel, dim3(blocks), dim3(threads), 0, s, static_cast<uint4*>(c.latent),
-      (int64_t)c.num_pages * c.page_size, static_cast<uint8_t*>(c.index_keys), c.index_scales, c.key_format,
-      c.latent_format, c.latent_scales, static_cast<const uint4*>(c_kv), static_cast<const uint4*>(k_rope), static_cast<const uint8_t*>(k_idx),
-      k_idx_format, k_idx_scales, slot_mapping, num_tokens);
+  const int blocks = (a.num_tokens + per_block - 1) / per_block;
+  cudaError_t e = launch_pdl(kv_append_kernel, dim3(blocks, num_layers), dim3(threads), 0, s, a);
   count_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

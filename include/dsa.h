@@ -190,6 +190,22 @@ DSA_API dsa_status dsa_kv_append(const dsa_cache* cache, const void* c_kv, const
                          int32_t num_tokens, void* stream);
 
 /*
+ * dsa_kv_append for num_layers layers in one launch: a decoder step appends the same tokens at the
+ * same slots in every layer, each layer with its own rows (and, on an indexer-owning layer, keys).
+ *   caches        host array [num_layers] of the layers' caches (1 <= num_layers <= 16).
+ *   c_kv, k_rope  host arrays [num_layers] of device pointers, as for dsa_kv_append.
+ *   k_idx         host array [num_layers] of device pointers, NULL where the layer has no index keys
+ *                 (or NULL altogether when none has); k_idx_scales likewise (pre-quantised keys only).
+ *   k_idx_format, slot_mapping, num_tokens  as for dsa_kv_append, shared by the layers.
+ * Every layer is validated before anything is launched; the result is that of num_layers calls of
+ * dsa_kv_append.
+ */
+DSA_API dsa_status dsa_kv_append_layers(const dsa_cache* caches, int32_t num_layers, const void* const* c_kv,
+                                        const void* const* k_rope, const void* const* k_idx, int32_t k_idx_format,
+                                        const float* const* k_idx_scales, const int64_t* slot_mapping,
+                                        int32_t num_tokens, void* stream);
+
+/*
  * Lightning indexer scores and top-k selection for every query row.
  * ("vLLM Inference Path", "DSA Indexer"; "Making GLM-5.2 Sparse on TPUs", "Separate the indexer
  * from the attention it controls".)

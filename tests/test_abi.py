@@ -214,3 +214,21 @@ def test_latent_format_is_checked(lib):
     assert call(DsaCache(A, 0, 0, 16, 64, 0, 0, A)) == INVALID          # scales on a bf16 latent
     assert call(DsaCache(A, 0, 0, 16, 64, 0, 3, A)) == INVALID          # not a latent format
     assert call(DsaCache(A, 0, 0, 16, 64, 0, 1, A + 4)) == INVALID      # unaligned scales
+
+
+def test_multi_layer_append_rejects_bad_arguments(lib):
+    from deepseek_sparse_mla_gb300._lib import DsaCache
+    P = ctypes.c_void_p
+    two = (DsaCache * 2)(DsaCache(A, A, A, 16, 64, 1, 0, 0), DsaCache(A, 0, 0, 16, 64, 0, 0, 0))
+    arr = lambda *v: (ctypes.c_void_p * len(v))(*v)       # noqa: E731
+    ok_args = (arr(A, A), arr(A, A), arr(A, None), 0, None, P(A), 0, None)
+    assert lib.dsa_kv_append_layers(two, 2, *ok_args) == 0                       # no tokens: a no-op
+    assert lib.dsa_kv_append_layers(two, 0, *ok_args) == UNSUPPORTED
+    assert lib.dsa_kv_append_layers(two, 17, *ok_args) == UNSUPPORTED
+    assert lib.dsa_kv_append_layers(None, 2, *ok_args) == INVALID
+    # the owner layer without its keys, and keys for the shared layer: rejected before any launch
+    assert lib.dsa_kv_append_layers(two, 2, arr(A, A), arr(A, A), arr(None, None), 0, None, P(A), 8, None) == INVALID
+    assert "layer 0" in _err(lib)
+    assert lib.dsa_kv_append_layers(two, 2, arr(A, A), arr(A, A), arr(A, A), 0, None, P(A), 8, None) == INVALID
+    assert "layer 1" in _err(lib)
+    assert lib.dsa_kv_append_layers(two, 2, arr(A, A), arr(A, A + 8), arr(A, None), 0, None, P(A), 8, None) == INVALID
