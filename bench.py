@@ -163,6 +163,25 @@ class DeviceProblem:
                              max_seq_len=self.wl.max_seq_len)
 
 
+def capture_step(prob, lib, io=None):
+    """The step captured once into a CUDA graph (the library's calls allocate nothing and never
+    synchronise, so they capture as they are, programmatic launch edges included).  Returns the
+    graph and the number of the library's kernels one replay runs."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        prob.step(io=io)                                 # a first run outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    n0 = lib.dsa_kernel_launches()
+    with torch.cuda.graph(g):
+        prob.step(io=io)
+    torch.cuda.synchronize()
+    return g, int(lib.dsa_kernel_launches() - n0)
+
+
 def torch_empty_like(t):
     import torch
     return torch.empty_like(t)
@@ -596,6 +615,8 @@ def main():
     ap.add_argument("--selection", choices=["token", "page"], default="token",
                     help="token top-k (the method's selection), or page-granular selection of topk / page_size pages")
     ap.add_argument("--cpu-sample-requests", type=int, default=64)
+    ap.add_argument("--eager", action="store_true",
+                    help="launch the step call by call instead of replaying it from a CUDA graph")
     ap.add_argument("--latent", choices=["bf16", "fp8"], default="bf16",
                     help="latent cache format: bf16, or packed 8-bit (e4m3 c_KV with a scale per token, bf16 k_R)")
     ap.add_argument("--dcp", type=int, default=0,
@@ -620,10 +641,20 @@ def main():
     lib = _lib.load()
 
     # ---- device-resident timing --------------------------------------------------------
+    # The step is replayed from a CUDA graph (one host call per step instead of one per library call;
+    # small batches are otherwise bound by the host's launch rate), or launched call by call (--eager).
+    graph, per_step = None, 0
+    if not args.eager:
+        try:
+            graph, per_step = capture_step(prob, lib)
+        except Exception as e:                           # capture unavailable: launch call by call
+            print(f"graph capture failed ({e}); timing eager launches", file=sys.stderr)
+            graph = None
+    run_step = graph.replay if graph is not None else prob.step
     clocks = ClockSampler()
     clocks.start()
     for _ in range(args.warmup):
-        prob.step()
+        run_step()
     torch.cuda.synchronize()
     time.sleep(0.5)                      # nvidia-smi is up and sampling before the timed region
     barrier(world)
@@ -633,12 +664,13 @@ def main():
     clocks.mark_begin()
     t0.record()
     for _ in range(args.steps):
-        prob.step()
+        run_step()
     t1.record()
     torch.cuda.synchronize()
     clocks.mark_end()
     clk = clocks.stop()
-    launches = int(lib.dsa_kernel_launches() - launches0)
+    # a replay launches the captured kernels without a host call into the library
+    launches = per_step * args.steps if graph is not None else int(lib.dsa_kernel_launches() - launches0)
     barrier(world)
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world)
     ms_per_step = elapsed_ms / args.steps
@@ -700,6 +732,13 @@ def main():
     ready = [torch.cuda.Event(), torch.cuda.Event()]
     done = [torch.cuda.Event(), torch.cuda.Event()]
 
+    e2e_graphs = None
+    if graph is not None:
+        try:
+            e2e_graphs = [capture_step(prob, lib, io)[0] for io in ios]
+        except Exception as e:
+            print(f"graph capture failed ({e}); end-to-end steps launch eagerly", file=sys.stderr)
+
     def e2e_run(n):
         copy.wait_stream(comp)
         with torch.cuda.stream(copy):
@@ -708,7 +747,10 @@ def main():
         for i in range(n):
             s = i & 1
             comp.wait_event(ready[s])
-            prob.step(io=ios[s])
+            if e2e_graphs is not None:
+                e2e_graphs[s].replay()
+            else:
+                prob.step(io=ios[s])
             done[s].record(comp)
             with torch.cuda.stream(copy):
                 if i + 1 < n:
@@ -745,6 +787,8 @@ def main():
                            "selection": ("page budget: %d pages of %d positions" % (prob.page_budget, wl.page_size)
                                          if page_mode else "token top-k"),
                            "l2": "no flush: each step reads %.0f MB (> 129 MB L2)" % (alg["step"] / 1e6),
+                           "launch": ("the step captured once in a CUDA graph and replayed (%d kernels a step)" % per_step
+                                      if graph is not None else "eager: one host call per library call"),
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "clocks": clk, "kernels": kernels,
