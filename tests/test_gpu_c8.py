@@ -109,3 +109,27 @@ def test_c8_exactly_representable_rows_match_the_bf16_cache():
         if fmt == "fp8":
             assert np.all(c.latent_scales.cpu().numpy() == np.float32(1 / 512))
         check_attention(bf16_tensor_to_f64(out), lse.cpu().numpy(), o_out, o_lse)
+
+
+def test_c8_attention_with_row_counts():
+    """The packed latent with a compacted buffer and row counts (a DCP rank's share): the same
+    result as the oracle over the leading entries."""
+    import torch
+    import deepseek_sparse_mla_gb300 as dsa
+    wl = wlm.Workload("c8_ragged", [4000, 2500, 900, 3100], [1] * 4, 64, "bf16", 1024, 1, 5500, latent_format="fp8")
+    hp = HostProblem(wl)
+    gp = GpuProblem(hp)
+    gp.append_step()
+    o_idx, _ = hp.oracle_topk()
+    counts = [0, 65, 1024, 300]
+    buf = np.full_like(o_idx, -1)
+    for r, c in enumerate(counts):
+        sel = o_idx[r][o_idx[r] >= 0]
+        counts[r] = min(c, len(sel))
+        buf[r, :counts[r]] = sel[:counts[r]]
+    lse = torch.empty((wl.num_rows, 64), dtype=torch.float32, device="cuda")
+    out, _ = dsa.sparse_mla_decode(gp.caches[0], gp.batch, gp.q[0], torch.from_numpy(buf).cuda(), wl.scale, lse=lse,
+                                   row_counts=torch.tensor(counts, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    o_out, o_lse = hp.oracle_attention(0, buf)
+    check_attention(bf16_tensor_to_f64(out), lse.cpu().numpy(), o_out, o_lse)

@@ -41,13 +41,24 @@ def key_values(bits: np.ndarray, key_format: str) -> np.ndarray:
     return o.bf16_to_f64(bits)
 
 
-@pytest.mark.parametrize("name", ["decode_b32_8k", "decode_b64_fp8_indexshare", "prefill_chunk_4096",
-                                  "verify_b8x4_240k"])
-def test_full_size_sampled_rows(name):
+def latent_values(bits: np.ndarray, latent_format: str) -> np.ndarray:
+    """Cached rows as attention sees them: bf16, or the packed 8-bit c_KV (code * scale) with bf16 k_R."""
+    rows = o.bf16_to_f64(bits)
+    if latent_format == "fp8":
+        codes, scales = o.quantize_latent(bits[:, :512])
+        rows[:, :512] = o.e4m3_to_f64(codes) * scales.astype(np.float64)[:, None]
+    return rows
+
+
+@pytest.mark.parametrize("name,latent", [("decode_b32_8k", "bf16"), ("decode_b64_fp8_indexshare", "bf16"),
+                                         ("prefill_chunk_4096", "bf16"), ("verify_b8x4_240k", "bf16"),
+                                         ("decode_b64_fp8_indexshare", "fp8")])
+def test_full_size_sampled_rows(name, latent):
+    import dataclasses
     import torch
     import bench
     import deepseek_sparse_mla_gb300 as dsa
-    wl = wlm.FULL[name]()
+    wl = dataclasses.replace(wlm.FULL[name](), latent_format=latent)
     prob = bench.DeviceProblem(wl)
     # the step's append of the new tokens, as the benchmark step does it
     for layer in range(wl.layers):
@@ -119,5 +130,5 @@ def test_full_size_sampled_rows(name):
         for n, r in enumerate(rows):
             b, p = int(req[r]), int(pos[r])
             sel = o.valid_selection(oracle_idx[r], p)
-            o_out, o_lse = o.attend(o.bf16_to_f64(q[r]), o.bf16_to_f64(host_lat[(b, layer)][sel]), wl.scale)
+            o_out, o_lse = o.attend(o.bf16_to_f64(q[r]), latent_values(host_lat[(b, layer)][sel], latent), wl.scale)
             check_attention(o.bf16_to_f64(out_bits[n]), lse[n], o_out, o_lse)
