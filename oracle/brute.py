@@ -114,3 +114,18 @@ def page_select(scores: list, page_size: int, budget: int) -> tuple[list, list]:
     kept = sorted(pg for _, pg in ranked[:budget])
     positions = [s for pg in kept for s in range(pg * page_size, min(n, (pg + 1) * page_size))]
     return kept, positions
+
+
+def membership(page_lists: list, union: list) -> list:
+    """Row-by-slot membership by loops: [[union[j] in row's pages for j] for row]."""
+    out = []
+    for pages in page_lists:
+        row = []
+        for u in union:
+            hit = False
+            for p in pages:
+                if p >= 0 and p == u:
+                    hit = True
+            row.append(hit)
+        out.append(row)
+    return out

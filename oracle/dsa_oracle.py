@@ -63,6 +63,14 @@ Definitions (R query rows, B requests, P page size):
   vLLM Ascend", section 7) without fixing the scale rule: amax/448 is the
   reading taken here.  The e4m3 format is the OCP 8-bit floating point
   specification's E4M3 (bias 7, no infinities, S.1111.111 = NaN, max 448);
+* query-blocked union reuse -- a block of QB query rows loads the sorted,
+  compacted union of the pages they selected once; each row keeps its own
+  support through a membership mask indexed by union slot, before the online
+  softmax, and causality and valid lengths still apply; the union is never
+  truncated (its capacity is min(QB x Kp, units)), so the operation equals each
+  row's attention over its own pages ("Making GLM-5.2 Sparse on TPUs", "Reuse
+  pages across queries"); the page-load reduction is QB x Kp / U and the score
+  work grows by U / Kp;
 * packed 8-bit latent cache (SFA C8) -- the 512 c_KV values of a token are
   stored as e4m3 codes with one float32 scale per token, by the same rule as
   the fp8 index keys (``scale = amax / 448``, 1 if amax = 0, ``code =
@@ -461,6 +469,51 @@ def lse_merge(parts) -> tuple[np.ndarray, np.ndarray]:
         out = np.where(tot[:, None] > 0, out / tot[:, None], 0.0)
         merged = np.where(tot > 0, safe + np.log(tot), -np.inf)
     return out, merged
+
+
+# ---------------------------------------------------------------------------
+# query-blocked union reuse
+# ---------------------------------------------------------------------------
+def page_union(page_lists) -> np.ndarray:
+    """The sorted, compacted union of a query block's selected pages (page ids, -1 padding ignored)."""
+    pages = np.concatenate([np.asarray(p, dtype=np.int64).ravel() for p in page_lists])
+    return np.unique(pages[pages >= 0])
+
+
+def union_membership(page_lists, union) -> np.ndarray:
+    """[QB, U] bool: row q selected the page in union slot j (indexed by slot, not by page id)."""
+    union = np.asarray(union, dtype=np.int64)
+    return np.stack([np.isin(union, np.asarray(p, dtype=np.int64)) for p in page_lists])
+
+
+def union_capacity(qb: int, kp: int, units: int) -> int:
+    """Lossless capacity of the union buffer: min(QB x Kp, number of units)."""
+    return min(qb * kp, units)
+
+
+def page_load_reduction(qb: int, kp: int, u: int) -> float:
+    return qb * kp / u
+
+
+def score_work_expansion(u: int, kp: int) -> float:
+    return u / kp
+
+
+def blocked_attend(q_rows, union_rows, union_pos, member_tokens, row_pos, scale: float, d_latent: int = 512):
+    """Attention of a block of query rows over the tokens of their page union, loaded once.
+
+    q_rows [QB, H, D]; union_rows [n, D] the cached rows of every token of the union's pages, at
+    logical positions union_pos [n]; member_tokens [QB, n] each row's membership (its own pages);
+    row_pos [QB] each row's position.  A token takes part in row q's softmax only if it is a member
+    and visible (position <= row_pos[q]).  Returns (out [QB, H, d_latent], lse [QB, H])."""
+    outs, lses = [], []
+    union_pos = np.asarray(union_pos)
+    for q in range(len(q_rows)):
+        keep = np.asarray(member_tokens[q], dtype=bool) & (union_pos <= row_pos[q])
+        o, l = attend(q_rows[q], np.asarray(union_rows)[keep], scale, d_latent)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)
 
 
 # ---------------------------------------------------------------------------
