@@ -7,6 +7,10 @@
  *      IndexShare layers reuse without rescoring;
  *   2. absorbed sparse MLA attention runs over the selected positions only.
  * The step's own new tokens are first scattered into the caches (append).
+ * Beside the step itself: page-granular selection (dsa_indexer_page_topk), a
+ * packed 8-bit latent cache (dsa_cache.latent_format), the device steps of
+ * decode context parallelism (dsa_dcp_*, dsa_sparse_mla_decode_ragged), and
+ * the append of every layer of a step in one launch (dsa_kv_append_layers).
  *
  * Sources: "GLM-5.2 on vLLM Ascend: Request-to-Backend Inference Path",
  * section 8 "The SFA backend, step by step" (write paged cache, select tokens,
