@@ -71,20 +71,21 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, 
   return r;
 }
 
-// One radix pass of the select: histogram of the digit (key >> shift) & (2^bits - 1) over the keys
-// that match prefix under mask, then the digit (from the top) holding the krem-th largest key.
-// Updates prefix / mask / krem and returns the number of keys in the chosen digit.
+// One radix pass of the select over 32-bit values: histogram of the digit (v >> shift) & (2^bits - 1)
+// over the values v[i] whose bit i of `live` is set and that match prefix under mask, then the digit
+// (from the top) holding the krem-th largest.  Updates prefix / mask / krem and returns the number of
+// values in the chosen digit.
 template <int KPT>
-__device__ __forceinline__ uint32_t radix_pass(const uint64_t (&key)[KPT], int shift, int bits, uint64_t& prefix,
-                                               uint64_t& mask, uint32_t& krem, uint32_t* hist, uint32_t* wsum,
-                                               uint32_t* sh) {
+__device__ __forceinline__ uint32_t radix_pass32(const uint32_t (&v)[KPT], uint32_t live, int shift, int bits,
+                                                 uint32_t& prefix, uint32_t& mask, uint32_t& krem, uint32_t* hist,
+                                                 uint32_t* wsum, uint32_t* sh) {
   const int tid = threadIdx.x;
   const int nb = 1 << bits;
   for (int i = tid; i < nb; i += kSelThreads) hist[i] = 0;
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < KPT; ++i)
-    if (key[i] != 0 && (key[i] & mask) == prefix) atomicAdd(&hist[(key[i] >> shift) & (uint64_t)(nb - 1)], 1u);
+    if (((live >> i) & 1u) && (v[i] & mask) == prefix) atomicAdd(&hist[(v[i] >> shift) & (uint32_t)(nb - 1)], 1u);
   __syncthreads();
   // thread t holds digits nb-1-2t and nb-2-2t (descending)
   const int b0 = nb - 1 - 2 * tid, b1 = b0 - 1;
@@ -101,8 +102,8 @@ __device__ __forceinline__ uint32_t radix_pass(const uint64_t (&key)[KPT], int s
     sh[2] = c1;
   }
   __syncthreads();
-  prefix |= (uint64_t)sh[0] << shift;
-  mask |= (uint64_t)(nb - 1) << shift;
+  prefix |= sh[0] << shift;
+  mask |= (uint32_t)(nb - 1) << shift;
   krem = sh[1];
   const uint32_t cnt = sh[2];
   __syncthreads();
@@ -110,13 +111,13 @@ __device__ __forceinline__ uint32_t radix_pass(const uint64_t (&key)[KPT], int s
 }
 
 // Top-k of one row's candidates [world][rows][k] (score, global position; position -1 = empty).
-// Candidate keys (order_key(score) << 32 | ~position) are unique and rank larger score first, then
-// the smaller position.  Three radix passes (11/11/10 bits) over the score half find the k-th
-// largest score; only when that score is shared by more keys than still needed do three more
-// passes over the position half pick the smaller positions.  The selection is put in ascending
-// order through a bitmap over the positions when they are below 262,144 (each thread emits its
-// words' set bits at its prefix), else compacted and bitonic-sorted; it is written with this rank's
-// share (local positions, compacted) and the share's size.
+// A candidate is the pair (order_key(score), ~position), unique, ranking larger score first, then the
+// smaller position.  Three radix passes (11/11/10 bits) over the score half find the k-th largest
+// score; only when that score is shared by more candidates than still needed do three more passes
+// over the position half pick the smaller positions.  The selection is put in ascending order
+// through a bitmap over the positions when they are below 262,144 (each thread emits its words' set
+// bits at its prefix), else compacted and bitonic-sorted; it is written with this rank's share (local
+// positions, compacted) and the share's size.
 __global__ void __launch_bounds__(kSelThreads) dcp_select_kernel(const float* __restrict__ cand_score,
                                                                  const int32_t* __restrict__ cand_pos, int world,
                                                                  int rows, int k, int rank,
@@ -124,59 +125,71 @@ __global__ void __launch_bounds__(kSelThreads) dcp_select_kernel(const float* __
                                                                  int32_t* __restrict__ local_idx,
                                                                  int32_t* __restrict__ local_count) {
   __shared__ uint32_t hist[2048];
-  __shared__ int32_t spos[kMaxCand / 2];               // the selection (k <= DSA_MAX_TOPK = 8192)
+  __shared__ int32_t spos[kMaxCand / 2];               // bitmap or sort buffer (k <= DSA_MAX_TOPK = 8192)
   __shared__ uint32_t wsum[33];
   __shared__ uint32_t sh[4];
   pdl_wait();
   pdl_trigger();
   const int r = blockIdx.x, tid = threadIdx.x;
-  const int n = world * k;
-  uint64_t key[kPerThread];
-  uint32_t nvalid = 0;
+  uint32_t hi[kPerThread], lo[kPerThread];             // order key of the score (0: empty), ~position
+  uint32_t nvalid = 0, live = 0;
   {
-    // every load is issued before any is used (a score load behind a test of its position would
-    // wait for that position first)
+    // thread t takes candidates t + i kSelThreads, walked as (rank w, entry j) without divisions;
+    // every load is issued before any is used
     int32_t pos[kPerThread];
     float sc[kPerThread];
+    int w = tid / k, j = tid - w * k;
 #pragma unroll
     for (int i = 0; i < kPerThread; ++i) {
-      const int c = tid + i * kSelThreads;
       pos[i] = -1;
       sc[i] = 0.f;
-      if (c < n) {
-        const int w = c / k, j = c - w * k;
+      if (w < world) {
         const int64_t at = ((int64_t)w * rows + r) * k + j;
         pos[i] = __ldg(cand_pos + at);
         sc[i] = __ldg(cand_score + at);
       }
+      j += kSelThreads;
+      while (j >= k && w < world) {
+        j -= k;
+        ++w;
+      }
     }
 #pragma unroll
     for (int i = 0; i < kPerThread; ++i) {
-      key[i] = pos[i] >= 0 ? ((uint64_t)dcp_order_key(sc[i]) << 32) | (uint32_t)~(uint32_t)pos[i] : 0ull;
-      nvalid += pos[i] >= 0 ? 1u : 0u;
+      const bool v = pos[i] >= 0;
+      hi[i] = v ? dcp_order_key(sc[i]) : 0u;
+      lo[i] = v ? ~(uint32_t)pos[i] : 0u;
+      nvalid += v ? 1u : 0u;
+      live |= (v ? 1u : 0u) << i;
     }
   }
   uint32_t V;
   block_excl_scan(nvalid, wsum, &V);
-  uint64_t T = 1;                                      // select every valid candidate
+  uint32_t t_hi = 1, t_lo = 0;                         // select every valid candidate
   if (V > (uint32_t)k) {
-    uint64_t prefix = 0, mask = 0;
-    uint32_t krem = (uint32_t)k;
-    radix_pass(key, 53, 11, prefix, mask, krem, hist, wsum, sh);
-    radix_pass(key, 42, 11, prefix, mask, krem, hist, wsum, sh);
-    const uint32_t tied = radix_pass(key, 32, 10, prefix, mask, krem, hist, wsum, sh);
+    uint32_t prefix = 0, mask = 0, krem = (uint32_t)k;
+    radix_pass32(hi, live, 21, 11, prefix, mask, krem, hist, wsum, sh);
+    radix_pass32(hi, live, 10, 11, prefix, mask, krem, hist, wsum, sh);
+    const uint32_t tied = radix_pass32(hi, live, 0, 10, prefix, mask, krem, hist, wsum, sh);
+    t_hi = prefix;
     if (tied > krem) {                                 // uniform across the block
-      radix_pass(key, 21, 11, prefix, mask, krem, hist, wsum, sh);
-      radix_pass(key, 10, 11, prefix, mask, krem, hist, wsum, sh);
-      radix_pass(key, 0, 10, prefix, mask, krem, hist, wsum, sh);
+      uint32_t live_lo = 0;
+#pragma unroll
+      for (int i = 0; i < kPerThread; ++i) live_lo |= (hi[i] == t_hi ? 1u : 0u) << i;
+      uint32_t p2 = 0, m2 = 0;
+      radix_pass32(lo, live_lo, 21, 11, p2, m2, krem, hist, wsum, sh);
+      radix_pass32(lo, live_lo, 10, 11, p2, m2, krem, hist, wsum, sh);
+      radix_pass32(lo, live_lo, 0, 10, p2, m2, krem, hist, wsum, sh);
+      t_lo = p2;
     }
-    T = prefix;                                        // exactly k keys are >= T
   }
+  // exactly k candidates (or every valid one) satisfy this
+  auto selected = [&](int i) { return hi[i] != 0u && (hi[i] > t_hi || (hi[i] == t_hi && lo[i] >= t_lo)); };
   // the largest selected position decides how the selection is put in order
   uint32_t pmax = 0;
 #pragma unroll
   for (int i = 0; i < kPerThread; ++i)
-    if (key[i] != 0 && key[i] >= T) pmax = max(pmax, ~(uint32_t)key[i]);
+    if (selected(i)) pmax = max(pmax, ~lo[i]);
   if (tid == 0) sh[3] = 0;
   __syncthreads();
   pmax = __reduce_max_sync(0xffffffffu, pmax);
@@ -195,22 +208,29 @@ __global__ void __launch_bounds__(kSelThreads) dcp_select_kernel(const float* __
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kPerThread; ++i)
-      if (key[i] != 0 && key[i] >= T) {
-        const uint32_t p = ~(uint32_t)key[i];
+      if (selected(i)) {
+        const uint32_t p = ~lo[i];
         atomicOr(&bm[p >> 5], 1u << (p & 31));
       }
     __syncthreads();
     constexpr int WPT = kBitmapWords / kSelThreads;
-    uint32_t w[WPT], c_all = 0, c_mine = 0;
+    // this rank's positions in word wi are the bits b with (32 wi + b) mod world == rank: every
+    // world-th bit from s = (rank - 32 wi) mod world
+    uint32_t base = 0;
+    for (int bit = 0; bit < 32; bit += world) base |= 1u << bit;
+    const uint32_t step = 32u % (uint32_t)world;
+    uint32_t off = (32u * (uint32_t)(tid * WPT)) % (uint32_t)world;
+    uint32_t w[WPT], mine_bits[WPT], c_all = 0, c_mine = 0;
 #pragma unroll
     for (int e = 0; e < WPT; ++e) {
       const int wi = tid * WPT + e;
       w[e] = wi < words ? bm[wi] : 0u;
+      const uint32_t sft = (uint32_t)rank >= off ? (uint32_t)rank - off : (uint32_t)rank + (uint32_t)world - off;
+      mine_bits[e] = base << sft;
+      off += step;
+      if (off >= (uint32_t)world) off -= (uint32_t)world;
       c_all += __popc(w[e]);
-      for (uint32_t x = w[e]; x; x &= x - 1) {
-        const uint32_t p = (uint32_t)wi * 32u + (uint32_t)(__ffs(x) - 1);
-        c_mine += p % (uint32_t)world == (uint32_t)rank ? 1u : 0u;
-      }
+      c_mine += __popc(w[e] & mine_bits[e]);
     }
     uint32_t total;
     uint32_t at_all = block_excl_scan(c_all, wsum, &total);
@@ -220,21 +240,21 @@ __global__ void __launch_bounds__(kSelThreads) dcp_select_kernel(const float* __
     for (int e = 0; e < WPT; ++e) {
       const int wi = tid * WPT + e;
       for (uint32_t x = w[e]; x; x &= x - 1) {
-        const uint32_t p = (uint32_t)wi * 32u + (uint32_t)(__ffs(x) - 1);
+        const uint32_t b = (uint32_t)(__ffs(x) - 1), p = (uint32_t)wi * 32u + b;
         if (at_all < (uint32_t)k) global_idx[(int64_t)r * k + at_all] = (int32_t)p;
         ++at_all;
-        if (p % (uint32_t)world == (uint32_t)rank) local_idx[(int64_t)r * k + at_mine++] = (int32_t)(p / (uint32_t)world);
+        if ((mine_bits[e] >> b) & 1u) local_idx[(int64_t)r * k + at_mine++] = (int32_t)(p / (uint32_t)world);
       }
     }
   } else {
     // compact the selected positions, then sort them ascending
     if (tid == 0) sh[3] = 0;
     __syncthreads();
-  #pragma unroll
+#pragma unroll
     for (int i = 0; i < kPerThread; ++i)
-      if (key[i] != 0 && key[i] >= T) {
+      if (selected(i)) {
         const uint32_t slot = atomicAdd(&sh[3], 1u);
-        if (slot < (uint32_t)k) spos[slot] = (int32_t)~(uint32_t)key[i];  // more only if a position repeats
+        if (slot < (uint32_t)k) spos[slot] = (int32_t)~lo[i];   // more only if a position repeats
       }
     __syncthreads();
     cnt = min((int)sh[3], k);
@@ -261,13 +281,13 @@ __global__ void __launch_bounds__(kSelThreads) dcp_select_kernel(const float* __
     // this rank's share, in order: thread t takes the contiguous entries [t E, t E + E)
     constexpr int E = (kMaxCand / 2) / kSelThreads;
     uint32_t mine = 0;
-  #pragma unroll
+#pragma unroll
     for (int e = 0; e < E; ++e) {
       const int i = tid * E + e;
       mine += (i < cnt && spos[i] % world == rank) ? 1u : 0u;
     }
     uint32_t at = block_excl_scan(mine, wsum, &nlocal);
-  #pragma unroll
+#pragma unroll
     for (int e = 0; e < E; ++e) {
       const int i = tid * E + e;
       if (i < cnt && spos[i] % world == rank) local_idx[(int64_t)r * k + at++] = spos[i] / world;
