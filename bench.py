@@ -518,11 +518,12 @@ def dcp_main(args):
     Rank 0 holds every request's interleaved share (ceil(L / world) tokens) in its own caches and
     runs: append, the indexer and top-k over its keys, dcp_candidates, dcp_select, and per layer the
     sparse MLA over its share plus dcp_merge.  The two all-gathers cross GPUs in a deployment; here
-    each is stood in by a device copy of the same bytes (every rank's slot holds this rank's tensor,
-    candidate positions relabelled to that rank's interleave and scores scaled by 1 + r 2^-20 so that
-    they do not tie), so the line measures the rank's kernels; the copies are timed as their own
-    phase and the line also gives the step without them.  Every request's new token is appended on this rank (the worst
-    case)."""
+    their results are prepared once before the timed region, as if the exchange had delivered them:
+    every rank's slot holds this rank's tensor, candidate positions relabelled to that rank's
+    interleave and scores scaled by 1 + r 2^-20 so that they do not tie (a copy would tie every score
+    world ways) while each rank still holds about 1/world of the selection.  The timed step is the
+    rank's kernels only, replayed from a CUDA graph.  Every request's new token is appended on this
+    rank (the worst case)."""
     import torch
     import deepseek_sparse_mla_gb300 as dsa
     from deepseek_sparse_mla_gb300 import _lib
@@ -540,67 +541,76 @@ def dcp_main(args):
     gidx = torch.empty((R, k), dtype=torch.int32, device=dev)
     lidx = torch.empty((R, k), dtype=torch.int32, device=dev)
     lcnt = torch.empty((R,), dtype=torch.int32, device=dev)
-    rel = torch.arange(W, dtype=torch.int32, device=dev).view(W, 1, 1)
-    # rank r's stand-in scores are this rank's times 1 + r 2^-20: distinct (a copy would tie every
-    # score world ways and send every row down the select's tie-breaking passes) but in the same
-    # order, so each rank still holds about 1/world of the selection
-    relf = 1.0 + torch.arange(W, dtype=torch.float32, device=dev).view(W, 1, 1) * 2.0 ** -20
     merged = [torch.empty((R, 64, 512), dtype=torch.bfloat16, device=dev) for _ in range(wl.layers)]
     merged_lse = [torch.empty((R, 64), dtype=torch.float32, device=dev) for _ in range(wl.layers)]
+    ex = {}
 
-    def step(marks=None):
-        m = marks.mark if marks is not None else (lambda name: None)
-        m("append")
+    def step():
         dsa.kv_append_layers(prob.caches, prob.new_c, prob.new_r, prob.slots,
                              k_idx=[prob.new_k] + [None] * (wl.layers - 1))
-        m("indexer")
         dsa.indexer_scores_topk(prob.caches[0], prob.batch, prob.q_idx, prob.w, k, topk_idx=prob.topk_idx,
                                 scores_out=scores, workspace=prob.ws_idx)
-        m("dcp_candidates")
         dsa.dcp_candidates(scores, prob.topk_idx, 0, W, cand_scores=cs, cand_pos=cp)
-        m("exchange")
-        all_s = (cs.unsqueeze(0) * relf).contiguous()                          # exchange 1 stand-in
-        all_p = torch.where(cp.unsqueeze(0) >= 0, cp.unsqueeze(0) + rel, cp.unsqueeze(0)).contiguous()
-        m("dcp_select")
-        dsa.dcp_select(all_s, all_p, 0, global_idx=gidx, local_idx=lidx, local_count=lcnt)
+        dsa.dcp_select(ex["s"], ex["p"], 0, global_idx=gidx, local_idx=lidx, local_count=lcnt)
         for l in range(wl.layers):
-            m("attention")
             dsa.sparse_mla_decode(prob.caches[l], prob.batch, prob.q[l], lidx, wl.scale, out=prob.out[l],
                                   lse=prob.lse[l], workspace=prob.ws_mla, row_counts=lcnt)
-            m("exchange")
-            outs = prob.out[l].unsqueeze(0).expand(W, R, 64, 512).contiguous()  # exchange 2 stand-in
-            lses = prob.lse[l].unsqueeze(0).expand(W, R, 64).contiguous()
-            m("merge")
-            dsa.dcp_merge(outs, lses, out=merged[l], lse=merged_lse[l])
-        m(None)
+            dsa.dcp_merge(ex["o"][l], ex["l"][l], out=merged[l], lse=merged_lse[l])
+
+    # the exchanged tensors, from one pass of the rank's own steps
+    dsa.indexer_scores_topk(prob.caches[0], prob.batch, prob.q_idx, prob.w, k, topk_idx=prob.topk_idx,
+                            scores_out=scores, workspace=prob.ws_idx)
+    dsa.dcp_candidates(scores, prob.topk_idx, 0, W, cand_scores=cs, cand_pos=cp)
+    rel = torch.arange(W, dtype=torch.int32, device=dev).view(W, 1, 1)
+    relf = 1.0 + torch.arange(W, dtype=torch.float32, device=dev).view(W, 1, 1) * 2.0 ** -20
+    ex["s"] = (cs.unsqueeze(0) * relf).contiguous()
+    ex["p"] = torch.where(cp.unsqueeze(0) >= 0, cp.unsqueeze(0) + rel, cp.unsqueeze(0)).contiguous()
+    dsa.dcp_select(ex["s"], ex["p"], 0, global_idx=gidx, local_idx=lidx, local_count=lcnt)
+    ex["o"], ex["l"] = [], []
+    for l in range(wl.layers):
+        dsa.sparse_mla_decode(prob.caches[l], prob.batch, prob.q[l], lidx, wl.scale, out=prob.out[l],
+                              lse=prob.lse[l], workspace=prob.ws_mla, row_counts=lcnt)
+        ex["o"].append(prob.out[l].unsqueeze(0).expand(W, R, 64, 512).contiguous())
+        ex["l"].append(prob.lse[l].unsqueeze(0).expand(W, R, 64).contiguous())
+    torch.cuda.synchronize()
 
     lib = _lib.load()
+    graph, per_step = None, 0
+    if not args.eager:
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                step()
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            n0 = lib.dsa_kernel_launches()
+            with torch.cuda.graph(graph):
+                step()
+            per_step = int(lib.dsa_kernel_launches() - n0)
+        except Exception as e:
+            print(f"graph capture failed ({e}); timing eager launches", file=sys.stderr)
+            graph = None
+    run_step = graph.replay if graph is not None else step
     for _ in range(args.warmup):
-        step()
+        run_step()
     torch.cuda.synchronize()
     launches0 = lib.dsa_kernel_launches()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     for _ in range(args.steps):
-        step()
+        run_step()
     t1.record()
     torch.cuda.synchronize()
-    launches = int(lib.dsa_kernel_launches() - launches0)
+    launches = per_step * args.steps if graph is not None else int(lib.dsa_kernel_launches() - launches0)
     ms = t0.elapsed_time(t1) / args.steps
-    marks = Marks()
-    for _ in range(max(3, min(args.steps, 20))):
-        step(marks)
-        torch.cuda.synchronize()
-        marks.collect()
-    spans = {n: float(np.sum(v)) / max(3, min(args.steps, 20)) for n, v in marks.spans.items()}
-    # the stand-in copies run on the device inside the timed steps; their time is reported apart
-    excl = ms - spans.get("exchange", 0.0)
-    line = {"metric": f"DCP rank decode layer-steps/s (world {W}, exchanges stood in by local copies)",
+    line = {"metric": f"DCP rank decode layer-steps/s (world {W}, the rank's kernels; exchanges excluded)",
             "value": wl.layers / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": full.name, "world": W, "rank_share": wl.summary()},
-            "ms_per_step_by_phase": spans, "ms_per_step_without_exchange_stand_ins": excl,
-            "value_without_exchange_stand_ins": wl.layers / (excl * 1e-3), "gpu_launches": launches}
+            "config": {"workload": full.name, "world": W, "rank_share": wl.summary(),
+                       "launch": "CUDA graph replay" if graph is not None else "eager"},
+            "gpu_launches": launches}
     print(json.dumps(line), flush=True)
 
 
