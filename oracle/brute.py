@@ -53,6 +53,60 @@ def quantize_key(values_f32: list) -> tuple[list, float]:
     return [e4m3_encode(f32(v / scale)) for v in values_f32], scale
 
 
+def f16_value(bits: int) -> float:
+    """Value of an IEEE binary16 pattern (sign, 5-bit exponent with bias 15, 10-bit mantissa)."""
+    bits = int(bits) & 0xFFFF
+    sign = -1.0 if bits & 0x8000 else 1.0
+    e = (bits >> 10) & 0x1F
+    m = bits & 0x3FF
+    if e == 0x1F:
+        return sign * math.inf if m == 0 else math.nan
+    if e == 0:
+        return sign * m * 2.0 ** -24
+    return sign * (1024 + m) * 2.0 ** (e - 25)
+
+
+_F16_POSITIVE = None
+
+
+def f16_nearest(x: float) -> int:
+    """Bits of the finite binary16 value nearest to x >= 0, found by searching every positive finite
+    pattern; ties go to the even pattern; values beyond the largest finite half give 65504."""
+    global _F16_POSITIVE
+    if _F16_POSITIVE is None:
+        _F16_POSITIVE = [(f16_value(b), b) for b in range(0x7C00)]     # increasing with the bits
+    best, best_d = None, None
+    for v, b in _F16_POSITIVE:
+        d = abs(x - v)
+        if best is None or d < best_d or (d == best_d and (b & 1) == 0):
+            best, best_d = b, d
+        elif v > x:
+            break
+    return best
+
+
+def nearest_int8(x: float) -> int:
+    """Integer code in [-127, 127] nearest to x by search over all of them; ties go to the even code."""
+    best, best_d = None, None
+    for c in range(-127, 128):
+        d = abs(x - c)
+        if best is None or d < best_d or (d == best_d and c % 2 == 0):
+            best, best_d = c, d
+    return best
+
+
+def quantize_key_int8(values_f32: list) -> tuple[list, int]:
+    """(int8 codes, binary16 scale bits) of one key: scale = half(amax / 127) (1 if amax = 0, the
+    smallest positive half if it would round to 0), code = nearest integer to the float32 x / scale."""
+    amax = max(abs(v) for v in values_f32)
+    if amax == 0:
+        sbits = f16_nearest(1.0)
+    else:
+        sbits = f16_nearest(f32(amax / 127.0)) or 1
+    scale = f16_value(sbits)
+    return [nearest_int8(f32(v / scale)) for v in values_f32], sbits
+
+
 def score(q_heads: list, w: list, key: list) -> float:
     """sum over heads of w[h] * ReLU(sum_d q[h][d] * key[d])."""
     total = 0.0

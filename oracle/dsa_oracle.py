@@ -79,13 +79,26 @@ Definitions (R query rows, B requests, P page size):
   C8 packs the main latent KV and uses the quantized sparse-attention operator,
   while the non-RoPE / RoPE split is preserved; "vLLM Inference Path", "MLA
   Projections and KV State": an explicit FP8 KV setting narrows the main MLA
-  cache).  The per-token amax / 448 rule and bf16 k_R are the readings taken.
+  cache).  The per-token amax / 448 rule and bf16 k_R are the readings taken;
+* int8 index-key append -- per token, ``scale = fp16(amax / 127)`` (the float32
+  quotient rounded to IEEE binary16, nearest-even, held at the largest finite
+  half 65504 above it and at the smallest positive half 2^-24 below it; 1 if
+  amax = 0) and ``code = clamp(rne(x / scale), -127, 127)`` with the IEEE
+  float32 quotient by the stored scale; the key is ``code * scale``.  The pages
+  give "INT8 keys with FP16 scales" as the indexer cache of one hardware
+  family beside e4m3 keys with float32 scales ("GLM-5.2 on vLLM Ascend",
+  section 7 and "Quantization and Hardware Branches") without the rule: the
+  symmetric amax / 127 scale, held to its half-precision value before the
+  division so that ``code * scale`` reproduces the key, is the reading taken.
 """
 from __future__ import annotations
 
 import numpy as np
 
 E4M3_MAX = 448.0
+INT8_MAX = 127
+F16_MAX = 65504.0            # largest finite IEEE binary16 value
+F16_MIN_SUBNORMAL = 2.0 ** -24
 
 
 # ---------------------------------------------------------------------------
@@ -159,13 +172,73 @@ def quantize_index_keys(bits) -> tuple[np.ndarray, np.ndarray]:
     return codes, scale
 
 
+def f16_to_f64(bits) -> np.ndarray:
+    """IEEE binary16 bit patterns -> float64 (exact).
+
+    Field layout s.eeeee.mmmmmmmmmm, exponent bias 15.  Exponent field 0 is
+    subnormal: (m/1024) * 2^-14.  Otherwise (1 + m/1024) * 2^(e-15); field 31
+    is infinity (m = 0) or NaN.
+    """
+    c = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    sign = np.where((c & 0x8000) != 0, -1.0, 1.0)
+    e = (c >> 10) & 0x1F
+    m = (c & 0x3FF).astype(np.float64)
+    mag = np.where(e == 0, (m / 1024.0) * 2.0 ** -14, (1.0 + m / 1024.0) * np.exp2(e.astype(np.float64) - 15.0))
+    mag = np.where(e == 0x1F, np.where(m == 0, np.inf, np.nan), mag)
+    return sign * mag
+
+
+def f32_to_f16(x) -> np.ndarray:
+    """float32 -> IEEE binary16 bits, round to nearest (ties to even), held at +-65504.
+
+    For |x| in [2^e, 2^(e+1)) with e >= -14 the spacing of binary16 is 2^(e-10);
+    below 2^-14 (the subnormal range) it is 2^-24.  Same construction as the
+    e4m3 encoder: divide by the spacing (exact in float64), np.rint, rebuild.
+    """
+    v = np.asarray(x, dtype=np.float32).astype(np.float64)
+    neg = np.signbit(v)
+    a = np.abs(v)
+    _, ex = np.frexp(a)
+    e = np.maximum(ex - 1, -14)
+    step = np.ldexp(1.0, e - 10)
+    q = np.minimum(np.rint(a / step) * step, F16_MAX)
+    _, qex = np.frexp(np.where(q > 0, q, 1.0))
+    qe = qex - 1
+    normal = q >= 2.0 ** -14
+    exp_field = np.where(normal, qe + 15, 0)
+    mant = np.where(normal, (q / np.ldexp(1.0, qe) - 1.0) * 1024.0, q / F16_MIN_SUBNORMAL)
+    code = (exp_field.astype(np.int64) << 10) | np.rint(mant).astype(np.int64)
+    code = np.where(q == 0, 0, code) | np.where(neg, 0x8000, 0)
+    return code.astype(np.uint16)
+
+
+def quantize_index_keys_int8(bits) -> tuple[np.ndarray, np.ndarray]:
+    """bf16 index keys [T, 128] -> (int8 codes [T, 128], binary16 scale bits [T]).
+
+    scale = fp16(amax / 127): the float32 quotient rounded to binary16 (nearest,
+    ties to even), at most 65504 and at least 2^-24; 1 when amax = 0.  code =
+    rne(x / scale) with the float32 quotient by that stored scale, clamped to
+    [-127, 127] (the rounded scale can sit a hair below amax / 127).
+    """
+    x = bf16_to_f64(bits).astype(np.float32)
+    amax = np.max(np.abs(x), axis=-1)
+    s16 = f32_to_f16((amax / np.float32(INT8_MAX)).astype(np.float32))
+    s16 = np.where(s16 == 0, np.uint16(1), s16)                 # below 2^-25: the smallest positive half
+    s16 = np.where(amax > 0, s16, f32_to_f16(np.float32(1.0))).astype(np.uint16)
+    scale = f16_to_f64(s16).astype(np.float32)                  # exact: every half is a float32
+    quot = (x / scale[..., None]).astype(np.float32)
+    codes = np.clip(np.rint(quot.astype(np.float64)), -INT8_MAX, INT8_MAX).astype(np.int8)
+    return codes, s16
+
+
 # ---------------------------------------------------------------------------
 # the paged caches
 # ---------------------------------------------------------------------------
 class PagedCache:
     """One layer's caches: latent pages [N_pg, P, 576] bf16 and, for an
-    indexer-owning layer, index-key pages [N_pg, P, 128] (bf16, or e4m3 codes
-    with float32 scales [N_pg, P]).  Unwritten slots hold 0."""
+    indexer-owning layer, index-key pages [N_pg, P, 128] (bf16, e4m3 codes
+    with float32 scales [N_pg, P], or int8 codes with binary16 scale bits
+    [N_pg, P]).  Unwritten slots hold 0."""
 
     def __init__(self, num_pages: int, page_size: int, key_format: str | None, d_latent=512, d_rope=64, d_index=128,
                  latent_format: str = "bf16"):
@@ -188,6 +261,9 @@ class PagedCache:
         elif key_format == "fp8":
             self.index_keys = np.zeros((num_pages, page_size, d_index), dtype=np.uint8)
             self.index_scales = np.zeros((num_pages, page_size), dtype=np.float32)
+        elif key_format == "int8":
+            self.index_keys = np.zeros((num_pages, page_size, d_index), dtype=np.int8)
+            self.index_scales = np.zeros((num_pages, page_size), dtype=np.uint16)
         elif key_format is not None:
             raise ValueError(key_format)
 
@@ -195,7 +271,7 @@ class PagedCache:
         """Write new tokens at their slots (page = slot // P, offset = slot % P).
 
         The latent row is the bit-exact concatenation [c_KV | k_R].  Index keys
-        are stored as given (bf16), quantised here (bf16 given, fp8 cache), or
+        are stored as given (bf16), quantised here (bf16 given, fp8 or int8 cache), or
         stored as given codes + scales (pre-quantised input)."""
         slot = np.asarray(slot_mapping, dtype=np.int64)
         pg, off = slot // self.page_size, slot % self.page_size
@@ -214,7 +290,8 @@ class PagedCache:
             self.index_keys[pg, off] = k_idx_codes
             self.index_scales[pg, off] = k_idx_scales
         else:
-            codes, scales = quantize_index_keys(k_idx_bits)
+            quantize = quantize_index_keys_int8 if self.key_format == "int8" else quantize_index_keys
+            codes, scales = quantize(k_idx_bits)
             self.index_keys[pg, off] = codes
             self.index_scales[pg, off] = scales
 
@@ -234,10 +311,12 @@ class PagedCache:
         return rows
 
     def index_key_rows(self, block_row, positions) -> np.ndarray:
-        """[n, 128] float64 index keys: the bf16 value, or e4m3 value times the token's scale."""
+        """[n, 128] float64 index keys: the bf16 value, or the e4m3 / int8 code times the token's scale."""
         pg, off = self.slots(block_row, positions)
         if self.key_format == "bf16":
             return bf16_to_f64(self.index_keys[pg, off])
+        if self.key_format == "int8":
+            return self.index_keys[pg, off].astype(np.float64) * f16_to_f64(self.index_scales[pg, off])[:, None]
         return e4m3_to_f64(self.index_keys[pg, off]) * self.index_scales[pg, off].astype(np.float64)[:, None]
 
 
