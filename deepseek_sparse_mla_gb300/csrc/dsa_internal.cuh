@@ -6,6 +6,8 @@
 #include <cuda_fp8.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/dsa.h"
 
 namespace dsa {
@@ -26,6 +28,41 @@ constexpr size_t kWorkspaceHeader = 256;
 constexpr int kTopkChunkMin = 32768;
 constexpr int kTopkChunkCap = 4096;
 constexpr int kTopkMaxChunks = 32;
+
+// ---------------------------------------------------------------------------
+// per-device host set-up
+// ---------------------------------------------------------------------------
+// The runtime applies a kernel's opt-in to more than 48 KB of dynamic shared memory to the current
+// device only, so set-up of that kind runs once per device: bit d of `done` records device d.
+// Concurrent first calls may both run `setup`, which must therefore be idempotent (setting a kernel
+// attribute is).  Devices 64 and above run it on every call.
+template <class Setup>
+inline cudaError_t once_per_device(std::atomic<uint64_t>& done, Setup setup) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? uint64_t(1) << dev : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = setup();
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// SM count of the current device (persistent grids take one CTA per SM), looked up once per device.
+inline int device_sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kMlaCtas;
+  const bool slot = dev >= 0 && dev < 64;
+  if (slot) {
+    const int n = cached[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kMlaCtas;
+  if (slot) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 
 // ---------------------------------------------------------------------------
 // launch plans: shared by the *_workspace_bytes functions and the launches

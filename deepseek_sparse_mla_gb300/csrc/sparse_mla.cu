@@ -884,15 +884,15 @@ MlaPlan plan_mla(int num_rows, int topk) {
 cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows, const void* q,
                               const int32_t* topk_idx, int topk, float scale, void* out, float* lse,
                               void* workspace, const MlaPlan& plan, cudaStream_t s, const int32_t* row_count) {
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t set = once_per_device(configured, [] {
     cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          mla::kSmemBytes);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(sparse_mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+    return e;
+  });
+  if (set != cudaSuccess) return set;
   const bool c8 = c.latent_format == DSA_LATENT_E4M3;
   const float* ls = c8 ? c.latent_scales : nullptr;
   CUtensorMap kv_map, q_map;

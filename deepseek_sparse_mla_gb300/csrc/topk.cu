@@ -530,14 +530,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RowMeta m, int row0,
 cudaError_t launch_topk(const RowMeta& m, int row0, int nrows, const float* scores, int64_t score_stride,
                         int max_seq_len, int topk, int32_t* topk_idx, const TopkChunks& ch, cudaStream_t s,
                         int unit_shift) {
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t set = once_per_device(configured, [] {
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChunkSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+    return e != cudaSuccess ? e
+                            : cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)kChunkSmem);
+  });
+  if (set != cudaSuccess) return set;
   if (ch.chunks > 0) {
     cudaError_t e = launch_pdl(topk_chunk_kernel, dim3(ch.chunks, nrows), dim3(kChunkThreads), kChunkSmem, s, m, row0,
                                scores, score_stride, max_seq_len, topk, ch.chunk, ch.chunks, (int)kTopkChunkCap,
