@@ -629,6 +629,9 @@ def main():
                     help="launch the step call by call instead of replaying it from a CUDA graph")
     ap.add_argument("--latent", choices=["bf16", "fp8"], default="bf16",
                     help="latent cache format: bf16, or packed 8-bit (e4m3 c_KV with a scale per token, bf16 k_R)")
+    ap.add_argument("--keys", choices=["default", "bf16", "fp8", "int8"], default="default",
+                    help="index-key format of the owner layer (default: the workload's own; int8 keys carry a "
+                         "binary16 scale per token)")
     ap.add_argument("--dcp", type=int, default=0,
                     help="time one rank's device work of decode context parallelism over this many ranks")
     args = ap.parse_args()
@@ -646,6 +649,9 @@ def main():
     if args.latent != "bf16":
         import dataclasses
         wl = dataclasses.replace(wl, name=f"{wl.name}_latent_{args.latent}", latent_format=args.latent)
+    if args.keys not in ("default", wl.key_format):
+        import dataclasses
+        wl = dataclasses.replace(wl, name=f"{wl.name}_keys_{args.keys}", key_format=args.keys)
     prob = DeviceProblem(wl, selection=args.selection)
     page_mode = args.selection == "page"
     lib = _lib.load()

@@ -18,11 +18,11 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import DsaError, KEY_BF16, KEY_FP8_E4M3  # noqa: F401
+from ._lib import DsaError, KEY_BF16, KEY_FP8_E4M3, KEY_INT8  # noqa: F401
 
 INDEX_HEADS, INDEX_DIM, HEADS, LATENT_DIM, ROPE_DIM, ROW_DIM = 32, 128, 64, 512, 64, 576
 DEFAULT_SCALE = 1.0 / 16.0     # 1/sqrt(192 + 64)
-_FORMATS = {"bf16": KEY_BF16, "fp8": KEY_FP8_E4M3, None: KEY_BF16}
+_FORMATS = {"bf16": KEY_BF16, "fp8": KEY_FP8_E4M3, "int8": KEY_INT8, None: KEY_BF16}
 _LATENT_FORMATS = {"bf16": _lib.LATENT_BF16, "fp8": _lib.LATENT_E4M3}
 
 __all__ = ["LayerCache", "Batch", "kv_append", "kv_append_layers", "indexer_scores_topk", "indexer_page_topk", "sparse_mla_decode", "sparse_mla_prefill",
@@ -56,9 +56,9 @@ class LayerCache:
     latent [num_pages, page_size, 576] bf16 (or, with latent_format "fp8", packed 8-bit rows
     [num_pages, page_size, 640] uint8 = 512 e4m3 codes of c_KV + k_R as 64 bf16, with latent_scales
     [num_pages, page_size] fp32); for an indexer-owning layer also
-    index_keys [num_pages, page_size, 128] (bf16, or uint8 e4m3 codes) and, for
-    e4m3, index_scales [num_pages, page_size] fp32.  key_format None makes an
-    IndexShare layer that holds only latent pages."""
+    index_keys [num_pages, page_size, 128] (bf16, uint8 e4m3 codes, or int8 codes) and
+    index_scales [num_pages, page_size] (fp32 for e4m3, float16 for int8).  key_format None
+    makes an IndexShare layer that holds only latent pages."""
 
     def __init__(self, num_pages: int, page_size: int, key_format: str | None = None, device="cuda",
                  latent_format: str = "bf16"):
@@ -80,6 +80,9 @@ class LayerCache:
         elif key_format == "fp8":
             self.index_keys = torch.zeros((num_pages, page_size, INDEX_DIM), dtype=torch.uint8, device=device)
             self.index_scales = torch.zeros((num_pages, page_size), dtype=torch.float32, device=device)
+        elif key_format == "int8":
+            self.index_keys = torch.zeros((num_pages, page_size, INDEX_DIM), dtype=torch.int8, device=device)
+            self.index_scales = torch.zeros((num_pages, page_size), dtype=torch.float16, device=device)
         elif key_format is not None:
             raise ValueError(f"key_format {key_format!r}")
 
@@ -134,7 +137,8 @@ def _workspace(nbytes, device):
 
 
 def kv_append(cache: LayerCache, c_kv, k_rope, slot_mapping, k_idx=None, k_idx_scales=None, stream=None):
-    """Scatter T new tokens into the layer's pages (bf16 keys are quantised for an fp8 cache)."""
+    """Scatter T new tokens into the layer's pages (bf16 keys are quantised for an fp8 or int8 cache;
+    pre-quantised keys are uint8 e4m3 codes with float32 scales, or int8 codes with float16 scales)."""
     T = int(slot_mapping.shape[0])
     _need(c_kv, torch.bfloat16, (T, LATENT_DIM), "c_kv")
     _need(k_rope, torch.bfloat16, (T, ROPE_DIM), "k_rope")
@@ -145,6 +149,10 @@ def kv_append(cache: LayerCache, c_kv, k_rope, slot_mapping, k_idx=None, k_idx_s
             fmt = KEY_FP8_E4M3
             _need(k_idx, torch.uint8, (T, INDEX_DIM), "k_idx")
             _need(k_idx_scales, torch.float32, (T,), "k_idx_scales")
+        elif k_idx.dtype == torch.int8:
+            fmt = KEY_INT8
+            _need(k_idx, torch.int8, (T, INDEX_DIM), "k_idx")
+            _need(k_idx_scales, torch.float16, (T,), "k_idx_scales")
         else:
             _need(k_idx, torch.bfloat16, (T, INDEX_DIM), "k_idx")
     c = cache.struct()

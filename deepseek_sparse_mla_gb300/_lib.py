@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(_PKG, "libdsa.so")
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE, DSA_ERR_CUDA = 0, -1, -2, -3, -4
 STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_INVALID_ARG", -2: "DSA_ERR_UNSUPPORTED", -3: "DSA_ERR_WORKSPACE",
                 -4: "DSA_ERR_CUDA"}
-KEY_BF16, KEY_FP8_E4M3 = 0, 1
+KEY_BF16, KEY_FP8_E4M3, KEY_INT8 = 0, 1, 2
 LATENT_BF16, LATENT_E4M3 = 0, 1
 
 # every entry point include/dsa.h declares

@@ -83,11 +83,13 @@ static dsa_status check_cache(const dsa_cache* c, bool need_keys) {
   if (c->latent_scales && (reinterpret_cast<uintptr_t>(c->latent_scales) & 15u))
     return fail(DSA_ERR_INVALID_ARG, "cache.latent_scales is not 16-byte aligned");
   if (c->index_keys) {
-    if (c->key_format != DSA_KEY_BF16 && c->key_format != DSA_KEY_FP8_E4M3)
+    if (c->key_format != DSA_KEY_BF16 && c->key_format != DSA_KEY_FP8_E4M3 && c->key_format != DSA_KEY_INT8)
       return fail(DSA_ERR_INVALID_ARG, "cache.key_format %d is not a dsa_key_format", c->key_format);
     if (!aligned16(c->index_keys)) return fail(DSA_ERR_INVALID_ARG, "cache.index_keys is not 16-byte aligned");
     if (c->key_format == DSA_KEY_FP8_E4M3 && !c->index_scales)
       return fail(DSA_ERR_INVALID_ARG, "e4m3 index keys need cache.index_scales");
+    if (c->key_format == DSA_KEY_INT8 && !c->index_scales)
+      return fail(DSA_ERR_INVALID_ARG, "int8 index keys need cache.index_scales (binary16)");
     if (c->key_format == DSA_KEY_BF16 && c->index_scales)
       return fail(DSA_ERR_INVALID_ARG, "bf16 index keys take no cache.index_scales (layouts are not interchangeable)");
     if (c->index_scales && (reinterpret_cast<uintptr_t>(c->index_scales) & 15u))
@@ -177,6 +179,7 @@ size_t dsa_cache_bytes(int32_t num_pages, int32_t page_size, int32_t key_format,
   if (owner) {
     if (key_format == DSA_KEY_BF16) bytes += slots * kIndexDim * 2;
     else if (key_format == DSA_KEY_FP8_E4M3) bytes += slots * (kIndexDim + sizeof(float));
+    else if (key_format == DSA_KEY_INT8) bytes += slots * (kIndexDim + 2);
     else return 0;
   }
   return bytes;
@@ -203,9 +206,14 @@ static dsa_status check_append_layer(const dsa_cache* cache, const void* c_kv, c
     if (!aligned16(k_idx)) return fail(DSA_ERR_INVALID_ARG, "k_idx is not 16-byte aligned");
     if (k_idx_format == DSA_KEY_FP8_E4M3) {
       if (cache->key_format != DSA_KEY_FP8_E4M3)
-        return fail(DSA_ERR_INVALID_ARG, "e4m3 index keys cannot be stored into a bf16 indexer cache");
+        return fail(DSA_ERR_INVALID_ARG, "e4m3 index keys can only be stored into an e4m3 indexer cache");
       if (!k_idx_scales) return fail(DSA_ERR_INVALID_ARG, "pre-quantised e4m3 keys need k_idx_scales");
       if (reinterpret_cast<uintptr_t>(k_idx_scales) & 3u) return fail(DSA_ERR_INVALID_ARG, "k_idx_scales is not 4-byte aligned");
+    } else if (k_idx_format == DSA_KEY_INT8) {
+      if (cache->key_format != DSA_KEY_INT8)
+        return fail(DSA_ERR_INVALID_ARG, "int8 index keys can only be stored into an int8 indexer cache");
+      if (!k_idx_scales) return fail(DSA_ERR_INVALID_ARG, "pre-quantised int8 keys need k_idx_scales (binary16)");
+      if (reinterpret_cast<uintptr_t>(k_idx_scales) & 1u) return fail(DSA_ERR_INVALID_ARG, "k_idx_scales is not 2-byte aligned");
     } else if (k_idx_format != DSA_KEY_BF16) {
       return fail(DSA_ERR_INVALID_ARG, "k_idx_format %d is not a dsa_key_format", k_idx_format);
     }

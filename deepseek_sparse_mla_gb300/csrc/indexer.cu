@@ -15,7 +15,11 @@
 // head) query vector is scaled by an exact power of two and split into two
 // e4m3 terms q' = t1 + t2/16 that represent it exactly (query_exponent below),
 // so the two accumulators give q . k exactly up to fp32 rounding; bf16 keys
-// use kind::f16 with the bf16 queries as they are.
+// use kind::f16 with the bf16 queries as they are.  int8 keys (binary16
+// scales) have no tensor path of their own on sm_103a (no integer MMA): three
+// converter warps split each landed tile byte for byte into two e4m3 tiles,
+// hi = e4m3(v) in place and lo = v - hi beside it (both exact, |lo| <= 4), and
+// the issuer runs the e4m3 chain over both into the same accumulators.
 //
 // Per CTA (persistent, one per SM, 448 threads), over one contiguous range of
 // the flattened (group, key tile) list:
@@ -28,10 +32,15 @@
 //              into the B operand, 128-byte swizzled, K-major;
 //   warps 6-13 two epilogue warpgroups, even and odd tiles (fed by the
 //              matching issuer); the one that reads a tile's scales frees
-//              its scale slot.
+//              its scale slot;
+//   warps 14-16 (int8 keys only) converters, tile i by warp i % 3, each with
+//              its own lo tile that the MMA of its previous tile releases.
 // The key ring holds up to 6 stages: enough bytes in flight to cover HBM
 // latency, few enough not to congest the memory system.
 #include <mutex>
+#include <type_traits>
+
+#include <cuda_fp16.h>
 
 #include "dsa_internal.cuh"
 #include "sm100.cuh"
@@ -45,6 +54,10 @@ constexpr int kTileKeys = 128;
 constexpr int kProducers = 3;                      // warps issuing the key copies (TMA issue is per-warp limited)
 constexpr int kMmaWarps = 2;                       // MMA issuers: even and odd tiles
 constexpr int kThreads = 32 * (kProducers + kMmaWarps + 1 + 8);  // producers, MMA, B loader, two epilogue warpgroups
+constexpr int kConvWarps = 3;                      // int8 keys: tile converters (a divisor of the 6 key stages)
+constexpr int kThreadsI8 = kThreads + 32 * kConvWarps;
+constexpr int kI8Stages = 6;                       // int8 keys: always 6 stages (stage s is converted by warp s % 3)
+constexpr int kI8MaxRows = 2;                      // int8 keys: rows per group, so that 6 stages and 3 lo tiles fit
 constexpr int kBBytes = 65536;                      // B operand at most: 256 (row, head) query vectors
 // Dynamic shared memory: [B buffers | key-scale ring | key ring].  The B buffers take only what the
 // group size needs (16 KB in decode), and the key ring gets the rest, up to kMaxStages stages.
@@ -53,7 +66,7 @@ constexpr int kSmemBytes = 200 * 1024;
 // 6 stages of 16 KB measured 3 % faster than 10 and 12 % faster than 4.
 constexpr int kMaxStages = 6;
 constexpr int kScStages = 16;                       // key-scale ring (e4m3): 16 tiles x 128 fp32
-constexpr int kScRingBytes = kScStages * 128 * 4;
+constexpr int kScRingBytes = kScStages * 128 * 4;   // fp32 scales (e4m3 keys); binary16 scales take half
 static_assert((kScStages & (kScStages - 1)) == 0 && kScStages >= kMaxStages + 4, "scale ring: power of two, deep");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPolls = 1u << 22;
@@ -158,12 +171,40 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
          ((uint32_t)__nv_cvt_float_to_fp8(d, __NV_SATFINITE, __NV_E4M3) << 24);
 }
 
-template <bool kFp8>
-__global__ void __launch_bounds__(idx::kThreads, 1)
+// Four int8 codes (one 32-bit word) -> the e4m3 codes of hi = e4m3(v) (nearest-even) and lo = v - hi,
+// byte for byte.  For |v| <= 127 both are exact e4m3 values (|lo| <= 4), so hi + lo = v.  Each v is
+// first made a half exactly: the bits 0x64XX with XX = v + 128 are the half 1024 + v + 128.
+__device__ __forceinline__ void split_int8_e4m3(uint32_t w, uint32_t& hi, uint32_t& lo) {
+  const uint32_t u = w ^ 0x80808080u;
+  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));     // 1152
+  const uint32_t pairs[2] = {__byte_perm(u, 0x64646464u, 0x5140), __byte_perm(u, 0x64646464u, 0x5342)};
+  uint32_t h[2], l[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&pairs[j]), bias);
+    const __nv_fp8x2_storage_t hc = __nv_cvt_halfraw2_to_fp8x2(__half2_raw(v), __NV_SATFINITE, __NV_E4M3);
+    const __half2 hv = __half2(__nv_cvt_fp8x2_to_halfraw2(hc, __NV_E4M3));
+    const __nv_fp8x2_storage_t lc = __nv_cvt_halfraw2_to_fp8x2(__half2_raw(__hsub2(v, hv)), __NV_SATFINITE, __NV_E4M3);
+    h[j] = hc;
+    l[j] = lc;
+  }
+  hi = h[0] | (h[1] << 16);
+  lo = l[0] | (l[1] << 16);
+}
+
+__device__ __forceinline__ float scale_value(float v) { return v; }
+__device__ __forceinline__ float scale_value(uint16_t v) { return __half2float(__ushort_as_half(v)); }
+
+// kKind: 0 bf16 keys, 1 e4m3 keys (fp32 scales), 2 int8 keys (binary16 scales).
+template <int kKind>
+__global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap key_map, const IdxArgs a) {
   using namespace idx;
+  constexpr bool kFp8 = kKind != 0;                   // 8-bit keys: the e4m3 MMA path
+  constexpr bool kI8 = kKind == 2;
+  using ScaleT = std::conditional_t<kI8, uint16_t, float>;   // a key scale as stored
   constexpr int kStageBytes = kFp8 ? 16384 : 32768;
-  constexpr int kRowsMax = kFp8 ? 4 : 8;
+  constexpr int kRowsMax = kFp8 ? (kI8 ? kI8MaxRows : 4) : 8;
   constexpr int kTerms = kFp8 ? 2 : 1;               // B rows per (row, head): e4m3 split terms
   constexpr int kLoaderWarp = kProducers + kMmaWarps;
   constexpr int kEpiWarp0 = kLoaderWarp + 1;           // two epilogue warpgroups take alternate tiles
@@ -175,15 +216,24 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
   const int nB = n_cap * row_bytes <= kBBytes / 2 ? 2 : 1;         // B buffers (queries of one group each)
   const int b_bytes = (n_cap * row_bytes + 1023) / 1024 * 1024;
   // an even stage count: a stage's consecutive tiles then have the same parity, i.e. the same issuer
-  constexpr int kScBytes = kFp8 ? kScRingBytes : 0;                // bf16 keys carry no scales
-  const int kStages = min(kMaxStages, (kSmemBytes - 1024 - nB * b_bytes - kScBytes) / kStageBytes) & ~1;
+  constexpr int kScBytes = kFp8 ? kScRingBytes * (int)sizeof(ScaleT) / 4 : 0;   // bf16 keys carry no scales
+  constexpr int kLoBytes = kI8 ? kConvWarps * 16384 : 0;           // int8 keys: one lo tile per converter
+  const int kStages = kI8 ? kI8Stages
+                          : min(kMaxStages, (kSmemBytes - 1024 - nB * b_bytes - kScBytes) / kStageBytes) & ~1;
   uint8_t* sB = smem;
-  float* sScale = reinterpret_cast<float*>(smem + nB * b_bytes);   // [kScStages][128], e4m3 keys only
+  ScaleT* sScale = reinterpret_cast<ScaleT*>(smem + nB * b_bytes);  // [kScStages][128], 8-bit keys only
   uint8_t* sRing = smem + nB * b_bytes + kScBytes;
+  uint8_t* sLo = sRing + kStages * kStageBytes;                      // int8 keys: [kConvWarps][16 KB]
+  if (kI8 && (a.rows_per_group > kI8MaxRows || 1024 + nB * b_bytes + kScBytes + kStages * kStageBytes + kLoBytes >
+                                                   kSmemBytes)) {
+    if (threadIdx.x == 0) atomicOr(a.err, kErrConfig);            // the host never launches this shape
+    return;
+  }
 
   __shared__ uint64_t st_full[kMaxStages], st_empty[kMaxStages], sc_full[kScStages], sc_empty[kScStages];
   __shared__ uint64_t d_full[4], d_empty[4], b_full[2], b_empty[2];
   __shared__ uint64_t mma_done[kMmaWarps];
+  __shared__ uint64_t cv_full[kI8 ? kMaxStages : 1], lo_empty[kI8 ? kConvWarps : 1];   // int8 keys only
   __shared__ float wq_e[2][kMaxRows][32];   // each epilogue warpgroup's head weights for its current group
   __shared__ int4 gcache[kGroupCache];
   __shared__ int tcache[kGroupCache + 1];
@@ -211,6 +261,10 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
       mbar_init(&b_empty[b], kMmaWarps);         // every issuer commits when it leaves a group
     }
     for (int m = 0; m < kMmaWarps; ++m) mbar_init(&mma_done[m], 1);
+    if (kI8) {
+      for (int s = 0; s < kStages; ++s) mbar_init(&cv_full[s], 1);   // its converter, once converted
+      for (int c = 0; c < kConvWarps; ++c) mbar_init(&lo_empty[c], 1);   // the MMA's commit frees a lo tile
+    }
     fence_mbar_init();
   }
   if (warp == kProducers) {
@@ -244,7 +298,9 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
     // ------------------------------------------------------------------ producers (tiles round-robin)
     // Each warp keeps a register window of 32 page ids (one per lane) and loads the next window
     // ahead of use, so page-table reads never sit between a free stage and its copy.
-    const bool bulk_scales = kFp8 && a.box_rows >= 4;
+    // scale rows are bulk-copied when a sub-box's scales make 16 bytes (4 fp32 or 8 binary16)
+    const bool bulk_scales = kFp8 && a.box_rows * (int)sizeof(ScaleT) >= 16;
+    const ScaleT* key_scales = reinterpret_cast<const ScaleT*>(a.key_scales);
     const uint32_t key_tx = (kFp8 ? 1u : 2u) * box_bytes;
     const bool windowed = loads_per_tile <= 32;
     TileCursor cur;
@@ -294,7 +350,7 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
       if (n > 0 && !mbar_wait(&st_empty[s], (n - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
       if (kFp8 && scn > 0 && !mbar_wait(&sc_empty[sci], (scn - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
       uint8_t* stage = sRing + s * kStageBytes;
-      float* sc = sScale + sci * kTileKeys;
+      ScaleT* sc = sScale + sci * kTileKeys;
       // sub-box j holds keys k0 + j*box_rows ..; it is loaded when it starts at a visible key of a valid page
       uint32_t nvalid = 0;
       int my_page[4];
@@ -315,15 +371,15 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
           nvalid += __popc(__ballot_sync(0xffffffffu, v));
         }
       }
-      if (kFp8 && !bulk_scales) {        // pages of fewer than 4 keys: scales through registers
+      if (kFp8 && !bulk_scales) {        // small pages (under 16 bytes of scales): scales through registers
         for (int k = lane; k < kTileKeys; k += 32) {
           const int key = k0 + k;
           const int lp = key >> a.log2_page;
-          float v = 0.f;
+          ScaleT v = 0;
           if (key <= pos_last && lp < a.m.block_table_stride) {
             const int page = bt[lp];
             if (page >= 0 && page < a.num_pages)
-              v = a.key_scales[((int64_t)page << a.log2_page) + (key & ((1 << a.log2_page) - 1))];
+              v = key_scales[((int64_t)page << a.log2_page) + (key & ((1 << a.log2_page) - 1))];
           }
           sc[k] = v;
         }
@@ -331,7 +387,8 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(&st_full[s], nvalid * key_tx);
-        if (kFp8) mbar_arrive_expect_tx(&sc_full[sci], bulk_scales ? nvalid * (uint32_t)a.box_rows * 4u : 0u);
+        if (kFp8)
+          mbar_arrive_expect_tx(&sc_full[sci], bulk_scales ? nvalid * (uint32_t)a.box_rows * (uint32_t)sizeof(ScaleT) : 0u);
       }
       __syncwarp();
 #pragma unroll
@@ -343,7 +400,8 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
         const int y = (page << a.log2_page) + (key & ((1 << a.log2_page) - 1));
         tma_load_2d_hint(stage + j * box_bytes, &key_map, 0, y, &st_full[s], l2_evict_first());
         if (!kFp8) tma_load_2d_hint(stage + 16384 + j * box_bytes, &key_map, 64, y, &st_full[s], l2_evict_first());
-        if (bulk_scales) bulk_load(sc + j * a.box_rows, a.key_scales + y, (uint32_t)a.box_rows * 4u, &sc_full[sci]);
+        if (bulk_scales)
+          bulk_load(sc + j * a.box_rows, key_scales + y, (uint32_t)a.box_rows * (uint32_t)sizeof(ScaleT), &sc_full[sci]);
       }
       last_tile = i;
     }
@@ -364,7 +422,7 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
       bool ok = true, new_group = true;
       uint32_t b_addr = 0, idesc = 0;
       int N = 0, ub = 0;
-      int s = 0, n = 0, db = 0, nd = 0;
+      int s = 0, n = 0, db = 0, nd = 0, li = 0;    // li: lo tile of tile i (int8 keys), i % kConvWarps
       for (int i = 0; cur.valid() && ok; ++i) {
         if (new_group) {
           if (i > 0) {
@@ -378,8 +436,9 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
           b_addr = smem_u32(sB + ub * b_bytes);
         }
         if ((i & 1) == mw) {
-          // the issuer paces the pipeline: poll without suspending (a suspended wait wakes late)
-          if (!mbar_spin(&st_full[s], n & 1, a.err, kErrTmaTimeout)) { ok = false; break; }
+          // the issuer paces the pipeline: poll without suspending (a suspended wait wakes late);
+          // int8 tiles are ready once their converter has split them
+          if (!mbar_spin(kI8 ? &cv_full[s] : &st_full[s], n & 1, a.err, kErrTmaTimeout)) { ok = false; break; }
           if (nd > 0 && !mbar_spin(&d_empty[db], (nd - 1) & 1, a.err, kErrMmaTimeout)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d = tmem + db * (uint32_t)n_cap;
@@ -389,6 +448,11 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
             const uint64_t da = smem_desc(stage, 16, 1024, kSwizzle128B), dbq = smem_desc(b_addr, 16, 1024, kSwizzle128B);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) mma_ss_f8(d, da + (uint64_t)(2 * kk), dbq + (uint64_t)(2 * kk), idesc, kk > 0);
+            if (kI8) {        // the lo terms of int8 keys into the same accumulators
+              const uint64_t dl = smem_desc(smem_u32(sLo + li * 16384), 16, 1024, kSwizzle128B);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) mma_ss_f8(d, dl + (uint64_t)(2 * kk), dbq + (uint64_t)(2 * kk), idesc, true);
+            }
           } else {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
@@ -397,9 +461,11 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
           }
           mma_commit(&d_full[db]);
           mma_commit(&st_empty[s]);
+          if (kI8) mma_commit(&lo_empty[li]);
         }
         if (++s == kStages) { s = 0; ++n; }
         if (++db == DD) { db = 0; ++nd; }
+        if (++li == kConvWarps) li = 0;
         new_group = cursor_next(cur, a, gcache, tcache);
       }
       mma_commit(&mma_done[mw]);
@@ -463,6 +529,37 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
       }
       new_group = cursor_next(cur, a, gcache, tcache);
     }
+  } else if (kI8 && warp >= kEpiWarp0 + 8) {
+    // ------------------------------------------------------------------ converters (int8 keys): tile i by warp i % 3
+    // Stage s = i % 6 is always converted by warp s % 3, which waits on that stage's tiles in order; its
+    // lo tile is rewritten only after the MMA of the warp's previous tile has committed.  A tile's
+    // sub-boxes that were not loaded hold stale codes: any byte splits into finite terms, and the
+    // epilogue masks those keys.
+    const int cw = warp - (kEpiWarp0 + 8);
+    const int ntiles = tau1 - tau0;
+    int s = cw, n = 0;
+    for (int i = cw, k = 0; i < ntiles; i += kConvWarps, ++k) {
+      if (!mbar_wait(&st_full[s], n & 1, a.err, kErrTmaTimeout, kPolls)) break;
+      if (k > 0 && !mbar_wait(&lo_empty[cw], (k - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
+      uint4* hi = reinterpret_cast<uint4*>(sRing + s * kStageBytes);
+      uint4* lo = reinterpret_cast<uint4*>(sLo + cw * 16384);
+#pragma unroll 2
+      for (int c = lane; c < kStageBytes / 16; c += 32) {
+        const uint4 v = hi[c];
+        uint4 h, l;
+        split_int8_e4m3(v.x, h.x, l.x);
+        split_int8_e4m3(v.y, h.y, l.y);
+        split_int8_e4m3(v.z, h.z, l.z);
+        split_int8_e4m3(v.w, h.w, l.w);
+        hi[c] = h;
+        lo[c] = l;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cv_full[s]);
+      s += kConvWarps;
+      if (s >= kStages) { s -= kStages; ++n; }
+    }
   } else {
     // ------------------------------------------------------------------ epilogues: ReLU . w, scale, mask, store
     const int eg = (warp - kEpiWarp0) >> 2;          // warpgroup 0 takes even tiles, 1 odd tiles
@@ -522,7 +619,7 @@ __global__ void __launch_bounds__(idx::kThreads, 1)
         if (kFp8) {
           // the tile's key scales sit in their own ring slot, refilled only after this read
           if (!mbar_wait(&sc_full[sci], scn & 1, a.err, kErrTmaTimeout, kPolls)) break;
-          const float ks = sScale[sci * kTileKeys + key_local];
+          const float ks = scale_value(sScale[sci * kTileKeys + key_local]);
           named_bar_sync(4 + eg, 128);
           if (et == 0) mbar_arrive(&sc_empty[sci]);
 #pragma unroll
@@ -709,7 +806,7 @@ struct KeyMapCache {
         return true;
       }
     CUtensorMap m;
-    const bool ok = format == DSA_KEY_FP8_E4M3
+    const bool ok = format != DSA_KEY_BF16          // e4m3 and int8 keys: 128 bytes per key
                         ? encode_2d(&m, p, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kIndexDim, nrows, kIndexDim, 128, box_rows)
                         : encode_2d(&m, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kIndexDim, nrows, kIndexDim * 2, 64,
                                     box_rows);
@@ -725,11 +822,11 @@ struct KeyMapCache {
   }
 };
 KeyMapCache g_key_maps;
-int g_sm_count = 0;
 }  // namespace
 
 static int indexer_rows_per_group(const dsa_cache& c, bool decode) {
   if (decode) return 1;
+  if (c.key_format == DSA_KEY_INT8) return idx::kI8MaxRows;
   return c.key_format == DSA_KEY_FP8_E4M3 ? 4 : idx::kMaxRows;
 }
 
@@ -737,23 +834,18 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
                                   const void* q_idx, const float* w, float* scores, int64_t score_stride,
                                   bool fill_tail, int32_t* group_scratch, uint32_t* err, cudaStream_t s,
                                   int page_log2) {
-  const bool fp8 = c.key_format == DSA_KEY_FP8_E4M3;
+  const int kind = c.key_format == DSA_KEY_FP8_E4M3 ? 1 : c.key_format == DSA_KEY_INT8 ? 2 : 0;
   const bool decode = m.query_start_loc == nullptr;
-  static bool configured[2] = {false, false};
-  if (!configured[fp8]) {
-    cudaError_t e = fp8 ? cudaFuncSetAttribute(indexer_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               idx::kSmemBytes)
-                        : cudaFuncSetAttribute(indexer_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               idx::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[fp8] = true;
-  }
-  if (g_sm_count == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (g_sm_count <= 0) g_sm_count = kMlaCtas;
-  }
+  static std::atomic<uint64_t> configured{0};
+  const cudaError_t set = once_per_device(configured, [] {
+    cudaError_t r = cudaFuncSetAttribute(indexer_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         idx::kSmemBytes);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(indexer_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, idx::kSmemBytes);
+    return r != cudaSuccess ? r : cudaFuncSetAttribute(indexer_tc_kernel<0>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, idx::kSmemBytes);
+  });
+  if (set != cudaSuccess) return set;
   const uint32_t box_rows = (uint32_t)(c.page_size < idx::kTileKeys ? c.page_size : idx::kTileKeys);
   CUtensorMap map;
   if (!g_key_maps.get(c.index_keys, (uint64_t)c.num_pages * c.page_size, c.key_format, box_rows, &map))
@@ -790,9 +882,10 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
   const int unit_log2 = page_log2 < 5 ? page_log2 : 5;
   a.max_pages = page_log2 >= 0 ? (max_seq_len + (1 << unit_log2) - 1) >> unit_log2 : 0;
   a.err = err;
-  const int grid = g_sm_count;
-  e = fp8 ? launch_pdl(indexer_tc_kernel<true>, dim3(grid), dim3(idx::kThreads), idx::kSmemBytes, s, map, a)
-          : launch_pdl(indexer_tc_kernel<false>, dim3(grid), dim3(idx::kThreads), idx::kSmemBytes, s, map, a);
+  const int grid = device_sm_count();
+  e = kind == 1   ? launch_pdl(indexer_tc_kernel<1>, dim3(grid), dim3(idx::kThreads), idx::kSmemBytes, s, map, a)
+      : kind == 2 ? launch_pdl(indexer_tc_kernel<2>, dim3(grid), dim3(idx::kThreadsI8), idx::kSmemBytes, s, map, a)
+                  : launch_pdl(indexer_tc_kernel<0>, dim3(grid), dim3(idx::kThreads), idx::kSmemBytes, s, map, a);
   count_launches(1);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();

@@ -7,6 +7,8 @@
 // and moves its 1152-byte latent row (or its packed 8-bit 640-byte row and
 // scale) with 16-byte stores straight into its slot; nothing else in the pool
 // is read or written.
+#include <cuda_fp16.h>
+
 #include "dsa_internal.cuh"
 
 namespace dsa {
@@ -68,13 +70,17 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendArgs a) {
       reinterpret_cast<uint4*>(L.index_keys)[slot * 16 + lane] = reinterpret_cast<const uint4*>(L.k_idx)[(int64_t)t * 16 + lane];
     return;
   }
-  if (L.k_idx_format == DSA_KEY_FP8_E4M3) {           // pre-quantised: 128 code bytes + scale, copied
+  if (L.k_idx_format != DSA_KEY_BF16) {                // pre-quantised: 128 code bytes + scale, copied
     if (lane < 8)
       reinterpret_cast<uint4*>(L.index_keys)[slot * 8 + lane] = reinterpret_cast<const uint4*>(L.k_idx)[(int64_t)t * 8 + lane];
-    if (lane == 0) L.index_scales[slot] = L.k_idx_scales[t];
+    if (lane == 0) {
+      if (L.key_format == DSA_KEY_INT8)                // binary16 scales
+        reinterpret_cast<uint16_t*>(L.index_scales)[slot] = reinterpret_cast<const uint16_t*>(L.k_idx_scales)[t];
+      else
+        L.index_scales[slot] = L.k_idx_scales[t];
+    }
     return;
   }
-  // quantise a bf16 key into e4m3: scale = amax / 448 (1 if amax = 0), code = rne_satfinite(x / scale)
   const uint2 raw = reinterpret_cast<const uint2*>(L.k_idx)[(int64_t)t * 32 + lane];   // 4 bf16 per lane
   float x[4];
   {
@@ -85,6 +91,25 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendArgs a) {
   float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (L.key_format == DSA_KEY_INT8) {
+    // quantise into int8 with a binary16 scale: scale = half(amax / 127) (nearest-even, held at
+    // 65504 above and at the smallest positive half 2^-24 below; 1 if amax = 0), code =
+    // rne(x / scale) with the stored scale, clamped to [-127, 127]
+    uint16_t hb = __half_as_ushort(__float2half_rn(fminf(__fdiv_rn(amax, 127.0f), 65504.0f)));
+    if (!(amax > 0.f)) hb = 0x3C00;
+    else if (hb == 0) hb = 1;
+    const float scale = __half2float(__ushort_as_half(hb));
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float c = fminf(fmaxf(rintf(__fdiv_rn(x[i], scale)), -127.0f), 127.0f);
+      packed |= ((uint32_t)(int)c & 0xFFu) << (8 * i);
+    }
+    reinterpret_cast<uint32_t*>(L.index_keys)[slot * 32 + lane] = packed;
+    if (lane == 0) reinterpret_cast<uint16_t*>(L.index_scales)[slot] = hb;
+    return;
+  }
+  // quantise a bf16 key into e4m3: scale = amax / 448 (1 if amax = 0), code = rne_satfinite(x / scale)
   const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
   uint32_t packed = 0;
 #pragma unroll

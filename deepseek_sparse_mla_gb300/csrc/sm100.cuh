@@ -20,6 +20,7 @@ enum : uint32_t {
   kErrTmaTimeout = 1u << 0,
   kErrMmaTimeout = 1u << 1,
   kErrBadPage = 1u << 2,
+  kErrConfig = 1u << 3,     // a kernel was launched with a shape it cannot hold (the host prevents it)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -79,7 +79,10 @@ typedef enum {
 
 typedef enum {
   DSA_KEY_BF16 = 0,     /* index keys stored as bf16 [.., 128]                        */
-  DSA_KEY_FP8_E4M3 = 1  /* index keys stored as e4m3 codes [.., 128] + fp32 scale per token */
+  DSA_KEY_FP8_E4M3 = 1, /* index keys stored as e4m3 codes [.., 128] + fp32 scale per token */
+  DSA_KEY_INT8 = 2      /* index keys stored as int8 codes [.., 128] + binary16 scale per token
+                           ("GLM-5.2 on vLLM Ascend", section 7 and "Quantization and Hardware
+                           Branches": INT8 indexer keys with FP16 scales)                    */
 } dsa_key_format;
 
 typedef enum {
@@ -97,11 +100,12 @@ typedef enum {
  *   latent_scales [num_pages, page_size] fp32, DSA_LATENT_E4M3 only: c_KV = code * scale, with
  *                scale = amax(c_KV) / 448 per token (1 if amax = 0) as written by dsa_kv_append;
  *                NULL otherwise.
- *   index_keys   [num_pages, page_size, 128] bf16 or e4m3 codes; only on a layer that owns
- *                an indexer.  NULL on an IndexShare (shared) layer, which keeps only its
- *                latent pages and reuses the owner's index buffer.
- *   index_scales [num_pages, page_size] fp32, e4m3 keys only (dequantised key = code * scale);
- *                NULL otherwise.
+ *   index_keys   [num_pages, page_size, 128] bf16, e4m3 codes or int8 codes; only on a layer
+ *                that owns an indexer.  NULL on an IndexShare (shared) layer, which keeps only
+ *                its latent pages and reuses the owner's index buffer.
+ *   index_scales [num_pages, page_size] per-token scales (dequantised key = code * scale):
+ *                fp32 for e4m3 keys; IEEE binary16 for int8 keys (the pointer then addresses
+ *                2-byte halves despite its type); NULL for bf16 keys.
  * Token s of request b is stored at slot block_table[b][s / page_size] * page_size
  * + s % page_size ("GLM-5.2 on vLLM Ascend", section 8: the slot mapping scatters new
  * latent KV and indexer keys into their physical cache pages).
@@ -153,7 +157,7 @@ DSA_API uint64_t dsa_kernel_launches(void);
 
 /*
  * Bytes of one layer's caches: latent pages, plus for an owner layer (owner != 0) the index
- * keys and, for e4m3 keys, their fp32 scales.  Counting the indexer keys matters: leaving
+ * keys and, for e4m3 / int8 keys, their fp32 / binary16 scales.  Counting the indexer keys matters: leaving
  * them out of admission left memory unbudgeted ("Making GLM-5.2 Sparse on TPUs", "Use
  * independent oracles and test the tests").  Returns 0 for invalid arguments.
  */
@@ -182,9 +186,14 @@ DSA_API size_t dsa_mla_workspace_bytes(int32_t num_rows, int32_t topk);
  *                 has index_keys, rejected when it has none.  k_idx_format says how it is
  *                 stored: DSA_KEY_BF16 (copied to a bf16 cache, or quantised into an e4m3
  *                 cache: scale = amax / 448 in fp32, or 1 if amax = 0; code =
- *                 round-to-nearest-even, saturating e4m3 of x / scale in IEEE fp32) or
- *                 DSA_KEY_FP8_E4M3 (pre-quantised codes, copied with k_idx_scales [num_tokens]
- *                 fp32 into an e4m3 cache).
+ *                 round-to-nearest-even, saturating e4m3 of x / scale in IEEE fp32; or into
+ *                 an int8 cache: scale = the fp32 quotient amax / 127 rounded to binary16
+ *                 (nearest-even, at most 65504, at least 2^-24; 1 if amax = 0), code =
+ *                 round-to-nearest-even of x / scale in IEEE fp32 with the stored scale,
+ *                 clamped to [-127, 127]), DSA_KEY_FP8_E4M3 (pre-quantised codes, copied with
+ *                 k_idx_scales [num_tokens] fp32 into an e4m3 cache) or DSA_KEY_INT8
+ *                 (pre-quantised codes, copied with k_idx_scales [num_tokens] binary16 into an
+ *                 int8 cache).
  *   slot_mapping  device int64 [num_tokens]: physical slot (page * page_size + offset) of each
  *                 token; a negative slot skips that token, as does one >= num_pages*page_size.
  * Rows are copied bit-exactly.  num_tokens = 0 is a no-op.
@@ -214,7 +223,8 @@ DSA_API dsa_status dsa_kv_append_layers(const dsa_cache* caches, int32_t num_lay
  * ("vLLM Inference Path", "DSA Indexer"; "Making GLM-5.2 Sparse on TPUs", "Separate the indexer
  * from the attention it controls".)
  *   I(r, s) = sum_{h<32} w[r,h] * max(0, sum_{d<128} q_idx[r,h,d] * K[s,d])  for 0 <= s <= pos(r),
- *   K[s] = bf16 key, or e4m3 code * scale[s].
+ *   K[s] = bf16 key, or e4m3 / int8 code * scale[s].  int8 codes are split exactly on chip into
+ *   two e4m3 terms (sm_103a has no integer MMA), so every key format runs on the tensor cores.
  *   topk_idx[r] = the topk positions with the largest I (ties: smaller position first), sorted
  *   ascending; every visible position when pos(r) + 1 <= topk; padded with -1.
  *   owner       cache of the indexer-owning layer (index_keys must be non-NULL).

@@ -153,10 +153,12 @@ def check_cache_bytes(gp: GpuProblem, hp: HostProblem):
         else:
             assert np.array_equal(wlm.torch_to_bits(g.latent), h.latent), f"latent pages differ (layer {layer})"
         if h.index_keys is not None:
-            gk = g.index_keys.cpu().numpy() if g.index_keys.dtype == torch.uint8 else wlm.torch_to_bits(g.index_keys)
+            gk = (g.index_keys.cpu().numpy() if g.index_keys.dtype in (torch.uint8, torch.int8)
+                  else wlm.torch_to_bits(g.index_keys))
             assert np.array_equal(gk, h.index_keys), "index-key pages differ"
-            if h.index_scales is not None:
-                assert np.array_equal(g.index_scales.cpu().numpy().view(np.uint32), h.index_scales.view(np.uint32)), \
+            if h.index_scales is not None:          # fp32 scales (e4m3 keys) or binary16 bits (int8 keys)
+                bits = np.uint16 if h.index_scales.dtype == np.uint16 else np.uint32
+                assert np.array_equal(g.index_scales.cpu().numpy().view(bits), h.index_scales.view(bits)), \
                     "index scales differ"
 
 

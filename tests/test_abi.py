@@ -68,6 +68,8 @@ def test_cache_bytes_counts_index_keys_and_scales(lib):
     assert lib.dsa_cache_bytes(pages, P, 1, 0, 1) == pages * P * (512 + 128 + 4)
     assert lib.dsa_cache_bytes(pages, P, 1, 1, 1) == pages * P * (512 + 128 + 4 + 128 + 4)
     assert lib.dsa_cache_bytes(pages, P, 1, 1, 5) == 0
+    # int8 index keys: 128 codes + a 2-byte binary16 scale per slot
+    assert lib.dsa_cache_bytes(pages, P, 2, 1, 0) == latent + pages * P * (128 + 2)
 
 
 def test_workspace_sizes_depend_only_on_shape(lib):
@@ -106,6 +108,22 @@ def test_append_rejects_bad_arguments(lib):
     assert lib.dsa_kv_append(ctypes.byref(bad_layout), P(A), P(A), P(A), 0, None, P(A), T, None) == INVALID
     assert "not interchangeable" in _err(lib)
     assert lib.dsa_kv_append(ctypes.byref(c), P(A), P(A), P(A), 0, None, P(A), 0, None) == 0   # empty: no-op
+
+
+def test_int8_keys_are_checked(lib):
+    T, P = 4, ctypes.c_void_p
+    int8_cache = _cache(fmt=2)
+    assert lib.dsa_kv_append(ctypes.byref(int8_cache), P(A), P(A), P(A), 0, None, P(A), 0, None) == 0
+    no_scales = _cache(scales=0, fmt=2)                                 # int8 keys need their half scales
+    assert lib.dsa_kv_append(ctypes.byref(no_scales), P(A), P(A), P(A), 0, None, P(A), T, None) == INVALID
+    assert "int8 index keys need" in _err(lib)
+    # pre-quantised codes only go into a cache of their own format, with their scales
+    assert lib.dsa_kv_append(ctypes.byref(int8_cache), P(A), P(A), P(A), 1, P(A), P(A), T, None) == INVALID
+    fp8_cache = _cache(fmt=1)
+    assert lib.dsa_kv_append(ctypes.byref(fp8_cache), P(A), P(A), P(A), 2, P(A), P(A), T, None) == INVALID
+    assert lib.dsa_kv_append(ctypes.byref(int8_cache), P(A), P(A), P(A), 2, None, P(A), T, None) == INVALID
+    assert lib.dsa_kv_append(ctypes.byref(int8_cache), P(A), P(A), P(A), 2, P(A + 1), P(A), T, None) == INVALID
+    assert lib.dsa_kv_append(ctypes.byref(_cache(fmt=3)), P(A), P(A), P(A), 0, None, P(A), T, None) == INVALID
 
 
 def test_indexer_rejects_bad_arguments(lib):

@@ -46,7 +46,7 @@ class Workload:
     seq_lens: list            # L_b: KV length of request b after this step's append
     q_lens: list              # query rows of request b (1 = decode)
     page_size: int
-    key_format: str           # "bf16" | "fp8"
+    key_format: str           # "bf16" | "fp8" | "int8"
     topk: int
     layers: int               # attention calls per step: 1 owner + (layers-1) IndexShare layers
     seed: int
@@ -109,7 +109,7 @@ class Workload:
 
     # ---- algorithmic sizes (bytes the step must move) -----------------------
     def key_bytes_per_token(self) -> int:
-        return D_I * 2 if self.key_format == "bf16" else D_I + 4
+        return {"bf16": D_I * 2, "fp8": D_I + 4, "int8": D_I + 2}[self.key_format]
 
     def summary(self) -> dict:
         return {"workload": self.name, "requests": self.num_requests, "rows": self.num_rows,
