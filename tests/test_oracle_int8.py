@@ -102,6 +102,18 @@ def test_round_trip_is_within_half_a_code_step():
     assert codes.min() >= -127
 
 
+def test_every_int8_code_splits_into_two_exact_e4m3_terms():
+    """The GPU reads int8 keys as hi + lo with hi = e4m3(v) (nearest-even) and lo = v - hi: for every code
+    both terms are exact e4m3 values, so the two MMA chains sum to v exactly; int8 values are also bf16 values."""
+    v = np.arange(-127, 128, dtype=np.float32)
+    hi = o.e4m3_to_f64(o.f32_to_e4m3(v))
+    lo = v - hi
+    assert np.array_equal(o.e4m3_to_f64(o.f32_to_e4m3(lo.astype(np.float32))), lo)
+    assert np.array_equal(hi + lo, v) and np.abs(lo).max() == 4.0
+    assert all(brute.e4m3_value(brute.e4m3_encode(float(x))) == x for x in hi)      # hi exact by exhaustive search
+    assert np.array_equal(o.bf16_to_f64(wlm.bf16_bits(v)), v)
+
+
 def _brute_row_int8(case, r, b, pos):
     q = [[brute.bf16(x) for x in h] for h in case.q_idx[r]]
     w = [float(x) for x in case.w[r]]
