@@ -64,6 +64,35 @@ def test_union_and_membership_against_loops():
         assert np.all(m.sum(axis=1) == [(np.asarray(p) >= 0).sum() for p in lists])
 
 
+def test_locality_shaped_selections_reach_the_pages_regime():
+    """Nearby rows whose page preferences mostly agree (workloads.locality_page_scores) select their top
+    Kp pages with the oracle's page budget: at the calibrated noise the union is about the page's 69 of
+    880 and the ratios about its 29.7x and 2.16x; no noise gives one shared selection (QB x fewer loads);
+    very large noise tends to the uniform-random closed form; the union never exceeds its capacity."""
+    import workloads as wlm
+    g = _golden()
+    qb, kp, n = int(g["qb"]), int(g["kp"]), int(g["random_pages"])
+
+    def unions(noise, seeds):
+        out = []
+        for seed in seeds:
+            sc = wlm.locality_page_scores(qb, n, noise, seed)
+            u = o.page_union([o.page_topk_select(sc[q], kp) for q in range(qb)])
+            assert len(u) <= o.union_capacity(qb, kp, n)
+            out.append(len(u))
+        return np.asarray(out, dtype=float)
+
+    u = unions(0.17, range(30)).mean()
+    assert abs(u - g["union"]) <= 0.1 * g["union"]
+    assert abs(o.page_load_reduction(qb, kp, u) - g["page_load_reduction"]) <= 0.1 * g["page_load_reduction"]
+    assert abs(o.score_work_expansion(u, kp) - g["score_work_expansion"]) <= 0.1 * g["score_work_expansion"]
+    assert np.all(unions(0.0, range(3)) == kp) and o.page_load_reduction(qb, kp, kp) == qb
+    means = [unions(s, range(10)).mean() for s in (0.05, 0.17, 1.0)]
+    assert means[0] < means[1] < means[2]
+    closed = n * (1 - (1 - kp / n) ** qb)
+    assert abs(unions(50.0, range(10)).mean() - closed) <= 0.02 * closed
+
+
 def test_identical_and_disjoint_selections_bound_the_ratios():
     kp, qb = 6, 5
     same = [np.arange(kp)] * qb

@@ -207,6 +207,18 @@ def request_index_keys_device(wl: Workload, b: int, device, lo: int = 0, hi: int
     return x[lo:hi].to(torch.bfloat16)
 
 
+def locality_page_scores(qb: int, num_pages: int, noise: float, seed: int) -> np.ndarray:
+    """[qb, num_pages] float64 page scores of qb nearby query rows whose preferences mostly agree: one
+    shared N(0, 1) score per page plus N(0, noise^2) per row.  The locality-shaped selection regime of
+    the query-blocking microbenchmark ("Making GLM-5.2 Sparse on TPUs", "Reuse pages across queries"),
+    for which the pages print no data: noise 0 gives every row the same pages, and large noise tends to
+    uniformly random selections.  At 64 rows, 32 pages per row and 880 pages, noise 0.17 gives a union
+    of about 69 pages, the page's figure."""
+    rng = _rng(seed, _TAG_PAGES, qb, num_pages)
+    shared = rng.standard_normal(num_pages)
+    return shared[None, :] + noise * rng.standard_normal((qb, num_pages))
+
+
 def torch_to_bits(t) -> np.ndarray:
     """bf16 torch tensor -> numpy uint16 bit patterns (host copy)."""
     import torch
