@@ -713,7 +713,7 @@ def main():
                          "page_expand_kernel" if page_mode else
                          "indexer_scores_topk: indexer_groups_kernel + indexer_tc_kernel + topk_chunk_kernel + topk_kernel"),
              "attention": (("sparse_mla.cu",), "sparse_mla_decode: sparse_mla_tc_kernel (clusters merge in shared memory; "
-                                               "mla_merge_kernel when rows are cut between CTAs) + mla_status_kernel"),
+                                               "mla_merge_kernel when rows are cut between CTAs)"),
              "append": (("kv_append.cu",), "kv_append_layers: kv_append_kernel (every layer in one launch)")}
     dom = max(share, key=share.get)
     achieved = bytes_of[dom] / (per_call[dom] * 1e-3) / 1e9

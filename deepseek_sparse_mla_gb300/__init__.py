@@ -19,6 +19,7 @@ import torch
 
 from . import _lib
 from ._lib import DsaError, KEY_BF16, KEY_FP8_E4M3, KEY_INT8  # noqa: F401
+from ._lib import DEVICE_BAD_PAGE, DEVICE_CONFIG, DEVICE_MMA_TIMEOUT, DEVICE_TMA_TIMEOUT  # noqa: F401
 
 INDEX_HEADS, INDEX_DIM, HEADS, LATENT_DIM, ROPE_DIM, ROW_DIM = 32, 128, 64, 512, 64, 576
 DEFAULT_SCALE = 1.0 / 16.0     # 1/sqrt(192 + 64)
@@ -27,7 +28,7 @@ _LATENT_FORMATS = {"bf16": _lib.LATENT_BF16, "fp8": _lib.LATENT_E4M3}
 
 __all__ = ["LayerCache", "Batch", "kv_append", "kv_append_layers", "indexer_scores_topk", "indexer_page_topk", "sparse_mla_decode", "sparse_mla_prefill",
            "cache_bytes", "indexer_workspace_bytes", "mla_workspace_bytes", "DsaError", "DEFAULT_SCALE",
-           "dcp_candidates", "dcp_select", "dcp_merge"]
+           "dcp_candidates", "dcp_select", "dcp_merge", "read_status"]
 
 
 def _ptr(t):
@@ -136,6 +137,25 @@ def _workspace(nbytes, device):
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
+def read_status(workspace=None, stream=None, device=None) -> int:
+    """The DSA_DEVICE_* bits of the last call that used `workspace` (None: the static scratch of
+    dsa_indexer_scores_topk_static on the current device); 0 means no device-side problem.
+    Synchronises the stream to read the value."""
+    dev = workspace.device if workspace is not None else (device or torch.device("cuda", torch.cuda.current_device()))
+    out = torch.zeros(1, dtype=torch.int32, device=dev)
+    _lib.check(_lib.load().dsa_read_status(_ptr(workspace), _ptr(out), _stream(stream)))
+    (stream if stream is not None else torch.cuda.current_stream()).synchronize()
+    return int(out.item()) & 0xFFFFFFFF
+
+
+def _check_device(workspace, stream):
+    """Raise DsaError(DSA_ERR_DEVICE_CHECK) when the call that used `workspace` set device status bits."""
+    bits = read_status(workspace, stream)
+    if bits:
+        lib = _lib.load()
+        raise DsaError(lib.dsa_check_device_status(bits), lib.dsa_last_error().decode())
+
+
 def kv_append(cache: LayerCache, c_kv, k_rope, slot_mapping, k_idx=None, k_idx_scales=None, stream=None):
     """Scatter T new tokens into the layer's pages (bf16 keys are quantised for an fp8 or int8 cache;
     pre-quantised keys are uint8 e4m3 codes with float32 scales, or int8 codes with float16 scales)."""
@@ -181,8 +201,10 @@ def kv_append_layers(caches, c_kv, k_rope, slot_mapping, k_idx=None, stream=None
 
 
 def indexer_scores_topk(owner: LayerCache, batch: Batch, q_idx, w, topk: int, topk_idx=None, scores_out=None,
-                        workspace=None, stream=None):
-    """Lightning-indexer scores and top-k selection; returns the index buffer [R, topk] int32."""
+                        workspace=None, stream=None, check=False):
+    """Lightning-indexer scores and top-k selection; returns the index buffer [R, topk] int32.
+    check=True reads the call's device status afterwards (synchronising) and raises DsaError on a
+    non-zero status."""
     R = batch.num_rows
     _need(q_idx, torch.bfloat16, (R, INDEX_HEADS, INDEX_DIM), "q_idx")
     _need(w, torch.float32, (R, INDEX_HEADS), "w")
@@ -198,11 +220,13 @@ def indexer_scores_topk(owner: LayerCache, batch: Batch, q_idx, w, topk: int, to
     _lib.check(_lib.load().dsa_indexer_scores_topk(ctypes.byref(c), ctypes.byref(b), _ptr(q_idx), _ptr(w), topk,
                                                    _ptr(topk_idx), _ptr(scores_out), _ptr(workspace),
                                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+    if check:
+        _check_device(workspace, stream)
     return topk_idx
 
 
 def indexer_page_topk(owner: LayerCache, batch: Batch, q_idx, w, page_budget: int, page_idx=None, token_idx=None,
-                      expand=True, page_scores_out=None, workspace=None, stream=None):
+                      expand=True, page_scores_out=None, workspace=None, stream=None, check=False):
     """Page-granular selection: page scores (max over visible tokens), the page budget, and (unless
     expand is False) the selected pages' positions.  Returns (page_idx [R, page_budget],
     token_idx [R, page_budget * page_size] or None)."""
@@ -225,10 +249,12 @@ def indexer_page_topk(owner: LayerCache, batch: Batch, q_idx, w, page_budget: in
                                                  _ptr(page_idx), _ptr(token_idx), _ptr(page_scores_out),
                                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
                                                  _stream(stream)))
+    if check:
+        _check_device(workspace, stream)
     return page_idx, token_idx
 
 
-def _sparse_mla(fn, layer, batch, q, topk_idx, scale, out, lse, workspace, stream, row_counts=None):
+def _sparse_mla(fn, layer, batch, q, topk_idx, scale, out, lse, workspace, stream, row_counts=None, check=False):
     R = batch.num_rows
     _need(q, torch.bfloat16, (R, HEADS, ROW_DIM), "q")
     if topk_idx is None:
@@ -251,22 +277,26 @@ def _sparse_mla(fn, layer, batch, q, topk_idx, scale, out, lse, workspace, strea
         _lib.check(_lib.load().dsa_sparse_mla_decode_ragged(
             ctypes.byref(c), ctypes.byref(b), _ptr(q), _ptr(topk_idx), topk, _ptr(row_counts), float(scale), _ptr(out),
             _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    if check:
+        _check_device(workspace, stream)
     return out, lse
 
 
 def sparse_mla_decode(layer: LayerCache, batch: Batch, q, topk_idx, scale: float = DEFAULT_SCALE, out=None, lse=None,
-                      workspace=None, stream=None, row_counts=None):
+                      workspace=None, stream=None, row_counts=None, check=False):
     """Sparse absorbed MLA for decode rows (one per request); returns (out [R,64,512] bf16, lse).
     row_counts (optional int32 [R]): row r's valid entries lead its buffer and entries from
-    row_counts[r] on are -1; the call then spends time only on those leading entries."""
+    row_counts[r] on are -1; the call then spends time only on those leading entries.
+    check=True reads the call's device status afterwards and raises DsaError on a non-zero one."""
     return _sparse_mla(_lib.load().dsa_sparse_mla_decode, layer, batch, q, topk_idx, scale, out, lse, workspace, stream,
-                       row_counts)
+                       row_counts, check)
 
 
 def sparse_mla_prefill(layer: LayerCache, batch: Batch, q, topk_idx, scale: float = DEFAULT_SCALE, out=None, lse=None,
-                       workspace=None, stream=None):
+                       workspace=None, stream=None, check=False):
     """Sparse absorbed MLA for extend/prefill/verify rows (causal per row); returns (out, lse)."""
-    return _sparse_mla(_lib.load().dsa_sparse_mla_prefill, layer, batch, q, topk_idx, scale, out, lse, workspace, stream)
+    return _sparse_mla(_lib.load().dsa_sparse_mla_prefill, layer, batch, q, topk_idx, scale, out, lse, workspace, stream,
+                       check=check)
 
 
 def dcp_candidates(local_scores, local_idx, rank: int, world: int, cand_scores=None, cand_pos=None, stream=None):

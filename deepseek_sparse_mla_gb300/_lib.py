@@ -12,8 +12,11 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdsa.so")
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE, DSA_ERR_CUDA = 0, -1, -2, -3, -4
+DSA_ERR_DEVICE_CHECK = -5
 STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_INVALID_ARG", -2: "DSA_ERR_UNSUPPORTED", -3: "DSA_ERR_WORKSPACE",
-                -4: "DSA_ERR_CUDA"}
+                -4: "DSA_ERR_CUDA", -5: "DSA_ERR_DEVICE_CHECK"}
+# device status bits (dsa_read_status)
+DEVICE_TMA_TIMEOUT, DEVICE_MMA_TIMEOUT, DEVICE_BAD_PAGE, DEVICE_CONFIG = 0x1, 0x2, 0x4, 0x8
 KEY_BF16, KEY_FP8_E4M3, KEY_INT8 = 0, 1, 2
 LATENT_BF16, LATENT_E4M3 = 0, 1
 
@@ -22,7 +25,7 @@ EXPORTS = ("dsa_abi_version", "dsa_last_error", "dsa_kernel_launches", "dsa_cach
            "dsa_mla_workspace_bytes", "dsa_kv_append", "dsa_indexer_scores_topk", "dsa_indexer_scores_topk_static",
            "dsa_indexer_page_workspace_bytes", "dsa_indexer_page_topk", "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill",
            "dsa_dcp_candidates", "dsa_dcp_select", "dsa_dcp_merge", "dsa_sparse_mla_decode_ragged",
-           "dsa_kv_append_layers")
+           "dsa_kv_append_layers", "dsa_read_status", "dsa_check_device_status")
 
 
 class DsaCache(ctypes.Structure):
@@ -61,6 +64,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_last_error.argtypes = []
     lib.dsa_kernel_launches.restype = ctypes.c_uint64
     lib.dsa_kernel_launches.argtypes = []
+    lib.dsa_read_status.restype = I32
+    lib.dsa_read_status.argtypes = [P, P, P]
+    lib.dsa_check_device_status.restype = I32
+    lib.dsa_check_device_status.argtypes = [ctypes.c_uint32]
     lib.dsa_cache_bytes.restype = SZ
     lib.dsa_cache_bytes.argtypes = [I32, I32, I32, I32, I32]
     lib.dsa_indexer_workspace_bytes.restype = SZ

@@ -40,6 +40,19 @@ static dsa_status cuda_status(cudaError_t e, const char* what) {
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// dsa_read_status: the OR of a workspace header's call-wide word and its per-CTA words (one warp).
+__global__ void __launch_bounds__(32) status_read_kernel(const uint32_t* ws, uint32_t* out) {
+  pdl_wait();
+  pdl_trigger();
+  const uint32_t n = min(__ldcg(ws + 1), (uint32_t)kMlaCtas);
+  uint32_t bits = threadIdx.x == 0 ? __ldcg(ws) : 0u;
+  for (uint32_t c = threadIdx.x; c < n; c += 32) bits |= __ldcg(ws + kStatusCtaWords + c);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o);
+  if (threadIdx.x == 0) *out = bits;
+}
+
 static bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 IndexerPlan plan_indexer(int num_rows, int max_seq_len, int topk) {
@@ -165,6 +178,46 @@ extern "C" {
 int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
 
 const char* dsa_last_error(void) { return g_last_error.c_str(); }
+
+dsa_status dsa_read_status(const void* workspace, uint32_t* status_out, void* stream) {
+  if (!status_out) return fail(DSA_ERR_INVALID_ARG, "status_out is NULL");
+  if (reinterpret_cast<uintptr_t>(status_out) & 3u) return fail(DSA_ERR_INVALID_ARG, "status_out is not 4-byte aligned");
+  const void* ws = workspace;
+  if (!ws) {
+    void* scratch = nullptr;
+    const dsa_status st = static_scratch_of_current_device(&scratch);
+    if (st != DSA_OK) return st;
+    ws = scratch;
+  } else if (reinterpret_cast<uintptr_t>(ws) & 255u) {
+    return fail(DSA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  }
+  cudaError_t e = launch_pdl(status_read_kernel, dim3(1), dim3(32), 0, (cudaStream_t)stream,
+                             static_cast<const uint32_t*>(ws), status_out);
+  count_launches(1);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_status(e, "status read launch");
+}
+
+dsa_status dsa_check_device_status(uint32_t bits) {
+  if (bits == 0) return DSA_OK;
+  std::string names;
+  const struct { uint32_t bit; const char* name; } known[] = {
+      {DSA_DEVICE_TMA_TIMEOUT, "DSA_DEVICE_TMA_TIMEOUT"}, {DSA_DEVICE_MMA_TIMEOUT, "DSA_DEVICE_MMA_TIMEOUT"},
+      {DSA_DEVICE_BAD_PAGE, "DSA_DEVICE_BAD_PAGE"}, {DSA_DEVICE_CONFIG, "DSA_DEVICE_CONFIG"}};
+  uint32_t rest = bits;
+  for (const auto& k : known)
+    if (bits & k.bit) {
+      names += names.empty() ? "" : " | ";
+      names += k.name;
+      rest &= ~k.bit;
+    }
+  if (rest) {
+    char buf[32];
+    snprintf(buf, sizeof(buf), "%s0x%x", names.empty() ? "" : " | ", rest);
+    names += buf;
+  }
+  return fail(DSA_ERR_DEVICE_CHECK, "device status 0x%x: %s", bits, names.c_str());
+}
 
 uint64_t dsa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 

@@ -94,6 +94,14 @@ MlaPlan plan_mla(int num_rows, int topk);
 // Counts every kernel launch the library issues (reported by dsa_kernel_launches).
 void count_launches(int n);
 
+// Workspace header (the first kWorkspaceHeader bytes of every workspace, and of the static scratch):
+// word 0 holds the call's call-wide status bits, word 1 the number of per-CTA status words that
+// follow at byte kWorkspaceHeader (attention calls; 0 for the indexer).  dsa_read_status ORs them.
+constexpr int kStatusCtaWords = kWorkspaceHeader / 4;   // index of the first per-CTA word
+
+// Device address of the static scratch array on the current device (looked up on first use).
+dsa_status static_scratch_of_current_device(void** out);
+
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Every kernel of the library is launched as a programmatic
 // dependent of the kernel before it in the stream, so that its launch and its prologue overlap that

@@ -669,9 +669,12 @@ __global__ void __launch_bounds__(1024) indexer_groups_kernel(RowMeta m, int row
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   pdl_wait();
   pdl_trigger();
-  // the call's status word starts at zero: the indexer kernels set bits only after their own wait
-  // on this grid (status is null after the call's first row block)
-  if (status != nullptr && tid == 0) *status = 0u;
+  // the workspace header starts clear: no call-wide bits yet (the indexer kernels set them only after
+  // their own wait on this grid; status is null after the call's first row block) and no per-CTA words
+  if (status != nullptr && tid == 0) {
+    status[0] = 0u;
+    status[1] = 0u;
+  }
   // number of groups: in decode one per row; otherwise walk the requests
   int ngroups = 0;
   if (m.query_start_loc == nullptr) {

@@ -86,8 +86,8 @@ struct MlaArgs {
   float* lse;
   float* part_o;                  // [2 * ctas][64][512]
   float* part_ml;                 // [2 * ctas][64][2]
-  uint32_t* cta_err;              // [ctas]: each CTA's timeout bits (zeroed by the CTA itself)
-  uint32_t* err;                  // the call's status word: the OR of cta_err, written by the merge
+  uint32_t* cta_err;              // [ctas]: each CTA's status bits (zeroed by the CTA itself)
+  uint32_t* err;                  // the workspace header: [0] call-wide bits (0 here), [1] number of cta_err words
 };
 
 __device__ __forceinline__ int unit_start(int c, int units, int ctas) {
@@ -215,9 +215,16 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     u0 = (cta / split) * T + (cta % split) * Tr / split;
     u1 = (cta / split) * T + (cta % split + 1) * Tr / split;
   }
-  // this CTA's timeout bits: cleared after the wait (the previous call's merge has read them) and
-  // before the barrier below, after which a bounded wait may set them
-  if (threadIdx.x == 0) *err = 0u;
+  // this CTA's status bits: cleared after the wait (every earlier kernel of the stream has completed)
+  // and before the barrier below, after which a bounded wait may set them.  CTA 0 also writes the
+  // workspace header: no call-wide bits, and the number of per-CTA words that dsa_read_status ORs.
+  if (threadIdx.x == 0) {
+    *err = 0u;
+    if (cta == 0) {
+      a.err[0] = 0u;
+      a.err[1] = (uint32_t)a.ctas;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -241,7 +248,10 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       const int g = warp + kProducers * (lane >> 2);
       const int t = j * kTok + 4 * g + (lane & 3);
       const int e = (lane < 4 * ng && t < a.topk) ? a.topk_idx[(int64_t)r * a.topk + t] : -1;
-      return (e >= 0 && e <= pos) ? token_slot(a.m, req, e, a.log2_page, a.num_pages) : -1;
+      if (e < 0 || e > pos) return -1;
+      const int64_t slot = token_slot(a.m, req, e, a.log2_page, a.num_pages);
+      if (slot < 0) atomicOr(err, kErrBadPage);    // a visible entry whose page is outside the pool: skipped
+      return slot;
     };
     constexpr int kPieces = kC8 ? 5 : kChunks;        // 128-byte pieces gathered per row
     // the scale of a looked-up entry (packed 8-bit latent; 0 where the entry is invalid)
@@ -819,18 +829,6 @@ __global__ void __launch_bounds__(512, 2) mla_merge_kernel(MlaArgs a) {
   if (a.lse && (tid & 31) == 0) a.lse[(int64_t)r * kHeads + h] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
-// The call's status word: the OR of the attention CTAs' timeout bits (one warp, the call's last
-// kernel; no host reset needed).
-__global__ void __launch_bounds__(32) mla_status_kernel(MlaArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  uint32_t bits = 0;
-  for (int c = threadIdx.x; c < a.ctas; c += 32) bits |= __ldcg(a.cta_err + c);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o);
-  if (threadIdx.x == 0) *a.err = bits;
-}
-
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -950,9 +948,6 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
     count_launches(1);
     if (e != cudaSuccess) return e;
   }
-  e = launch_pdl(mla_status_kernel, dim3(1), dim3(32), 0, s, a);
-  count_launches(1);
-  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -7,16 +7,20 @@
 // launches on it.  Nothing is allocated or freed on any call.
 //
 // Set-up: the first call on a device (with that device current) looks up the array's device
-// address with cudaGetSymbolAddress and keeps it for later calls on that device.  Make that
-// first call before capturing the stream into a graph.
+// address with cudaGetSymbolAddress and keeps it, keyed by the device's current CUDA context,
+// for later calls; a call under another context (after a device reset re-created the primary
+// context, say) looks it up again.  Make that first call before capturing the stream into a graph.
 //
-// Zeroing: only the status word must start at zero; the call's first kernel clears it on the
+// Zeroing: only the status header must start at zero; the call's first kernel clears it on the
 // device, as in the workspace entry point.  The group table, the score block and the top-k
-// candidate lists are fully written before they are read.
+// candidate lists are fully written before they are read.  dsa_read_status(NULL, ...) reads the
+// header's status bits.
 //
 // Concurrency: there is one array per device.  Two calls whose work overlaps on the device
 // (different streams, or different host threads) share it and race; serialise them.
 #include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "dsa_internal.cuh"
 
@@ -29,26 +33,47 @@ static __device__ __align__(256) unsigned char g_indexer_scratch[DSA_STATIC_SCRA
 
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of this device's scratch array, looked up once per device.
-dsa_status scratch_of_current_device(void** out) {
+// The calling thread's current CUDA context (the driver entry point is looked up once).
+CUcontext current_context() {
+  static PFN_cuCtxGetCurrent_v4000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    return cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+                   q == cudaDriverEntryPointSuccess
+               ? reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p)
+               : nullptr;
+  }();
+  CUcontext c = nullptr;
+  if (fn) fn(&c);
+  return c;
+}
+
+}  // namespace
+
+// Device address of this device's scratch array, looked up once per device and context.
+dsa_status static_scratch_of_current_device(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return report_error(DSA_ERR_CUDA, "static scratch: cudaGetDevice failed");
   if (dev < 0 || dev >= kMaxDevices) return report_error(DSA_ERR_UNSUPPORTED, "static scratch: device ordinal >= 64");
+  e = cudaFree(nullptr);                              // make the device's primary context current
+  if (e != cudaSuccess) return report_error(DSA_ERR_CUDA, "static scratch: no CUDA context on the current device");
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> g(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_indexer_scratch);
     if (e != cudaSuccess || p == nullptr)
       return report_error(DSA_ERR_CUDA, "static scratch: cudaGetSymbolAddress of the scratch array failed");
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
   return DSA_OK;
 }
 
-}  // namespace
 }  // namespace dsa
 
 extern "C" {
@@ -65,7 +90,7 @@ dsa_status dsa_indexer_scores_topk_static(const dsa_cache* owner, const dsa_batc
                                "(DSA_STATIC_SCRATCH_BYTES); use dsa_indexer_scores_topk with a caller workspace");
   }
   void* scratch = nullptr;
-  dsa_status st = dsa::scratch_of_current_device(&scratch);
+  dsa_status st = dsa::static_scratch_of_current_device(&scratch);
   if (st != DSA_OK) return st;
   return dsa_indexer_scores_topk(owner, batch, q_idx, w, topk, topk_idx, scores_out, scratch,
                                  (size_t)DSA_STATIC_SCRATCH_BYTES, stream);

@@ -37,6 +37,12 @@
  *   - Device-side metadata (block tables, lengths, slot mappings, indices)
  *     cannot be checked on the host: kernels skip a slot, page id or index
  *     that falls outside its buffer rather than touching memory out of range.
+ *   - Kernels never trap.  Every wait on the device is bounded; a wait that
+ *     runs out, and a visible position whose page id is out of range, set a
+ *     DSA_DEVICE_* bit in the call's workspace instead ("GLM-5.2 on vLLM
+ *     Ascend: Request-to-Backend Inference Path", "Failure and Correctness
+ *     Boundaries": wrong metadata must surface, not silently change results).
+ *     dsa_read_status reads those bits.
  *   - bf16 is IEEE bfloat16; e4m3 is the OCP FP8 E4M3 format.
  *   - All pointers to 16-bit or 8-bit data, and cache.index_scales, must be 16-byte aligned.
  */
@@ -67,15 +73,28 @@ extern "C" {
 #define DSA_MAX_TOPK 8192    /* largest supported top-k budget                   */
 #define DSA_STATIC_SCRATCH_BYTES (16u << 20)  /* scratch of dsa_indexer_scores_topk_static */
 
-#define DSA_ABI_VERSION 2
+#define DSA_ABI_VERSION 3
 
 typedef enum {
   DSA_OK = 0,
   DSA_ERR_INVALID_ARG = -1, /* NULL/unaligned pointer, bad size, incompatible layout */
   DSA_ERR_UNSUPPORTED = -2, /* valid request outside what this build implements     */
   DSA_ERR_WORKSPACE = -3,   /* workspace missing or smaller than the *_workspace_bytes figure */
-  DSA_ERR_CUDA = -4         /* a kernel launch failed                                */
+  DSA_ERR_CUDA = -4,        /* a kernel launch failed                                */
+  DSA_ERR_DEVICE_CHECK = -5 /* a call's device status held DSA_DEVICE_* bits (dsa_check_device_status) */
 } dsa_status;
+
+/* Device status bits of a call (dsa_read_status).  0 means the call ran to completion as specified. */
+#define DSA_DEVICE_TMA_TIMEOUT 0x1u /* a bounded wait for a TMA copy into shared memory ran out; the
+                                       call's outputs are incomplete                                   */
+#define DSA_DEVICE_MMA_TIMEOUT 0x2u /* a bounded wait for tensor-core work or for another warp ran out;
+                                       the call's outputs are incomplete                               */
+#define DSA_DEVICE_BAD_PAGE 0x4u    /* a visible position's page id in block_table was outside
+                                       [0, num_pages), or the table row was shorter than the position
+                                       needs: no kernel reads through it; attention skips such entries,
+                                       and the indexer's scores at those positions are unspecified      */
+#define DSA_DEVICE_CONFIG 0x8u      /* a kernel met a launch shape it cannot hold (the entry points never
+                                       launch one)                                                      */
 
 typedef enum {
   DSA_KEY_BF16 = 0,     /* index keys stored as bf16 [.., 128]                        */
@@ -154,6 +173,28 @@ DSA_API const char* dsa_last_error(void);
 
 /* Number of CUDA kernels this library has launched since it was loaded (all threads). */
 DSA_API uint64_t dsa_kernel_launches(void);
+
+/*
+ * Device status of the last call that used `workspace`: the OR of the DSA_DEVICE_* bits its kernels
+ * set.  workspace is a workspace passed to dsa_indexer_scores_topk, dsa_indexer_page_topk or
+ * dsa_sparse_mla_decode / _decode_ragged / _prefill (the bits live in its first bytes, which every
+ * such call rewrites), or NULL for the static scratch of dsa_indexer_scores_topk_static on the
+ * current device.  ("GLM-5.2 on vLLM Ascend: Request-to-Backend Inference Path", "Failure and
+ * Correctness Boundaries".)
+ *   status_out  4 bytes of device memory, or of page-locked host memory mapped into the device's
+ *               address space (cudaHostAlloc / cudaHostRegister), 4-byte aligned: receives the bits.
+ * Enqueues one small kernel on `stream` after the call it reports on (same stream, or an event
+ * between streams); *status_out is valid once the stream has passed that point.  Allocates nothing,
+ * never synchronises, and may be captured in a graph.  Returns DSA_ERR_INVALID_ARG for a NULL or
+ * misaligned status_out or a workspace not 256-byte aligned, DSA_ERR_CUDA if the launch fails.
+ */
+DSA_API dsa_status dsa_read_status(const void* workspace, uint32_t* status_out, void* stream);
+
+/*
+ * DSA_OK when bits == 0; otherwise DSA_ERR_DEVICE_CHECK, with dsa_last_error() naming the bits
+ * (for example "device status 0x4: DSA_DEVICE_BAD_PAGE").  A host-side helper: no device access.
+ */
+DSA_API dsa_status dsa_check_device_status(uint32_t bits);
 
 /*
  * Bytes of one layer's caches: latent pages, plus for an owner layer (owner != 0) the index
@@ -235,7 +276,8 @@ DSA_API dsa_status dsa_kv_append_layers(const dsa_cache* caches, int32_t num_lay
  *   scores_out  optional device fp32 [num_rows, max_seq_len]: I(r, s) for s <= pos(r), -inf
  *               beyond; NULL to skip.
  *   workspace   device scratch of at least dsa_indexer_workspace_bytes(num_rows, max_seq_len,
- *               topk) bytes, 256-byte aligned.
+ *               topk) bytes, 256-byte aligned; dsa_read_status(workspace, ...) gives the call's device
+ *               status (DSA_DEVICE_BAD_PAGE for an out-of-range page of a visible key).
  */
 DSA_API dsa_status dsa_indexer_scores_topk(const dsa_cache* owner, const dsa_batch* batch, const void* q_idx,
                                    const float* w, int32_t topk, int32_t* topk_idx, float* scores_out,
@@ -267,7 +309,7 @@ DSA_API size_t dsa_indexer_page_workspace_bytes(int32_t num_rows, int32_t max_se
  *   page_scores_out optional device fp32 [num_rows, ceil(max_seq_len / page_size)]: S, -inf beyond
  *                  the row's last page; NULL to skip.
  *   workspace      device scratch of at least dsa_indexer_page_workspace_bytes(...) bytes, 256-byte
- *                  aligned; its first word is the device status word, as for dsa_indexer_scores_topk.
+ *                  aligned; dsa_read_status(workspace, ...) gives the call's device status.
  * The library has no page counterpart of the static-scratch entry point.
  */
 DSA_API dsa_status dsa_indexer_page_topk(const dsa_cache* owner, const dsa_batch* batch, const void* q_idx,
@@ -285,10 +327,11 @@ DSA_API dsa_status dsa_indexer_page_topk(const dsa_cache* owner, const dsa_batch
  *     exceeds it return DSA_ERR_WORKSPACE before anything is launched (for example, with topk
  *     2048, 32 rows of 90,000 keys or 64 rows of 40,000 keys fit; 64 rows of 131,072 keys do not).
  *   Set-up: the first call on a device, made with that device current, looks the array up
- *     (cudaGetSymbolAddress) and keeps its address; make that first call before capturing the
- *     stream.  A failed look-up returns DSA_ERR_CUDA.
- *   Zeroing: the call's first kernel clears the array's status word; nothing else in it needs
- *     to start at zero.
+ *     (cudaGetSymbolAddress) and keeps its address for that device's current CUDA context (a new
+ *     context, after a device reset say, looks it up again); make that first call before capturing
+ *     the stream.  A failed look-up returns DSA_ERR_CUDA.
+ *   Zeroing: the call's first kernel clears the array's status header; nothing else in it needs
+ *     to start at zero.  dsa_read_status(NULL, ...) reads the last call's device status.
  *   Concurrency: calls whose work overlaps on one device share the array and race; the caller
  *     serialises them (one stream, or an event between streams).
  */
@@ -317,7 +360,9 @@ DSA_API dsa_status dsa_indexer_scores_topk_static(const dsa_cache* owner, const 
  *             Correctness Boundaries": a shared layer without the shared buffer is rejected).
  *   scale     softmax scale, normally 1/sqrt(192 + 64) = 1/16.
  *   out       device bf16 [num_rows, 64, 512];  lse: optional device fp32 [num_rows, 64].
- *   workspace device scratch of at least dsa_mla_workspace_bytes(num_rows, topk) bytes.
+ *   workspace device scratch of at least dsa_mla_workspace_bytes(num_rows, topk) bytes, 256-byte
+ *             aligned; dsa_read_status(workspace, ...) gives the call's device status
+ *             (DSA_DEVICE_BAD_PAGE for a valid entry whose page id is out of range).
  */
 DSA_API dsa_status dsa_sparse_mla_decode(const dsa_cache* layer, const dsa_batch* batch, const void* q,
                                  const int32_t* topk_idx, int32_t topk, float scale, void* out, float* lse,

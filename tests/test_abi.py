@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in declared():
         assert hasattr(lib, n), n
     assert set(declared()) == set(_lib.EXPORTS)
-    assert lib.dsa_abi_version() == 2
+    assert lib.dsa_abi_version() == 3
 
 
 def test_missing_library_fails_loudly(tmp_path):
@@ -250,3 +250,18 @@ def test_multi_layer_append_rejects_bad_arguments(lib):
     assert lib.dsa_kv_append_layers(two, 2, arr(A, A), arr(A, A), arr(A, A), 0, None, P(A), 8, None) == INVALID
     assert "layer 1" in _err(lib)
     assert lib.dsa_kv_append_layers(two, 2, arr(A, A), arr(A, A + 8), arr(A, None), 0, None, P(A), 8, None) == INVALID
+
+
+def test_device_status_helpers(lib):
+    """dsa_check_device_status names the bits; dsa_read_status validates its arguments before any launch."""
+    assert lib.dsa_check_device_status(0) == 0
+    assert lib.dsa_check_device_status(0x4) == -5
+    assert "DSA_DEVICE_BAD_PAGE" in _err(lib)
+    assert lib.dsa_check_device_status(0x3) == -5
+    msg = _err(lib)
+    assert "DSA_DEVICE_TMA_TIMEOUT" in msg and "DSA_DEVICE_MMA_TIMEOUT" in msg
+    assert lib.dsa_check_device_status(0x30) == -5 and "0x30" in _err(lib)
+    P = ctypes.c_void_p
+    assert lib.dsa_read_status(P(A), None, None) == INVALID
+    assert lib.dsa_read_status(P(A), P(A + 2), None) == INVALID           # misaligned output word
+    assert lib.dsa_read_status(P(A + 16), P(A), None) == INVALID          # workspace not 256-byte aligned
