@@ -23,20 +23,20 @@
 //
 // Per CTA (persistent, one per SM, 448 threads), over one contiguous range of
 // the flattened (group, key tile) list:
-//   warps 0-2  producers, tiles round-robin: page lookups from a register
+//   warps 0-5  producers, tiles round-robin: page lookups from a register
 //              window of the block table, TMA loads of the key pages into a
 //              ring of 16 KB (e4m3) or 32 KB (bf16) stages, and bulk copies of
 //              the keys' fp32 scales into a separate ring of scale slots;
-//   warps 3-4  MMA issuers, even and odd tiles; a commit frees the key stage;
-//   warp 5     B loader: each group's queries (split into e4m3 terms, or bf16)
+//   warps 6-7  MMA issuers, even and odd tiles; a commit frees the key stage;
+//   warp 8     B loader: each group's queries (split into e4m3 terms, or bf16)
 //              into the B operand, 128-byte swizzled, K-major;
-//   warps 6-13 two epilogue warpgroups, even and odd tiles (fed by the
+//   warps 9-16 two epilogue warpgroups, even and odd tiles (fed by the
 //              matching issuer); the one that reads a tile's scales frees
 //              its scale slot;
-//   warps 14-16 (int8 keys only) converters, tile i by warp i % 3, each with
+//   warps 17-19 (int8 keys only) converters, tile i by warp i % 3, each with
 //              its own lo tile that the MMA of its previous tile releases.
-// The key ring holds up to 6 stages: enough bytes in flight to cover HBM
-// latency, few enough not to congest the memory system.
+// The key ring holds up to 8 stages (6 with int8 keys): enough bytes in flight
+// to cover HBM latency, few enough not to congest the memory system.
 #include <mutex>
 #include <type_traits>
 
@@ -51,7 +51,7 @@ using namespace sm100;
 
 namespace idx {
 constexpr int kTileKeys = 128;
-constexpr int kProducers = 3;                      // warps issuing the key copies (TMA issue is per-warp limited)
+constexpr int kProducers = 6;                      // warps issuing the key copies, tiles round-robin (at most the stages)
 constexpr int kMmaWarps = 2;                       // MMA issuers: even and odd tiles
 constexpr int kThreads = 32 * (kProducers + kMmaWarps + 1 + 8);  // producers, MMA, B loader, two epilogue warpgroups
 constexpr int kConvWarps = 3;                      // int8 keys: tile converters (a divisor of the 6 key stages)
@@ -62,9 +62,9 @@ constexpr int kBBytes = 65536;                      // B operand at most: 256 (r
 // Dynamic shared memory: [B buffers | key-scale ring | key ring].  The B buffers take only what the
 // group size needs (16 KB in decode), and the key ring gets the rest, up to kMaxStages stages.
 constexpr int kSmemBytes = 200 * 1024;
-// More key stages in flight than this only lengthen the memory system's queues: across 152 SMs,
-// 6 stages of 16 KB measured 3 % faster than 10 and 12 % faster than 4.
-constexpr int kMaxStages = 6;
+// Key stages in flight (16 KB e4m3 or 32 KB bf16).  With 6 producer warps, 8 stages of 16 KB
+// measured 3.5 % faster than 3 producers over 6 stages, and 10 stages no faster than 8.
+constexpr int kMaxStages = 8;
 constexpr int kScStages = 16;                       // key-scale ring (e4m3): 16 tiles x 128 fp32
 constexpr int kScRingBytes = kScStages * 128 * 4;   // fp32 scales (e4m3 keys); binary16 scales take half
 static_assert((kScStages & (kScStages - 1)) == 0 && kScStages >= kMaxStages + 4, "scale ring: power of two, deep");
@@ -305,6 +305,7 @@ __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 
     const bool windowed = loads_per_tile <= 32;
     TileCursor cur;
     cursor_init(cur, a, gcache, tcache, ngroups, tau0, tau1);
+    const uint64_t key_policy = l2_evict_first();
     int win_base = -1, win_req = -1, win_page = -1, nxt_page = -1;
     int last_tile = -1;
     // ring positions of tile i, stepped once per tile (no division on the issue path)
@@ -398,8 +399,8 @@ __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 
         if (page < 0) continue;
         const int key = k0 + j * a.box_rows;
         const int y = (page << a.log2_page) + (key & ((1 << a.log2_page) - 1));
-        tma_load_2d_hint(stage + j * box_bytes, &key_map, 0, y, &st_full[s], l2_evict_first());
-        if (!kFp8) tma_load_2d_hint(stage + 16384 + j * box_bytes, &key_map, 64, y, &st_full[s], l2_evict_first());
+        tma_load_2d_hint(stage + j * box_bytes, &key_map, 0, y, &st_full[s], key_policy);
+        if (!kFp8) tma_load_2d_hint(stage + 16384 + j * box_bytes, &key_map, 64, y, &st_full[s], key_policy);
         if (bulk_scales)
           bulk_load(sc + j * a.box_rows, key_scales + y, (uint32_t)a.box_rows * (uint32_t)sizeof(ScaleT), &sc_full[sci]);
       }
