@@ -46,7 +46,7 @@ class DeviceProblem:
     prefix (drawn on the device with torch's seeded generator and appended through the
     library), and the step's inputs (new tokens, queries, metadata) are on the device."""
 
-    def __init__(self, wl: wlm.Workload, device="cuda", selection="token"):
+    def __init__(self, wl: wlm.Workload, device="cuda", selection="token", locality_noise=0.17):
         import torch
         import deepseek_sparse_mla_gb300 as dsa
         self.wl, self.dev, self.selection = wl, device, selection
@@ -87,6 +87,9 @@ class DeviceProblem:
         self.ws_idx = torch.empty(dsa.indexer_workspace_bytes(R, wl.max_seq_len, wl.topk), dtype=torch.uint8,
                                   device=device)
         self.ws_mla = torch.empty(dsa.mla_workspace_bytes(R, wl.topk), dtype=torch.uint8, device=device)
+        self.loc_idx = None
+        if selection == "locality":
+            self.loc_idx = torch.from_numpy(locality_selection(wl, locality_noise)).to(device)
         if selection == "page":
             # page-granular selection: topk / page_size pages, expanded into the same-size index buffer
             self.page_budget = wl.topk // wl.page_size
@@ -97,17 +100,21 @@ class DeviceProblem:
                                        dtype=torch.uint8, device=device)
         torch.cuda.synchronize()
 
-    def step(self, marks=None, io=None):
+    def step(self, marks=None, io=None, calls=None):
         """One DSA step of the layer group on the current stream.  io: the set of per-step inputs
-        and outputs to use (this object's own by default, or one made by io_set())."""
+        and outputs to use (this object's own by default, or one made by io_set()).  calls: issue only
+        the step's first `calls` library calls (append, indexer, then one attention call per layer)."""
         import deepseek_sparse_mla_gb300 as dsa
         wl = self.wl
         io = self if io is None else io
+        n_calls = 2 + wl.layers if calls is None else calls
         mla = dsa.sparse_mla_decode if wl.is_decode else dsa.sparse_mla_prefill
         if marks is not None:
             marks.mark("append")
         dsa.kv_append_layers(self.caches, io.new_c, io.new_r, io.slots,
                              k_idx=[io.new_k] + [None] * (wl.layers - 1))
+        if n_calls < 2:
+            return
         if marks is not None:
             marks.mark("indexer")
         if self.selection == "page":
@@ -116,10 +123,11 @@ class DeviceProblem:
         else:
             dsa.indexer_scores_topk(self.caches[0], io.batch, io.q_idx, io.w, wl.topk, topk_idx=self.topk_idx,
                                     workspace=self.ws_idx)
-        for l in range(wl.layers):
+        idx = self.topk_idx if self.loc_idx is None else self.loc_idx
+        for l in range(min(wl.layers, n_calls - 2)):
             if marks is not None:
                 marks.mark("attention")
-            mla(self.caches[l], io.batch, io.q[l], self.topk_idx, wl.scale, out=io.out[l], lse=io.lse[l],
+            mla(self.caches[l], io.batch, io.q[l], idx, wl.scale, out=io.out[l], lse=io.lse[l],
                 workspace=self.ws_mla)
         if marks is not None:
             marks.mark(None)
@@ -163,23 +171,65 @@ class DeviceProblem:
                              max_seq_len=self.wl.max_seq_len)
 
 
-def capture_step(prob, lib, io=None):
-    """The step captured once into a CUDA graph (the library's calls allocate nothing and never
-    synchronise, so they capture as they are, programmatic launch edges included).  Returns the
-    graph and the number of the library's kernels one replay runs."""
+def capture_step(prob, lib, io=None, calls=None):
+    """The step (or its first `calls` library calls) captured once into a CUDA graph (the library's
+    calls allocate nothing and never synchronise, so they capture as they are, programmatic launch
+    edges included).  Returns the graph and the number of the library's kernels one replay runs."""
     import torch
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
-        prob.step(io=io)                                 # a first run outside the capture
+        prob.step(io=io, calls=calls)                    # a first run outside the capture
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     n0 = lib.dsa_kernel_launches()
     with torch.cuda.graph(g):
-        prob.step(io=io)
+        prob.step(io=io, calls=calls)
     torch.cuda.synchronize()
     return g, int(lib.dsa_kernel_launches() - n0)
+
+
+def replay_ms(graph, reps=30, warm=5):
+    """Mean device time of one replay of `graph` (CUDA events on the current stream, back to back)."""
+    import torch
+    for _ in range(warm):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def locality_selection(wl: wlm.Workload, noise: float) -> np.ndarray:
+    """Index buffer [R, topk] of locality-shaped page selections: the rows of a request, in blocks of up
+    to 64, rank its pages by one shared N(0, 1) score per page plus N(0, noise^2) per row
+    (workloads.locality_page_scores), and each row keeps the topk / page_size best pages among those it
+    can see, expanded to their visible positions (ascending, -1 padded).  A small noise makes the rows
+    of a block select nearly the same pages ("Making GLM-5.2 Sparse on TPUs", "Reuse pages across
+    queries"); a large one, independent uniformly random pages."""
+    P, k = wl.page_size, wl.topk
+    budget = max(1, k // P)
+    out = np.full((wl.num_rows, k), -1, dtype=np.int32)
+    pos = wl.row_position()
+    r0 = 0
+    for b, (L, q) in enumerate(zip(wl.seq_lens, wl.q_lens)):
+        pages = -(-L // P)
+        for blk in range(0, q, 64):
+            rows = range(r0 + blk, r0 + min(q, blk + 64))
+            sc = wlm.locality_page_scores(len(rows), pages, noise, wl.seed * 1000 + b * 64 + blk // 64)
+            for i, r in enumerate(rows):
+                vis = int(pos[r]) // P + 1                       # pages holding a visible position
+                keep = np.sort(np.argsort(-sc[i, :vis], kind="stable")[:budget])
+                toks = (keep[:, None] * P + np.arange(P)).ravel()
+                toks = toks[toks <= pos[r]][:k]
+                out[r, :toks.size] = toks
+        r0 += q
+    return out
 
 
 def torch_empty_like(t):
@@ -479,6 +529,11 @@ def cpu_baseline(wl, device, n_req=64):
 # main arms
 # ---------------------------------------------------------------------------
 def reference_main(args):
+    """The oracle on the host cores, timed as it stands.  Every step (warm-up and timed alike) runs the
+    same stratified sample of the workload's requests (spread over the context lengths) through append,
+    indexer, top-k and every attention layer; the rate counts the layer-steps that sample makes up
+    (a layer-step is one layer's work for the whole batch), so it is not extrapolated from one
+    request.  ms_per_step is the time the sample step took."""
     rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
@@ -487,25 +542,28 @@ def reference_main(args):
     device = "cuda" if torch.cuda.is_available() else "cpu"
     q_idx, w = wlm.indexer_queries(wl)
     qs = [wlm.mla_queries(wl, l) for l in range(wl.layers)]
-    picked = stratified_requests(wl, max(1, args.steps + args.warmup))
+    picked = stratified_requests(wl, min(wl.num_requests, args.reference_requests))
+    probs = [oracle_request_problem(wl, b, device) for b in picked]
     times = []
     for i in range(args.warmup + args.steps):
-        b = picked[i % len(picked)]
-        caches, bt = oracle_request_problem(wl, b, device)
-        t = time_oracle_request(wl, b, caches, bt, q_idx, w, qs)
+        t = sum(time_oracle_request(wl, b, caches, bt, q_idx, w, qs) for b, (caches, bt) in zip(picked, probs))
         if i >= args.warmup:
-            times.append(t * wl.num_requests)        # one request's share, scaled to the whole step
+            times.append(t)
     step_s = float(np.mean(times))
-    value = wl.layers / step_s
+    frac = len(picked) / wl.num_requests                       # share of a full group step one step covers
+    value = wl.layers * frac / step_s
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    sample = (f"each step: float64 numpy oracle on one request of {wl.num_requests} (stratified by context "
-              f"length), append + indexer + top-k + {wl.layers} attention layers, scaled by request count")
+    sample = (f"each step: the float64 numpy oracle on the same {len(picked)} of {wl.num_requests} requests "
+              f"(stratified by context length: {[wl.seq_lens[b] for b in picked]}), append + indexer + top-k + "
+              f"{wl.layers} attention layers; the rate counts the {wl.layers * frac:.3f} layer-steps that "
+              f"sample makes up")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, **{k: v for k, v in wl.summary().items() if k != "workload"}},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "full_group_step_ms_estimate": step_s * 1e3 / frac}
     print(json.dumps(line), flush=True)
 
 
@@ -622,8 +680,16 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wlm.FULL) + sorted(wlm.PROFILE))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--selection", choices=["token", "page"], default="token",
-                    help="token top-k (the method's selection), or page-granular selection of topk / page_size pages")
+    ap.add_argument("--selection", choices=["token", "page", "locality"], default="token",
+                    help="token top-k (the method's selection), page-granular selection of topk / page_size "
+                         "pages, or attention over locality-shaped page selections (to measure L2 reuse; the "
+                         "indexer still runs)")
+    ap.add_argument("--locality-noise", type=float, default=0.17,
+                    help="--selection locality: per-row noise on the shared page scores (large: uniform pages)")
+    ap.add_argument("--reference-requests", type=int, default=8,
+                    help="--impl reference: requests per oracle step (a fixed stratified sample)")
+    ap.add_argument("--sustained-seconds", type=float, default=2.0,
+                    help="length of the sustained replay measurement after the timed region")
     ap.add_argument("--cpu-sample-requests", type=int, default=64)
     ap.add_argument("--eager", action="store_true",
                     help="launch the step call by call instead of replaying it from a CUDA graph")
@@ -652,7 +718,7 @@ def main():
     if args.keys not in ("default", wl.key_format):
         import dataclasses
         wl = dataclasses.replace(wl, name=f"{wl.name}_keys_{args.keys}", key_format=args.keys)
-    prob = DeviceProblem(wl, selection=args.selection)
+    prob = DeviceProblem(wl, selection=args.selection, locality_noise=args.locality_noise)
     page_mode = args.selection == "page"
     lib = _lib.load()
 
@@ -692,14 +758,51 @@ def main():
     ms_per_step = elapsed_ms / args.steps
     value = aggregate_rate(elapsed_ms, world, wl.layers, args.steps)
 
-    # ---- per-call breakdown (events between the library calls) --------------------------
-    marks = Marks()
-    for _ in range(max(3, min(args.steps, 20))):
-        prob.step(marks)
+    # ---- sustained: the same replays for a few seconds, clocks sampled throughout -------------
+    sustained = None
+    if args.sustained_seconds > 0:
+        n_sus = max(args.steps, int(math.ceil(args.sustained_seconds * 1e3 / ms_per_step)))
+        clocks_s = ClockSampler()
+        clocks_s.start()
+        for _ in range(args.warmup):
+            run_step()
         torch.cuda.synchronize()
-        marks.collect()
-    per_call = {k: float(np.mean(v)) for k, v in marks.spans.items()}     # ms per call
-    per_call["append"] /= wl.layers                                         # one span covers every layer's append
+        time.sleep(0.5)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clocks_s.mark_begin()
+        s0.record()
+        for _ in range(n_sus):
+            run_step()
+        s1.record()
+        torch.cuda.synchronize()
+        clocks_s.mark_end()
+        sus_ms = max_over_ranks(s0.elapsed_time(s1), world)
+        sustained = {"value": aggregate_rate(sus_ms, world, wl.layers, n_sus), "unit": UNIT, "steps": n_sus,
+                     "ms_per_step": sus_ms / n_sus, "seconds": sus_ms / 1e3, "clocks": clocks_s.stop()}
+
+    # ---- per-call breakdown ----------------------------------------------------------------
+    # With graph replay: the step's first j library calls captured as graphs of their own; a call's
+    # time is what it adds to the replayed prefix (programmatic-launch overlap with the call before
+    # it included), so the calls' times add up to the replayed step.  Eager: events between calls.
+    per_call = None
+    if graph is not None:
+        try:
+            n_calls = 2 + wl.layers
+            pre = [0.0] + [replay_ms(capture_step(prob, lib, calls=j)[0]) for j in range(1, n_calls + 1)]
+            marg = [pre[j] - pre[j - 1] for j in range(1, n_calls + 1)]
+            per_call = {"append": marg[0] / wl.layers, "indexer": marg[1], "attention": float(np.mean(marg[2:]))}
+            breakdown = "marginal times of the replayed step's call prefixes (CUDA graphs)"
+        except Exception as e:
+            print(f"prefix capture failed ({e}); per-call times from eager calls", file=sys.stderr)
+    if per_call is None:
+        marks = Marks()
+        for _ in range(max(3, min(args.steps, 20))):
+            prob.step(marks)
+            torch.cuda.synchronize()
+            marks.collect()
+        per_call = {k: float(np.mean(v)) for k, v in marks.spans.items()}     # ms per call
+        per_call["append"] /= wl.layers                                         # one span covers every layer's append
+        breakdown = "CUDA events between eager library calls"
     calls = {"append": wl.layers, "indexer": 1, "attention": wl.layers}
     share = {k: per_call[k] * calls[k] for k in per_call}
     tot = sum(share.values())
@@ -801,13 +904,16 @@ def main():
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": wl.name, **{k: v for k, v in summary.items() if k != "workload"},
                            "selection": ("page budget: %d pages of %d positions" % (prob.page_budget, wl.page_size)
-                                         if page_mode else "token top-k"),
+                                         if page_mode else
+                                         ("attention over locality-shaped page selections (noise %g; the indexer "
+                                          "still runs)" % args.locality_noise if args.selection == "locality"
+                                          else "token top-k")),
                            "l2": "no flush: each step reads %.0f MB (> 129 MB L2)" % (alg["step"] / 1e6),
                            "launch": ("the step captured once in a CUDA graph and replayed (%d kernels a step)" % per_step
                                       if graph is not None else "eager: one host call per library call"),
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-                "clocks": clk, "kernels": kernels,
+                "clocks": clk, "sustained": sustained, "kernels": kernels, "kernels_from": breakdown,
                 "step_algorithmic_GBps": step_gbps, "step_frac_of_peak": step_gbps / peak,
                 "step_frac_of_8TBps": step_gbps / 8000.0}
         print(json.dumps(line), flush=True)

@@ -249,3 +249,59 @@ def test_e4m3_scales_of_small_pages():
     four page rows), with ragged lengths that leave part of the last group without a page."""
     run_and_check(wlm.Workload("fp8_p16", [700, 1500, 333], [1, 1, 1], 16, "fp8", 256, 1, 3012))
     run_and_check(wlm.Workload("fp8_p32", [1111, 2050], [1, 1], 32, "fp8", 512, 1, 3013))
+
+
+def _sampled_positions(n):
+    """Positions the top-k sample threshold reads in a row of n >= 4096 scores: 512 runs of 8
+    consecutive scores, run j starting at the multiple of 8 at or below j n / 512."""
+    j = np.arange(512, dtype=np.int64)
+    return ((((j * n) >> 9) & ~7)[:, None] + np.arange(8)).ravel()
+
+
+def _order_key(x):
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return np.where(u & 0x80000000, ~u & 0xFFFFFFFF, u | 0x80000000).astype(np.uint64)
+
+
+@pytest.mark.parametrize("seq_lens", [[20000, 9000], [100000, 70001]])
+def test_planted_sample_pushes_threshold_above_kth_score(seq_lens):
+    """High scores planted exactly on the positions the sample threshold reads put that threshold far
+    above the row's true k-th score, so fewer than k positions clear it and the full-row select runs
+    (rows scanned by one CTA, and rows split into chunks).  Every query head is the unit vector e_0 and
+    the head weights are positive, so a position's score is ReLU(key[0]): a descending ramp on the
+    sampled positions (shuffled over them), -1 elsewhere."""
+    wl = wlm.Workload("planted_sample", list(seq_lens), [1] * len(seq_lens), 64, "bf16", 2048, 1, 3020)
+    hp = HostProblem(wl)
+    rng = np.random.default_rng(3021)
+    for b, L in enumerate(wl.seq_lens):
+        keys = o.bf16_to_f64(hp.keys[b]).astype(np.float32)
+        keys[:, 0] = -1.0
+        sp = _sampled_positions(L)
+        keys[sp, 0] = rng.permutation(np.linspace(1.0, 1000.0, sp.size)).astype(np.float32)
+        hp.keys[b] = wlm.bf16_bits(keys)
+    q = np.zeros((wl.num_rows, 32, 128), dtype=np.float32)
+    q[:, :, 0] = 1.0
+    hp.q_idx = wlm.bf16_bits(q)
+    hp.w = np.full((wl.num_rows, 32), 1.0 / 32, dtype=np.float32)
+    hp.caches[0] = o.PagedCache(wl.num_pages, wl.page_size, wl.key_format)
+    for b, L in enumerate(wl.seq_lens):
+        hp.caches[0].append(hp.latent[0][b][:, :512], hp.latent[0][b][:, 512:], wl.slots(b, np.arange(L)),
+                            k_idx_bits=hp.keys[b])
+    o_idx, o_sc = hp.oracle_topk()
+    # the construction does what it is for: fewer than k positions reach the sample threshold's bin
+    k = wl.topk
+    for r, L in enumerate(wl.seq_lens):
+        samp = np.sort(_order_key(o_sc[r][_sampled_positions(L)]))[::-1]
+        rank = k * 4096 // L
+        margin = 3 * int(np.sqrt(rank + 1.0)) + 8
+        edge = (samp[rank + margin] >> 20) << 20
+        assert np.count_nonzero(_order_key(o_sc[r][:L]) >= edge) < k
+    gp = GpuProblem(hp)
+    gp.append_step()
+    idx, sc = gp.indexer()
+    import torch
+    torch.cuda.synchronize()
+    g_idx, g_sc = idx.cpu().numpy(), sc.cpu().numpy()
+    for r, L in enumerate(wl.seq_lens):
+        check_scores(g_sc[r], o_sc[r], L - 1, wl.max_seq_len)
+        check_topk(g_idx[r], o_idx[r], o_sc[r], L - 1, k)
