@@ -690,6 +690,9 @@ def main():
                     help="--impl reference: requests per oracle step (a fixed stratified sample)")
     ap.add_argument("--sustained-seconds", type=float, default=2.0,
                     help="length of the sustained replay measurement after the timed region")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="for profilers: set up, run this many steps (replayed from the step's graph unless "
+                         "--eager) and exit without timing")
     ap.add_argument("--cpu-sample-requests", type=int, default=64)
     ap.add_argument("--eager", action="store_true",
                     help="launch the step call by call instead of replaying it from a CUDA graph")
@@ -733,6 +736,14 @@ def main():
             print(f"graph capture failed ({e}); timing eager launches", file=sys.stderr)
             graph = None
     run_step = graph.replay if graph is not None else prob.step
+    if args.profile_steps > 0:
+        for _ in range(args.profile_steps):
+            run_step()
+        torch.cuda.synchronize()
+        if rank == 0:
+            print(json.dumps({"profile_steps": args.profile_steps, "workload": wl.name, "kernels_per_step": per_step}),
+                  flush=True)
+        return
     clocks = ClockSampler()
     clocks.start()
     for _ in range(args.warmup):

@@ -198,7 +198,7 @@ __device__ __forceinline__ float scale_value(uint16_t v) { return __half2float(_
 // kKind: 0 bf16 keys, 1 e4m3 keys (fp32 scales), 2 int8 keys (binary16 scales).
 template <int kKind>
 __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 1)
-    indexer_tc_kernel(const __grid_constant__ CUtensorMap key_map, const IdxArgs a) {
+    indexer_tc_kernel(const __grid_constant__ CUtensorMap key_map, const IdxArgs a, int groups_share_keys) {
   using namespace idx;
   constexpr bool kFp8 = kKind != 0;                   // 8-bit keys: the e4m3 MMA path
   constexpr bool kI8 = kKind == 2;
@@ -305,7 +305,9 @@ __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 
     const bool windowed = loads_per_tile <= 32;
     TileCursor cur;
     cursor_init(cur, a, gcache, tcache, ngroups, tau0, tau1);
-    const uint64_t key_policy = l2_evict_first();
+    // keys read by one row group only are evicted first (the score block stays in L2 for the top-k);
+    // keys that a request's other row groups read again keep their normal priority
+    const uint64_t key_policy = groups_share_keys ? l2_evict_normal() : l2_evict_first();
     int win_base = -1, win_req = -1, win_page = -1, nxt_page = -1;
     int last_tile = -1;
     // ring positions of tile i, stepped once per tile (no division on the issue path)
@@ -887,9 +889,11 @@ cudaError_t launch_indexer_scores(const dsa_cache& c, const RowMeta& m, int row0
   a.max_pages = page_log2 >= 0 ? (max_seq_len + (1 << unit_log2) - 1) >> unit_log2 : 0;
   a.err = err;
   const int grid = device_sm_count();
-  e = kind == 1   ? launch_pdl(indexer_tc_kernel<1>, dim3(grid), dim3(idx::kThreads), idx::kSmemBytes, s, map, a)
-      : kind == 2 ? launch_pdl(indexer_tc_kernel<2>, dim3(grid), dim3(idx::kThreadsI8), idx::kSmemBytes, s, map, a)
-                  : launch_pdl(indexer_tc_kernel<0>, dim3(grid), dim3(idx::kThreads), idx::kSmemBytes, s, map, a);
+  // more rows than row groups per request: some request's keys are read by several groups
+  const int share = (int64_t)nrows > (int64_t)m.num_requests * rg ? 1 : 0;
+  e = kind == 1   ? launch_pdl(indexer_tc_kernel<1>, dim3(grid), dim3(idx::kThreads), idx::kSmemBytes, s, map, a, share)
+      : kind == 2 ? launch_pdl(indexer_tc_kernel<2>, dim3(grid), dim3(idx::kThreadsI8), idx::kSmemBytes, s, map, a, share)
+                  : launch_pdl(indexer_tc_kernel<0>, dim3(grid), dim3(idx::kThreads), idx::kSmemBytes, s, map, a, share);
   count_launches(1);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();

@@ -192,7 +192,15 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
   return p;
 }
 
-// tma_load_2d with an L2 cache policy (l2_evict_first()).
+// L2 policy for data other CTAs of the same call read again (a prefill request's latent rows and
+// index keys, shared by its many query rows): ordinary priority, so the reuse stays in L2.
+__device__ __forceinline__ uint64_t l2_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_2d with an L2 cache policy (l2_evict_first() or l2_evict_normal()).
 __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int32_t x, int32_t y, uint64_t* bar,
                                                  uint64_t policy) {
   asm volatile(

@@ -142,7 +142,7 @@ __device__ __forceinline__ uint16_t half_pow2_bits(int e) {
 template <bool kC8>
 __global__ void __launch_bounds__(mla::kThreads, 1)
     sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
-                         const MlaArgs a, const float* __restrict__ latent_scales) {
+                         const MlaArgs a, const float* __restrict__ latent_scales, int rows_share_pool) {
   using namespace mla;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -239,6 +239,9 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     // l % 4 of its group l / 4 one tile ahead, so the index-buffer and page-table loads stay off
     // the critical path; lane l < 9 ng gathers 128-byte column chunk l % 9 of group l / 9.
     const int ng = (kGroups - warp + kProducers - 1) / kProducers;   // groups of this warp (2 or 3)
+    // a row read by one query row only is evicted first (the index buffer, queries and partials stay
+    // in L2); rows that a request's other query rows may select again keep their normal priority
+    const uint64_t gather_policy = rows_share_pool ? l2_evict_normal() : l2_evict_first();
     int q_loads = 0, cur_row = -1;
     int filled[2] = {0, 0};
     auto lookup = [&](int u) -> int64_t {
@@ -367,7 +370,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         uint8_t* stage = sKV + b * kStageBytes;
         const int g = warp + kProducers * q;
         tma_gather4_hint(stage + c * kChunkBytes + g * 512, &kv_map, c * 64, y[0], y[1], y[2], y[3], land,
-                         l2_evict_first());
+                         gather_policy);
       }
       if constexpr (kC8) {
        if (new_q) {
@@ -935,8 +938,12 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
     at[1].val.clusterDim.z = 1;
     c.attrs = at;
     c.numAttrs = plan.split > 1 ? 2 : 1;
-    e = c8 ? cudaLaunchKernelEx(&c, sparse_mla_tc_kernel<true>, kv_map, q_map, a, ls)
-           : cudaLaunchKernelEx(&c, sparse_mla_tc_kernel<false>, kv_map, q_map, a, ls);
+    // prefill-like calls (at least 8 query rows per request on average): a request's rows select many of
+    // the same cached rows, which keep their normal L2 priority (a 4096-row prefill chunk then reads
+    // 1.7 GB from DRAM instead of 8.3 GB); with fewer rows per request (verify) evicting first is faster
+    const int share = m.query_start_loc != nullptr && num_rows >= 8 * m.num_requests ? 1 : 0;
+    e = c8 ? cudaLaunchKernelEx(&c, sparse_mla_tc_kernel<true>, kv_map, q_map, a, ls, share)
+           : cudaLaunchKernelEx(&c, sparse_mla_tc_kernel<false>, kv_map, q_map, a, ls, share);
   }
   count_launches(1);
   if (e != cudaSuccess) return e;
