@@ -21,7 +21,7 @@
 // hi = e4m3(v) in place and lo = v - hi beside it (both exact, |lo| <= 4), and
 // the issuer runs the e4m3 chain over both into the same accumulators.
 //
-// Per CTA (persistent, one per SM, 448 threads), over one contiguous range of
+// Per CTA (persistent, one per SM, 544 threads), over one contiguous range of
 // the flattened (group, key tile) list:
 //   warps 0-5  producers, tiles round-robin: page lookups from a register
 //              window of the block table, TMA loads of the key pages into a
@@ -29,7 +29,8 @@
 //              the keys' fp32 scales into a separate ring of scale slots;
 //   warps 6-7  MMA issuers, even and odd tiles; a commit frees the key stage;
 //   warp 8     B loader: each group's queries (split into e4m3 terms, or bf16)
-//              into the B operand, 128-byte swizzled, K-major;
+//              into the B operand, 128-byte swizzled, K-major; the CTA's first
+//              group together with the epilogue warps, which have no tile yet;
 //   warps 9-16 two epilogue warpgroups, even and odd tiles (fed by the
 //              matching issuer); the one that reads a tile's scales frees
 //              its scale slot;
@@ -171,6 +172,55 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
          ((uint32_t)__nv_cvt_float_to_fp8(d, __NV_SATFINITE, __NV_E4M3) << 24);
 }
 
+// The B operand of row group G: its 32 G.z (row, head) query vectors, for 8-bit keys each as the two
+// exact e4m3 terms t1 (B row 64 rr + h) and t2 (B row 64 rr + 32 + h), for bf16 keys as they are
+// (B row 32 rr + h, two 64-element K halves), all in the 128-byte swizzled layout.  This thread
+// writes vectors p0, p0 + dp, ...
+template <bool kFp8>
+__device__ __forceinline__ void fill_group_queries(const IdxArgs& a, int4 G, uint8_t* bbuf, int p0, int dp) {
+  const int N = 32 * (kFp8 ? 2 : 1) * G.z;
+  for (int p = p0; p < 32 * G.z; p += dp) {
+    const int rr = p >> 5, h = p & 31;
+    uint4 raw[16];
+    if (kFp8) {
+      const int e = query_exponent(a, G.y + rr, h, raw);
+      const float up = ldexpf(1.f, 7 - e);
+      const int n_hi = rr * 64 + h, n_lo = rr * 64 + 32 + h;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {        // 16-byte units of the 128-byte e4m3 rows
+        uint32_t t1[4], t2[4];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw[2 * c + half]);
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const float2 f0 = __bfloat1622float2(v[2 * e2]), f1 = __bfloat1622float2(v[2 * e2 + 1]);
+            const float x[4] = {f0.x * up, f0.y * up, f1.x * up, f1.y * up};
+            float r[4];
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+              const float v1 = __half2float(__nv_cvt_fp8_to_halfraw(
+                  __nv_cvt_float_to_fp8(x[z], __NV_SATFINITE, __NV_E4M3), __NV_E4M3));
+              r[z] = (x[z] - v1) * 16.f;
+            }
+            t1[2 * half + e2] = e4m3x4(x[0], x[1], x[2], x[3]);
+            t2[2 * half + e2] = e4m3x4(r[0], r[1], r[2], r[3]);
+          }
+        }
+        *reinterpret_cast<uint4*>(bbuf + sw128_offset(n_hi, c)) = make_uint4(t1[0], t1[1], t1[2], t1[3]);
+        *reinterpret_cast<uint4*>(bbuf + sw128_offset(n_lo, c)) = make_uint4(t2[0], t2[1], t2[2], t2[3]);
+      }
+    } else {
+      const __nv_bfloat16* qv = a.q_idx + ((int64_t)(G.y + rr) * kIndexHeads + h) * kIndexDim;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) raw[c] = reinterpret_cast<const uint4*>(qv)[c];
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        *reinterpret_cast<uint4*>(bbuf + (c >> 3) * (N * 128) + sw128_offset(p, c & 7)) = raw[c];
+    }
+  }
+}
+
 // Four int8 codes (one 32-bit word) -> the e4m3 codes of hi = e4m3(v) (nearest-even) and lo = v - hi,
 // byte for byte.  For |v| <= 127 both are exact e4m3 values (|lo| <= 4), so hi + lo = v.  Each v is
 // first made a half exactly: the bits 0x64XX with XX = v + 128 are the half 1024 + v + 128.
@@ -208,6 +258,9 @@ __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 
   constexpr int kTerms = kFp8 ? 2 : 1;               // B rows per (row, head): e4m3 split terms
   constexpr int kLoaderWarp = kProducers + kMmaWarps;
   constexpr int kEpiWarp0 = kLoaderWarp + 1;           // two epilogue warpgroups take alternate tiles
+  // named barriers: 2 + eg and kScaleBar0 + eg within epilogue warpgroup eg; kPrologueBar for the
+  // loader and the epilogue warps filling the first group's queries together
+  constexpr int kScaleBar0 = 4, kPrologueBar = 6, kPrologueThreads = 32 * 9;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // carve-up (uniform across the CTA): B buffers sized for the group, then scales, then keys
@@ -234,7 +287,7 @@ __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 
   __shared__ uint64_t d_full[4], d_empty[4], b_full[2], b_empty[2];
   __shared__ uint64_t mma_done[kMmaWarps];
   __shared__ uint64_t cv_full[kI8 ? kMaxStages : 1], lo_empty[kI8 ? kConvWarps : 1];   // int8 keys only
-  __shared__ float wq_e[2][kMaxRows][32];   // each epilogue warpgroup's head weights for its current group
+  __shared__ __align__(16) float wq_e[2][kMaxRows][32];   // each epilogue warpgroup's head weights for its group
   __shared__ int4 gcache[kGroupCache];
   __shared__ int tcache[kGroupCache + 1];
   __shared__ uint32_t tmem_base;
@@ -439,10 +492,11 @@ __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 
           b_addr = smem_u32(sB + ub * b_bytes);
         }
         if ((i & 1) == mw) {
-          // the issuer paces the pipeline: poll without suspending (a suspended wait wakes late);
-          // int8 tiles are ready once their converter has split them
-          if (!mbar_spin(kI8 ? &cv_full[s] : &st_full[s], n & 1, a.err, kErrTmaTimeout)) { ok = false; break; }
-          if (nd > 0 && !mbar_spin(&d_empty[db], (nd - 1) & 1, a.err, kErrMmaTimeout)) { ok = false; break; }
+          // int8 tiles are ready once their converter has split them.  A suspending wait: an issuer
+          // that polls takes issue slots from the epilogue warps of its SM sub-partition (measured 5 %
+          // slower in decode)
+          if (!mbar_wait(kI8 ? &cv_full[s] : &st_full[s], n & 1, a.err, kErrTmaTimeout, kPolls)) { ok = false; break; }
+          if (nd > 0 && !mbar_wait(&d_empty[db], (nd - 1) & 1, a.err, kErrMmaTimeout, kPolls)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d = tmem + db * (uint32_t)n_cap;
           const uint32_t stage = smem_u32(sRing + s * kStageBytes);
@@ -482,50 +536,13 @@ __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 
     bool new_group = true;
     for (int i = 0; cur.valid(); ++i) {
       if (new_group) {
-        const int N = 32 * kTerms * cur.G.z, ub = gcount % nB;
+        const int ub = gcount % nB;
         uint8_t* bbuf = sB + ub * b_bytes;
         if (gcount >= nB && !mbar_wait(&b_empty[ub], (gcount / nB - 1) & 1, a.err, kErrMmaTimeout, kPolls)) break;
-        for (int p = lane; p < 32 * cur.G.z; p += 32) {
-          const int rr = p >> 5, h = p & 31;
-          uint4 raw[16];
-          if (kFp8) {
-            const int e = query_exponent(a, cur.G.y + rr, h, raw);
-            const float up = ldexpf(1.f, 7 - e);
-            const int n_hi = rr * 64 + h, n_lo = rr * 64 + 32 + h;
-#pragma unroll 1
-            for (int c = 0; c < 8; ++c) {        // 16-byte units of the 128-byte e4m3 rows
-              uint32_t t1[4], t2[4];
-#pragma unroll
-              for (int half = 0; half < 2; ++half) {
-                const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw[2 * c + half]);
-#pragma unroll
-                for (int e2 = 0; e2 < 2; ++e2) {
-                  const float2 f0 = __bfloat1622float2(v[2 * e2]), f1 = __bfloat1622float2(v[2 * e2 + 1]);
-                  const float x[4] = {f0.x * up, f0.y * up, f1.x * up, f1.y * up};
-                  float r[4];
-#pragma unroll
-                  for (int z = 0; z < 4; ++z) {
-                    const float v1 = __half2float(__nv_cvt_fp8_to_halfraw(
-                        __nv_cvt_float_to_fp8(x[z], __NV_SATFINITE, __NV_E4M3), __NV_E4M3));
-                    r[z] = (x[z] - v1) * 16.f;
-                  }
-                  t1[2 * half + e2] = e4m3x4(x[0], x[1], x[2], x[3]);
-                  t2[2 * half + e2] = e4m3x4(r[0], r[1], r[2], r[3]);
-                }
-              }
-              *reinterpret_cast<uint4*>(bbuf + sw128_offset(n_hi, c)) = make_uint4(t1[0], t1[1], t1[2], t1[3]);
-              *reinterpret_cast<uint4*>(bbuf + sw128_offset(n_lo, c)) = make_uint4(t2[0], t2[1], t2[2], t2[3]);
-            }
-          } else {
-            const __nv_bfloat16* qv = a.q_idx + ((int64_t)(cur.G.y + rr) * kIndexHeads + h) * kIndexDim;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) raw[c] = reinterpret_cast<const uint4*>(qv)[c];
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-              *reinterpret_cast<uint4*>(bbuf + (c >> 3) * (N * 128) + sw128_offset(p, c & 7)) = raw[c];
-          }
-        }
+        // the CTA's first group is filled together with the epilogue warps, idle until its first tile
+        fill_group_queries<kFp8>(a, cur.G, bbuf, lane, gcount == 0 ? kPrologueThreads : 32);
         fence_proxy_async_smem();
+        if (gcount == 0) named_bar_sync(kPrologueBar, kPrologueThreads);
         __syncwarp();
         if (lane == 0) mbar_arrive(&b_full[ub]);
         ++gcount;
@@ -572,6 +589,12 @@ __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 
     const int et = threadIdx.x - 32 * (kEpiWarp0 + 4 * eg);   // 0..127 within the warpgroup
     TileCursor cur;
     cursor_init(cur, a, gcache, tcache, ngroups, tau0, tau1);
+    if (cur.valid()) {
+      // the first group's queries, with the loader warp (B buffer 0; the loader signals it)
+      fill_group_queries<kFp8>(a, cur.G, sB, threadIdx.x - 32 * kLoaderWarp, kPrologueThreads);
+      fence_proxy_async_smem();
+      named_bar_sync(kPrologueBar, kPrologueThreads);
+    }
     bool new_group = true;
     int db = 0, nd = 0, sci = 0, scn = 0;
     for (int i = 0; cur.valid();
@@ -598,7 +621,8 @@ __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 
           score[rr] = 0.f;
           if (rr < cur.G.z) {
             uint32_t v[32];
-            float acc = 0.f;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};     // four partial sums: a short dependency chain
+            const float4* wr = reinterpret_cast<const float4*>(wq_e[eg][rr]);
             const uint32_t col = tmem + lane_base + db * (uint32_t)n_cap + 32 * kTerms * rr;
             tmem_ld32(col, v);
             if (kFp8) {
@@ -606,24 +630,37 @@ __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 
               tmem_ld32(col + 32, lo);
               tmem_wait_ld();
 #pragma unroll
-              for (int h = 0; h < 32; ++h)
-                acc = fmaf(wq_e[eg][rr][h], fmaxf(fmaf(__uint_as_float(lo[h]), 0.0625f, __uint_as_float(v[h])), 0.f), acc);
+              for (int h4 = 0; h4 < 8; ++h4) {
+                const float4 w4 = wr[h4];
+                const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const int h = 4 * h4 + j;
+                  acc[j] = fmaf(wv[j], fmaxf(fmaf(__uint_as_float(lo[h]), 0.0625f, __uint_as_float(v[h])), 0.f), acc[j]);
+                }
+              }
             } else {
               tmem_wait_ld();
 #pragma unroll
-              for (int h = 0; h < 32; ++h) acc = fmaf(wq_e[eg][rr][h], fmaxf(__uint_as_float(v[h]), 0.f), acc);
+              for (int h4 = 0; h4 < 8; ++h4) {
+                const float4 w4 = wr[h4];
+                const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[j] = fmaf(wv[j], fmaxf(__uint_as_float(v[4 * h4 + j]), 0.f), acc[j]);
+              }
             }
-            score[rr] = acc;
+            score[rr] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&d_empty[db]);
         if (kFp8) {
-          // the tile's key scales sit in their own ring slot, refilled only after this read
+          // the tile's key scales sit in their own ring slot, refilled only after this read (reading
+          // them before the accumulators' wait measured slower)
           if (!mbar_wait(&sc_full[sci], scn & 1, a.err, kErrTmaTimeout, kPolls)) break;
           const float ks = scale_value(sScale[sci * kTileKeys + key_local]);
-          named_bar_sync(4 + eg, 128);
+          named_bar_sync(kScaleBar0 + eg, 128);
           if (et == 0) mbar_arrive(&sc_empty[sci]);
 #pragma unroll
           for (int rr = 0; rr < kRowsMax; ++rr) score[rr] *= ks;
