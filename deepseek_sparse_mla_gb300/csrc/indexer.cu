@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 
     }
     for (int s = 0; s < kScStages; ++s) {
       mbar_init(&sc_full[s], 1);
-      mbar_init(&sc_empty[s], 1);                  // the epilogue frees a scale slot once it has read it
+      mbar_init(&sc_empty[s], 4);                  // the epilogue frees a scale slot once it has read it
     }
     for (int b = 0; b < 4; ++b) {
       mbar_init(&d_full[b], 1);
@@ -660,8 +660,8 @@ __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 
           // them before the accumulators' wait measured slower)
           if (!mbar_wait(&sc_full[sci], scn & 1, a.err, kErrTmaTimeout, kPolls)) break;
           const float ks = scale_value(sScale[sci * kTileKeys + key_local]);
-          named_bar_sync(kScaleBar0 + eg, 128);
-          if (et == 0) mbar_arrive(&sc_empty[sci]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sc_empty[sci]);
 #pragma unroll
           for (int rr = 0; rr < kRowsMax; ++rr) score[rr] *= ks;
         }
