@@ -36,6 +36,7 @@ METRIC = "sparse-DSA decode layer-steps/s (indexer+top-k+MLA) @128K ctx; % of HB
 UNIT = "layer-steps/s"
 DEFAULT_WORKLOAD = "decode_b64_fp8_indexshare"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 # ---------------------------------------------------------------------------
@@ -292,7 +293,12 @@ def algorithmic_bytes(wl: wlm.Workload) -> dict:
     key_out = wl.key_bytes_per_token()
     append_owner = R * (1152 + row + key_in + key_out)
     append_shared = R * (1152 + row)
+    # useful flops: a (row, visible key) costs 32 heads x 128 multiply-adds in the indexer; a (row, selected
+    # entry) costs 64 heads x (576 + 512) multiply-adds in attention (QK over [c_KV | k_R], PV over c_KV)
+    indexer_flops = float((pos + 1).sum()) * 2 * 32 * 128
+    attention_flops = float(selected) * 2 * 64 * (576 + 512)
     return {"indexer": float(indexer), "attention": float(attention), "append_owner": float(append_owner),
+            "indexer_flops": indexer_flops, "attention_flops": attention_flops,
             "append_shared": float(append_shared), "index_key_bytes": float(keys),
             "gather_bytes_per_layer": float(selected * row),
             "step": float(indexer + wl.layers * attention + append_owner + (wl.layers - 1) * append_shared)}
@@ -306,6 +312,17 @@ def load_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def load_tensor_peak():
+    """Dense bf16 TFLOP/s: the burst figure (each call is timed alone, not over a seconds-long loop)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def source_digest(files) -> str:
@@ -830,14 +847,32 @@ def main():
                                                "mla_merge_kernel when rows are cut between CTAs)"),
              "append": (("kv_append.cu",), "kv_append_layers: kv_append_kernel (every layer in one launch)")}
     dom = max(share, key=share.get)
-    achieved = bytes_of[dom] / (per_call[dom] * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": files[dom][1], "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_kind": peak_kind,
-                "traffic": kernel_traffic(dom, files[dom][0], wl.name + (" (page selection)" if page_mode else "")),
-                "algorithmic_bytes_per_launch": bytes_of[dom]}
+    # the dominant call's bound: its useful flops per algorithmic byte against the ridge (measured bf16
+    # rate / measured HBM rate); above it the call is a dense contraction, rated in TFLOP/s
+    tpeak, tpeak_kind = load_tensor_peak()
+    flops_of = {"indexer": alg["indexer_flops"], "attention": alg["attention_flops"]}
+    ridge = tpeak * 1e12 / (peak * 1e9)
+    intensity = flops_of.get(dom, 0.0) / bytes_of[dom]
+    traffic = kernel_traffic(dom, files[dom][0], wl.name + (" (page selection)" if page_mode else ""))
+    if intensity > ridge:
+        achieved = flops_of[dom] / (per_call[dom] * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": files[dom][1], "achieved": achieved, "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": achieved / tpeak, "peak_kind": tpeak_kind, "traffic": traffic,
+                    "algorithmic_flops_per_launch": flops_of[dom], "algorithmic_bytes_per_launch": bytes_of[dom],
+                    "intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge}
+    else:
+        achieved = bytes_of[dom] / (per_call[dom] * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": files[dom][1], "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                    "algorithmic_bytes_per_launch": bytes_of[dom], "intensity_flop_per_byte": intensity,
+                    "ridge_flop_per_byte": ridge}
     kernels = {k: {"ms_per_call": per_call[k], "calls_per_step": calls[k], "share": share[k] / tot,
                    "algorithmic_GBps": bytes_of[k] / (per_call[k] * 1e-3) / 1e9,
                    "frac_of_peak": bytes_of[k] / (per_call[k] * 1e-3) / 1e9 / peak} for k in per_call}
+    for k in flops_of:
+        if k in kernels:
+            kernels[k]["algorithmic_TFLOPs"] = flops_of[k] / (per_call[k] * 1e-3) / 1e12
+            kernels[k]["frac_of_tensor_peak"] = kernels[k]["algorithmic_TFLOPs"] / tpeak
     step_gbps = alg["step"] / (ms_per_step * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers ---------------------------

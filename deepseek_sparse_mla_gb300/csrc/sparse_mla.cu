@@ -106,13 +106,14 @@ __device__ __forceinline__ int cta_of_unit(int u, int units, int ctas) {
 // Cluster merge, push side: a softmax thread's latent dims d = 128 k + (this thread's offset in
 // `rows`) of the 32 heads h0 .. h0 + 31, read from TMEM (O^T at `src` + 64 k) and stored into the
 // shared memory of each head's owner CTA (head h belongs to CTA h / HS), at row h % HS of the
-// block `rows` (this piece's block, mapped into the owner's window).
+// block `rows` (this piece's block, mapped into the owner's window).  Heads this CTA (cluster rank
+// `self`) owns take plain local stores.
 template <int HS>
-__device__ __forceinline__ void push_piece(uint32_t src, const float* rows, int h0, bool has_valid) {
+__device__ __forceinline__ void push_piece(uint32_t src, const float* rows, int h0, bool has_valid, int self) {
   constexpr int kOwners = 32 / HS;
   uint32_t ob[kOwners];
 #pragma unroll
-  for (int i = 0; i < kOwners; ++i) ob[i] = cluster_map(rows, (uint32_t)(h0 / HS + i));
+  for (int i = 0; i < kOwners; ++i) ob[i] = h0 / HS + i == self ? smem_u32(rows) : cluster_map(rows, (uint32_t)(h0 / HS + i));
   tc_fence_after();
 #pragma unroll 1
   for (int k = 0; k < 4; ++k) {
@@ -122,8 +123,11 @@ __device__ __forceinline__ void push_piece(uint32_t src, const float* rows, int 
 #pragma unroll
     for (int jj = 0; jj < 32; ++jj) {
       const uint32_t dst = ob[jj / HS] + (uint32_t)(((jj % HS) * kLatent + 128 * k) * 4);
-      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(has_valid ? __uint_as_float(o[jj]) : 0.f)
-                   : "memory");
+      if (h0 / HS + jj / HS == self)
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst), "f"(has_valid ? __uint_as_float(o[jj]) : 0.f) : "memory");
+      else
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(has_valid ? __uint_as_float(o[jj]) : 0.f)
+                     : "memory");
     }
   }
 }
@@ -698,9 +702,9 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       const bool has_valid = lfin[h0] > 0.f;   // a piece without valid entries never set its accumulator
       const uint32_t src = tmem + lane_base + kColO + h0;
       const float* my_rows = buf + (q * HS) * kLatent + 32 * quarter + lane;
-      if (HS == 32) push_piece<32>(src, my_rows, h0, has_valid);
-      else if (HS == 16) push_piece<16>(src, my_rows, h0, has_valid);
-      else push_piece<8>(src, my_rows, h0, has_valid);
+      if (HS == 32) push_piece<32>(src, my_rows, h0, has_valid, q);
+      else if (HS == 16) push_piece<16>(src, my_rows, h0, has_valid, q);
+      else push_piece<8>(src, my_rows, h0, has_valid, q);
       if (st < 32) {
         const int h = h0 + st, owner = h / HS;
         const uint32_t dst = cluster_map(mlb + 2 * (q * HS + (h - owner * HS)), owner);
