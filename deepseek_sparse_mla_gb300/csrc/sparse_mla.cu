@@ -206,8 +206,9 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     prefetch_tmap(&q_map);
   }
   // the index buffer, the queries and the caches are complete past this point (programmatic
-  // dependent launch: the prologue above overlaps the previous kernel).  No early trigger: the merge
-  // kernel launched while this grid still runs made each call about 5 us slower.
+  // dependent launch: the prologue above overlaps the previous kernel).  The unit split triggers its
+  // merge kernel only at exit (launched while this grid still ran, it made each call about 5 us
+  // slower); cluster mode triggers as each CTA enters the cluster merge (4 us off a benchmark step).
   pdl_wait();
   // With row counts (cluster mode only) a row spans only the tiles that hold its first row_count
   // entries, at least one per piece; entries past the count are -1 by contract, so the unit split,
@@ -694,6 +695,9 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     float* buf = reinterpret_cast<float*>(sKV);
     float* mlb = reinterpret_cast<float*>(sP);
     float* wts = mlb + 2 * kHeads;                       // [split][HS]
+    // the next call (the next layer's attention) may be launched now: its CTAs take SMs as this
+    // grid's CTAs leave, and it reads nothing before its own wait for this grid's completion
+    pdl_trigger();
     cluster_sync();                     // every CTA of the cluster is done with its gather stages
     if (warp >= kSoftmaxWarp0) {
       const int sg = (warp - kSoftmaxWarp0) >> 2, quarter = warp & 3, h0 = 32 * sg;
