@@ -81,13 +81,17 @@ class DeviceProblem:
         q_idx, w = wlm.indexer_queries(wl)
         self.q_idx = wlm.bits_to_torch(q_idx, device)
         self.w = torch.from_numpy(w).to(device)
-        self.q = [wlm.bits_to_torch(wlm.mla_queries(wl, l), device) for l in range(layers)]
+        # the layers' queries and outputs lie back to back ([layers, R, ...]), so a layer group's attention
+        # can run as one call over the stacked tensors
+        self.q = list(torch.stack([wlm.bits_to_torch(wlm.mla_queries(wl, l), device) for l in range(layers)]).unbind(0))
         self.topk_idx = torch.empty((R, wl.topk), dtype=torch.int32, device=device)
-        self.out = [torch.empty((R, 64, 512), dtype=torch.bfloat16, device=device) for _ in range(layers)]
-        self.lse = [torch.empty((R, 64), dtype=torch.float32, device=device) for _ in range(layers)]
+        self.out = list(torch.empty((layers, R, 64, 512), dtype=torch.bfloat16, device=device).unbind(0))
+        self.lse = list(torch.empty((layers, R, 64), dtype=torch.float32, device=device).unbind(0))
+        # decode layer groups (one index buffer for every layer): one attention call for all layers
+        self.group_attention = wl.is_decode and layers > 1
         self.ws_idx = torch.empty(dsa.indexer_workspace_bytes(R, wl.max_seq_len, wl.topk), dtype=torch.uint8,
                                   device=device)
-        self.ws_mla = torch.empty(dsa.mla_workspace_bytes(R, wl.topk), dtype=torch.uint8, device=device)
+        self.ws_mla = torch.empty(dsa.mla_workspace_bytes(layers * R, wl.topk), dtype=torch.uint8, device=device)
         self.loc_idx = None
         if selection == "locality":
             self.loc_idx = torch.from_numpy(locality_selection(wl, locality_noise)).to(device)
@@ -108,7 +112,7 @@ class DeviceProblem:
         import deepseek_sparse_mla_gb300 as dsa
         wl = self.wl
         io = self if io is None else io
-        n_calls = 2 + wl.layers if calls is None else calls
+        n_calls = self.num_calls() if calls is None else calls
         mla = dsa.sparse_mla_decode if wl.is_decode else dsa.sparse_mla_prefill
         if marks is not None:
             marks.mark("append")
@@ -125,6 +129,14 @@ class DeviceProblem:
             dsa.indexer_scores_topk(self.caches[0], io.batch, io.q_idx, io.w, wl.topk, topk_idx=self.topk_idx,
                                     workspace=self.ws_idx)
         idx = self.topk_idx if self.loc_idx is None else self.loc_idx
+        if self.group_attention and n_calls > 2:
+            if marks is not None:
+                marks.mark("attention")
+            dsa.sparse_mla_decode_layers(self.caches, io.batch, stacked(io.q), idx, wl.scale, out=stacked(io.out),
+                                         lse=stacked(io.lse), workspace=self.ws_mla)
+            if marks is not None:
+                marks.mark(None)
+            return
         for l in range(min(wl.layers, n_calls - 2)):
             if marks is not None:
                 marks.mark("attention")
@@ -132,6 +144,11 @@ class DeviceProblem:
                 workspace=self.ws_mla)
         if marks is not None:
             marks.mark(None)
+
+    def num_calls(self):
+        """Library calls in a step: append, indexer, then the attention (one call per layer, or one for
+        the layer group)."""
+        return 3 if self.group_attention else 2 + self.wl.layers
 
     def io_set(self):
         """A second set of the step's device inputs and outputs (same values), so that the copies of
@@ -141,9 +158,10 @@ class DeviceProblem:
         c = lambda t: None if t is None else t.clone()   # noqa: E731
         io = types.SimpleNamespace(new_c=[c(t) for t in self.new_c], new_r=[c(t) for t in self.new_r],
                                    new_k=c(self.new_k), slots=c(self.slots), q_idx=c(self.q_idx), w=c(self.w),
-                                   q=[c(t) for t in self.q], block_table=c(self.block_table),
+                                   q=list(c(stacked(self.q)).unbind(0)), block_table=c(self.block_table),
                                    seq_lens=c(self.seq_lens), qsl=c(self.qsl),
-                                   out=[torch_empty_like(t) for t in self.out], lse=[torch_empty_like(t) for t in self.lse])
+                                   out=list(torch_empty_like(stacked(self.out)).unbind(0)),
+                                   lse=list(torch_empty_like(stacked(self.lse)).unbind(0)))
         io.batch = dsa.Batch(io.block_table, io.seq_lens, io.qsl, num_rows=self.wl.num_rows,
                              max_seq_len=self.wl.max_seq_len)
         return io
@@ -236,6 +254,17 @@ def locality_selection(wl: wlm.Workload, noise: float) -> np.ndarray:
 def torch_empty_like(t):
     import torch
     return torch.empty_like(t)
+
+
+def stacked(ts):
+    """[len(ts), ...] view of equally shaped contiguous tensors that lie back to back in memory."""
+    import torch
+    t0 = ts[0]
+    step = t0.numel()
+    for i, t in enumerate(ts):
+        if not t.is_contiguous() or t.shape != t0.shape or t.data_ptr() != t0.data_ptr() + i * step * t0.element_size():
+            raise ValueError("the layers' tensors do not lie back to back")
+    return torch.as_strided(t0, (len(ts),) + tuple(t0.shape), (step,) + tuple(t0.stride()))
 
 
 def pack_views(tensors, device):
@@ -815,7 +844,7 @@ def main():
     per_call = None
     if graph is not None:
         try:
-            n_calls = 2 + wl.layers
+            n_calls = prob.num_calls()
             pre = [0.0] + [replay_ms(capture_step(prob, lib, calls=j)[0]) for j in range(1, n_calls + 1)]
             marg = [pre[j] - pre[j - 1] for j in range(1, n_calls + 1)]
             per_call = {"append": marg[0] / wl.layers, "indexer": marg[1], "attention": float(np.mean(marg[2:]))}
@@ -831,26 +860,31 @@ def main():
         per_call = {k: float(np.mean(v)) for k, v in marks.spans.items()}     # ms per call
         per_call["append"] /= wl.layers                                         # one span covers every layer's append
         breakdown = "CUDA events between eager library calls"
-    calls = {"append": wl.layers, "indexer": 1, "attention": wl.layers}
+    # a layer group's attention runs as one call over every layer (its bytes and flops are the layers')
+    att_layers = wl.layers if prob.group_attention else 1
+    calls = {"append": wl.layers, "indexer": 1, "attention": wl.layers // att_layers}
     share = {k: per_call[k] * calls[k] for k in per_call}
     tot = sum(share.values())
     alg = algorithmic_bytes(wl)
     peak, peak_kind = load_peaks()
-    bytes_of = {"indexer": alg["indexer"], "attention": alg["attention"],
+    bytes_of = {"indexer": alg["indexer"], "attention": alg["attention"] * att_layers,
                 "append": (alg["append_owner"] + (wl.layers - 1) * alg["append_shared"]) / wl.layers}
     # each timed call, the kernels it launches and the sources they come from
     files = {"indexer": (("indexer.cu", "topk.cu"),
                          "indexer_page_topk: indexer_groups_kernel + indexer_tc_kernel (page scores) + topk_kernel + "
                          "page_expand_kernel" if page_mode else
                          "indexer_scores_topk: indexer_groups_kernel + indexer_tc_kernel + topk_chunk_kernel + topk_kernel"),
-             "attention": (("sparse_mla.cu",), "sparse_mla_decode: sparse_mla_tc_kernel (clusters merge in shared memory; "
-                                               "mla_merge_kernel when rows are cut between CTAs)"),
+             "attention": (("sparse_mla.cu",),
+                           f"sparse_mla_decode_layers: sparse_mla_tc_kernel over the {wl.layers} layers' (layer, row, tile) "
+                           "units on every SM + mla_merge_kernel for rows cut between CTAs" if prob.group_attention else
+                           "sparse_mla_decode: sparse_mla_tc_kernel (clusters merge in shared memory; "
+                           "mla_merge_kernel when rows are cut between CTAs)"),
              "append": (("kv_append.cu",), "kv_append_layers: kv_append_kernel (every layer in one launch)")}
     dom = max(share, key=share.get)
     # the dominant call's bound: its useful flops per algorithmic byte against the ridge (measured bf16
     # rate / measured HBM rate); above it the call is a dense contraction, rated in TFLOP/s
     tpeak, tpeak_kind = load_tensor_peak()
-    flops_of = {"indexer": alg["indexer_flops"], "attention": alg["attention_flops"]}
+    flops_of = {"indexer": alg["indexer_flops"], "attention": alg["attention_flops"] * att_layers}
     ridge = tpeak * 1e12 / (peak * 1e9)
     intensity = flops_of.get(dom, 0.0) / bytes_of[dom]
     traffic = kernel_traffic(dom, files[dom][0], wl.name + (" (page selection)" if page_mode else ""))

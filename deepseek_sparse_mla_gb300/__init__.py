@@ -26,7 +26,7 @@ DEFAULT_SCALE = 1.0 / 16.0     # 1/sqrt(192 + 64)
 _FORMATS = {"bf16": KEY_BF16, "fp8": KEY_FP8_E4M3, "int8": KEY_INT8, None: KEY_BF16}
 _LATENT_FORMATS = {"bf16": _lib.LATENT_BF16, "fp8": _lib.LATENT_E4M3}
 
-__all__ = ["LayerCache", "Batch", "kv_append", "kv_append_layers", "indexer_scores_topk", "indexer_page_topk", "sparse_mla_decode", "sparse_mla_prefill",
+__all__ = ["LayerCache", "Batch", "kv_append", "kv_append_layers", "indexer_scores_topk", "indexer_page_topk", "sparse_mla_decode", "sparse_mla_decode_layers", "sparse_mla_prefill",
            "cache_bytes", "indexer_workspace_bytes", "mla_workspace_bytes", "DsaError", "DEFAULT_SCALE",
            "dcp_candidates", "dcp_select", "dcp_merge", "read_status"]
 
@@ -290,6 +290,34 @@ def sparse_mla_decode(layer: LayerCache, batch: Batch, q, topk_idx, scale: float
     check=True reads the call's device status afterwards and raises DsaError on a non-zero one."""
     return _sparse_mla(_lib.load().dsa_sparse_mla_decode, layer, batch, q, topk_idx, scale, out, lse, workspace, stream,
                        row_counts, check)
+
+
+def sparse_mla_decode_layers(layers, batch: Batch, q, topk_idx, scale: float = DEFAULT_SCALE, out=None, lse=None,
+                             workspace=None, stream=None, check=False):
+    """sparse_mla_decode for the layers of an IndexShare group in one call (they share topk_idx):
+    q [L, R, 64, 576] bf16 with layer l's queries at [l]; returns (out [L, R, 64, 512] bf16, lse
+    [L, R, 64] fp32 or None).  The layers' caches agree in page size, page count and latent format."""
+    L, R = len(layers), batch.num_rows
+    _need(q, torch.bfloat16, (L, R, HEADS, ROW_DIM), "q")
+    if topk_idx is None:
+        raise ValueError("topk_idx is required: the shared layers reuse the owner layer's index buffer")
+    topk = int(topk_idx.shape[1])
+    _need(topk_idx, torch.int32, (R, topk), "topk_idx")
+    if out is None:
+        out = torch.empty((L, R, HEADS, LATENT_DIM), dtype=torch.bfloat16, device=q.device)
+    _need(out, torch.bfloat16, (L, R, HEADS, LATENT_DIM), "out")
+    if lse is not None:
+        _need(lse, torch.float32, (L, R, HEADS), "lse")
+    if workspace is None:
+        workspace = _workspace(mla_workspace_bytes(L * R, topk), q.device)
+    structs = (_lib.DsaCache * L)(*[c.struct() for c in layers])
+    b = batch.struct()
+    _lib.check(_lib.load().dsa_sparse_mla_decode_layers(
+        structs, L, ctypes.byref(b), _ptr(q), _ptr(topk_idx), topk, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    if check:
+        _check_device(workspace, stream)
+    return out, lse
 
 
 def sparse_mla_prefill(layer: LayerCache, batch: Batch, q, topk_idx, scale: float = DEFAULT_SCALE, out=None, lse=None,

@@ -25,7 +25,7 @@ EXPORTS = ("dsa_abi_version", "dsa_last_error", "dsa_kernel_launches", "dsa_cach
            "dsa_mla_workspace_bytes", "dsa_kv_append", "dsa_indexer_scores_topk", "dsa_indexer_scores_topk_static",
            "dsa_indexer_page_workspace_bytes", "dsa_indexer_page_topk", "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill",
            "dsa_dcp_candidates", "dsa_dcp_select", "dsa_dcp_merge", "dsa_sparse_mla_decode_ragged",
-           "dsa_kv_append_layers", "dsa_read_status", "dsa_check_device_status")
+           "dsa_kv_append_layers", "dsa_read_status", "dsa_check_device_status", "dsa_sparse_mla_decode_layers")
 
 
 class DsaCache(ctypes.Structure):
@@ -91,6 +91,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = I32
         fn.argtypes = [ctypes.POINTER(DsaCache), ctypes.POINTER(DsaBatch), P, P, I32, ctypes.c_float, P, P, P, SZ, P]
+    lib.dsa_sparse_mla_decode_layers.restype = I32
+    lib.dsa_sparse_mla_decode_layers.argtypes = [ctypes.POINTER(DsaCache), I32, ctypes.POINTER(DsaBatch), P, P, I32,
+                                                 ctypes.c_float, P, P, P, SZ, P]
     lib.dsa_kv_append_layers.restype = I32
     lib.dsa_kv_append_layers.argtypes = [ctypes.POINTER(DsaCache), I32, P, P, P, I32, P, P, I32, P]
     lib.dsa_dcp_candidates.restype = I32

@@ -143,10 +143,18 @@ static RowMeta row_meta(const dsa_batch* b, bool decode) {
 static dsa_status sparse_mla_common(const dsa_cache* layer, const dsa_batch* batch, const void* q,
                                     const int32_t* topk_idx, int32_t topk, float scale, void* out, float* lse,
                                     void* workspace, size_t workspace_bytes, void* stream, bool decode,
-                                    const int32_t* row_counts = nullptr) {
-  dsa_status st = check_cache(layer, false);
-  if (st != DSA_OK) return st;
-  st = check_batch(batch, !decode);
+                                    const int32_t* row_counts = nullptr, int num_layers = 1) {
+  if (!layer) return fail(DSA_ERR_INVALID_ARG, "cache is NULL");
+  if (num_layers < 1 || num_layers > kMlaMaxLayers)
+    return fail(DSA_ERR_UNSUPPORTED, "num_layers %d outside 1..%d", num_layers, kMlaMaxLayers);
+  for (int l = 0; l < num_layers; ++l) {
+    dsa_status st = check_cache(&layer[l], false);
+    if (st != DSA_OK) return num_layers > 1 ? fail(st, "layer %d: %s", l, dsa_last_error()) : st;
+    if (layer[l].page_size != layer[0].page_size || layer[l].num_pages != layer[0].num_pages ||
+        layer[l].latent_format != layer[0].latent_format)
+      return fail(DSA_ERR_INVALID_ARG, "layer %d: page size, page count and latent format must match layer 0's", l);
+  }
+  dsa_status st = check_batch(batch, !decode);
   if (st != DSA_OK) return st;
   if (!topk_idx)
     return fail(DSA_ERR_INVALID_ARG, "topk_idx is NULL: a shared layer must be given the owner layer's index buffer");
@@ -158,14 +166,30 @@ static dsa_status sparse_mla_common(const dsa_cache* layer, const dsa_batch* bat
     return fail(DSA_ERR_INVALID_ARG, "decode takes one row per request (num_rows %d, num_requests %d)",
                 batch->num_rows, batch->num_requests);
   if (batch->num_rows == 0) return ok();
-  MlaPlan plan = plan_mla(batch->num_rows, topk);
+  if ((int64_t)num_layers * batch->num_rows > INT32_MAX / kHeads)
+    return fail(DSA_ERR_UNSUPPORTED, "num_layers * num_rows is too large");
+  MlaPlan plan = plan_mla(num_layers * batch->num_rows, topk);
   if (plan.workspace_bytes > 0 && (!workspace || workspace_bytes < plan.workspace_bytes))
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes dsa_mla_workspace_bytes requires",
                 workspace_bytes, plan.workspace_bytes);
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(DSA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
   RowMeta m = row_meta(batch, decode);
-  cudaError_t e = launch_sparse_mla(*layer, m, batch->num_rows, q, topk_idx, topk, scale, out, lse, workspace, plan,
-                                    (cudaStream_t)stream, row_counts);
+  if (num_layers > 1 && layer[0].latent_format == DSA_LATENT_E4M3) {
+    // a packed 8-bit latent carries one scale array per layer: one call per layer, in order, on the
+    // same workspace (the stream orders them)
+    const size_t rows = (size_t)batch->num_rows;
+    const MlaPlan one = plan_mla(batch->num_rows, topk);
+    for (int l = 0; l < num_layers; ++l) {
+      cudaError_t e = launch_sparse_mla(&layer[l], 1, m, batch->num_rows,
+                                        static_cast<const char*>(q) + l * rows * kHeads * kRow * 2, topk_idx, topk,
+                                        scale, static_cast<char*>(out) + l * rows * kHeads * kLatent * 2,
+                                        lse ? lse + l * rows * kHeads : nullptr, workspace, one, (cudaStream_t)stream);
+      if (e != cudaSuccess) return cuda_status(e, "sparse MLA launch");
+    }
+    return ok();
+  }
+  cudaError_t e = launch_sparse_mla(layer, num_layers, m, batch->num_rows, q, topk_idx, topk, scale, out, lse, workspace,
+                                    plan, (cudaStream_t)stream, row_counts);
   return cuda_status(e, "sparse MLA launch");
 }
 
@@ -457,6 +481,14 @@ dsa_status dsa_sparse_mla_decode(const dsa_cache* layer, const dsa_batch* batch,
                                  int32_t topk, float scale, void* out, float* lse, void* workspace,
                                  size_t workspace_bytes, void* stream) {
   return sparse_mla_common(layer, batch, q, topk_idx, topk, scale, out, lse, workspace, workspace_bytes, stream, true);
+}
+
+dsa_status dsa_sparse_mla_decode_layers(const dsa_cache* layers, int32_t num_layers, const dsa_batch* batch,
+                                        const void* q, const int32_t* topk_idx, int32_t topk, float scale, void* out,
+                                        float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!layers) return fail(DSA_ERR_INVALID_ARG, "layers is NULL");
+  return sparse_mla_common(layers, batch, q, topk_idx, topk, scale, out, lse, workspace, workspace_bytes, stream, true,
+                           nullptr, num_layers);
 }
 
 dsa_status dsa_sparse_mla_decode_ragged(const dsa_cache* layer, const dsa_batch* batch, const void* q,

@@ -189,7 +189,11 @@ cudaError_t launch_page_pool(const RowMeta& m, int row0, int nrows, const float*
 cudaError_t launch_page_expand(const RowMeta& m, int row0, int nrows, const int32_t* page_idx, int kp, int page_log2,
                                int32_t* token_idx, cudaStream_t s);
 
-cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows, const void* q,
+// layers[0 .. num_layers) share one index buffer, page size, pool size and latent format; q, out and
+// lse hold num_layers * num_rows rows, layer-major; plan is plan_mla(num_layers * num_rows, topk).
+// A packed 8-bit latent takes one layer per call.
+constexpr int kMlaMaxLayers = 4;
+cudaError_t launch_sparse_mla(const dsa_cache* layers, int num_layers, const RowMeta& m, int num_rows, const void* q,
                               const int32_t* topk_idx, int topk, float scale, void* out, float* lse,
                               void* workspace, const MlaPlan& plan, cudaStream_t s,
                               const int32_t* row_count = nullptr);

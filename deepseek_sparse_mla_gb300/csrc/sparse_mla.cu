@@ -143,10 +143,20 @@ __device__ __forceinline__ uint16_t half_pow2_bits(int e) {
 // into the tile's usual swizzled 576-wide layout in fp16: c_KV = code * scale, k_R converted.  The
 // query row is converted to fp16 in place once it lands, P^T is written in fp16, and both MMAs take
 // fp16 operands (kind::f16 with A and B of one type).
-template <bool kC8>
+// One call may cover the layers of an IndexShare group (one index buffer): its rows are then the
+// layers' rows stacked layer-major (q, out, lse and the split-k slots by that combined row), and
+// a tile gathers from the latent pool of its own layer, layer = combined row / layer_rows.
+// A one-layer call passes a single map (kNL = 1: no layer arithmetic, the smallest parameter block).
+template <int kNL>
+struct MlaKvMaps {
+  CUtensorMap layer[kNL];
+};
+
+template <bool kC8, int kNL>
 __global__ void __launch_bounds__(mla::kThreads, 1)
-    sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
-                         const MlaArgs a, const float* __restrict__ latent_scales, int rows_share_pool) {
+    sparse_mla_tc_kernel(const __grid_constant__ MlaKvMaps<kNL> kv, const __grid_constant__ CUtensorMap q_map,
+                         const MlaArgs a, const float* __restrict__ latent_scales, int rows_share_pool,
+                         int layer_rows) {
   using namespace mla;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -202,7 +212,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     reinterpret_cast<uint4*>(sKV)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&kv_map);
+    prefetch_tmap(&kv.layer[0]);
     prefetch_tmap(&q_map);
   }
   // the index buffer, the queries and the caches are complete past this point (programmatic
@@ -250,7 +260,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     int q_loads = 0, cur_row = -1;
     int filled[2] = {0, 0};
     auto lookup = [&](int u) -> int64_t {
-      const int r = u / T, j = u - r * T;
+      const int rr = u / T, j = u - rr * T, r = kNL > 1 ? rr % layer_rows : rr;   // the row within its layer
       int req, pos;
       row_info(a.m, r, req, pos);
       const int g = warp + kProducers * (lane >> 2);
@@ -374,8 +384,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
       if (lane < kPieces * ng && gbits) {
         uint8_t* stage = sKV + b * kStageBytes;
         const int g = warp + kProducers * q;
-        tma_gather4_hint(stage + c * kChunkBytes + g * 512, &kv_map, c * 64, y[0], y[1], y[2], y[3], land,
-                         gather_policy);
+        tma_gather4_hint(stage + c * kChunkBytes + g * 512, &kv.layer[kNL > 1 ? r / layer_rows : 0], c * 64,
+                         y[0], y[1], y[2], y[3], land, gather_policy);
       }
       if constexpr (kC8) {
        if (new_q) {
@@ -890,26 +900,40 @@ MlaPlan plan_mla(int num_rows, int topk) {
   return p;
 }
 
-cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows, const void* q,
+cudaError_t launch_sparse_mla(const dsa_cache* layers, int num_layers, const RowMeta& m, int num_rows, const void* q,
                               const int32_t* topk_idx, int topk, float scale, void* out, float* lse,
                               void* workspace, const MlaPlan& plan, cudaStream_t s, const int32_t* row_count) {
   static std::atomic<uint64_t> configured{0};
   cudaError_t set = once_per_device(configured, [] {
-    cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel<false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          mla::kSmemBytes);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(sparse_mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::kSmemBytes);
+      e = cudaFuncSetAttribute(sparse_mla_tc_kernel<false, kMlaMaxLayers>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               mla::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(sparse_mla_tc_kernel<true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               mla::kSmemBytes);
     return e;
   });
   if (set != cudaSuccess) return set;
+  if (num_layers < 1 || num_layers > kMlaMaxLayers) return cudaErrorInvalidValue;
+  const dsa_cache& c = layers[0];              // the layers share page size, pool size and latent format
   const bool c8 = c.latent_format == DSA_LATENT_E4M3;
+  if (c8 && num_layers > 1) return cudaErrorInvalidValue;   // one scale array per call
   const float* ls = c8 ? c.latent_scales : nullptr;
-  CUtensorMap kv_map, q_map;
-  // a packed 8-bit row is 640 bytes: 320 16-bit columns, gathered as five 64-column pieces
-  if (!(c8 ? g_kv8_maps.get(c.latent, (uint64_t)c.num_pages * c.page_size, 1, &kv_map, 320)
-           : g_kv_maps.get(c.latent, (uint64_t)c.num_pages * c.page_size, 1, &kv_map)))
-    return cudaErrorInvalidValue;
-  if (!g_q_maps.get(q, (uint64_t)num_rows * kHeads, 64, &q_map)) return cudaErrorInvalidValue;
+  MlaKvMaps<kMlaMaxLayers> kv_maps;
+  CUtensorMap q_map;
+  for (int l = 0; l < num_layers; ++l) {
+    const dsa_cache& cl = layers[l];
+    // a packed 8-bit row is 640 bytes: 320 16-bit columns, gathered as five 64-column pieces
+    if (!(c8 ? g_kv8_maps.get(cl.latent, (uint64_t)cl.num_pages * cl.page_size, 1, &kv_maps.layer[l], 320)
+             : g_kv_maps.get(cl.latent, (uint64_t)cl.num_pages * cl.page_size, 1, &kv_maps.layer[l])))
+      return cudaErrorInvalidValue;
+  }
+  for (int l = num_layers; l < kMlaMaxLayers; ++l) kv_maps.layer[l] = kv_maps.layer[0];
+  // the rows of every layer, stacked layer-major
+  const int rows = num_rows * num_layers;
+  if (!g_q_maps.get(q, (uint64_t)rows * kHeads, 64, &q_map)) return cudaErrorInvalidValue;
   uint32_t* err = static_cast<uint32_t*>(workspace);
   cudaError_t e = cudaSuccess;
   MlaArgs a;
@@ -920,7 +944,7 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
   a.topk = topk;
   a.tiles = plan.tiles;
   a.units = plan.units;
-  a.ctas = plan.split > 1 ? num_rows * plan.split : plan.ctas;
+  a.ctas = plan.split > 1 ? rows * plan.split : plan.ctas;
   a.split = plan.split;
   a.log2_page = ilog2(c.page_size);
   a.num_pages = c.num_pages;
@@ -950,8 +974,12 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
     // the same cached rows, which keep their normal L2 priority (a 4096-row prefill chunk then reads
     // 1.7 GB from DRAM instead of 8.3 GB); with fewer rows per request (verify) evicting first is faster
     const int share = m.query_start_loc != nullptr && num_rows >= 8 * m.num_requests ? 1 : 0;
-    e = c8 ? cudaLaunchKernelEx(&c, sparse_mla_tc_kernel<true>, kv_map, q_map, a, ls, share)
-           : cudaLaunchKernelEx(&c, sparse_mla_tc_kernel<false>, kv_map, q_map, a, ls, share);
+    MlaKvMaps<1> one_map;
+    one_map.layer[0] = kv_maps.layer[0];
+    e = c8               ? cudaLaunchKernelEx(&c, sparse_mla_tc_kernel<true, 1>, one_map, q_map, a, ls, share, num_rows)
+        : num_layers > 1 ? cudaLaunchKernelEx(&c, sparse_mla_tc_kernel<false, kMlaMaxLayers>, kv_maps, q_map, a, ls,
+                                              share, num_rows)
+                         : cudaLaunchKernelEx(&c, sparse_mla_tc_kernel<false, 1>, one_map, q_map, a, ls, share, num_rows);
   }
   count_launches(1);
   if (e != cudaSuccess) return e;
@@ -959,7 +987,7 @@ cudaError_t launch_sparse_mla(const dsa_cache& c, const RowMeta& m, int num_rows
   if (e != cudaSuccess) return e;
   if (plan.split == 1) {
     // the merge may be scheduled while the attention grid drains (it waits for that grid's writes)
-    e = launch_pdl(mla_merge_kernel, dim3(num_rows, kHeads / kMergeHeads), dim3(512), 0, s, a);
+    e = launch_pdl(mla_merge_kernel, dim3(rows, kHeads / kMergeHeads), dim3(512), 0, s, a);
     count_launches(1);
     if (e != cudaSuccess) return e;
   }

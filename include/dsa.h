@@ -73,7 +73,7 @@ extern "C" {
 #define DSA_MAX_TOPK 8192    /* largest supported top-k budget                   */
 #define DSA_STATIC_SCRATCH_BYTES (16u << 20)  /* scratch of dsa_indexer_scores_topk_static */
 
-#define DSA_ABI_VERSION 3
+#define DSA_ABI_VERSION 4
 
 typedef enum {
   DSA_OK = 0,
@@ -367,6 +367,26 @@ DSA_API dsa_status dsa_indexer_scores_topk_static(const dsa_cache* owner, const 
 DSA_API dsa_status dsa_sparse_mla_decode(const dsa_cache* layer, const dsa_batch* batch, const void* q,
                                  const int32_t* topk_idx, int32_t topk, float scale, void* out, float* lse,
                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dsa_sparse_mla_decode for the layers of an IndexShare group in one call: every layer attends with
+ * the same index buffer (the owner's), so one launch covers all of them, its units (layer, row,
+ * 64-entry tile) spread over every SM.  The result equals num_layers dsa_sparse_mla_decode calls,
+ * one per layer, up to the floating-point order of the split-k merge.  ("GLM-5.2 on vLLM Ascend",
+ * section 7, "GLM-5.2 shared-indexer construction": shared layers reuse the owner's top-k.)
+ *   layers      host array [num_layers] of the layers' caches, 1 <= num_layers <= 4; they must agree in
+ *               page_size, num_pages and latent_format (the block table is shared).  A packed 8-bit
+ *               latent runs as one launch per layer.
+ *   q           device bf16 [num_layers, num_rows, 64, 576]: layer l's queries at [l].
+ *   out         device bf16 [num_layers, num_rows, 64, 512];  lse: optional device fp32
+ *               [num_layers, num_rows, 64].
+ *   workspace   at least dsa_mla_workspace_bytes(num_layers * num_rows, topk) bytes, 256-byte aligned.
+ *   Other arguments as for dsa_sparse_mla_decode; DSA_ERR_UNSUPPORTED for num_layers outside 1..4.
+ */
+DSA_API dsa_status dsa_sparse_mla_decode_layers(const dsa_cache* layers, int32_t num_layers, const dsa_batch* batch,
+                                        const void* q, const int32_t* topk_idx, int32_t topk, float scale,
+                                        void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                        void* stream);
 
 /*
  * dsa_sparse_mla_decode over index buffers whose valid entries lead each row: row r's entries at

@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in declared():
         assert hasattr(lib, n), n
     assert set(declared()) == set(_lib.EXPORTS)
-    assert lib.dsa_abi_version() == 3
+    assert lib.dsa_abi_version() == 4
 
 
 def test_missing_library_fails_loudly(tmp_path):

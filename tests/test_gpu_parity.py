@@ -305,3 +305,57 @@ def test_planted_sample_pushes_threshold_above_kth_score(seq_lens):
     for r, L in enumerate(wl.seq_lens):
         check_scores(g_sc[r], o_sc[r], L - 1, wl.max_seq_len)
         check_topk(g_idx[r], o_idx[r], o_sc[r], L - 1, k)
+
+
+def _layer_group_workload(kind):
+    if kind == "clusters":
+        return wlm.reduced("decode_b64_fp8_indexshare")          # 6 rows x 4 layers: clusters of 4 CTAs
+    lens = np.random.default_rng(2203).integers(1500, 3200, 20).tolist()
+    if kind == "unit_split":                                       # 80 stacked rows: rows cut between CTAs
+        return wlm.Workload("decode_b20_ctx1500-3200_fp8_layers4", lens, [1] * 20, 64, "fp8", 512, 4, 2203)
+    return wlm.Workload("decode_b3_ctx1500-3200_c8_layers2", lens[:3], [1] * 3, 64, "fp8", 512, 2, 2204,
+                        latent_format="fp8")
+
+
+@pytest.mark.parametrize("kind", ["clusters", "unit_split", "packed_latent"])
+def test_layer_group_attention_in_one_call(kind):
+    """dsa_sparse_mla_decode_layers: an IndexShare group's layers attend with the owner's buffer in
+    one call (stacked q / out / lse), each layer against the oracle on the oracle's selection and
+    against the one-layer call."""
+    import torch
+    import deepseek_sparse_mla_gb300 as dsa
+    wl = _layer_group_workload(kind)
+    hp = HostProblem(wl)
+    gp = GpuProblem(hp)
+    gp.append_step()
+    o_idx, _ = hp.oracle_topk()
+    idx = torch.from_numpy(o_idx).to("cuda")
+    q = torch.stack(gp.q).contiguous()
+    lse = torch.empty((wl.layers, wl.num_rows, 64), dtype=torch.float32, device="cuda")
+    out, _ = dsa.sparse_mla_decode_layers(gp.caches, gp.batch, q, idx, wl.scale, lse=lse, check=True)
+    torch.cuda.synchronize()
+    for layer in range(wl.layers):
+        o_out, o_lse = hp.oracle_attention(layer, o_idx)
+        check_attention(bf16_tensor_to_f64(out[layer]), lse[layer].cpu().numpy(), o_out, o_lse)
+        one, one_lse = gp.attention(layer, idx)
+        assert (out[layer].float() - one.float()).abs().max().item() <= 2e-2
+        fin = torch.isfinite(one_lse)
+        assert torch.equal(fin, torch.isfinite(lse[layer]))
+        assert (lse[layer][fin] - one_lse[fin]).abs().max().item() <= 1e-4
+
+
+def test_layer_group_call_rejects_mismatched_layers():
+    import torch
+    import deepseek_sparse_mla_gb300 as dsa
+    wl = wlm.reduced("decode_b64_fp8_indexshare")
+    hp = HostProblem(wl)
+    gp = GpuProblem(hp)
+    other = dsa.LayerCache(wl.num_pages * 2, wl.page_size, None, "cuda")
+    idx = torch.zeros((wl.num_rows, wl.topk), dtype=torch.int32, device="cuda")
+    q = torch.zeros((2, wl.num_rows, 64, 576), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dsa.DsaError):
+        dsa.sparse_mla_decode_layers([gp.caches[0], other], gp.batch, q, idx, wl.scale)
+    with pytest.raises(dsa.DsaError):
+        dsa.sparse_mla_decode_layers([gp.caches[0]] * 5, gp.batch,
+                                     torch.zeros((5, wl.num_rows, 64, 576), dtype=torch.bfloat16, device="cuda"),
+                                     idx, wl.scale)
