@@ -768,15 +768,23 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
 // LSE merge of the pieces of rows that were cut between CTAs:
 //   out = sum_j e^{m_j - M} O_j / sum_j e^{m_j - M} l_j,  lse = M + ln sum_j e^{m_j - M} l_j.
-// CTA (row, 16 heads), thread (head, 16 consecutive latent dims); the pieces are read two at a time
-// with all loads of a pair in flight, and merged online across pairs (the running maximum rescales
-// what is already summed).  Launched as a programmatic dependent of the attention kernel: the wait
-// below orders every read after that grid's writes.
+// One CTA per (CTA boundary b = 1 .. ctas - 1, 16 heads): a boundary inside a row stands for that row,
+// once (its first boundary; rows that are not cut are written by the attention kernel), so the grid
+// has one CTA per cut row and head group.  Thread (head, 16 consecutive latent dims); the pieces are
+// read two at a time with all loads of a pair in flight, and merged online across pairs (the running
+// maximum rescales what is already summed).  Launched as a programmatic dependent of the attention
+// kernel: the wait below orders every read after that grid's writes.
 constexpr int kMergeHeads = 16;
 __global__ void __launch_bounds__(512, 2) mla_merge_kernel(MlaArgs a) {
-  const int r = blockIdx.x, tid = threadIdx.x;
+  const int tid = threadIdx.x, T = a.tiles;
   const int h = blockIdx.y * kMergeHeads + (tid >> 5), d0 = (tid & 31) * 16;
-  const int T = a.tiles;
+  const int ub = unit_start(blockIdx.x + 1, a.units, a.ctas), r = ub / T;
+  // no cut here, or not the row's first cut: nothing to do (the wait still orders this grid's end)
+  if (ub == r * T || unit_start(blockIdx.x, a.units, a.ctas) > r * T) {
+    pdl_wait();
+    pdl_trigger();
+    return;
+  }
   __shared__ int span[3];
   if (tid == 0) {
     // the pieces of row r: CTAs c_first .. c_last.  The first piece sits in its CTA's first-row slot
@@ -790,7 +798,6 @@ __global__ void __launch_bounds__(512, 2) mla_merge_kernel(MlaArgs a) {
   const int c_first = span[0], c_last = span[1], first_slot = span[2];
   pdl_wait();
   pdl_trigger();
-  if (c_first == c_last) return;    // written directly by the attention kernel
   constexpr int G = 2;
   float M = -INFINITY, L = 0.f;
   float acc[16];
@@ -987,7 +994,7 @@ cudaError_t launch_sparse_mla(const dsa_cache* layers, int num_layers, const Row
   if (e != cudaSuccess) return e;
   if (plan.split == 1) {
     // the merge may be scheduled while the attention grid drains (it waits for that grid's writes)
-    e = launch_pdl(mla_merge_kernel, dim3(rows, kHeads / kMergeHeads), dim3(512), 0, s, a);
+    if (a.ctas > 1) e = launch_pdl(mla_merge_kernel, dim3(a.ctas - 1, kHeads / kMergeHeads), dim3(512), 0, s, a);
     count_launches(1);
     if (e != cudaSuccess) return e;
   }
