@@ -280,8 +280,17 @@ def profile_decode_b24_ctx48k_96k() -> Workload:
 
 
 # workloads that exist for profiler captures only (not parity or benchmark configurations)
+def profile_decode_b64_ctx8k_12k_layers4() -> Workload:
+    """The headline's layer group (64 rows x 4 layers sharing one top-2048 index buffer) at 8K-12K
+    contexts: about 3 GB resident, for a capture of the one-call attention over the four layers (whose
+    cost depends on the selected rows, not on the context length)."""
+    lens = _rng(4003, _TAG_LENS).integers(8192, 12288 + 1, 64)
+    return Workload("profile_decode_b64_ctx8k-12k_fp8_layers4", lens, [1] * 64, 64, "fp8", 2048, 4, 4003)
+
+
 PROFILE = {"profile_decode_b64_ctx16k_32k": profile_decode_b64_ctx16k_32k,
-           "profile_decode_b24_ctx48k_96k": profile_decode_b24_ctx48k_96k}
+           "profile_decode_b24_ctx48k_96k": profile_decode_b24_ctx48k_96k,
+           "profile_decode_b64_ctx8k_12k_layers4": profile_decode_b64_ctx8k_12k_layers4}
 
 
 def reduced(name: str) -> Workload:
