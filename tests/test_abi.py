@@ -252,6 +252,32 @@ def test_multi_layer_append_rejects_bad_arguments(lib):
     assert lib.dsa_kv_append_layers(two, 2, arr(A, A), arr(A, A + 8), arr(A, None), 0, None, P(A), 8, None) == INVALID
 
 
+def test_layer_group_attention_rejects_bad_arguments(lib):
+    """dsa_sparse_mla_decode_layers: the layers' caches must agree in page size, page count and latent
+    format, 1 to 4 layers, a workspace for every layer's rows; all checked before any launch."""
+    from deepseek_sparse_mla_gb300._lib import DsaCache
+    P = ctypes.c_void_p
+    layer = lambda pages=16, size=64, fmt=0, scales=0: DsaCache(A, 0, 0, pages, size, 0, fmt, scales)   # noqa: E731
+    b = _batch()
+    call = lib.dsa_sparse_mla_decode_layers
+    ws4 = lib.dsa_mla_workspace_bytes(8, 128)
+    four = (DsaCache * 5)(*[layer() for _ in range(5)])
+    assert call(None, 2, ctypes.byref(b), P(A), P(A), 128, 0.0625, P(A), None, P(A), ws4, None) == INVALID
+    assert call(four, 0, ctypes.byref(b), P(A), P(A), 128, 0.0625, P(A), None, P(A), ws4, None) == UNSUPPORTED
+    assert call(four, 5, ctypes.byref(b), P(A), P(A), 128, 0.0625, P(A), None, P(A), ws4, None) == UNSUPPORTED
+    for other in (layer(pages=32), layer(size=128), layer(fmt=1, scales=A)):
+        pair = (DsaCache * 2)(layer(), other)
+        assert call(pair, 2, ctypes.byref(b), P(A), P(A), 128, 0.0625, P(A), None, P(A), ws4, None) == INVALID
+        assert "layer 1" in _err(lib)
+    # the workspace covers every layer's rows: one sized for a single layer's rows is too small here
+    small = lib.dsa_mla_workspace_bytes(2, 128)
+    assert small < ws4
+    assert call(four, 4, ctypes.byref(b), P(A), P(A), 128, 0.0625, P(A), None, P(A), small, None) == WORKSPACE
+    # a shared index buffer is required, as for the one-layer call
+    assert call(four, 4, ctypes.byref(b), P(A), None, 128, 0.0625, P(A), None, P(A), ws4, None) == INVALID
+    assert "owner layer's index buffer" in _err(lib)
+
+
 def test_device_status_helpers(lib):
     """dsa_check_device_status names the bits; dsa_read_status validates its arguments before any launch."""
     assert lib.dsa_check_device_status(0) == 0
