@@ -258,9 +258,9 @@ __global__ void __launch_bounds__(kKind == 2 ? idx::kThreadsI8 : idx::kThreads, 
   constexpr int kTerms = kFp8 ? 2 : 1;               // B rows per (row, head): e4m3 split terms
   constexpr int kLoaderWarp = kProducers + kMmaWarps;
   constexpr int kEpiWarp0 = kLoaderWarp + 1;           // two epilogue warpgroups take alternate tiles
-  // named barriers: 2 + eg and kScaleBar0 + eg within epilogue warpgroup eg; kPrologueBar for the
-  // loader and the epilogue warps filling the first group's queries together
-  constexpr int kScaleBar0 = 4, kPrologueBar = 6, kPrologueThreads = 32 * 9;
+  // named barriers: 2 + eg within epilogue warpgroup eg; kPrologueBar for the loader and the
+  // epilogue warps filling the first group's queries together
+  constexpr int kPrologueBar = 6, kPrologueThreads = 32 * 9;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // carve-up (uniform across the CTA): B buffers sized for the group, then scales, then keys

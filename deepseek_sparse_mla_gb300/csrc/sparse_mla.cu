@@ -642,7 +642,13 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
           if ((lane & 15) == 0) red[quarter][hh + h] = v;
         }
         named_bar_sync(bar, 128);
-        if (st < 32) lfin[h0 + st] = (red[0][h0 + st] + red[1][h0 + st]) + (red[2][h0 + st] + red[3][h0 + st]);
+        if (st < 32) {
+          const float L = (red[0][h0 + st] + red[1][h0 + st]) + (red[2][h0 + st] + red[3][h0 + st]);
+          lfin[h0 + st] = L;
+          // 1 / l for a whole row's output, in alpha (this tile's rescale factors are no longer read):
+          // a division per output element made the epilogue of a whole row about 3 times slower
+          alpha[h0 + st] = L > 0.f ? 1.f / L : 0.f;
+        }
         named_bar_sync(bar, 128);
         if (!mbar_wait(&o_full, seg & 1, err, kErrMmaTimeout, kPolls)) break;
         tc_fence_after();
@@ -661,11 +667,9 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
           if (whole) {
             __nv_bfloat16* dst = a.out + (int64_t)r * kHeads * kLatent + d;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const int h = h0 + jj;
-              const float L = lfin[h];
-              dst[(int64_t)h * kLatent] = __float2bfloat16_rn(L > 0.f ? __uint_as_float(o[jj]) / L : 0.f);
-            }
+            for (int jj = 0; jj < 32; ++jj)
+              dst[(int64_t)(h0 + jj) * kLatent] =
+                  __float2bfloat16_rn(has_valid ? __uint_as_float(o[jj]) * alpha[h0 + jj] : 0.f);
           } else if (split > 1) {
             // cluster mode: the piece stays in TMEM, with its m (mref, log2 units) and l (lfin) in
             // shared memory, until the cluster merge below
