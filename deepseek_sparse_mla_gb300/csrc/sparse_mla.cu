@@ -65,8 +65,13 @@ constexpr int kGroups = kTok / 4;                  // gather4 groups of a tile: 
 constexpr int kMmaWarp = 7;                        // last warp of warpgroup 1
 constexpr int kSoftmaxWarp0 = 8;                   // warpgroups 2 and 3: heads 0-31 and heads 32-63
 constexpr int kThreads = 512;
-// register split (sums to 61,440 of the 512 x 128 launched): producers / MMA 80, softmax 160
-constexpr uint32_t kRegsLow = 80, kRegsSoftmax = 160;
+// register split (sums to 61,440 of the 512 x 128 launched): producers / MMA and the two softmax
+// warpgroups.  At 80 the one-layer bf16 kernel spills in its producer code; at 88 it does not, and
+// prefill's attention takes 2.17 ms instead of 2.19.  The layer-group kernel, spill-free at 80, is
+// about 1 % slower at 88, and the packed 8-bit latent's producers keep 80 too.
+constexpr uint32_t kRegsTotal = 240;
+template <bool kC8, int kNL>
+constexpr uint32_t kRegsLow = !kC8 && kNL == 1 ? 88u : 80u;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;                      // S^T of stage b at columns 64 b
 constexpr uint32_t kColO = 128;                    // O^T chunk k (dims 128k..) at columns 128 + 64 k
@@ -247,7 +252,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
   // one register split per warpgroup, executed by all of its warps at one instruction: producers and
   // the MMA issuer (warpgroups 0-1) give registers to the two softmax warpgroups
   if (warp < kSoftmaxWarp0) {
-  regs_dec<kRegsLow>();
+  regs_dec<kRegsLow<kC8, kNL>>();
   if (warp < kProducers) {
     // ------------------------------------------------------------------ producers
     // Warp w owns the tile's gather4 groups w, w + 7 (and w + 14): lane l < 4 ng looks up entry
@@ -520,7 +525,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
     }
   }
   } else {
-    regs_inc<kRegsSoftmax>();
+    regs_inc<kRegsTotal - kRegsLow<kC8, kNL>>();
     // ------------------------------------------------------------------ softmax + epilogue (warps 8-15)
     // Warpgroup sg (0: warps 8-11, 1: warps 12-15) owns heads 32 sg .. 32 sg + 31: their running
     // maxima, rescales, denominators and outputs.  S^T row (token) tok sits in TMEM lane
