@@ -89,6 +89,37 @@ def test_empty_and_out_of_range_selections():
     check_attention(g_out, g_lse, o_out, o_lse)
 
 
+def test_unit_split_rows_with_empty_pieces():
+    """80 rows x 2 tiles (160 units on 152 CTAs): rows 9, 19, ..., 79 are whole in one CTA and written there, the
+    other 72 are cut between two CTAs and finished by the merge kernel.  Selections cycle through empty, full and
+    one valid tile only (the other piece, or the other half of a whole row, holds no valid entry), each pattern on
+    whole and on cut rows: an empty row must come out as zeros with lse = -inf, and an empty piece adds nothing."""
+    import torch
+    rng = np.random.default_rng(3011)
+    seq_lens = rng.integers(150, 400, size=80)
+    wl = wlm.Workload("unit_split_edge", seq_lens, [1] * 80, 16, "bf16", 128, 1, 3011)
+    hp = HostProblem(wl)
+    gp = GpuProblem(hp)
+    gp.append_step()
+    idx = np.full((80, 128), -1, dtype=np.int32)
+    pattern = (np.arange(80) // 10 + np.arange(80) % 10) % 4
+    for r, L in enumerate(seq_lens):
+        sel = rng.choice(int(L), size=128, replace=False).astype(np.int32)
+        if pattern[r] == 1:
+            idx[r] = sel
+        elif pattern[r] == 2:
+            idx[r, 64:] = sel[64:]                   # only the second tile has valid entries
+        elif pattern[r] == 3:
+            idx[r, :64] = sel[:64]                   # only the first tile has valid entries
+    out, lse = gp.attention(0, torch.from_numpy(idx).cuda())
+    o_out, o_lse = hp.oracle_attention(0, idx)
+    g_out, g_lse = bf16_tensor_to_f64(out), lse.cpu().numpy()
+    empty = pattern == 0
+    assert not g_out[empty].any() and np.all(np.isneginf(g_lse[empty]))
+    assert np.all(np.isfinite(g_lse[~empty]))
+    check_attention(g_out, g_lse, o_out, o_lse)
+
+
 def test_page_permutation_gives_identical_results():
     """Same logical tokens under two physical page layouts: bitwise identical outputs."""
     import torch
